@@ -1,0 +1,17 @@
+"""fp64 CPU oracle -- test infrastructure only (see ssm_oracle's header)."""
+from .ssm_oracle import (  # noqa: F401
+    BadTree,
+    softplus,
+    silu,
+    tree_layout,
+    node_window,
+    conv_silu,
+    split_xbc,
+    ssm_step,
+    ssm_out,
+    verify,
+    accept,
+    commit,
+    draft_step,
+    replay,
+)
