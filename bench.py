@@ -1,0 +1,510 @@
+#!/usr/bin/env python3
+"""Throughput of SpecMamba-style tree verification on one GB300 (or N, one process each).
+
+One step = one speculative round of the target's SSM side over one batch:
+ssm_tree_verify (tree conv + SiLU, Δ, state update, y for every node) ->
+ssm_accept_path -> ssm_commit (selective recompute of the accepted path, conv
+ring advance), for every layer of every sequence.  Metric: verified tree-node
+SSM updates per second = nodes x layers x sequences / step time.
+
+Default workload: batched target verify on the Mamba2-2.7B layer shape
+(80 heads x 64, d_state 128), 64 layers, batch 16, one seed-generated 16-node
+tree per sequence (<= 3 children, depth <= 4).  Inputs (8.9 GB per step) are
+larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload on the host cores.  Under
+torchrun each rank runs its own 16 sequences (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified tree-node SSM updates/s (all layers, 2.7B shape)"
+UNIT = "updates/s"
+DEFAULT_WORKLOAD = 3
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# byte counts (algorithmic: every tensor the step must touch, once)
+# ---------------------------------------------------------------------------
+def verify_bytes_per_instance(H, P, N, n):
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    return H * P * N * 4 + n * conv_dim * 2 + n * H * 2 + 3 * conv_dim * 2 + n * d_inner * 4 + 4
+
+
+def params_bytes_per_layer(H, P, N):
+    conv_dim = H * P + 2 * N
+    return conv_dim * 4 * 4 + conv_dim * 4 + 3 * H * 4
+
+
+def commit_bytes_per_instance(H, P, N, path_len):
+    conv_dim = H * P + 2 * N
+    return (2 * H * P * N * 4 + (path_len + 3) * conv_dim * 2 + path_len * H * 2
+            + min(path_len, 3) * conv_dim * 2 + 8)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host side; no collective touches the data path)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def shard_sequences(batch: int, rank: int):
+    """Weak scaling: rank r owns sequences [r*batch, (r+1)*batch) of the seed space."""
+    return list(range(rank * batch, (rank + 1) * batch))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        self.t0 = time.time()
+
+    def mark(self):
+        self.t_begin = time.time()
+
+    def stop(self):
+        self.t_end = time.time()
+        time.sleep(0.12)
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        # samples are ~50 ms apart; keep those from the second half (under load)
+        load = rows[len(rows) // 3:] or rows
+        sm = [float(r[1]) for r in load if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in load for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(load)}
+
+
+# ---------------------------------------------------------------------------
+# fp64 oracle as the CPU baseline / reference arm (host cores, spawn pool)
+# ---------------------------------------------------------------------------
+def _oracle_task(args):
+    """One instance of the step on the CPU oracle: verify + accept + commit."""
+    import numpy as np
+
+    import oracle
+    prm, parent, xBC, dt, h0, ring, head, tok, tgt = args
+    oracle.verify(prm, parent, xBC, dt, h0, ring, head)
+    path, _ = oracle.accept(parent, tok, tgt)
+    oracle.commit(prm, parent, path, xBC, dt, h0, ring, head)
+    return len(parent)
+
+
+def _oracle_inputs(w, seq, layer):
+    import numpy as np
+
+    from synth import batch
+    from tests.helpers import f64, params_at
+    b = batch(w, seqs=[seq], layers=[layer])
+    return (params_at(b["params"], 0), b["parent"][0], f64(b["xBC"][0, 0]), f64(b["dt"][0, 0]),
+            b["h0"][0, 0].astype(np.float64), f64(b["ring"][0, 0]), int(b["ring_head"][0, 0]), b["tok"][0],
+            b["tgt"][0])
+
+
+class OracleRunner:
+    """Spawn pool of single-threaded numpy workers over sampled instances."""
+
+    def __init__(self, w, n_inputs=None):
+        import multiprocessing as mp
+        self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        self.pool = mp.get_context("spawn").Pool(self.cores)
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k)
+            else:
+                os.environ[k] = v
+        import random
+        rnd = random.Random(0x5EED)
+        insts = [(0, 0), (w.batch - 1, w.n_layers - 1)]
+        while len(insts) < (n_inputs or self.cores):
+            insts.append((rnd.randrange(w.batch), rnd.randrange(w.n_layers)))
+        self.insts = insts
+        self.inputs = [_oracle_inputs(w, s, l) for s, l in insts]
+        self.cursor = 0
+
+    def step(self):
+        """One bounded sample: `cores` instances in parallel; returns (units, seconds)."""
+        batch = [self.inputs[(self.cursor + i) % len(self.inputs)] for i in range(self.cores)]
+        self.cursor += self.cores
+        t0 = time.perf_counter()
+        units = sum(self.pool.map(_oracle_task, batch, chunksize=1))
+        return units, time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(w, steps=3):
+    r = OracleRunner(w)
+    r.step()  # warm the workers (imports)
+    units = secs = 0.0
+    for _ in range(steps):
+        u, s = r.step()
+        units += u
+        secs += s
+    r.close()
+    return {"value": units / secs, "unit": UNIT, "cores": r.cores, "kind": "oracle",
+            "sample": f"{steps} x {r.cores} instances (seq, layer) of the same workload, each verify+accept+commit "
+                      f"of one 16-node tree in fp64 numpy, one instance per core; "
+                      f"{int(units)} node updates in {secs:.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    r = OracleRunner(w)
+    for _ in range(args.warmup):
+        r.step()
+    units = secs = 0.0
+    for _ in range(args.steps):
+        u, s = r.step()
+        units += u
+        secs += s
+    r.close()
+    value = units / secs
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "sample": f"{r.cores} instances per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": r.cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps x {r.cores} instances (seq, layer), fp64 numpy "
+                                       "oracle, one instance per core"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(kernel, units):
+    """DRAM bytes per launch from a committed ncu summary (profiles/dram_traffic.txt),
+    scaled to `units` instances; None if absent or taken on other kernel source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if kv.get("kernel") != kernel:
+            continue
+        src = os.path.join(ROOT, "speculative_decoding_mamba2_gb300", "csrc", kv.get("source", ""))
+        if not os.path.exists(src) or source_digest(src) != kv.get("sha"):
+            return None
+        return float(kv["bytes_per_unit"]) * units
+    return None
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_commit, ssm_tree_layout_build,
+                                                   ssm_tree_verify)
+    from speculative_decoding_mamba2_gb300 import build as _build
+    from synth import batch
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    _build.build()
+    dev = torch.device("cuda", local)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w)  # spawn pool before any CUDA work is queued
+
+    # ---- inputs: this rank's sequences, all layers, resident in HBM ----
+    seqs = shard_sequences(w.batch, rank)
+    b = batch(w, seqs=seqs)
+    S, L, n = len(seqs), w.n_layers, w.n_nodes()
+    H, P, N = w.shape.H, w.shape.P, w.shape.N
+    I = S * L
+    dims = Dims(n_heads=H, n_layers=L, ring_cap=w.ring_cap)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    layout_h, depth = ssm_tree_layout_build(b["parent"], max_branches=3, max_depth=4)
+    max_path = depth + 1
+    prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in b["params"].items()}
+    layout = torch.from_numpy(layout_h).to(dev)
+    xBC, dt = bf16(b["xBC"]), bf16(b["dt"])
+    h = torch.from_numpy(b["h0"]).to(dev)
+    ring = bf16(b["ring"])
+    head = torch.from_numpy(b["ring_head"]).to(dev)
+    tok, tgt = torch.from_numpy(b["tok"]).to(dev), torch.from_numpy(b["tgt"]).to(dev)
+    y = torch.empty((I, n, H * P), device=dev)
+    path = torch.empty((S, max_path), dtype=torch.int32, device=dev)
+    plen = torch.empty(S, dtype=torch.int32, device=dev)
+    bonus = torch.empty(S, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ssm_tree_verify(dims, prm, S, n, depth, layout, xBC, dt, h, ring, head, y, status)
+        if ev is not None:
+            ev[1].record(stream)
+        ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status)
+        if ev is not None:
+            ev[2].record(stream)
+        ssm_commit(dims, prm, S, n, layout, max_path, path, plen, xBC, dt, h, ring, head, status)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+    path_lens = plen.cpu().numpy()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.mark()
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms, world, dev)
+    verify_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    accept_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    commit_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    units_per_step = n * L * S * world
+    value = units_per_step / (ms / 1e3)
+
+    # ---- roofline of the dominant kernel ----
+    peak, peak_kind = measured_peaks()
+    vb = I * verify_bytes_per_instance(H, P, N, n) + L * params_bytes_per_layer(H, P, N)
+    cb = sum(L * commit_bytes_per_instance(H, P, N, int(pl)) for pl in path_lens) + L * params_bytes_per_layer(H, P, N)
+    kernels = {
+        "ssm_tree_verify": {"ms": verify_ms, "bytes": vb, "GB/s": vb / verify_ms / 1e6,
+                            "launches_per_step": 1},
+        "ssm_accept_path": {"ms": accept_ms, "launches_per_step": 1},
+        "ssm_commit": {"ms": commit_ms, "bytes": cb, "GB/s": cb / commit_ms / 1e6, "launches_per_step": 2},
+    }
+    dom = max(("ssm_tree_verify", "ssm_commit"), key=lambda k: kernels[k]["ms"])
+    ach = kernels[dom]["GB/s"]
+    kname = {"ssm_tree_verify": ("tree_verify_kernel", "verify.cu"),
+             "ssm_commit": ("commit_kernel", "commit.cu")}[dom]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                "traffic": ncu_traffic(kname[0], I),
+                "algorithmic_bytes": kernels[dom]["bytes"]}
+    step_bytes = vb + cb
+    for k in kernels.values():
+        if "GB/s" in k:
+            k["frac_of_hbm_peak"] = k["GB/s"] / peak
+
+    # ---- end to end through the public API, host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, b, dims, prm, h, ring, head, dev, stream, world)
+
+    if status.item() != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed steps")
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": w.name, "sequences_per_gpu": S, "layers": L, "nodes_per_tree": n,
+                           "heads": H, "head_dim": P, "d_state": N, "mean_accepted_path": float(path_lens.mean()),
+                           "l2": f"inputs exceed L2 ({step_bytes / 1e9:.2f} GB touched per step); no flush"},
+                "roofline": roofline, "kernels": kernels, "step_GB/s": step_bytes / ms / 1e6,
+                "step_frac_of_hbm_peak": step_bytes / ms / 1e6 / peak,
+                "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk}
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, w, b, dims, prm, h, ring, head, dev, stream, world):
+    """Same step through the public API with the step's inputs in pinned host
+    memory: host layout build, H2D of xBC/dt/layout/tokens, verify, accept,
+    commit, D2H of the accepted paths and bonus tokens, all inside the timed
+    region (wall clock, synchronised)."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import ssm_accept_path, ssm_commit, ssm_tree_layout_build, ssm_tree_verify
+    S, L, n = len(b["seqs"]), w.n_layers, w.n_nodes()
+    I = S * L
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    xBC_h = pin(b["xBC"].view(np.int16))
+    dt_h = pin(b["dt"].view(np.int16))
+    par_h = np.ascontiguousarray(b["parent"])
+    tok_h, tgt_h = pin(b["tok"]), pin(b["tgt"])
+    xBC_d = torch.empty(xBC_h.shape, dtype=torch.int16, device=dev)
+    dt_d = torch.empty(dt_h.shape, dtype=torch.int16, device=dev)
+    lay_d = torch.empty((S, n, 8), dtype=torch.int32, device=dev)
+    tok_d = torch.empty(tok_h.shape, dtype=torch.int32, device=dev)
+    tgt_d = torch.empty(tgt_h.shape, dtype=torch.int32, device=dev)
+    y = torch.empty((I, n, dims.d_inner), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        lay, depth = ssm_tree_layout_build(par_h, max_branches=3, max_depth=4)
+        max_path = depth + 1
+        lay_h = torch.from_numpy(lay).pin_memory()
+        lay_d.copy_(lay_h, non_blocking=True)
+        xBC_d.copy_(xBC_h, non_blocking=True)
+        dt_d.copy_(dt_h, non_blocking=True)
+        tok_d.copy_(tok_h, non_blocking=True)
+        tgt_d.copy_(tgt_h, non_blocking=True)
+        path = torch.empty((S, max_path), dtype=torch.int32, device=dev)
+        plen = torch.empty(S, dtype=torch.int32, device=dev)
+        bonus = torch.empty(S, dtype=torch.int32, device=dev)
+        xb, d = xBC_d.view(torch.bfloat16), dt_d.view(torch.bfloat16)
+        ssm_tree_verify(dims, prm, S, n, depth, lay_d, xb, d, h, ring, head, y, status)
+        ssm_accept_path(S, n, max_path, lay_d, tok_d, tgt_d, path, plen, bonus, status)
+        ssm_commit(dims, prm, S, n, lay_d, max_path, path, plen, xb, d, h, ring, head, status)
+        out = torch.empty((S, max_path + 2), dtype=torch.int32).pin_memory()
+        out[:, :max_path].copy_(path, non_blocking=True)
+        out[:, max_path].copy_(plen, non_blocking=True)
+        out[:, max_path + 1].copy_(bonus, non_blocking=True)
+        torch.cuda.synchronize()
+        return out, max_path
+
+    for _ in range(2):
+        one()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        out, max_path = one()
+    secs = (time.perf_counter() - t0) / steps
+    secs = max_over_ranks(secs, world, dev)
+    h2d = xBC_h.numel() * 2 + dt_h.numel() * 2 + S * n * 32 + 2 * S * n * 4
+    d2h = S * (max_path + 2) * 4
+    return {"value": n * L * S * world / secs, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": secs * 1e3}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[2, 3])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from synth import workload
+    w = workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,209 @@
+/*
+ * ssm_tree.h -- C ABI of libssmtree: SpecMamba-style tree verification for a
+ * Mamba2 selective-SSM layer, on one GB300 (sm_103a).
+ *
+ * Method, by page and section:
+ *   - "FPGA加速Mamba推理：SpecMamba方案与优化实践" §1.2: a draft model proposes
+ *     tokens, the target model verifies them in parallel; §2.1: a rejection
+ *     forces the SSM state back to the last accepted token; §3.1: the draft
+ *     keeps only light intermediates (Δ, A, B, X) and recovers from them, the
+ *     target recomputes only the affected path; §3.2: the token tree is
+ *     flattened breadth-first and each node's children are updated from the
+ *     node's state, which is released once they are done; §5.2: tree_config
+ *     (max_branches, max_depth).
+ *   - "FPGA 加速器完全拆解（二）…LightMamba", section "为什么 Mamba 难加速":
+ *     X, B, C, Δ from the input projection; X through conv1d into the SSM with
+ *     state h_t; the update terms Ā·h_{t-1} and B̄·X.
+ * Read in the Mamba2 form (ngroups = 1):
+ *     post = SiLU(conv_b + Σ_k conv_w[k]·row[k])      (width-4 causal conv, oldest tap first)
+ *     x | B | C = post split as [d_inner | N | N]    (head h owns x[h·P, (h+1)·P))
+ *     Δ = softplus(dt + dt_bias),  A = -exp(A_log),  Ā = exp(Δ·A)   (per head)
+ *     h_v = Ā_v·h_parent(v) + Δ_v·(x_v ⊗ B_v),   h_parent(root) = h0
+ *     y_v = C_v·h_v + D·x_v
+ *
+ * Conventions for every call:
+ *   - Sizes: H heads, P head_dim, N d_state, W conv width (= 4),
+ *     d_inner = H·P, conv_dim = d_inner + 2·N, L layers, S sequences,
+ *     I = S·L instances, instance i = seq·L + layer (sequence-major), n nodes
+ *     per tree.  Every array is dense, row-major, in the order its comment gives.
+ *   - "device" pointers are CUDA device memory owned by the caller; the library
+ *     never allocates, frees or keeps them.  "host" pointers are host memory.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device calls
+ *     only enqueue work on it and return; results are ready when the stream is.
+ *   - Return value: SSM_OK or a negative SSM_ERR_*; on error nothing was
+ *     enqueued and ssm_last_error() (thread-local) says why.
+ *   - `dev_status` (device, may be NULL): one int32 that kernels OR the
+ *     SSM_STATUS_* bits into when device-resident data is inconsistent (a
+ *     layout record out of range, a path or k out of range).  The offending item
+ *     is clamped or skipped, never read or written out of bounds.  The caller
+ *     zeroes it and reads it back when it wants to know.
+ */
+#ifndef SSM_TREE_H
+#define SSM_TREE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSM_OK 0
+#define SSM_ERR_INVALID_ARG (-1) /* null pointer, bad size, unsupported shape   */
+#define SSM_ERR_BAD_TREE (-2)    /* parent[] not a breadth-first tree          */
+#define SSM_ERR_CAPACITY (-3)    /* tree or ring larger than the caps          */
+#define SSM_ERR_CUDA (-4)        /* a CUDA runtime call failed                 */
+#define SSM_ERR_RANGE (-5)       /* a scalar argument out of range             */
+
+#define SSM_STATUS_BAD_LAYOUT 1  /* a layout record points outside its tree     */
+#define SSM_STATUS_PATH_RANGE 2  /* path_len or a path entry out of range       */
+#define SSM_STATUS_K_RANGE 4     /* replay k larger than the logged steps       */
+#define SSM_STATUS_WALK_TRUNCATED 8 /* accept walk longer than max_path         */
+
+/* Limits of this build (checked on the host; larger inputs get SSM_ERR_CAPACITY). */
+#define SSM_MAX_NODES 64         /* nodes per tree for ssm_tree_verify          */
+#define SSM_MAX_DEPTH 15         /* deepest node below the root                 */
+#define SSM_MAX_PATH 256         /* accept / commit path length                 */
+
+typedef struct ssm_dims {
+  int32_t n_heads;    /* H                                                     */
+  int32_t head_dim;   /* P (this build: 64)                                    */
+  int32_t d_state;    /* N (this build: 128)                                   */
+  int32_t conv_width; /* W (must be 4)                                         */
+  int32_t n_layers;   /* L                                                     */
+  int32_t ring_cap;   /* R: conv-ring rows per instance (>= 3)                 */
+} ssm_dims;
+
+/* Per-layer parameters, all device fp32. */
+typedef struct ssm_params {
+  const float *conv_w;  /* [L][conv_dim][W], tap 0 is the oldest row          */
+  const float *conv_b;  /* [L][conv_dim]                                      */
+  const float *dt_bias; /* [L][H]                                             */
+  const float *A_log;   /* [L][H]  (A = -exp(A_log))                          */
+  const float *D;       /* [L][H]                                             */
+} ssm_params;
+
+/* One node of a breadth-first token tree (32 bytes). */
+typedef struct ssm_node {
+  int32_t parent;      /* -1 for the root (node 0)                             */
+  int32_t depth;       /* 0 for the root                                        */
+  int32_t child_begin; /* children are the contiguous range                     */
+  int32_t child_count; /*   [child_begin, child_begin + child_count)            */
+  int32_t tap[3];      /* source of the pre-conv row d = 1, 2, 3 positions back */
+                       /* on the node's path: node index >= 0, or -j meaning   */
+                       /* conv-ring position ring_head - j (j = 1..3)           */
+  int32_t reserved;    /* 0                                                     */
+} ssm_node;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t ssm_version(void);
+
+/* Thread-local text of the last error returned on this thread ("" if none). */
+const char *ssm_last_error(void);
+
+/*
+ * ssm_tree_layout_build -- host-only (no CUDA call).  SpecMamba page §3.2
+ * (breadth-first flattening), §5.2 (max_branches, max_depth).
+ *   parent     host int32 [n_seq][n_nodes]: parent[0] = -1, 0 <= parent[v] < v,
+ *              non-decreasing (breadth-first: siblings contiguous).
+ *   max_branches, max_depth: caps (<= 0 means "no cap").
+ *   layout     host ssm_node [n_seq][n_nodes], written.
+ *   depth_out  host, may be NULL: deepest node over all trees.
+ * Errors: SSM_ERR_BAD_TREE (first offending sequence/node in ssm_last_error),
+ *         SSM_ERR_CAPACITY (a cap exceeded), SSM_ERR_INVALID_ARG.
+ */
+int ssm_tree_layout_build(const int32_t *parent, int32_t n_seq, int32_t n_nodes, int32_t max_branches,
+                          int32_t max_depth, ssm_node *layout, int32_t *depth_out);
+
+/*
+ * ssm_tree_verify -- SpecMamba page §3.2 (tree verification) with the Mamba2
+ * update above: for every node v of every instance, y_v = C_v·h_v + D·x_v where
+ * h_v is the state after the node's root-to-node path applied to h0.  The
+ * per-node states never reach memory; only h0, the inputs and y do.
+ *   layout     device ssm_node [S][n] (from ssm_tree_layout_build), max_depth
+ *              = its deepest node (<= SSM_MAX_DEPTH); n <= SSM_MAX_NODES.
+ *   xBC        device bf16 [I][n][conv_dim]  pre-conv rows of the tree nodes
+ *   dt         device bf16 [I][n][H]         raw dt
+ *   h0         device fp32 [I][H][P][N]      committed state (read only)
+ *   ring       device bf16 [I][R][conv_dim]  conv ring (read only)
+ *   ring_head  device int32 [I]               committed positions; the rows
+ *              before the root are ring positions head-3 .. head-1 (mod R)
+ *   y          device fp32 [I][n][d_inner]    written
+ */
+int ssm_tree_verify(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
+                    int32_t max_depth, const ssm_node *layout, const uint16_t *xBC, const uint16_t *dt,
+                    const float *h0, const uint16_t *ring, const int32_t *ring_head, float *y,
+                    int32_t *dev_status, void *stream);
+
+/*
+ * ssm_accept_path -- SpecMamba page §1.2 (target verifies the draft): greedy
+ * walk from the root; at node u move to the first child c (breadth-first
+ * order) with tok[c] == tgt[u]; stop when none matches.
+ *   layout   device ssm_node [S][n]
+ *   tok      device int32 [S][n]   draft token of each node (tok[0] unused)
+ *   tgt      device int32 [S][n]   target's greedy token after each node
+ *   path     device int32 [S][max_path]  written: root..last, then -1 padding
+ *   path_len device int32 [S]            written (>= 1)
+ *   bonus    device int32 [S]            written: tgt[last]
+ * A walk longer than max_path stops there and sets SSM_STATUS_WALK_TRUNCATED.
+ */
+int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node *layout,
+                    const int32_t *tok, const int32_t *tgt, int32_t *path, int32_t *path_len, int32_t *bonus,
+                    int32_t *dev_status, void *stream);
+
+/*
+ * ssm_commit -- SpecMamba page §3.1 (target: selective recomputation of the
+ * affected path only) and §2.1 (roll back to the last accepted token).  The
+ * accepted path is re-run from h0; h is overwritten with the state after its
+ * last node, the last min(len, 3) pre-conv path rows go to ring positions
+ * head+len-3.. head+len-1 (mod R) and ring_head advances by len.  Ring rows
+ * outside the three before the new head are unspecified afterwards.
+ *   path, path_len  device int32 [S][max_path], [S] (from ssm_accept_path)
+ *   xBC, dt         as for ssm_tree_verify
+ *   h               device fp32 [I][H][P][N]  in: h0, out: committed state
+ *   ring, ring_head device, updated
+ */
+int ssm_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes, const ssm_node *layout,
+               int32_t max_path, const int32_t *path, const int32_t *path_len, const uint16_t *xBC,
+               const uint16_t *dt, float *h, uint16_t *ring, int32_t *ring_head, int32_t *dev_status,
+               void *stream);
+
+/*
+ * ssm_draft_step -- one draft token per instance (a one-node tree), SpecMamba
+ * page §3.1 (the draft logs only Δ, A, B, X).  Position = ring_head + step:
+ * the token's pre-conv row is written to that ring position, the conv window
+ * is the three ring rows before it, and
+ *     h_out = Ā·h_in + Δ·(x ⊗ B),   y = C·h_out + D·x,
+ * then log row `step` = {Δ [H], B [N], x [d_inner]} (fp32, post-conv) and
+ * log_len = step + 1.  A is constant per head, so Δ stands for A in the log.
+ *   step       0 <= step < log_cap and step + 3 < R
+ *   xBC_t      device bf16 [I][conv_dim]   dt_t device bf16 [I][H]
+ *   h_in/h_out device fp32 [I][H][P][N] (may be the same buffer)
+ *   ring       device bf16 [I][R][conv_dim] (row written), ring_head device [I] (read)
+ *   log_delta  device fp32 [I][log_cap][H]; log_B [I][log_cap][N];
+ *   log_x      [I][log_cap][d_inner]; log_len device int32 [I]
+ *   y          device fp32 [I][d_inner]
+ */
+int ssm_draft_step(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t step, int32_t log_cap,
+                   const uint16_t *xBC_t, const uint16_t *dt_t, const float *h_in, float *h_out, uint16_t *ring,
+                   const int32_t *ring_head, float *log_delta, float *log_B, float *log_x, int32_t *log_len,
+                   float *y, int32_t *dev_status, void *stream);
+
+/*
+ * ssm_replay -- SpecMamba page §3.1 (draft state recovery from the light log):
+ * h_ckpt <- the k[seq] logged updates applied in order (no conv, no input
+ * re-read; the same fp32 operations as ssm_draft_step, so the result equals
+ * the state that step k left, bit for bit); ring_head += k; log_len = 0.
+ *   k          device int32 [S], 0 <= k <= log_len (else clamped + status bit)
+ *   log_*      as written by ssm_draft_step
+ *   h_ckpt     device fp32 [I][H][P][N], in/out
+ */
+int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t log_cap, const int32_t *k,
+               const float *log_delta, const float *log_B, const float *log_x, int32_t *log_len, float *h_ckpt,
+               int32_t *ring_head, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_TREE_H */

@@ -1,0 +1,25 @@
+"""SpecMamba-style tree verification for Mamba2 on GB300 (sm_103a).
+
+The compute path is libssmtree.so (hand-written CUDA, C ABI in
+include/ssm_tree.h); this package holds its sources (csrc/), its build step
+(build.py) and a thin ctypes binding (binding.py) with the same names.
+"""
+from .binding import (  # noqa: F401
+    Dims,
+    SSMError,
+    lib,
+    library_path,
+    ssm_accept_path,
+    ssm_commit,
+    ssm_draft_step,
+    ssm_last_error,
+    ssm_replay,
+    ssm_tree_layout_build,
+    ssm_tree_verify,
+    ssm_version,
+)
+from .binding import (  # noqa: F401
+    SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_BAD_TREE, SSM_ERR_CAPACITY, SSM_ERR_CUDA, SSM_ERR_RANGE,
+    SSM_STATUS_BAD_LAYOUT, SSM_STATUS_PATH_RANGE, SSM_STATUS_K_RANGE, SSM_STATUS_WALK_TRUNCATED,
+    SSM_MAX_NODES, SSM_MAX_DEPTH, SSM_MAX_PATH, NODE_WORDS,
+)

@@ -1,0 +1,251 @@
+"""ctypes binding of libssmtree (include/ssm_tree.h), same names as the C ABI.
+
+Argument marshalling only: each wrapper checks that the torch tensors it is
+given have the dtype, device, contiguity and element count the C signature
+expects (the C side sees bare pointers and cannot), then calls the library on
+the current CUDA stream (or the one passed).  All arithmetic runs in the
+library's CUDA kernels; there is no fallback: if libssmtree.so is not built,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+SSM_OK = 0
+SSM_ERR_INVALID_ARG = -1
+SSM_ERR_BAD_TREE = -2
+SSM_ERR_CAPACITY = -3
+SSM_ERR_CUDA = -4
+SSM_ERR_RANGE = -5
+SSM_STATUS_BAD_LAYOUT = 1
+SSM_STATUS_PATH_RANGE = 2
+SSM_STATUS_K_RANGE = 4
+SSM_STATUS_WALK_TRUNCATED = 8
+SSM_MAX_NODES = 64
+SSM_MAX_DEPTH = 15
+SSM_MAX_PATH = 256
+NODE_WORDS = 8  # int32 words per ssm_node record
+
+
+class SSMError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class ssm_dims(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("d_state", ctypes.c_int32),
+                ("conv_width", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("ring_cap", ctypes.c_int32)]
+
+
+class ssm_params(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+                ("A_log", ctypes.c_void_p), ("D", ctypes.c_void_p)]
+
+
+@dataclass(frozen=True)
+class Dims:
+    n_heads: int
+    n_layers: int = 1
+    ring_cap: int = 20
+    head_dim: int = 64
+    d_state: int = 128
+    conv_width: int = 4
+
+    @property
+    def d_inner(self) -> int:
+        return self.n_heads * self.head_dim
+
+    @property
+    def conv_dim(self) -> int:
+        return self.d_inner + 2 * self.d_state
+
+    def c(self) -> ssm_dims:
+        return ssm_dims(self.n_heads, self.head_dim, self.d_state, self.conv_width, self.n_layers, self.ring_cap)
+
+
+_LIB = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SIGS = {
+    "ssm_version": (_I, []),
+    "ssm_last_error": (ctypes.c_char_p, []),
+    "ssm_tree_layout_build": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P]),
+    "ssm_tree_verify": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_accept_path": (ctypes.c_int, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_replay": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+}
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def lib():
+    """The loaded libssmtree (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libssmtree is not built ({path} missing): run "
+                               "`python -m speculative_decoding_mamba2_gb300.build` or __graft_entry__.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def ssm_version() -> int:
+    return int(lib().ssm_version())
+
+
+def ssm_last_error() -> str:
+    return lib().ssm_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != SSM_OK:
+        raise SSMError(rc, ssm_last_error())
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _dev(t: torch.Tensor, name: str, dtype, numel: int | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ptr(t: torch.Tensor, name: str, dtype, numel: int):
+    """Integer address (for ctypes struct fields)."""
+    return _dev(t, name, dtype, numel).value
+
+
+def _opt_status(status):
+    return None if status is None else _dev(status, "status", torch.int32, 1)
+
+
+def _stream(stream, like: torch.Tensor):
+    if stream is None:
+        stream = torch.cuda.current_stream(like.device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _params(prm: dict, d: Dims, layers: int) -> ssm_params:
+    return ssm_params(_ptr(prm["conv_w"], "conv_w", torch.float32, layers * d.conv_dim * d.conv_width),
+                      _ptr(prm["conv_b"], "conv_b", torch.float32, layers * d.conv_dim),
+                      _ptr(prm["dt_bias"], "dt_bias", torch.float32, layers * d.n_heads),
+                      _ptr(prm["A_log"], "A_log", torch.float32, layers * d.n_heads),
+                      _ptr(prm["D"], "D", torch.float32, layers * d.n_heads))
+
+
+# ---------------------------------------------------------------------------
+# the C ABI, one wrapper per entry point
+# ---------------------------------------------------------------------------
+def ssm_tree_layout_build(parent, max_branches: int = 0, max_depth: int = 0):
+    """Host call.  parent: int array [n_seq][n] (or [n]).  Returns (layout int32
+    [n_seq][n][8] = ssm_node records, deepest depth)."""
+    par = np.ascontiguousarray(np.asarray(parent, dtype=np.int32))
+    if par.ndim == 1:
+        par = par[None]
+    if par.ndim != 2 or par.shape[1] < 1:
+        raise ValueError("parent must be [n_seq][n_nodes]")
+    S, n = par.shape
+    out = np.zeros((S, n, NODE_WORDS), np.int32)
+    depth = ctypes.c_int32(0)
+    _check(lib().ssm_tree_layout_build(par.ctypes.data_as(_P), S, n, int(max_branches), int(max_depth),
+                                       out.ctypes.data_as(_P), ctypes.byref(depth)))
+    return out, int(depth.value)
+
+
+def ssm_tree_verify(dims: Dims, params: dict, n_seq: int, n_nodes: int, max_depth: int, layout, xBC, dt, h0, ring,
+                    ring_head, y, status=None, stream=None):
+    d, I, n = dims, n_seq * dims.n_layers, n_nodes
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    _check(lib().ssm_tree_verify(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, max_depth,
+        _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+        _dev(h0, "h0", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+        _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
+        _opt_status(status), _stream(stream, h0)))
+
+
+def ssm_accept_path(n_seq: int, n_nodes: int, max_path: int, layout, tok, tgt, path, path_len, bonus, status=None,
+                    stream=None):
+    S, n = n_seq, n_nodes
+    _check(lib().ssm_accept_path(
+        S, n, max_path, _dev(layout, "layout", torch.int32, S * n * NODE_WORDS),
+        _dev(tok, "tok", torch.int32, S * n), _dev(tgt, "tgt", torch.int32, S * n),
+        _dev(path, "path", torch.int32, S * max_path), _dev(path_len, "path_len", torch.int32, S),
+        _dev(bonus, "bonus", torch.int32, S), _opt_status(status), _stream(stream, tok)))
+
+
+def ssm_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, layout, max_path: int, path, path_len, xBC, dt, h,
+               ring, ring_head, status=None, stream=None):
+    d, I, n = dims, n_seq * dims.n_layers, n_nodes
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    _check(lib().ssm_commit(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        max_path, _dev(path, "path", torch.int32, n_seq * max_path), _dev(path_len, "path_len", torch.int32, n_seq),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+        _dev(h, "h", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+        _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h)))
+
+
+def ssm_draft_step(dims: Dims, params: dict, n_seq: int, step: int, log_cap: int, xBC_t, dt_t, h_in, h_out, ring,
+                   ring_head, log_delta, log_B, log_x, log_len, y, status=None, stream=None):
+    d, I = dims, n_seq * dims.n_layers
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    S = I * d.n_heads * d.head_dim * d.d_state
+    _check(lib().ssm_draft_step(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, step, log_cap,
+        _dev(xBC_t, "xBC_t", torch.bfloat16, I * d.conv_dim), _dev(dt_t, "dt_t", torch.bfloat16, I * d.n_heads),
+        _dev(h_in, "h_in", torch.float32, S), _dev(h_out, "h_out", torch.float32, S),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+        _dev(ring_head, "ring_head", torch.int32, I),
+        _dev(log_delta, "log_delta", torch.float32, I * log_cap * d.n_heads),
+        _dev(log_B, "log_B", torch.float32, I * log_cap * d.d_state),
+        _dev(log_x, "log_x", torch.float32, I * log_cap * d.d_inner), _dev(log_len, "log_len", torch.int32, I),
+        _dev(y, "y", torch.float32, I * d.d_inner), _opt_status(status), _stream(stream, h_out)))
+
+
+def ssm_replay(dims: Dims, params: dict, n_seq: int, log_cap: int, k, log_delta, log_B, log_x, log_len, h_ckpt,
+               ring_head, status=None, stream=None):
+    d, I = dims, n_seq * dims.n_layers
+    cd = d.c()
+    cp = ssm_params(None, None, None, _ptr(params["A_log"], "A_log", torch.float32, d.n_layers * d.n_heads), None)
+    _check(lib().ssm_replay(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, log_cap, _dev(k, "k", torch.int32, n_seq),
+        _dev(log_delta, "log_delta", torch.float32, I * log_cap * d.n_heads),
+        _dev(log_B, "log_B", torch.float32, I * log_cap * d.d_state),
+        _dev(log_x, "log_x", torch.float32, I * log_cap * d.d_inner), _dev(log_len, "log_len", torch.int32, I),
+        _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))

@@ -1,0 +1,227 @@
+// libssmtree C ABI: argument validation on the host, then kernel launches on
+// the caller's stream.  Nothing here allocates device memory.
+#include <stdio.h>
+
+#include <string>
+
+#include "common.cuh"
+
+namespace ssmtree {
+
+static thread_local std::string g_error;
+
+void set_error(const std::string& msg) { g_error = msg; }
+
+namespace {
+
+int fail(int code, const char* fn, const char* what) {
+  char buf[320];
+  snprintf(buf, sizeof buf, "%s: %s", fn, what);
+  g_error = buf;
+  return code;
+}
+
+int cuda_fail(const char* fn, cudaError_t e) {
+  char buf[320];
+  snprintf(buf, sizeof buf, "%s: CUDA error %d (%s)", fn, (int)e, cudaGetErrorString(e));
+  g_error = buf;
+  return SSM_ERR_CUDA;
+}
+
+// Shape checks common to every device call.
+int check_dims(const char* fn, const ssm_dims* d, bool need_params, const ssm_params* p) {
+  if (!d) return fail(SSM_ERR_INVALID_ARG, fn, "dims is NULL");
+  if (d->n_heads < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_heads must be >= 1");
+  if (d->head_dim != kP) return fail(SSM_ERR_INVALID_ARG, fn, "head_dim must be 64 in this build");
+  if (d->d_state != kN) return fail(SSM_ERR_INVALID_ARG, fn, "d_state must be 128 in this build");
+  if (d->conv_width != kW) return fail(SSM_ERR_INVALID_ARG, fn, "conv_width must be 4");
+  if (d->n_layers < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_layers must be >= 1");
+  if (d->ring_cap < 3) return fail(SSM_ERR_INVALID_ARG, fn, "ring_cap must be >= 3");
+  if ((long long)d->n_heads * kP > (1 << 24)) return fail(SSM_ERR_CAPACITY, fn, "n_heads too large");
+  if (need_params) {
+    if (!p) return fail(SSM_ERR_INVALID_ARG, fn, "params is NULL");
+    if (!p->conv_w || !p->conv_b || !p->dt_bias || !p->A_log || !p->D)
+      return fail(SSM_ERR_INVALID_ARG, fn, "a parameter pointer is NULL");
+  }
+  return SSM_OK;
+}
+
+int finish(const char* fn, cudaError_t e) {
+  if (e != cudaSuccess) return cuda_fail(fn, e);
+  g_error.clear();
+  return SSM_OK;
+}
+
+}  // namespace
+}  // namespace ssmtree
+
+using namespace ssmtree;
+
+extern "C" int32_t ssm_version(void) { return 100; }
+
+extern "C" const char* ssm_last_error(void) { return g_error.c_str(); }
+
+extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
+                               int32_t max_depth, const ssm_node* layout, const uint16_t* xBC, const uint16_t* dt,
+                               const float* h0, const uint16_t* ring, const int32_t* ring_head, float* y,
+                               int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_tree_verify";
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
+  if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
+  if (max_depth < 0 || max_depth >= n_nodes) return fail(SSM_ERR_RANGE, fn, "max_depth must be in [0, n_nodes)");
+  if (max_depth > SSM_MAX_DEPTH) return fail(SSM_ERR_CAPACITY, fn, "max_depth exceeds SSM_MAX_DEPTH");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!layout || !xBC || !dt || !h0 || !ring || !ring_head || !y)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  VerifyArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.max_depth = max_depth;
+  a.conv_w = prm->conv_w;
+  a.conv_b = prm->conv_b;
+  a.dt_bias = prm->dt_bias;
+  a.A_log = prm->A_log;
+  a.D = prm->D;
+  a.layout = layout;
+  a.xBC = xBC;
+  a.dt = dt;
+  a.ring = ring;
+  a.h0 = h0;
+  a.ring_head = ring_head;
+  a.y = y;
+  a.status = dev_status;
+  return finish(fn, launch_verify(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node* layout,
+                               const int32_t* tok, const int32_t* tgt, int32_t* path, int32_t* path_len,
+                               int32_t* bonus, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_accept_path";
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
+  if (max_path < 1 || max_path > SSM_MAX_PATH) return fail(SSM_ERR_RANGE, fn, "max_path must be in [1, SSM_MAX_PATH]");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!layout || !tok || !tgt || !path || !path_len || !bonus)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  AcceptArgs a;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.max_path = max_path;
+  a.layout = layout;
+  a.tok = tok;
+  a.tgt = tgt;
+  a.path = path;
+  a.path_len = path_len;
+  a.bonus = bonus;
+  a.status = dev_status;
+  return finish(fn, launch_accept(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_commit(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
+                          const ssm_node* layout, int32_t max_path, const int32_t* path, const int32_t* path_len,
+                          const uint16_t* xBC, const uint16_t* dt, float* h, uint16_t* ring, int32_t* ring_head,
+                          int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_commit";
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
+  if (max_path < 1 || max_path > SSM_MAX_PATH) return fail(SSM_ERR_RANGE, fn, "max_path must be in [1, SSM_MAX_PATH]");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!layout || !path || !path_len || !xBC || !dt || !h || !ring || !ring_head)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  CommitArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.max_path = max_path;
+  a.conv_w = prm->conv_w;
+  a.conv_b = prm->conv_b;
+  a.dt_bias = prm->dt_bias;
+  a.A_log = prm->A_log;
+  a.layout = layout;
+  a.path = path;
+  a.path_len = path_len;
+  a.xBC = xBC;
+  a.dt = dt;
+  a.h = h;
+  a.ring = ring;
+  a.ring_head = ring_head;
+  a.status = dev_status;
+  return finish(fn, launch_commit(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_draft_step(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t step,
+                              int32_t log_cap, const uint16_t* xBC_t, const uint16_t* dt_t, const float* h_in,
+                              float* h_out, uint16_t* ring, const int32_t* ring_head, float* log_delta, float* log_B,
+                              float* log_x, int32_t* log_len, float* y, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_draft_step";
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (log_cap < 1) return fail(SSM_ERR_INVALID_ARG, fn, "log_cap must be >= 1");
+  if (step < 0 || step >= log_cap) return fail(SSM_ERR_RANGE, fn, "step must be in [0, log_cap)");
+  if (step + 3 >= dims->ring_cap)
+    return fail(SSM_ERR_CAPACITY, fn, "ring_cap too small: need step + 3 < ring_cap so the committed rows survive");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!xBC_t || !dt_t || !h_in || !h_out || !ring || !ring_head || !log_delta || !log_B || !log_x || !log_len || !y)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  DraftArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.step = step;
+  a.log_cap = log_cap;
+  a.conv_w = prm->conv_w;
+  a.conv_b = prm->conv_b;
+  a.dt_bias = prm->dt_bias;
+  a.A_log = prm->A_log;
+  a.D = prm->D;
+  a.xBC_t = xBC_t;
+  a.dt_t = dt_t;
+  a.h_in = h_in;
+  a.h_out = h_out;
+  a.ring = ring;
+  a.ring_head = ring_head;
+  a.log_delta = log_delta;
+  a.log_B = log_B;
+  a.log_x = log_x;
+  a.log_len = log_len;
+  a.y = y;
+  a.status = dev_status;
+  return finish(fn, launch_draft_step(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_replay(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t log_cap,
+                          const int32_t* k, const float* log_delta, const float* log_B, const float* log_x,
+                          int32_t* log_len, float* h_ckpt, int32_t* ring_head, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_replay";
+  if (int rc = check_dims(fn, dims, false, nullptr)) return rc;
+  if (!prm || !prm->A_log) return fail(SSM_ERR_INVALID_ARG, fn, "params->A_log is NULL");
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (log_cap < 1) return fail(SSM_ERR_INVALID_ARG, fn, "log_cap must be >= 1");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!k || !log_delta || !log_B || !log_x || !log_len || !h_ckpt || !ring_head)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  ReplayArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.n_seq = n_seq;
+  a.log_cap = log_cap;
+  a.A_log = prm->A_log;
+  a.k = k;
+  a.log_delta = log_delta;
+  a.log_B = log_B;
+  a.log_x = log_x;
+  a.log_len = log_len;
+  a.h = h_ckpt;
+  a.ring_head = ring_head;
+  a.status = dev_status;
+  return finish(fn, launch_replay(a, (cudaStream_t)stream));
+}

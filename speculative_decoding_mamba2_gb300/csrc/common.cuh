@@ -1,0 +1,150 @@
+// Device helpers shared by the libssmtree kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssm_tree.h"
+
+namespace ssmtree {
+
+// Shape constants of this build: Mamba2 head_dim 64, d_state 128, conv width 4.
+constexpr int kP = 64;
+constexpr int kN = 128;
+constexpr int kW = 4;
+
+// bf16 bit pattern -> fp32 (exact).
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+
+// softplus(v) = log(1 + e^v); above 20 it equals v to fp32 precision.
+__device__ __forceinline__ float softplus_f(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
+
+// A = -exp(A_log) and the per-head decay exp(Δ·A).  Written with explicit
+// round-to-nearest operations so the draft step and the replay (which must
+// agree bit for bit) cannot be contracted differently by the compiler.
+__device__ __forceinline__ float neg_exp(float a_log) { return -expf(a_log); }
+__device__ __forceinline__ float decay_of(float delta, float A) { return expf(__fmul_rn(delta, A)); }
+
+// One element of the state update h' = a·h + (Δ·x)·B with u = Δ·x precomputed.
+__device__ __forceinline__ float ssm_update(float a, float h, float u, float b) {
+  return __fmaf_rn(a, h, __fmul_rn(u, b));
+}
+
+__device__ __forceinline__ int ring_pos(int head, int offset, int R) {
+  int p = (head + offset) % R;
+  return p < 0 ? p + R : p;
+}
+
+// Causal width-4 conv + SiLU for one channel given the four pre-conv values,
+// oldest first: SiLU(b + w0·r0 + w1·r1 + w2·r2 + w3·r3).
+__device__ __forceinline__ float conv4_silu(float4 w, float b, float r0, float r1, float r2, float r3) {
+  float acc = b;
+  acc = fmaf(w.x, r0, acc);
+  acc = fmaf(w.y, r1, acc);
+  acc = fmaf(w.z, r2, acc);
+  acc = fmaf(w.w, r3, acc);
+  return silu_f(acc);
+}
+
+// Pre-conv value of channel c for tap source `src` of a tree node: a node row
+// of this instance's xBC (src >= 0) or a ring row (src = -j: position head - j).
+__device__ __forceinline__ float tap_value(const uint16_t* __restrict__ xbc, const uint16_t* __restrict__ ring,
+                                           int head, int R, int conv_dim, int src, int c) {
+  if (src >= 0) return bf16f(xbc[(size_t)src * conv_dim + c]);
+  return bf16f(ring[(size_t)ring_pos(head, src, R) * conv_dim + c]);
+}
+
+// Post-conv value of channel c at tree node v (taps from its layout record).
+__device__ __forceinline__ float node_conv(const uint16_t* __restrict__ xbc, const uint16_t* __restrict__ ring,
+                                           int head, int R, int conv_dim, const int* tap /*[3]: d=1,2,3*/, int v,
+                                           int c, float4 w, float b) {
+  float r0 = tap_value(xbc, ring, head, R, conv_dim, tap[2], c);
+  float r1 = tap_value(xbc, ring, head, R, conv_dim, tap[1], c);
+  float r2 = tap_value(xbc, ring, head, R, conv_dim, tap[0], c);
+  float r3 = bf16f(xbc[(size_t)v * conv_dim + c]);
+  return conv4_silu(w, b, r0, r1, r2, r3);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void flag(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// cp.async (16-byte global -> shared, bypassing L1)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Kernel launchers (defined in the .cu files, called by api.cu).
+struct VerifyArgs {
+  int H, L, R, n_seq, n, max_depth;
+  const float *conv_w, *conv_b, *dt_bias, *A_log, *D;
+  const ssm_node* layout;
+  const uint16_t *xBC, *dt, *ring;
+  const float* h0;
+  const int32_t* ring_head;
+  float* y;
+  int32_t* status;
+};
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+
+struct AcceptArgs {
+  int n_seq, n, max_path;
+  const ssm_node* layout;
+  const int32_t *tok, *tgt;
+  int32_t *path, *path_len, *bonus, *status;
+};
+cudaError_t launch_accept(const AcceptArgs& a, cudaStream_t s);
+
+struct CommitArgs {
+  int H, L, R, n_seq, n, max_path;
+  const float *conv_w, *conv_b, *dt_bias, *A_log;
+  const ssm_node* layout;
+  const int32_t *path, *path_len;
+  const uint16_t *xBC, *dt;
+  float* h;
+  uint16_t* ring;
+  int32_t *ring_head, *status;
+};
+cudaError_t launch_commit(const CommitArgs& a, cudaStream_t s);
+
+struct DraftArgs {
+  int H, L, R, n_seq, step, log_cap;
+  const float *conv_w, *conv_b, *dt_bias, *A_log, *D;
+  const uint16_t *xBC_t, *dt_t;
+  const float* h_in;
+  float* h_out;
+  uint16_t* ring;
+  const int32_t* ring_head;
+  float *log_delta, *log_B, *log_x;
+  int32_t* log_len;
+  float* y;
+  int32_t* status;
+};
+cudaError_t launch_draft_step(const DraftArgs& a, cudaStream_t s);
+
+struct ReplayArgs {
+  int H, L, n_seq, log_cap;
+  const float* A_log;
+  const int32_t* k;
+  const float *log_delta, *log_B, *log_x;
+  int32_t* log_len;
+  float* h;
+  int32_t *ring_head, *status;
+};
+cudaError_t launch_replay(const ReplayArgs& a, cudaStream_t s);
+
+}  // namespace ssmtree

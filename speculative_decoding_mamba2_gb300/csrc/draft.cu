@@ -1,0 +1,243 @@
+// Draft side: one-token draft step with its light log, and replay from that log.
+//
+// SpecMamba page ("FPGA加速Mamba推理：SpecMamba方案与优化实践") §3.1: the draft
+// model stores only the small intermediates (Δ, A, B, X) instead of whole
+// states and recovers its state from them; §2.3: the draft is memory bound.
+// A is a per-head constant in Mamba2, so a log row is {Δ [H], B [N], x
+// [d_inner]}, all post-conv fp32.  Replay applies the logged updates with the
+// exact fp32 operation sequence of the step kernel (decay_of, __fmul_rn,
+// ssm_update), so it reproduces the stepped state bit for bit.
+#include "common.cuh"
+
+namespace ssmtree {
+namespace {
+
+constexpr int DG = 4;            // heads per CTA
+constexpr int DROWS = DG * kP;   // 256 state rows
+constexpr int DTHREADS = 256;
+
+__global__ void __launch_bounds__(DTHREADS) draft_step_kernel(DraftArgs a) {
+  __shared__ __align__(16) float Bs[kN];
+  __shared__ __align__(16) float Cs[kN];
+  __shared__ float xs[DROWS];
+  __shared__ float dls[DG], decs[DG], Dh[DG];
+
+  const int tid = threadIdx.x;
+  const int n_groups = (a.H + DG - 1) / DG;
+  const int grp = blockIdx.x % n_groups;
+  const int inst = blockIdx.x / n_groups;
+  const int layer = inst % a.L;
+  const int h_begin = grp * DG;
+  const int heads = min(DG, a.H - h_begin);
+  const int d_inner = a.H * kP;
+  const int conv_dim = d_inner + 2 * kN;
+  const int R = a.R;
+  const int pos = a.ring_head[inst] + a.step;
+
+  const uint16_t* xt = a.xBC_t + (size_t)inst * conv_dim;
+  uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
+  const uint16_t* r0 = ring + (size_t)ring_pos(pos, -3, R) * conv_dim;
+  const uint16_t* r1 = ring + (size_t)ring_pos(pos, -2, R) * conv_dim;
+  const uint16_t* r2 = ring + (size_t)ring_pos(pos, -1, R) * conv_dim;
+  uint16_t* rw = ring + (size_t)ring_pos(pos, 0, R) * conv_dim;
+  const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
+  const float* cb = a.conv_b + (size_t)layer * conv_dim;
+  float* lx = a.log_x + ((size_t)inst * a.log_cap + a.step) * d_inner;
+  float* lB = a.log_B + ((size_t)inst * a.log_cap + a.step) * kN;
+
+  // conv + SiLU of the one position: this group's x channels, and B, C
+  for (int job = tid; job < DROWS + 2 * kN; job += DTHREADS) {
+    int c;
+    if (job < DROWS) {
+      if (job >= heads * kP) continue;
+      c = h_begin * kP + job;
+    } else {
+      c = d_inner + (job - DROWS);  // every group needs B and C; group 0 also writes them out
+    }
+    const uint16_t cur = xt[c];
+    const float post = conv4_silu(cw[c], cb[c], bf16f(r0[c]), bf16f(r1[c]), bf16f(r2[c]), bf16f(cur));
+    if (job < DROWS) {
+      xs[job] = post;
+      lx[c] = post;
+      rw[c] = cur;
+    } else {
+      const int j = job - DROWS;
+      if (j < kN) Bs[j] = post;
+      else Cs[j - kN] = post;
+      if (grp == 0) {
+        rw[c] = cur;
+        if (j < kN) lB[j] = post;
+      }
+    }
+  }
+  if (tid < DG) {
+    float d = 0.f, e = 1.f, dd = 0.f;
+    if (tid < heads) {
+      const int h = h_begin + tid;
+      d = softplus_f(bf16f(a.dt_t[(size_t)inst * a.H + h]) + a.dt_bias[(size_t)layer * a.H + h]);
+      e = decay_of(d, neg_exp(a.A_log[(size_t)layer * a.H + h]));
+      dd = a.D[(size_t)layer * a.H + h];
+      a.log_delta[((size_t)inst * a.log_cap + a.step) * a.H + h] = d;
+    }
+    dls[tid] = d;
+    decs[tid] = e;
+    Dh[tid] = dd;
+  }
+  if (grp == 0 && tid == 0) a.log_len[inst] = a.step + 1;
+  __syncthreads();
+
+  // state rows: one warp per row, each lane 4 consecutive d_state elements
+  const int warp = tid >> 5, lane = tid & 31;
+  const float4 b4 = reinterpret_cast<const float4*>(Bs)[lane];
+  const float4 c4 = reinterpret_cast<const float4*>(Cs)[lane];
+  const float* hin = a.h_in + ((size_t)inst * a.H + h_begin) * kP * kN;
+  float* hout = a.h_out + ((size_t)inst * a.H + h_begin) * kP * kN;
+  const int rows = heads * kP;
+  constexpr int U = 4;
+  for (int r0w = warp * U; r0w < rows; r0w += (DTHREADS / 32) * U) {
+    float4 hv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (r0w + u < rows) hv[u] = reinterpret_cast<const float4*>(hin + (size_t)(r0w + u) * kN)[lane];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int row = r0w + u;
+      if (row >= rows) continue;
+      const int g = row / kP;
+      const float uu = __fmul_rn(dls[g], xs[row]);
+      const float dec = decs[g];
+      float4 h = hv[u];
+      h.x = ssm_update(dec, h.x, uu, b4.x);
+      h.y = ssm_update(dec, h.y, uu, b4.y);
+      h.z = ssm_update(dec, h.z, uu, b4.z);
+      h.w = ssm_update(dec, h.w, uu, b4.w);
+      reinterpret_cast<float4*>(hout + (size_t)row * kN)[lane] = h;
+      float s = c4.x * h.x;
+      s = fmaf(c4.y, h.y, s);
+      s = fmaf(c4.z, h.z, s);
+      s = fmaf(c4.w, h.w, s);
+      s = warp_sum(s);
+      if (lane == 0) a.y[(size_t)inst * d_inner + h_begin * kP + row] = fmaf(Dh[g], xs[row], s);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// replay
+// ---------------------------------------------------------------------------
+constexpr int RG = 4;
+constexpr int RROWS = RG * kP;
+constexpr int RT = 16;  // log rows per sweep
+constexpr int RTHREADS = 256;
+
+__device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool report) {
+  const int seq = inst / a.L;
+  int k = a.k[seq];
+  const int lim = max(0, min(a.log_len[inst], a.log_cap));
+  if (k < 0 || k > lim) {
+    if (report) flag(a.status, SSM_STATUS_K_RANGE);
+    k = k < 0 ? 0 : lim;
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(RTHREADS) replay_kernel(ReplayArgs a) {
+  __shared__ __align__(16) float Bs[RT][kN];
+  __shared__ float xs[RT][RROWS];
+  __shared__ float dls[RT][RG], decs[RT][RG];
+  const int tid = threadIdx.x;
+  const int n_groups = (a.H + RG - 1) / RG;
+  const int grp = blockIdx.x % n_groups;
+  const int inst = blockIdx.x / n_groups;
+  const int layer = inst % a.L;
+  const int h_begin = grp * RG;
+  const int heads = min(RG, a.H - h_begin);
+  const int d_inner = a.H * kP;
+  const int k = replay_k(a, inst, grp == 0 && tid == 0);
+  float* hs = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
+  const int n4 = heads * kP * kN / 4;
+
+  for (int t0 = 0; t0 < k; t0 += RT) {
+    const int cnt = min(RT, k - t0);
+    if (t0 > 0) __syncthreads();
+    for (int i = tid; i < cnt * kN; i += RTHREADS) {
+      const int t = i / kN, nn = i % kN;
+      Bs[t][nn] = a.log_B[((size_t)inst * a.log_cap + t0 + t) * kN + nn];
+    }
+    for (int i = tid; i < cnt * RROWS; i += RTHREADS) {
+      const int t = i / RROWS, r = i % RROWS;
+      xs[t][r] = r < heads * kP ? a.log_x[((size_t)inst * a.log_cap + t0 + t) * d_inner + h_begin * kP + r] : 0.f;
+    }
+    if (tid < cnt * RG) {
+      const int t = tid / RG, g = tid % RG;
+      float d = 0.f, e = 1.f;
+      if (g < heads) {
+        const int h = h_begin + g;
+        d = a.log_delta[((size_t)inst * a.log_cap + t0 + t) * a.H + h];
+        e = decay_of(d, neg_exp(a.A_log[(size_t)layer * a.H + h]));
+      }
+      dls[t][g] = d;
+      decs[t][g] = e;
+    }
+    __syncthreads();
+    for (int e0 = tid; e0 < n4; e0 += RTHREADS * 4) {
+      float4 hv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * RTHREADS;
+        if (e < n4) hv[u] = reinterpret_cast<const float4*>(hs)[e];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + u * RTHREADS;
+        if (e >= n4) continue;
+        const int row = e / (kN / 4);
+        const int g = row / kP;
+        const int nn = (e % (kN / 4)) * 4;
+        float4 h4 = hv[u];
+        for (int t = 0; t < cnt; ++t) {
+          const float uu = __fmul_rn(dls[t][g], xs[t][row]);
+          const float dec = decs[t][g];
+          const float4 b4 = *reinterpret_cast<const float4*>(&Bs[t][nn]);
+          h4.x = ssm_update(dec, h4.x, uu, b4.x);
+          h4.y = ssm_update(dec, h4.y, uu, b4.y);
+          h4.z = ssm_update(dec, h4.z, uu, b4.z);
+          h4.w = ssm_update(dec, h4.w, uu, b4.w);
+        }
+        reinterpret_cast<float4*>(hs)[e] = h4;
+      }
+    }
+  }
+}
+
+// head += k, log_len = 0 (after every replay CTA has read log_len)
+__global__ void replay_finish_kernel(ReplayArgs a, int n_inst) {
+  const int inst = blockIdx.x * blockDim.x + threadIdx.x;
+  if (inst >= n_inst) return;
+  const int k = replay_k(a, inst, false);
+  a.ring_head[inst] += k;
+  a.log_len[inst] = 0;
+}
+
+}  // namespace
+
+cudaError_t launch_draft_step(const DraftArgs& a, cudaStream_t s) {
+  const int n_groups = (a.H + DG - 1) / DG;
+  const long long inst = (long long)a.n_seq * a.L;
+  if (inst == 0) return cudaSuccess;
+  draft_step_kernel<<<(unsigned)(n_groups * inst), DTHREADS, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_replay(const ReplayArgs& a, cudaStream_t s) {
+  const int n_groups = (a.H + RG - 1) / RG;
+  const long long inst = (long long)a.n_seq * a.L;
+  if (inst == 0) return cudaSuccess;
+  replay_kernel<<<(unsigned)(n_groups * inst), RTHREADS, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  replay_finish_kernel<<<(unsigned)((inst + 255) / 256), 256, 0, s>>>(a, (int)inst);
+  return cudaGetLastError();
+}
+
+}  // namespace ssmtree

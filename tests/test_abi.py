@@ -1,0 +1,165 @@
+"""libssmtree's C ABI on the CPU: it builds, loads, exports every symbol the
+header declares, its host-only layout builder matches the oracle bit for bit,
+and every device entry point rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_mamba2_gb300 import binding as B
+from speculative_decoding_mamba2_gb300 import build as BLD
+from synth import WORKLOADS, Shape, Workload, tree_parents
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ssm_tree.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    BLD.build()
+    return B.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    fns = declared_functions()
+    for name in ["ssm_tree_layout_build", "ssm_tree_verify", "ssm_accept_path", "ssm_commit", "ssm_draft_step",
+                 "ssm_replay", "ssm_last_error", "ssm_version"]:
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert B.ssm_version() >= 100
+    assert B.library_path().endswith("libssmtree.so")
+
+
+def _oracle_records(parent):
+    lay = oracle.tree_layout(parent)
+    n = lay["n"]
+    out = np.zeros((n, 8), np.int32)
+    for v in range(n):
+        ch = lay["children"][v]
+        out[v] = [lay["parent"][v], lay["depth"][v], ch[0] if ch else n, len(ch), *lay["taps"][v], 0]
+    return out, max(lay["depth"])
+
+
+def test_layout_build_matches_oracle(L):
+    trees = [[-1], [-1, 0, 0, 1, 1, 2, 3], list(range(-1, 255))]
+    for cfg, tr in [(0, 0), (2, 0), (4, 0), (4, 1)]:
+        w = WORKLOADS[cfg]
+        trees += [tree_parents(w, s, tr) for s in range(6)]
+    w = Workload(97, "layout", Shape(H=1), 1, 1, trees=(("random", 40, 4, 9),))
+    trees += [tree_parents(w, s) for s in range(30)]
+    for par in trees:
+        got, depth = B.ssm_tree_layout_build(par)
+        ref, rdepth = _oracle_records(par)
+        np.testing.assert_array_equal(got[0], ref)
+        assert depth == rdepth
+
+
+def test_layout_build_batched_and_caps(L):
+    w = WORKLOADS[3]
+    par = np.stack([tree_parents(w, s) for s in range(16)])
+    got, depth = B.ssm_tree_layout_build(par, max_branches=3, max_depth=4)
+    assert got.shape == (16, 16, 8) and depth <= 4
+    for s in range(16):
+        np.testing.assert_array_equal(got[s], _oracle_records(par[s])[0])
+    with pytest.raises(B.SSMError) as e:
+        B.ssm_tree_layout_build(np.arange(-1, 9), max_depth=4)
+    assert e.value.code == B.SSM_ERR_CAPACITY
+    with pytest.raises(B.SSMError) as e:
+        B.ssm_tree_layout_build([-1, 0, 0, 0, 0], max_branches=3)
+    assert e.value.code == B.SSM_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("bad", [[0], [-1, 1], [-1, 0, 2], [-1, 0, 1, 0], [-1, -1], [5, 0]])
+def test_layout_build_rejects_what_the_oracle_rejects(L, bad):
+    with pytest.raises(oracle.BadTree):
+        oracle.tree_layout(bad)
+    with pytest.raises(B.SSMError) as e:
+        B.ssm_tree_layout_build(bad)
+    assert e.value.code == B.SSM_ERR_BAD_TREE
+    assert "ssm_tree_layout_build" in B.ssm_last_error()
+
+
+# ---------------------------------------------------------------------------
+# device entry points: argument validation happens before any CUDA call
+# ---------------------------------------------------------------------------
+def _dims(**kw):
+    d = dict(n_heads=4, head_dim=64, d_state=128, conv_width=4, n_layers=2, ring_cap=20)
+    d.update(kw)
+    return B.ssm_dims(**d)
+
+
+def _prm(null=False):
+    x = None if null else 16
+    return B.ssm_params(16, 16, 16, x, 16)
+
+
+FAKE = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
+
+
+def _verify(L, dims, prm, n_seq=1, n=16, depth=4, ptr=FAKE):
+    return L.ssm_tree_verify(ctypes.byref(dims) if dims is not None else None,
+                             ctypes.byref(prm) if prm is not None else None,
+                             n_seq, n, depth, ptr, ptr, ptr, ptr, ptr, ptr, ptr, None, None)
+
+
+def test_verify_validation(L):
+    assert _verify(L, None, _prm()) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(), None) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(head_dim=32), _prm()) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(d_state=64), _prm()) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(conv_width=3), _prm()) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(ring_cap=2), _prm()) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(), _prm(null=True)) == B.SSM_ERR_INVALID_ARG
+    assert _verify(L, _dims(), _prm(), n=65, depth=4) == B.SSM_ERR_CAPACITY
+    assert _verify(L, _dims(), _prm(), n=64, depth=16) == B.SSM_ERR_CAPACITY
+    assert _verify(L, _dims(), _prm(), n=8, depth=8) == B.SSM_ERR_RANGE
+    assert _verify(L, _dims(), _prm(), ptr=None) == B.SSM_ERR_INVALID_ARG
+    assert "NULL" in B.ssm_last_error()
+    assert _verify(L, _dims(), _prm(), n_seq=-1) == B.SSM_ERR_INVALID_ARG
+    # an empty batch is a valid no-op and enqueues nothing
+    assert _verify(L, _dims(), _prm(), n_seq=0, ptr=None) == B.SSM_OK
+
+
+def test_accept_commit_draft_replay_validation(L):
+    P = FAKE
+    assert L.ssm_accept_path(1, 16, 0, P, P, P, P, P, P, None, None) == B.SSM_ERR_RANGE
+    assert L.ssm_accept_path(1, 16, 257, P, P, P, P, P, P, None, None) == B.SSM_ERR_RANGE
+    assert L.ssm_accept_path(1, 0, 5, P, P, P, P, P, P, None, None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_accept_path(1, 16, 5, P, None, P, P, P, P, None, None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_accept_path(0, 16, 5, None, None, None, None, None, None, None, None) == B.SSM_OK
+    d, p = _dims(), _prm()
+    assert L.ssm_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 0, P, P, P, P, P, P, P, None,
+                        None) == B.SSM_ERR_RANGE
+    assert L.ssm_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 5, P, P, P, P, None, P, P, None,
+                        None) == B.SSM_ERR_INVALID_ARG
+    dd = _dims(ring_cap=10)
+    # step + 3 must stay below ring_cap so the three committed rows survive drafting
+    assert L.ssm_draft_step(ctypes.byref(dd), ctypes.byref(p), 1, 7, 16, P, P, P, P, P, P, P, P, P, P, P, None,
+                            None) == B.SSM_ERR_CAPACITY
+    assert L.ssm_draft_step(ctypes.byref(d), ctypes.byref(p), 1, 16, 16, P, P, P, P, P, P, P, P, P, P, P, None,
+                            None) == B.SSM_ERR_RANGE
+    assert L.ssm_draft_step(ctypes.byref(d), ctypes.byref(p), 1, -1, 16, P, P, P, P, P, P, P, P, P, P, P, None,
+                            None) == B.SSM_ERR_RANGE
+    assert L.ssm_replay(ctypes.byref(d), ctypes.byref(_prm(null=True)), 1, 16, P, P, P, P, P, P, P, None,
+                        None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_replay(ctypes.byref(d), ctypes.byref(p), 1, 0, P, P, P, P, P, P, P, None,
+                        None) == B.SSM_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(L):
+    import torch
+    t = torch.zeros(4)
+    with pytest.raises(ValueError):
+        B._dev(t, "t", torch.float32, 4)

@@ -1,0 +1,161 @@
+"""CUDA path against the fp64 oracle, element by element, through the C ABI.
+
+Bar: indices (layout, accepted path, bonus, ring rows, heads) bit-exact;
+floats max |gpu - ref| <= 1e-3 * (1 + |ref|) (fp32 state, bf16 inputs)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import WORKLOADS, Shape, Workload, batch, workload
+from tests.helpers import (f64, oracle_verify_instance, params_at, rel_err, ring_window, run_tree_step,
+                           upload_tree_batch)
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from speculative_decoding_mamba2_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+
+
+def check_instances(b, out, pairs, commit=True):
+    """Compare sampled instances (seq index i, layer index j) with the oracle."""
+    L = len(b["layers"])
+    for i, j in pairs:
+        inst = i * L + j
+        y_ref, st = oracle_verify_instance(b, i, j, return_states=True)
+        y = out["y"][inst].double().cpu().numpy()
+        e = rel_err(y, y_ref)
+        assert e <= TOL, f"y of instance ({i},{j}): {e}"
+        path_ref, bonus_ref = oracle.accept(b["parent"][i], b["tok"][i], b["tgt"][i])
+        plen = int(out["path_len"][i])
+        assert out["path"][i, :plen].cpu().tolist() == path_ref
+        assert int(out["bonus"][i]) == bonus_ref
+        if not commit:
+            continue
+        h_ref, ring_ref, head_ref = oracle.commit(params_at(b["params"], j), b["parent"][i], path_ref,
+                                                  f64(b["xBC"][i, j]), f64(b["dt"][i, j]),
+                                                  b["h0"][i, j].astype(np.float64), f64(b["ring"][i, j]),
+                                                  int(b["ring_head"][i, j]))
+        np.testing.assert_array_equal(h_ref, st[path_ref[-1]])  # oracle self-consistency
+        e = rel_err(out["h"][inst].double().cpu().numpy(), h_ref)
+        assert e <= TOL, f"committed h of instance ({i},{j}): {e}"
+        head = int(out["ring_head"][inst])
+        assert head == head_ref
+        ring_gpu = out["ring"][inst].view(torch.int16).cpu().numpy().view(np.uint16)
+        ring_exp = b["ring"][i, j].copy()
+        R = ring_exp.shape[0]
+        for jj, m in enumerate(path_ref):
+            ring_exp[(int(b["ring_head"][i, j]) + jj) % R] = b["xBC"][i, j, m]
+        np.testing.assert_array_equal(ring_window(ring_gpu, head), ring_window(ring_exp, head))
+    assert int(out["status"]) == 0
+
+
+def test_config0_every_element():
+    w = workload(0)
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(0, 0)])
+
+
+def test_ragged_heads_and_node_tiles():
+    # H = 6: head groups of 4 (+2 ragged) in verify, one ragged group of 8 in commit;
+    # 40 nodes: node tiles 16 + 16 + 8
+    w = Workload(50, "ragged", Shape(H=6), n_layers=2, batch=3, trees=(("full", 3, 3),), p_accept=0.9)
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(3) for j in range(2)])
+
+
+@pytest.mark.parametrize("spec", [("random", 16, 3, 4), ("random", 64, 4, 15), ("chain", 16), ("full", 2, 5)])
+def test_tree_shapes(spec):
+    w = Workload(51, "shapes", Shape(H=8), n_layers=2, batch=2, trees=(spec,), p_accept=0.85)
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
+def test_single_node_tree():
+    w = Workload(52, "root only", Shape(H=4), n_layers=3, batch=2, trees=(("chain", 1),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(3)])
+    assert out["path_len"].cpu().tolist() == [1, 1]
+
+
+def test_config2_full_size_sampled():
+    w = workload(2)
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(0, 0), (0, 31), (0, 63)])
+    assert torch.isfinite(out["y"]).all()
+
+
+def test_config3_full_size_sampled():
+    w = workload(3)
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(0, 0), (15, 63), (7, 40), (3, 5), (12, 17)])
+    assert torch.isfinite(out["y"]).all()
+    # accepted paths of every sequence against the oracle (integers: all of them)
+    for i in range(w.batch):
+        path_ref, bonus_ref = oracle.accept(b["parent"][i], b["tok"][i], b["tgt"][i])
+        assert out["path"][i, :int(out["path_len"][i])].cpu().tolist() == path_ref
+        assert int(out["bonus"][i]) == bonus_ref
+
+
+def test_config4_ternary_sampled():
+    w = workload(4)
+    b = batch(w, seqs=[0, 21, 63], tree=0)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(0, 0), (1, 24), (2, 47)])
+
+
+def test_chain_accept_and_commit_256():
+    # the 256-node chain of the stress workload: accept and commit (path up to 256)
+    w = workload(4)
+    b = batch(w, seqs=[0, 1], layers=[0, 47], tree=1)
+    d = upload_tree_batch(b, w)
+    from speculative_decoding_mamba2_gb300 import ssm_accept_path, ssm_commit
+    S, n, dims = d["n_seq"], d["n"], d["dims"]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    path = torch.empty((S, 256), dtype=torch.int32, device="cuda")
+    plen = torch.empty(S, dtype=torch.int32, device="cuda")
+    bonus = torch.empty(S, dtype=torch.int32, device="cuda")
+    ssm_accept_path(S, n, 256, d["layout"], d["tok"], d["tgt"], path, plen, bonus, status)
+    h, ring, head = d["h0"].clone(), d["ring"].clone(), d["ring_head"].clone()
+    ssm_commit(dims, d["params"], S, n, d["layout"], 256, path, plen, d["xBC"], d["dt"], h, ring, head, status)
+    torch.cuda.synchronize()
+    assert int(status) == 0
+    for i in range(S):
+        path_ref, bonus_ref = oracle.accept(b["parent"][i], b["tok"][i], b["tgt"][i])
+        assert path[i, :int(plen[i])].cpu().tolist() == path_ref and int(bonus[i]) == bonus_ref
+        for j in range(2):
+            h_ref, _, head_ref = oracle.commit(params_at(b["params"], j), b["parent"][i], path_ref,
+                                               f64(b["xBC"][i, j]), f64(b["dt"][i, j]),
+                                               b["h0"][i, j].astype(np.float64), f64(b["ring"][i, j]),
+                                               int(b["ring_head"][i, j]))
+            assert rel_err(h[i * 2 + j].double().cpu().numpy(), h_ref) <= TOL
+            assert int(head[i * 2 + j]) == head_ref
+
+
+def test_delta_zero_keeps_state_exactly():
+    w = Workload(53, "dt=-inf", Shape(H=4), n_layers=1, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    b["dt"][:] = 0xC61C  # bf16 -9984: softplus underflows to exactly 0
+    out = run_tree_step(upload_tree_batch(b, w))
+    np.testing.assert_array_equal(out["h"].cpu().numpy(), b["h0"].reshape(out["h"].shape))
+    check_instances(b, out, [(0, 0), (1, 0)])
+
+
+def test_verify_is_deterministic():
+    w = Workload(54, "det", Shape(H=8), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    d = upload_tree_batch(b, w)
+    a = run_tree_step(d)
+    c = run_tree_step(d)
+    assert torch.equal(a["y"], c["y"]) and torch.equal(a["h"], c["h"])
