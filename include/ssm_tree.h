@@ -59,6 +59,8 @@ extern "C" {
 #define SSM_STATUS_PATH_RANGE 2  /* path_len or a path entry out of range       */
 #define SSM_STATUS_K_RANGE 4     /* replay k larger than the logged steps       */
 #define SSM_STATUS_WALK_TRUNCATED 8 /* accept walk longer than max_path         */
+#define SSM_STATUS_TIMEOUT 16    /* a bounded wait on a copy gave up (results   */
+                                 /* of that call are invalid)                   */
 
 /* Limits of this build (checked on the host; larger inputs get SSM_ERR_CAPACITY). */
 #define SSM_MAX_NODES 64         /* nodes per tree for ssm_tree_verify          */

@@ -28,6 +28,7 @@ SSM_STATUS_BAD_LAYOUT = 1
 SSM_STATUS_PATH_RANGE = 2
 SSM_STATUS_K_RANGE = 4
 SSM_STATUS_WALK_TRUNCATED = 8
+SSM_STATUS_TIMEOUT = 16
 SSM_MAX_NODES = 64
 SSM_MAX_DEPTH = 15
 SSM_MAX_PATH = 256

@@ -1,5 +1,6 @@
 // libssmtree C ABI: argument validation on the host, then kernel launches on
 // the caller's stream.  Nothing here allocates device memory.
+#include <stdint.h>
 #include <stdio.h>
 
 #include <string>
@@ -75,7 +76,10 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!layout || !xBC || !dt || !h0 || !ring || !ring_head || !y)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)xBC | (uintptr_t)h0 | (uintptr_t)ring) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h0 and ring must be 16-byte aligned");
   VerifyArgs a;
+  a.gpc = 1;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
   a.R = dims->ring_cap;
