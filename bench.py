@@ -287,7 +287,7 @@ def run_ours(args, w):
     import torch
 
     from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_commit, ssm_tree_layout_build,
-                                                   ssm_tree_verify)
+                                                   ssm_tree_verify, ssm_tree_verify_workspace_size)
     from speculative_decoding_mamba2_gb300 import build as _build
     from synth import batch
 
@@ -328,12 +328,13 @@ def run_ours(args, w):
     plen = torch.empty(S, dtype=torch.int32, device=dev)
     bonus = torch.empty(S, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, depth), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        ssm_tree_verify(dims, prm, S, n, depth, layout, xBC, dt, h, ring, head, y, status)
+        ssm_tree_verify(dims, prm, S, n, depth, layout, xBC, dt, h, ring, head, y, ws, status)
         if ev is not None:
             ev[1].record(stream)
         ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status)
@@ -400,7 +401,7 @@ def run_ours(args, w):
     # ---- end to end through the public API, host buffers ----
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, b, dims, prm, h, ring, head, dev, stream, world)
+        e2e = run_e2e(args, w, b, dims, prm, h, ring, head, ws, dev, stream, world)
 
     if status.item() != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
@@ -422,7 +423,7 @@ def run_ours(args, w):
     return 0
 
 
-def run_e2e(args, w, b, dims, prm, h, ring, head, dev, stream, world):
+def run_e2e(args, w, b, dims, prm, h, ring, head, ws, dev, stream, world):
     """Same step through the public API with the step's inputs in pinned host
     memory: host layout build, H2D of xBC/dt/layout/tokens, verify, accept,
     commit, D2H of the accepted paths and bonus tokens, all inside the timed
@@ -460,7 +461,7 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, dev, stream, world):
         plen = torch.empty(S, dtype=torch.int32, device=dev)
         bonus = torch.empty(S, dtype=torch.int32, device=dev)
         xb, d = xBC_d.view(torch.bfloat16), dt_d.view(torch.bfloat16)
-        ssm_tree_verify(dims, prm, S, n, depth, lay_d, xb, d, h, ring, head, y, status)
+        ssm_tree_verify(dims, prm, S, n, depth, lay_d, xb, d, h, ring, head, y, ws, status)
         ssm_accept_path(S, n, max_path, lay_d, tok_d, tgt_d, path, plen, bonus, status)
         ssm_commit(dims, prm, S, n, lay_d, max_path, path, plen, xb, d, h, ring, head, status)
         out = torch.empty((S, max_path + 2), dtype=torch.int32).pin_memory()

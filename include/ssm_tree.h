@@ -42,6 +42,7 @@
 #ifndef SSM_TREE_H
 #define SSM_TREE_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -131,11 +132,23 @@ int ssm_tree_layout_build(const int32_t *parent, int32_t n_seq, int32_t n_nodes,
  *   ring_head  device int32 [I]               committed positions; the rows
  *              before the root are ring positions head-3 .. head-1 (mod R)
  *   y          device fp32 [I][n][d_inner]    written
+ *   workspace  device, 16-byte aligned, >= ssm_tree_verify_workspace_size()
+ *              bytes, caller-owned scratch; its contents on entry do not
+ *              matter and on return are unspecified.  Calls that overlap on
+ *              the GPU must not share one workspace.
  */
 int ssm_tree_verify(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
                     int32_t max_depth, const ssm_node *layout, const uint16_t *xBC, const uint16_t *dt,
                     const float *h0, const uint16_t *ring, const int32_t *ring_head, float *y,
-                    int32_t *dev_status, void *stream);
+                    void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * ssm_tree_verify_workspace_size -- host-only.  Bytes of device workspace
+ * ssm_tree_verify needs for this shape (per-instance conv outputs, path
+ * tables and path coefficients, written and read within one call); 0 if the
+ * shape is rejected (reason in ssm_last_error()).
+ */
+size_t ssm_tree_verify_workspace_size(const ssm_dims *dims, int32_t n_seq, int32_t n_nodes, int32_t max_depth);
 
 /*
  * ssm_accept_path -- SpecMamba page §1.2 (target verifies the draft): greedy

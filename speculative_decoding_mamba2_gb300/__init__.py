@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     ssm_replay,
     ssm_tree_layout_build,
     ssm_tree_verify,
+    ssm_tree_verify_workspace_size,
     ssm_version,
 )
 from .binding import (  # noqa: F401

@@ -80,7 +80,8 @@ _SIGS = {
     "ssm_version": (_I, []),
     "ssm_last_error": (ctypes.c_char_p, []),
     "ssm_tree_layout_build": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P]),
-    "ssm_tree_verify": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_tree_verify": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
+    "ssm_tree_verify_workspace_size": (ctypes.c_size_t, [_P, _I, _I, _I]),
     "ssm_accept_path": (ctypes.c_int, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -181,8 +182,17 @@ def ssm_tree_layout_build(parent, max_branches: int = 0, max_depth: int = 0):
     return out, int(depth.value)
 
 
+def ssm_tree_verify_workspace_size(dims: Dims, n_seq: int, n_nodes: int, max_depth: int) -> int:
+    """Bytes of device workspace ssm_tree_verify needs (host call)."""
+    cd = dims.c()
+    b = lib().ssm_tree_verify_workspace_size(ctypes.byref(cd), n_seq, n_nodes, max_depth)
+    if b == 0:
+        raise SSMError(SSM_ERR_CAPACITY, ssm_last_error())
+    return int(b)
+
+
 def ssm_tree_verify(dims: Dims, params: dict, n_seq: int, n_nodes: int, max_depth: int, layout, xBC, dt, h0, ring,
-                    ring_head, y, status=None, stream=None):
+                    ring_head, y, workspace, status=None, stream=None):
     d, I, n = dims, n_seq * dims.n_layers, n_nodes
     cd = d.c()
     cp = _params(params, d, d.n_layers)
@@ -193,6 +203,7 @@ def ssm_tree_verify(dims: Dims, params: dict, n_seq: int, n_nodes: int, max_dept
         _dev(h0, "h0", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
+        _dev(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
         _opt_status(status), _stream(stream, h0)))
 
 

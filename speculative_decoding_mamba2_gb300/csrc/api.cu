@@ -3,6 +3,8 @@
 #include <stdint.h>
 #include <stdio.h>
 
+#include <stddef.h>
+
 #include <string>
 
 #include "common.cuh"
@@ -62,22 +64,44 @@ extern "C" int32_t ssm_version(void) { return 100; }
 
 extern "C" const char* ssm_last_error(void) { return g_error.c_str(); }
 
-extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
-                               int32_t max_depth, const ssm_node* layout, const uint16_t* xBC, const uint16_t* dt,
-                               const float* h0, const uint16_t* ring, const int32_t* ring_head, float* y,
-                               int32_t* dev_status, void* stream) {
-  const char* fn = "ssm_tree_verify";
-  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+namespace {
+int check_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_seq, int32_t n_nodes, int32_t max_depth) {
+  if (int rc = check_dims(fn, dims, false, nullptr)) return rc;
   if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
   if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
   if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
   if (max_depth < 0 || max_depth >= n_nodes) return fail(SSM_ERR_RANGE, fn, "max_depth must be in [0, n_nodes)");
   if (max_depth > SSM_MAX_DEPTH) return fail(SSM_ERR_CAPACITY, fn, "max_depth exceeds SSM_MAX_DEPTH");
+  if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads) == 0 ||
+      verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads) > 232448)
+    return fail(SSM_ERR_CAPACITY, fn, "tree too large for the shared-memory plan of this build");
+  return SSM_OK;
+}
+}  // namespace
+
+extern "C" size_t ssm_tree_verify_workspace_size(const ssm_dims* dims, int32_t n_seq, int32_t n_nodes,
+                                                 int32_t max_depth) {
+  const char* fn = "ssm_tree_verify_workspace_size";
+  if (check_verify_shape(fn, dims, n_seq, n_nodes, max_depth) != SSM_OK) return 0;
+  g_error.clear();
+  const size_t b = verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers);
+  return b ? b : 16;
+}
+
+extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
+                               int32_t max_depth, const ssm_node* layout, const uint16_t* xBC, const uint16_t* dt,
+                               const float* h0, const uint16_t* ring, const int32_t* ring_head, float* y,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_tree_verify";
+  if (int rc = check_verify_shape(fn, dims, n_seq, n_nodes, max_depth)) return rc;
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
   if (n_seq == 0) return finish(fn, cudaSuccess);
-  if (!layout || !xBC || !dt || !h0 || !ring || !ring_head || !y)
+  if (!layout || !xBC || !dt || !h0 || !ring || !ring_head || !y || !workspace)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
-  if (((uintptr_t)xBC | (uintptr_t)h0 | (uintptr_t)ring) & 15)
-    return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h0 and ring must be 16-byte aligned");
+  if (((uintptr_t)xBC | (uintptr_t)h0 | (uintptr_t)ring | (uintptr_t)layout | (uintptr_t)workspace) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h0, ring, layout and workspace must be 16-byte aligned");
+  if (workspace_bytes < verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers))
+    return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_tree_verify_workspace_size()");
   VerifyArgs a;
   a.gpc = 1;
   a.H = dims->n_heads;
@@ -99,7 +123,7 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   a.ring_head = ring_head;
   a.y = y;
   a.status = dev_status;
-  return finish(fn, launch_verify(a, (cudaStream_t)stream));
+  return finish(fn, launch_verify(a, workspace, (cudaStream_t)stream));
 }
 
 extern "C" int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node* layout,

@@ -54,6 +54,14 @@ __device__ __forceinline__ float conv4_silu(float4 w, float b, float r0, float r
   return silu_f(acc);
 }
 
+// b + w0·r0 + w1·r1 + w2·r2 + w3·r3 (the conv before its SiLU), taps oldest first.
+__device__ __forceinline__ float conv4_acc(float4 w, float b, float r0, float r1, float r2, float r3) {
+  float acc = fmaf(w.x, r0, b);
+  acc = fmaf(w.y, r1, acc);
+  acc = fmaf(w.z, r2, acc);
+  return fmaf(w.w, r3, acc);
+}
+
 // Pre-conv value of channel c for tap source `src` of a tree node: a node row
 // of this instance's xBC (src >= 0) or a ring row (src = -j: position head - j).
 __device__ __forceinline__ float tap_value(const uint16_t* __restrict__ xbc, const uint16_t* __restrict__ ring,
@@ -86,6 +94,22 @@ __device__ __forceinline__ float pair_sum(unsigned long long p) {
   float lo, hi;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(p));
   return lo + hi;
+}
+
+// fp32 -> (hi, lo) TF32 pair with hi + lo = x to ~2^-22 relative (round-to-nearest splits)
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+// D += A·B on one m16n8k8 tile (TF32 inputs, fp32 accumulate), warp-wide.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -173,7 +197,10 @@ struct VerifyArgs {
   float* y;
   int32_t* status;
 };
-cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
+size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst);
+int verify_heads_per_group(int n, int max_depth, int H);  // 0: the plan does not fit in shared memory
+int verify_prep_smem_bytes(int n, int max_depth, int H);
 
 struct AcceptArgs {
   int n_seq, n, max_path;

@@ -1,5 +1,5 @@
-// Tree verification kernel: every node of a breadth-first token tree through a
-// Mamba2 selective-SSM layer, from the committed state h0.
+// Tree verification: every node of a breadth-first token tree through a Mamba2
+// selective-SSM layer, from the committed state h0.
 //
 // Method: SpecMamba page ("FPGA加速Mamba推理：SpecMamba方案与优化实践") §3.2,
 // FIFO-based tree verification: each child is updated from its parent's state,
@@ -12,36 +12,31 @@
 // and y_v = C_v·h_v + D·x_v becomes
 //     y_v[p] = e^{S_v}·(C_v·h0[p,:]) + Σ_{m ∈ path(v)} coef[v,m]·x_m[p] + D·x_v[p],
 //     coef[v,m] = e^{S_v - S_m}·Δ_m·(C_v·B_m).
-// The only O(P·N) work per node is the dot product C_v·h0[p,:]; the per-node
-// states are never formed at all (the extreme of "release after the children
-// are done").  h0 is read from HBM exactly once; everything else stays in
-// shared memory and registers.
+// The per-node states are never formed (the extreme of "release after the
+// children are done"); h0 is read from HBM exactly once.
 //
-// Work split: one CTA (256 threads) per (instance, run of `gpc` head groups of
-// G heads).  h0 of the CTA's heads streams through one continuous 4-stage ring
-// of 16-column chunks, each one 2-D bulk tensor copy (TMA, 64-byte swizzle)
-// issued by a single thread and tracked by full/empty mbarriers, so warps only
-// wait for their own data and for the stage they refill; the pre-conv input
-// rows (nodes plus the three ring rows above the root) arrive by 1-D bulk
-// copies, the B|C rows once per CTA and each group's x rows together with that
-// group's first h0 chunk.  Per CTA, once: B and C conv + SiLU for every node and the C_v·B_m
-// products along every path.  Per head group: x conv + SiLU, Δ, S, e^S and the
-// path coefficients; then the main loop accumulates Z = C_v·h0[row,:] for a
-// tile of 16 nodes with a G rows x 4 nodes register tile per thread, using
-// packed fp32 FMAs (fma.rn.f32x2) on (even k, odd k) partial sums, and the
-// epilogue writes y.
+// Two kernels per call:
+//  * tree_prep_kernel, one CTA per (layer, sequence) instance: B and C conv +
+//    SiLU for every node, the path tables, C_v·B_m along every path, Δ, S,
+//    e^S and coef[v,m] for every head, written to a caller-provided workspace
+//    (tens of KB per instance, L2-sized).
+//  * tree_verify_kernel, one CTA (256 threads) per (instance, run of head
+//    groups of G heads): its prologue is a handful of bulk copies from the
+//    workspace; per head group it runs the x conv + SiLU, then streams the
+//    group's h0 slice through a 4-stage ring of 16-column chunks (2-D bulk
+//    tensor copies with 64-byte swizzle, full/empty mbarriers, warp 0 as
+//    producer) and contracts each chunk against C on the tensor cores
+//    (mma m16n8k8 TF32 with a 3-term hi/lo split, fp32 accumulate: fp32-level
+//    accuracy), and the epilogue adds the path terms and D·x and writes y.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
 namespace ssmtree {
 
-int verify_smem_bytes(int n, int* heads_per_group);
-
 namespace {
-
-typedef unsigned long long u64;
 
 constexpr int NT = 16;           // nodes per tile
 constexpr int KC = 16;           // d_state columns per pipeline stage
@@ -51,16 +46,233 @@ constexpr int SROW = KC;         // stage row: 64 B, 16-byte pieces swizzled by 
 constexpr int THREADS = 256;
 constexpr int DMAX = SSM_MAX_DEPTH + 1;
 constexpr int XW = 256;          // channels per staged input row
+constexpr int CSTR = kN + 4;     // padded row of the C table (conflict-free B fragments)
 constexpr int MAX_GPC = 8;       // head groups per CTA
 constexpr int SMEM_LIMIT = 232448;
 static_assert(2 * kN == THREADS, "one thread per B|C channel");
 
+// ---------------------------------------------------------------------------
+// per-instance workspace written by the prep kernel (byte offsets)
+// ---------------------------------------------------------------------------
+struct Ws {
+  int NP;  // n rounded up to 4
+  int PP;  // path pairs n*(max_depth+1) rounded up to 4
+  size_t C, eS, coef, pathn, pairs, stride;
+};
+
+__host__ __device__ inline Ws ws_layout(int n, int max_depth, int H) {
+  Ws w;
+  w.NP = (n + 3) & ~3;
+  w.PP = (n * (max_depth + 1) + 3) & ~3;
+  size_t o = 0;
+  auto take = [&](size_t b) {
+    const size_t r = o;
+    o += (b + 15) & ~size_t(15);
+    return r;
+  };
+  w.C = take((size_t)n * CSTR * 4);        // post-conv C [n][CSTR]
+  w.eS = take((size_t)H * w.NP * 4);       // e^{S_v} [H][NP]
+  w.coef = take((size_t)H * w.PP * 4);     // coef [H][PP] in pair order
+  w.pathn = take((size_t)n * DMAX * 4);    // ancestor of v at depth j [n][DMAX]
+  w.pairs = take((size_t)(w.PP + 4) * 4);  // [count, v*DMAX+j ...]
+  w.stride = o;
+  return w;
+}
+
+// Validated copy of a layout record (bad fields are clamped and reported).
+__device__ ssm_node checked_node(const ssm_node* lay, int v, int max_depth, int32_t* status) {
+  ssm_node r = lay[v];
+  bool bad = false;
+  if (v == 0) {
+    bad |= r.parent != -1 || r.depth != 0;
+    r.parent = -1;
+    r.depth = 0;
+  } else if (r.parent < 0 || r.parent >= v) {
+    bad = true;
+    r.parent = 0;
+  }
+  if (r.depth < 0 || r.depth > max_depth) {
+    bad = true;
+    r.depth = r.depth < 0 ? 0 : max_depth;
+  }
+  for (int d = 0; d < 3; ++d)
+    if (r.tap[d] >= v || r.tap[d] < -3) {
+      bad = true;
+      r.tap[d] = -1;
+    }
+  if (bad) flag(status, SSM_STATUS_BAD_LAYOUT);
+  return r;
+}
+
+// staged row of each conv tap (rows 0..2 = ring positions head-3..head-1, 3+v = node v), oldest first
+__device__ __forceinline__ int4 tap_rows(const ssm_node& r, int v) {
+  return make_int4(r.tap[2] + 3, r.tap[1] + 3, r.tap[0] + 3, v + 3);
+}
+
+// ---------------------------------------------------------------------------
+// prep kernel: everything per instance that does not depend on the head group
+// ---------------------------------------------------------------------------
+struct PrepSmem {
+  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, total;
+};
+
+__host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP) {
+  PrepSmem s;
+  int o = 0;
+  auto take = [&](int b) {
+    const int r = o;
+    o += (b + 15) & ~15;
+    return r;
+  };
+  s.nodes = take(n * (int)sizeof(ssm_node));
+  s.pathn = take(n * DMAX * 4);
+  s.pairs = take((PP + 4) * 4);
+  s.xin = take((n + 3) * XW * 2);
+  s.Bs = take(n * kN * 4);
+  s.Cs = take(n * CSTR * 4);
+  s.Gm = take(n * DMAX * 4);
+  s.dl = take(n * H * 4);
+  s.S = take(n * H * 4);
+  s.total = o;
+  return s;
+}
+
+__global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int n = a.n, H = a.H;
+  const Ws W = ws_layout(n, a.max_depth, H);
+  const PrepSmem L = prep_layout(n, H, W.PP);
+  ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
+  int* pathn = reinterpret_cast<int*>(smem + L.pathn);
+  int* pairs = reinterpret_cast<int*>(smem + L.pairs);
+  uint16_t* xin = reinterpret_cast<uint16_t*>(smem + L.xin);
+  float* Bs = reinterpret_cast<float*>(smem + L.Bs);
+  float* Cs = reinterpret_cast<float*>(smem + L.Cs);
+  float* Gm = reinterpret_cast<float*>(smem + L.Gm);
+  float* dl = reinterpret_cast<float*>(smem + L.dl);
+  float* Sv = reinterpret_cast<float*>(smem + L.S);
+
+  const int tid = threadIdx.x;
+  const int inst = blockIdx.x;
+  const int seq = inst / a.L, layer = inst % a.L;
+  const int d_inner = H * kP, conv_dim = d_inner + 2 * kN, R = a.R;
+  const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
+  const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
+  const int head = a.ring_head[inst];
+  unsigned char* ws = ws_base + (size_t)inst * W.stride;
+
+  // B|C input rows (ring rows above the root, then the nodes) in flight first
+  for (int i = tid; i < (n + 3) * 32; i += THREADS) {
+    const int r = i >> 5, pc = i & 31;
+    const uint16_t* src = r < 3 ? ring + (size_t)ring_pos(head, r - 3, R) * conv_dim : xbc + (size_t)(r - 3) * conv_dim;
+    cp_async16(xin + r * XW + pc * 8, src + d_inner + pc * 8);
+  }
+  cp_async_commit();
+  const ssm_node* lay = a.layout + (size_t)seq * n;
+  for (int v = tid; v < n; v += THREADS) nodes[v] = checked_node(lay, v, a.max_depth, a.status);
+  for (int i = tid; i < n * H; i += THREADS) {
+    const int v = i / H, h = i - v * H;
+    dl[i] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
+  }
+  const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
+  const float4 w = cw[d_inner + tid];
+  const float bb = a.conv_b[(size_t)layer * conv_dim + d_inner + tid];
+  __syncthreads();
+  for (int v = tid; v < n; v += THREADS) {
+    int m = v;
+    const int dv = nodes[v].depth;
+    for (int j = dv; j >= 0; --j) {
+      pathn[v * DMAX + j] = m;
+      m = m > 0 ? nodes[m].parent : 0;
+      if (m < 0) m = 0;
+    }
+    int off = 0;
+    for (int u = 0; u < v; ++u) off += nodes[u].depth + 1;
+    for (int j = 0; j <= dv; ++j) pairs[1 + off + j] = v * DMAX + j;
+    if (v == n - 1) pairs[0] = off + dv + 1;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  {  // B and C conv + SiLU (thread = channel of B|C), four nodes at a time for ILP
+    float* __restrict__ dst = tid < kN ? Bs + tid : Cs + (tid - kN);
+    const int dstr = tid < kN ? kN : CSTR;
+    const uint16_t* __restrict__ xi = xin + tid;
+    int v = 0;
+    for (; v + 4 <= n; v += 4) {
+      float r[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int4 t = tap_rows(nodes[v + u], v + u);
+        r[u][0] = bf16f(xi[t.x * XW]);
+        r[u][1] = bf16f(xi[t.y * XW]);
+        r[u][2] = bf16f(xi[t.z * XW]);
+        r[u][3] = bf16f(xi[t.w * XW]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dst[(v + u) * dstr] = silu_fast(conv4_acc(w, bb, r[u][0], r[u][1], r[u][2], r[u][3]));
+    }
+    for (; v < n; ++v) {
+      const int4 t = tap_rows(nodes[v], v);
+      dst[v * dstr] = silu_fast(conv4_acc(w, bb, bf16f(xi[t.x * XW]), bf16f(xi[t.y * XW]), bf16f(xi[t.z * XW]),
+                                          bf16f(xi[t.w * XW])));
+    }
+  }
+  // S_v per head: Σ over the path of Δ·A, root first
+  for (int i = tid; i < n * H; i += THREADS) {
+    const int v = i / H, h = i - v * H;
+    const float A = neg_exp(a.A_log[(size_t)layer * H + h]);
+    float s = 0.f;
+    const int dv = nodes[v].depth;
+    for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * H + h], A, s);
+    Sv[i] = s;
+    reinterpret_cast<float*>(ws + W.eS)[h * W.NP + v] = expf(s);
+  }
+  __syncthreads();
+  const int n_pairs = pairs[0];
+  {  // Gm[v][j] = C_v · B_{path_j(v)}: one warp per pair
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int k = warp; k < n_pairs; k += THREADS / 32) {
+      const int pr = pairs[1 + k];
+      const int v = pr / DMAX, m = pathn[pr];
+      const float4 c4 = reinterpret_cast<const float4*>(Cs + v * CSTR)[lane];
+      const float4 b4 = reinterpret_cast<const float4*>(Bs + m * kN)[lane];
+      float s = c4.x * b4.x;
+      s = fmaf(c4.y, b4.y, s);
+      s = fmaf(c4.z, b4.z, s);
+      s = fmaf(c4.w, b4.w, s);
+      s = warp_sum(s);
+      if (lane == 0) Gm[pr] = s;
+    }
+  }
+  {  // workspace: C table, path tables
+    const float4* src = reinterpret_cast<const float4*>(Cs);
+    float4* dstC = reinterpret_cast<float4*>(ws + W.C);
+    for (int i = tid; i < n * CSTR / 4; i += THREADS) dstC[i] = src[i];
+    int* dp = reinterpret_cast<int*>(ws + W.pathn);
+    for (int i = tid; i < n * DMAX; i += THREADS) dp[i] = pathn[i];
+    int* dq = reinterpret_cast<int*>(ws + W.pairs);
+    for (int i = tid; i < W.PP + 4; i += THREADS) dq[i] = i <= n_pairs ? pairs[i] : 0;
+  }
+  __syncthreads();
+  // coef[h][k] = e^{S_v - S_m}·Δ_m·(C_v·B_m) for pair k = (v, depth-j ancestor m)
+  float* wc = reinterpret_cast<float*>(ws + W.coef);
+  for (int i = tid; i < n_pairs * H; i += THREADS) {
+    const int k = i / H, h = i - k * H;
+    const int pr = pairs[1 + k];
+    const int v = pr / DMAX, m = pathn[pr];
+    wc[h * W.PP + k] = expf(Sv[v * H + h] - Sv[m * H + h]) * dl[m * H + h] * Gm[pr];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// main kernel
+// ---------------------------------------------------------------------------
 struct Smem {
-  int bars, stage, nodes, rowidx, pathn, pairs, Cs, Bcoef, xsin, dl, S, eS, Gm, xinX, dts, prm, total;
+  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, pD, total;
 };
 
 template <int G>
-__host__ __device__ inline Smem smem_layout(int n) {
+__host__ __device__ inline Smem smem_layout(int n, int PP, int NP) {
   constexpr int ROWS = G * kP;
   Smem s;
   int o = 0;
@@ -69,68 +281,46 @@ __host__ __device__ inline Smem smem_layout(int n) {
     o += (bytes + 15) & ~15;
     return r;
   };
-  const int a = n * kN * 4, b = n * DMAX * G * 4, c = n * ROWS * 4, d = (n + 3) * XW * 2;
-  s.bars = take((2 * STAGES + 2) * 8 + 16);  // full[], empty[], B|C rows, x rows; abort flag
-  o = (o + 127) & ~127;                 // swizzled copies need 128-byte alignment
+  s.bars = take((2 * STAGES + 2) * 8 + 16);  // full[], empty[], prologue, group inputs; abort flag
+  o = (o + 127) & ~127;                      // swizzled copies need 128-byte alignment
   s.stage = take(STAGES * ROWS * SROW * 4);
   s.nodes = take(n * (int)sizeof(ssm_node));
   s.rowidx = take(n * 16);
+  s.poff = take(n * 4);
   s.pathn = take(n * DMAX * 4);
-  s.pairs = take((n * DMAX + 1) * 4);
-  s.Cs = take(n * kN * 4);
-  s.Bcoef = take(a > b ? a : b);  // B (prologue) | path coefficients (per group)
-  s.xsin = take(c > d ? c : d);   // staged B|C input rows (prologue) | post-conv x (per group)
-  s.dl = take(n * G * 4);
-  s.S = take(n * G * 4);
-  s.eS = take(n * G * 4);
-  s.Gm = take(n * DMAX * 4);
-  s.xinX = take(d);
-  s.dts = take(n * MAX_GPC * G * 4);
-  s.prm = take(3 * MAX_GPC * G * 4);
+  s.pairs = take((PP + 4) * 4);
+  s.Cs = take(n * CSTR * 4);
+  s.xs = take(n * ROWS * 4);
+  s.xinX = take((n + 3) * XW * 2);
+  s.eSg = take(2 * G * NP * 4);    // two groups in flight: the next group's inputs land
+  s.coefg = take(2 * G * PP * 4);  // before the current group's epilogue
+  s.pD = take(MAX_GPC * G * 4);
   s.total = o;
   return s;
 }
 
 template <int G>
-struct CoefVec;
-template <>
-struct CoefVec<4> {
-  typedef float4 T;
-  __device__ static float at(const float4& c, int i) { return i == 0 ? c.x : i == 1 ? c.y : i == 2 ? c.z : c.w; }
-};
-template <>
-struct CoefVec<2> {
-  typedef float2 T;
-  __device__ static float at(const float2& c, int i) { return i == 0 ? c.x : c.y; }
-};
-
-template <int G>
-__global__ void __launch_bounds__(THREADS, 2) tree_verify_kernel(VerifyArgs a, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(THREADS, 2)
+    tree_verify_kernel(VerifyArgs a, const unsigned char* __restrict__ ws_base, const __grid_constant__ CUtensorMap tmap) {
   constexpr int ROWS = G * kP;
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n;
-  const Smem L = smem_layout<G>(n);
+  const Ws W = ws_layout(n, a.max_depth, a.H);
+  const Smem L = smem_layout<G>(n, W.PP, W.NP);
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int4* rowidx = reinterpret_cast<int4*>(smem + L.rowidx);
+  int* poff = reinterpret_cast<int*>(smem + L.poff);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
-  int* pairs = reinterpret_cast<int*>(smem + L.pairs);  // [0] = count, then v*DMAX+j
+  int* pairs = reinterpret_cast<int*>(smem + L.pairs);
   float* Cs = reinterpret_cast<float*>(smem + L.Cs);
-  float* Bs = reinterpret_cast<float*>(smem + L.Bcoef);
-  float* coef = reinterpret_cast<float*>(smem + L.Bcoef);
-  uint16_t* xinBC = reinterpret_cast<uint16_t*>(smem + L.xsin);
-  float* xs = reinterpret_cast<float*>(smem + L.xsin);
-  float* dl = reinterpret_cast<float*>(smem + L.dl);
-  float* Sv = reinterpret_cast<float*>(smem + L.S);
-  float* eS = reinterpret_cast<float*>(smem + L.eS);
-  float* Gm = reinterpret_cast<float*>(smem + L.Gm);
+  float* xs = reinterpret_cast<float*>(smem + L.xs);
   uint16_t* xinX = reinterpret_cast<uint16_t*>(smem + L.xinX);
-  float* dts = reinterpret_cast<float*>(smem + L.dts);
-  float* pbias = reinterpret_cast<float*>(smem + L.prm);
-  float* pA = pbias + MAX_GPC * G;
-  float* pD = pA + MAX_GPC * G;
+  float* eSg = reinterpret_cast<float*>(smem + L.eSg);
+  float* coefg = reinterpret_cast<float*>(smem + L.coefg);
+  float* pD = reinterpret_cast<float*>(smem + L.pD);
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NG = (a.H + G - 1) / G;
   const int parts = (NG + a.gpc - 1) / a.gpc;
   const int part = blockIdx.x % parts;
@@ -147,28 +337,30 @@ __global__ void __launch_bounds__(THREADS, 2) tree_verify_kernel(VerifyArgs a, c
   const int n_tiles = (n + NT - 1) / NT;
   const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
   const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
-  const int head = a.ring_head[inst];
+  const unsigned char* ws = ws_base + (size_t)inst * W.stride;
 
   const uint32_t bar0 = smem_u32(smem + L.bars);
   auto full_bar = [&](int s) { return bar0 + 8 * s; };
   auto empty_bar = [&](int s) { return bar0 + 8 * (STAGES + s); };
-  const uint32_t bc_bar = bar0 + 8 * (2 * STAGES);
+  const uint32_t pro_bar = bar0 + 8 * (2 * STAGES);
   const uint32_t x_bar = bar0 + 8 * (2 * STAGES + 1);
   volatile int& s_abort = *reinterpret_cast<int*>(smem + L.bars + (2 * STAGES + 2) * 8);
   const int total = g_count * n_tiles * KCH;  // h0 chunks this CTA consumes
 
-  // staged input row r: rows 0..2 are ring positions head-3 .. head-1, row 3+v is node v
-  auto issue_inputs = [&](uint16_t* dst, int ch0, int nch, uint32_t bar) {  // one thread
-    const uint32_t bytes = (uint32_t)nch * 2;
-    mbar_arrive_expect_tx(bar, bytes * (n + 3));
-    for (int r = 0; r < n + 3; ++r) {
-      const uint16_t* src = r < 3 ? ring + (size_t)ring_pos(head, r - 3, R) * conv_dim : xbc + (size_t)(r - 3) * conv_dim;
-      bulk_load(smem_u32(dst + r * XW), src + ch0, bytes, bar);
-    }
-  };
-  // producer (thread 0): cursor over (group, tile, k-chunk); chunk c goes to stage c % STAGES
+  // swizzled tensor copies need a 128-byte aligned destination; refuse rather than copy
+  if (smem_u32(stage) & 127) {
+    if (tid == 0) flag(a.status, SSM_STATUS_TIMEOUT);
+    return;
+  }
+
+  // Producer = warp 0.  Chunk c goes to stage c % STAGES; the first chunk of a group also
+  // brings the group's inputs (x rows for the conv, e^S and coef of its heads) on x_bar.
+  // A group's x_bar phase completes before the next group's inputs are issued: those go
+  // out with the next group's first chunk, after every warp has released a stage of this
+  // group, i.e. after every warp has waited on this phase.
   int pf_g = 0, pf_t = 0, pf_k = 0, pf_n = 0;
-  auto produce = [&](int upto) {
+  const int head = a.ring_head[inst];
+  auto produce = [&](int upto) {  // warp 0, all lanes
     while (pf_n < upto && pf_n < total) {
       const int slot = pf_n % STAGES;
       if (pf_n >= STAGES && !mbar_wait(empty_bar(slot), ((pf_n / STAGES) - 1) & 1)) {
@@ -177,9 +369,26 @@ __global__ void __launch_bounds__(THREADS, 2) tree_verify_kernel(VerifyArgs a, c
         return;
       }
       const int hb = hc_begin + pf_g * G;
-      if (pf_t == 0 && pf_k == 0) issue_inputs(xinX, hb * kP, min(G, a.H - hb) * kP, x_bar);  // group's x rows
-      mbar_arrive_expect_tx(full_bar(slot), ROWS * SROW * 4);
-      tma_load_2d(smem_u32(stage + slot * ROWS * SROW), &tmap, pf_k * KC, (inst * a.H + hb) * kP, full_bar(slot));
+      if (pf_t == 0 && pf_k == 0) {
+        const int heads = min(G, a.H - hb);
+        const uint32_t xb = (uint32_t)heads * kP * 2;
+        const int buf = pf_g & 1;
+        if (lane == 0) mbar_arrive_expect_tx(x_bar, xb * (n + 3) + (uint32_t)heads * (W.NP + W.PP) * 4);
+        __syncwarp();
+        for (int r = lane; r < n + 3; r += 32) {
+          const uint16_t* src =
+              r < 3 ? ring + (size_t)ring_pos(head, r - 3, R) * conv_dim : xbc + (size_t)(r - 3) * conv_dim;
+          bulk_load(smem_u32(xinX + r * XW), src + hb * kP, xb, x_bar);
+        }
+        if (lane == 0)
+          bulk_load(smem_u32(eSg + buf * G * W.NP), ws + W.eS + (size_t)hb * W.NP * 4, heads * W.NP * 4, x_bar);
+        if (lane == 1)
+          bulk_load(smem_u32(coefg + buf * G * W.PP), ws + W.coef + (size_t)hb * W.PP * 4, heads * W.PP * 4, x_bar);
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full_bar(slot), ROWS * SROW * 4);
+        tma_load_2d(smem_u32(stage + slot * ROWS * SROW), &tmap, pf_k * KC, (inst * a.H + hb) * kP, full_bar(slot));
+      }
       if (++pf_k == KCH) {
         pf_k = 0;
         if (++pf_t == n_tiles) {
@@ -198,143 +407,95 @@ __global__ void __launch_bounds__(THREADS, 2) tree_verify_kernel(VerifyArgs a, c
     }
   };
 
-  // swizzled tensor copies need a 128-byte aligned destination; refuse rather than copy
-  if (smem_u32(stage) & 127) {
-    if (tid == 0) flag(a.status, SSM_STATUS_TIMEOUT);
-    return;
-  }
-  // ---- prologue: barriers, then every input copy in flight first ----
-  if (tid == 0) {
-    s_abort = 0;
-    for (int i = 0; i < STAGES; ++i) {
-      mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), THREADS / 32);
+  // ---- prologue: barriers, then every copy in flight ----
+  if (warp == 0) {
+    if (lane == 0) {
+      s_abort = 0;
+      for (int i = 0; i < STAGES; ++i) {
+        mbar_init(full_bar(i), 1);
+        mbar_init(empty_bar(i), THREADS / 32);
+      }
+      mbar_init(pro_bar, 1);
+      mbar_init(x_bar, 1);
+      fence_barrier_init();
+      mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4);
+      bulk_load(smem_u32(nodes), a.layout + (size_t)seq * n, n * (uint32_t)sizeof(ssm_node), pro_bar);
+      bulk_load(smem_u32(Cs), ws + W.C, n * CSTR * 4, pro_bar);
+      bulk_load(smem_u32(pathn), ws + W.pathn, n * DMAX * 4, pro_bar);
+      bulk_load(smem_u32(pairs), ws + W.pairs, (W.PP + 4) * 4, pro_bar);
     }
-    mbar_init(bc_bar, 1);
-    mbar_init(x_bar, 1);
-    fence_barrier_init();
-    issue_inputs(xinBC, d_inner, 2 * kN, bc_bar);
+    __syncwarp();
     produce(STAGES);
   }
-
-  const ssm_node* lay = a.layout + (size_t)seq * n;
-  for (int v = tid; v < n; v += THREADS) {
-    ssm_node r = lay[v];
-    bool bad = false;
-    if (v == 0) {
-      bad |= r.parent != -1 || r.depth != 0;
-      r.parent = -1;
-      r.depth = 0;
-    } else if (r.parent < 0 || r.parent >= v) {
-      bad = true;
-      r.parent = 0;
-    }
-    if (r.depth < 0 || r.depth > a.max_depth) {
-      bad = true;
-      r.depth = r.depth < 0 ? 0 : a.max_depth;
-    }
-    for (int d = 0; d < 3; ++d)
-      if (r.tap[d] >= v || r.tap[d] < -3) {
-        bad = true;
-        r.tap[d] = -1;
-      }
-    if (bad) flag(a.status, SSM_STATUS_BAD_LAYOUT);
-    nodes[v] = r;
-    // staged row of each conv tap, oldest first, then the node's own row
-    rowidx[v] = make_int4(r.tap[2] + 3, r.tap[1] + 3, r.tap[0] + 3, v + 3);
-  }
-  for (int i = tid; i < n * hc_count; i += THREADS) {
-    const int v = i / hc_count, hh = i - v * hc_count;
-    dts[v * (MAX_GPC * G) + hh] = bf16f(a.dt[((size_t)inst * n + v) * a.H + hc_begin + hh]);
-  }
-  if (tid < hc_count) {
-    const size_t pi = (size_t)layer * a.H + hc_begin + tid;
-    pbias[tid] = a.dt_bias[pi];
-    pA[tid] = neg_exp(a.A_log[pi]);
-    pD[tid] = a.D[pi];
-  }
+  if (tid < hc_count) pD[tid] = a.D[(size_t)layer * a.H + hc_begin + tid];
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float* cb = a.conv_b + (size_t)layer * conv_dim;
-  const float4 wbc = cw[d_inner + tid];  // B|C channel tid
-  const float bbc = cb[d_inner + tid];
   float4 wx = make_float4(0.f, 0.f, 0.f, 0.f);  // x conv weights of the next group
   float bx = 0.f;
   if (tid < min(G, a.H - hc_begin) * kP) {
     wx = cw[hc_begin * kP + tid];
     bx = cb[hc_begin * kP + tid];
   }
+  __syncthreads();  // barriers initialised
+  wait_or_abort(pro_bar, 0);
+  for (int v = tid; v < n; v += THREADS) {
+    // the prep kernel checked and reported the layout; clamp again so no index leaves its table
+    ssm_node r = nodes[v];
+    for (int d = 0; d < 3; ++d)
+      if (r.tap[d] >= v || r.tap[d] < -3) r.tap[d] = -1;
+    r.depth = v == 0 ? 0 : min(max(r.depth, 0), a.max_depth);
+    nodes[v] = r;
+    rowidx[v] = tap_rows(r, v);
+  }
   __syncthreads();
   for (int v = tid; v < n; v += THREADS) {
-    int m = v;  // pathn[v][j] = ancestor of v at depth j
-    const int dv = nodes[v].depth;
-    for (int j = dv; j >= 0; --j) {
-      pathn[v * DMAX + j] = m;
-      m = m > 0 ? nodes[m].parent : 0;
-      if (m < 0) m = 0;
-    }
-    int off = 0;  // compact (v, j) pair list: prefix over earlier nodes' path lengths
+    int off = 0;
     for (int u = 0; u < v; ++u) off += nodes[u].depth + 1;
-    for (int j = 0; j <= dv; ++j) pairs[1 + off + j] = v * DMAX + j;
-    if (v == n - 1) pairs[0] = off + dv + 1;
+    poff[v] = off;
   }
-  wait_or_abort(bc_bar, 0);  // B|C input rows have landed
-  __syncthreads();
-  {  // B and C conv + SiLU for every node (thread = channel of B|C)
-    float* dst = tid < kN ? Bs + tid : Cs + (tid - kN);
-    for (int v = 0; v < n; ++v) {
-      const int4 r = rowidx[v];
-      float s = fmaf(wbc.x, bf16f(xinBC[r.x * XW + tid]), bbc);
-      s = fmaf(wbc.y, bf16f(xinBC[r.y * XW + tid]), s);
-      s = fmaf(wbc.z, bf16f(xinBC[r.z * XW + tid]), s);
-      s = fmaf(wbc.w, bf16f(xinBC[r.w * XW + tid]), s);
-      dst[v * kN] = silu_fast(s);
-    }
-  }
-  __syncthreads();
-  const int n_pairs = pairs[0];
-  {  // Gm[v][j] = C_v · B_{path_j(v)}, one warp per pair
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int k = warp; k < n_pairs; k += THREADS / 32) {
-      const int pr = pairs[1 + k];
-      const int v = pr / DMAX;
-      const int m = pathn[pr];
-      const float4 c4 = reinterpret_cast<const float4*>(Cs + v * kN)[lane];
-      const float4 b4 = reinterpret_cast<const float4*>(Bs + m * kN)[lane];
-      float s = c4.x * b4.x;
-      s = fmaf(c4.y, b4.y, s);
-      s = fmaf(c4.z, b4.z, s);
-      s = fmaf(c4.w, b4.w, s);
-      s = warp_sum(s);
-      if (lane == 0) Gm[pr] = s;
-    }
-  }
-  // (B is dead from here on; its space holds the path coefficients)
 
-  const int t_row = tid & 63;  // p
-  const int t_nd = tid >> 6;   // node quad within the tile
-  u64 acc[G][4];
+  // Z tile of a group: 8 warps x (MT m16 tiles) rows x 16 nodes, mma m16n8k8 (TF32, split 3x)
+  constexpr int MT = G / 2;
+  const int fg = lane >> 2, ft = lane & 3;  // fragment row group / thread-in-group
+  const int wrow = warp * 16 * MT;          // first state row of this warp within the group
+  const int whead = wrow / kP;              // every row of a warp belongs to one head
+  float acc[MT][2][4];
   int q = 0;  // chunk index
   for (int gi = 0; gi < g_count; ++gi) {
     const int hb = hc_begin + gi * G, heads = min(G, a.H - hb);
-    const int hl = gi * G;  // first head of the group within the CTA's head arrays
+    const int hl = gi * G;
     for (int tile = 0; tile < n_tiles; ++tile) {
-      int vrow[4];
+      int brow[2];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vrow[j] = min(tile * NT + t_nd * 4 + j, n - 1) * kN;
+      for (int nt = 0; nt < 2; ++nt) brow[nt] = min(tile * NT + nt * 8 + fg, n - 1) * CSTR;
       for (int kc = 0; kc < KCH; ++kc, ++q) {
-        if (tid == 0) produce(q + STAGES);  // refill the stage chunk q-1 used
+        if (warp == 0) produce(q + STAGES);  // refill the stage chunk q-1 used
         if (tile == 0 && kc == 0) {
-          // ---- group set-up: x conv + SiLU, Δ, S, e^S, path coefficients ----
+          // ---- group set-up: x conv + SiLU (four nodes at a time for ILP) ----
           __syncthreads();  // every warp is past the previous group's epilogue
           wait_or_abort(x_bar, gi & 1);
           if (tid < heads * kP) {
-            for (int v = 0; v < n; ++v) {
-              const int4 r = rowidx[v];
-              float s = fmaf(wx.x, bf16f(xinX[r.x * XW + tid]), bx);
-              s = fmaf(wx.y, bf16f(xinX[r.y * XW + tid]), s);
-              s = fmaf(wx.z, bf16f(xinX[r.z * XW + tid]), s);
-              s = fmaf(wx.w, bf16f(xinX[r.w * XW + tid]), s);
-              xs[v * ROWS + tid] = silu_fast(s);
+            const uint16_t* __restrict__ xi = xinX + tid;
+            float* __restrict__ xo = xs + tid;
+            int v = 0;
+            for (; v + 4 <= n; v += 4) {
+              float r[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int4 t = rowidx[v + u];
+                r[u][0] = bf16f(xi[t.x * XW]);
+                r[u][1] = bf16f(xi[t.y * XW]);
+                r[u][2] = bf16f(xi[t.z * XW]);
+                r[u][3] = bf16f(xi[t.w * XW]);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; ++u)
+                xo[(v + u) * ROWS] = silu_fast(conv4_acc(wx, bx, r[u][0], r[u][1], r[u][2], r[u][3]));
+            }
+            for (; v < n; ++v) {
+              const int4 t = rowidx[v];
+              xo[v * ROWS] = silu_fast(conv4_acc(wx, bx, bf16f(xi[t.x * XW]), bf16f(xi[t.y * XW]),
+                                                 bf16f(xi[t.z * XW]), bf16f(xi[t.w * XW])));
             }
           }
           if (gi + 1 < g_count) {  // prefetch the next group's x conv weights
@@ -344,93 +505,99 @@ __global__ void __launch_bounds__(THREADS, 2) tree_verify_kernel(VerifyArgs a, c
               bx = cb[hn * kP + tid];
             }
           }
-          for (int i = tid; i < n * G; i += THREADS) {
-            const int v = i / G, g = i % G;
-            dl[i] = g < heads ? softplus_f(dts[v * (MAX_GPC * G) + hl + g] + pbias[hl + g]) : 0.f;
-          }
-          __syncthreads();
-          for (int i = tid; i < n * G; i += THREADS) {
-            const int v = i / G, g = i % G;
-            const float A = g < heads ? pA[hl + g] : 0.f;
-            float s = 0.f;
-            const int dv = nodes[v].depth;
-            for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * G + g], A, s);
-            Sv[i] = s;
-            eS[i] = expf(s);
-          }
-          __syncthreads();
-          for (int i = tid; i < n_pairs * G; i += THREADS) {
-            const int pr = pairs[1 + i / G], g = i % G;
-            const int v = pr / DMAX, m = pathn[pr];
-            coef[pr * G + g] = expf(Sv[v * G + g] - Sv[m * G + g]) * dl[m * G + g] * Gm[pr];
-          }
           __syncthreads();
         }
         if (kc == 0) {
 #pragma unroll
-          for (int i = 0; i < G; ++i)
+          for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
         }
         const int slot = q % STAGES;
         wait_or_abort(full_bar(slot), (q / STAGES) & 1);
-        const float* st = stage + slot * ROWS * SROW + t_row * SROW;
-        const float* cs = Cs + kc * KC;
-        // 64-byte swizzle: the 16-byte piece index is XORed with address bits 7..8
-        // (rows i*64 + t_row, 4 KB apart, share them)
-        const int swz = (smem_u32(st) >> 7) & 3;
+        // A fragment rows of this lane: wrow + 16*mt + fg (+8); the copy engine's 64-byte
+        // swizzle XORs the 16-byte piece index with shared-address bits 7..8
+        const unsigned char* st = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
 #pragma unroll
-        for (int k4 = 0; k4 < KC / 4; ++k4) {
-          ulonglong2 hv[G], cv[4];
+        for (int ks = 0; ks < KC / 8; ++ks) {
+          uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
-          for (int i = 0; i < G; ++i)
-            hv[i] = *reinterpret_cast<const ulonglong2*>(st + i * kP * SROW + ((k4 ^ swz) * 4));
+          for (int nt = 0; nt < 2; ++nt) {
+            const float* cb0 = Cs + brow[nt] + kc * KC + ks * 8 + ft;
+            split_tf32(cb0[0], bhi[nt][0], blo[nt][0]);
+            split_tf32(cb0[4], bhi[nt][1], blo[nt][1]);
+          }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) cv[j] = *reinterpret_cast<const ulonglong2*>(cs + vrow[j] + k4 * 4);
+          for (int mt = 0; mt < MT; ++mt) {
+            const unsigned char* r0 = st + (wrow + mt * 16 + fg) * (SROW * 4);
+            const int swz = (smem_u32(r0) >> 7) & 3;  // rows r0 and r0+8 (512 B apart) share it
+            const int o0 = (((2 * ks) ^ swz) << 4) + ft * 4, o1 = (((2 * ks + 1) ^ swz) << 4) + ft * 4;
+            uint32_t ahi[4], alo[4];
+            split_tf32(*reinterpret_cast<const float*>(r0 + o0), ahi[0], alo[0]);
+            split_tf32(*reinterpret_cast<const float*>(r0 + 8 * SROW * 4 + o0), ahi[1], alo[1]);
+            split_tf32(*reinterpret_cast<const float*>(r0 + o1), ahi[2], alo[2]);
+            split_tf32(*reinterpret_cast<const float*>(r0 + 8 * SROW * 4 + o1), ahi[3], alo[3]);
 #pragma unroll
-          for (int i = 0; i < G; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              acc[i][j] = ffma2(hv[i].x, cv[j].x, acc[i][j]);
-              acc[i][j] = ffma2(hv[i].y, cv[j].y, acc[i][j]);
+            for (int nt = 0; nt < 2; ++nt) {
+              mma_tf32(acc[mt][nt], alo, bhi[nt]);
+              mma_tf32(acc[mt][nt], ahi, blo[nt]);
+              mma_tf32(acc[mt][nt], ahi, bhi[nt]);
             }
+          }
         }
         __syncwarp();
-        if ((tid & 31) == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
-        if (kc == KCH - 1) {
+        if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
+        if (kc == KCH - 1 && whead < heads) {
           // ---- epilogue: y = e^{S_v}·Z + Σ_path coef·x_m + D·x_v ----
+          const float Dh = pD[hl + whead];
+          const float* eh = eSg + ((gi & 1) * G + whead) * W.NP;
+          const float* chd = coefg + ((gi & 1) * G + whead) * W.PP;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int v = tile * NT + t_nd * 4 + j;
-            if (v >= n) continue;
-            float yv[G];
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int i = 0; i < G; ++i) yv[i] = eS[v * G + i] * pair_sum(acc[i][j]);
-            const int dv = nodes[v].depth;
-            for (int jj = 0; jj <= dv; ++jj) {
-              const int pr = v * DMAX + jj;
-              const float* xm = xs + pathn[pr] * ROWS + t_row;
-              const typename CoefVec<G>::T cf = *reinterpret_cast<const typename CoefVec<G>::T*>(coef + pr * G);
+            for (int c = 0; c < 2; ++c) {
+              const int v = tile * NT + nt * 8 + 2 * ft + c;
+              if (v >= n) continue;
+              const float es = eh[v];
+              float yv[MT][2];
 #pragma unroll
-              for (int i = 0; i < G; ++i) yv[i] = fmaf(CoefVec<G>::at(cf, i), xm[i * kP], yv[i]);
+              for (int mt = 0; mt < MT; ++mt) {
+                yv[mt][0] = es * acc[mt][nt][c];
+                yv[mt][1] = es * acc[mt][nt][2 + c];
+              }
+              const int dv = nodes[v].depth;
+              const int pb = poff[v];
+              for (int jj = 0; jj <= dv; ++jj) {
+                const float cf = chd[pb + jj];
+                const float* xm = xs + pathn[v * DMAX + jj] * ROWS + wrow + fg;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  yv[mt][0] = fmaf(cf, xm[mt * 16], yv[mt][0]);
+                  yv[mt][1] = fmaf(cf, xm[mt * 16 + 8], yv[mt][1]);
+                }
+              }
+              const float* xv = xs + v * ROWS + wrow + fg;
+              float* yrow = a.y + ((size_t)inst * n + v) * d_inner + hb * kP + wrow + fg;
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                yrow[mt * 16] = fmaf(Dh, xv[mt * 16], yv[mt][0]);
+                yrow[mt * 16 + 8] = fmaf(Dh, xv[mt * 16 + 8], yv[mt][1]);
+              }
             }
-            float* yrow = a.y + ((size_t)inst * n + v) * d_inner + hb * kP + t_row;
-            const float* xv = xs + v * ROWS + t_row;
-#pragma unroll
-            for (int i = 0; i < G; ++i)
-              if (i < heads) yrow[i * kP] = fmaf(pD[hl + i], xv[i * kP], yv[i]);
-          }
         }
       }
     }
   }
-  if (tid == 0 && s_abort) {  // give copies still in flight a bounded chance to land
+  if (warp == 0 && s_abort) {  // give copies still in flight a bounded chance to land
     for (int c = pf_n - STAGES > 0 ? pf_n - STAGES : 0; c < pf_n; ++c) mbar_wait(full_bar(c % STAGES), (c / STAGES) & 1);
+    mbar_wait(x_bar, (g_count - 1) & 1);
   }
 }
 
 int g_sms[64] = {0};
-int g_configured[2][64] = {{0}};
+int g_configured[3][64] = {{0}};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -444,21 +611,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int G>
-cudaError_t launch_g(const VerifyArgs& a0, cudaStream_t s, int dev) {
-  VerifyArgs a = a0;
-  const Smem L = smem_layout<G>(a.n);
-  const int gi = G == 4 ? 0 : 1;
-  if (dev >= 64 || g_configured[gi][dev] < L.total) {
-    cudaError_t e = cudaFuncSetAttribute(tree_verify_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+template <typename K>
+cudaError_t ensure_smem(K kernel, int idx, int dev, int bytes) {
+  if (dev >= 64 || g_configured[idx][dev] < bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(tree_verify_kernel<G>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    if (dev < 64) g_configured[gi][dev] = L.total;
+    if (dev < 64) g_configured[idx][dev] = bytes;
   }
+  return cudaSuccess;
+}
+
+template <int G>
+cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStream_t s, int dev) {
+  VerifyArgs a = a0;
+  const Ws W = ws_layout(a.n, a.max_depth, a.H);
+  const Smem L = smem_layout<G>(a.n, W.PP, W.NP);
+  cudaError_t e = ensure_smem(tree_verify_kernel<G>, G == 4 ? 0 : 1, dev, L.total);
+  if (e != cudaSuccess) return e;
   int sms = dev < 64 ? g_sms[dev] : 0;
   if (sms == 0) {
-    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     if (dev < 64) g_sms[dev] = sms;
   }
@@ -474,9 +648,12 @@ cudaError_t launch_g(const VerifyArgs& a0, cudaStream_t s, int dev) {
     const int parts = (NG + target - 1) / target;
     gpc = (NG + parts - 1) / parts;
   }
+  if (const char* o = getenv("SSM_VERIFY_GROUPS_PER_CTA")) {  // tuning / test override
+    const int v = atoi(o);
+    if (v >= 1 && v <= MAX_GPC) gpc = v;
+  }
   a.gpc = gpc;
   const long long blocks = inst * ((NG + gpc - 1) / gpc);
-  if (blocks == 0) return cudaSuccess;
   // h0 as a 2-D tensor: rows (instance, head, p), 128 fp32 columns; one box = G*64 rows x 16 columns
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -489,30 +666,45 @@ cudaError_t launch_g(const VerifyArgs& a0, cudaStream_t s, int dev) {
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  tree_verify_kernel<G><<<(unsigned)blocks, THREADS, L.total, s>>>(a, tmap);
+  tree_verify_kernel<G><<<(unsigned)blocks, THREADS, L.total, s>>>(a, ws, tmap);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-// heads per group used for n nodes (4 while the shared-memory plan fits, else 2)
-int verify_smem_bytes(int n, int* heads_per_group) {
-  const int t4 = smem_layout<4>(n).total;
-  if (t4 <= SMEM_LIMIT) {
-    if (heads_per_group) *heads_per_group = 4;
-    return t4;
-  }
-  if (heads_per_group) *heads_per_group = 2;
-  return smem_layout<2>(n).total;
+size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst) {
+  return ws_layout(n, max_depth, H).stride * (size_t)n_inst;
 }
 
-cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
+// heads per group used for n nodes (4 while the shared-memory plan fits, else 2; 0 if neither fits)
+int verify_heads_per_group(int n, int max_depth, int H) {
+  const Ws W = ws_layout(n, max_depth, H);
+  if (smem_layout<4>(n, W.PP, W.NP).total <= SMEM_LIMIT) return 4;
+  if (smem_layout<2>(n, W.PP, W.NP).total <= SMEM_LIMIT) return 2;
+  return 0;
+}
+
+int verify_prep_smem_bytes(int n, int max_depth, int H) {
+  const Ws W = ws_layout(n, max_depth, H);
+  return prep_layout(n, H, W.PP).total;
+}
+
+cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int G = 4;
-  verify_smem_bytes(a.n, &G);
-  return G == 4 ? launch_g<4>(a, s, dev) : launch_g<2>(a, s, dev);
+  const long long inst = (long long)a.n_seq * a.L;
+  if (inst == 0) return cudaSuccess;
+  const int G = verify_heads_per_group(a.n, a.max_depth, a.H);
+  if (G == 0) return cudaErrorInvalidValue;
+  const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H);
+  e = ensure_smem(tree_prep_kernel, 2, dev, prep_bytes);
+  if (e != cudaSuccess) return e;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  tree_prep_kernel<<<(unsigned)inst, THREADS, prep_bytes, s>>>(a, ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return G == 4 ? launch_main<4>(a, ws, s, dev) : launch_main<2>(a, ws, s, dev);
 }
 
 }  // namespace ssmtree

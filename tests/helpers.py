@@ -68,14 +68,16 @@ def upload_tree_batch(b, w):
 def run_tree_step(d, max_path=None, commit=True):
     """verify -> accept -> commit through the C ABI; returns host copies."""
     import torch
-    from speculative_decoding_mamba2_gb300 import ssm_accept_path, ssm_commit, ssm_tree_verify
+    from speculative_decoding_mamba2_gb300 import (ssm_accept_path, ssm_commit, ssm_tree_verify,
+                                                   ssm_tree_verify_workspace_size)
     dims, S, n = d["dims"], d["n_seq"], d["n"]
     I = S * dims.n_layers
     max_path = d["depth"] + 1 if max_path is None else max_path
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     y = torch.full((I, n, dims.d_inner), float("nan"), device="cuda")
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, d["depth"]), dtype=torch.uint8, device="cuda")
     ssm_tree_verify(dims, d["params"], S, n, d["depth"], d["layout"], d["xBC"], d["dt"], d["h0"], d["ring"],
-                    d["ring_head"], y, status)
+                    d["ring_head"], y, ws, status)
     path = torch.empty((S, max_path), dtype=torch.int32, device="cuda")
     plen = torch.empty(S, dtype=torch.int32, device="cuda")
     bonus = torch.empty(S, dtype=torch.int32, device="cuda")

@@ -30,8 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     fns = declared_functions()
-    for name in ["ssm_tree_layout_build", "ssm_tree_verify", "ssm_accept_path", "ssm_commit", "ssm_draft_step",
-                 "ssm_replay", "ssm_last_error", "ssm_version"]:
+    for name in ["ssm_tree_layout_build", "ssm_tree_verify", "ssm_tree_verify_workspace_size", "ssm_accept_path",
+                 "ssm_commit", "ssm_draft_step", "ssm_replay", "ssm_last_error", "ssm_version"]:
         assert name in fns
 
 
@@ -108,10 +108,11 @@ def _prm(null=False):
 FAKE = ctypes.c_void_p(16)  # never dereferenced: every call below fails validation first
 
 
-def _verify(L, dims, prm, n_seq=1, n=16, depth=4, ptr=FAKE):
+def _verify(L, dims, prm, n_seq=1, n=16, depth=4, ptr=FAKE, ws_bytes=1 << 30):
     return L.ssm_tree_verify(ctypes.byref(dims) if dims is not None else None,
                              ctypes.byref(prm) if prm is not None else None,
-                             n_seq, n, depth, ptr, ptr, ptr, ptr, ptr, ptr, ptr, None, None)
+                             n_seq, n, depth, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ctypes.c_size_t(ws_bytes),
+                             None, None)
 
 
 def test_verify_validation(L):
@@ -130,6 +131,14 @@ def test_verify_validation(L):
     assert _verify(L, _dims(), _prm(), n_seq=-1) == B.SSM_ERR_INVALID_ARG
     # an empty batch is a valid no-op and enqueues nothing
     assert _verify(L, _dims(), _prm(), n_seq=0, ptr=None) == B.SSM_OK
+    # workspace: size query, too-small and misaligned workspaces are rejected before any CUDA call
+    need = B.ssm_tree_verify_workspace_size(B.Dims(n_heads=4, n_layers=2), 1, 16, 4)
+    assert need > 0 and need % 16 == 0
+    assert _verify(L, _dims(), _prm(), ws_bytes=need - 16) == B.SSM_ERR_CAPACITY
+    assert _verify(L, _dims(), _prm(), ptr=ctypes.c_void_p(24)) == B.SSM_ERR_INVALID_ARG
+    assert B.ssm_tree_verify_workspace_size(B.Dims(n_heads=4, n_layers=2), 3, 16, 4) == 3 * need
+    with pytest.raises(B.SSMError):
+        B.ssm_tree_verify_workspace_size(B.Dims(n_heads=4, n_layers=2), 1, 65, 4)
 
 
 def test_accept_commit_draft_replay_validation(L):

@@ -79,6 +79,17 @@ def test_tree_shapes(spec):
     check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
 
 
+@pytest.mark.parametrize("gpc", ["2", "3"])
+def test_several_head_groups_per_cta(gpc, monkeypatch):
+    # one CTA walks several head groups (the last one ragged): inputs of the next group
+    # arrive while the current group's epilogue still reads its own
+    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    w = Workload(55, "groups", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
 def test_single_node_tree():
     w = Workload(52, "root only", Shape(H=4), n_layers=3, batch=2, trees=(("chain", 1),))
     b = batch(w)
