@@ -217,6 +217,27 @@ int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
                const float *log_delta, const float *log_B, const float *log_x, int32_t *log_len, float *h_ckpt,
                int32_t *ring_head, int32_t *dev_status, void *stream);
 
+/*
+ * ssm_tree_verify_noalloc -- ssm_tree_verify for callers that cannot allocate
+ * device memory (a runtime that gives a plugin only the current op's tensors
+ * and owns all other device memory, an embedding with allocation forbidden
+ * after start-up, a C-ABI-only host with no allocator of its own).  The pages
+ * have no counterpart: this is a deployment convenience of this library.
+ * Same arguments and results as ssm_tree_verify, without the workspace: the
+ * scratch is one array of SSM_NOALLOC_WORKSPACE_BYTES bytes compiled into the
+ * library, held by every GPU that loads it until the process exits.  A batch
+ * whose ssm_tree_verify_workspace_size() exceeds that gets SSM_ERR_CAPACITY.
+ * Nothing here calls cudaMalloc/cudaFree or any allocating routine.  The first
+ * call on a device looks up the array's address (cudaGetSymbolAddress) with
+ * that device current; make it before any stream capture.  All calls share the
+ * array, so calls whose GPU work overlaps race; serialise them.
+ */
+#define SSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
+int ssm_tree_verify_noalloc(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
+                            int32_t max_depth, const ssm_node *layout, const uint16_t *xBC, const uint16_t *dt,
+                            const float *h0, const uint16_t *ring, const int32_t *ring_head, float *y,
+                            int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,11 +16,12 @@ from .binding import (  # noqa: F401
     ssm_replay,
     ssm_tree_layout_build,
     ssm_tree_verify,
+    ssm_tree_verify_noalloc,
     ssm_tree_verify_workspace_size,
     ssm_version,
 )
 from .binding import (  # noqa: F401
     SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_BAD_TREE, SSM_ERR_CAPACITY, SSM_ERR_CUDA, SSM_ERR_RANGE,
     SSM_STATUS_BAD_LAYOUT, SSM_STATUS_PATH_RANGE, SSM_STATUS_K_RANGE, SSM_STATUS_WALK_TRUNCATED,
-    SSM_MAX_NODES, SSM_MAX_DEPTH, SSM_MAX_PATH, NODE_WORDS,
+    SSM_STATUS_TIMEOUT, SSM_MAX_NODES, SSM_MAX_DEPTH, SSM_MAX_PATH, SSM_NOALLOC_WORKSPACE_BYTES, NODE_WORDS,
 )

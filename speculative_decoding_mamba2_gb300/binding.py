@@ -32,6 +32,7 @@ SSM_STATUS_TIMEOUT = 16
 SSM_MAX_NODES = 64
 SSM_MAX_DEPTH = 15
 SSM_MAX_PATH = 256
+SSM_NOALLOC_WORKSPACE_BYTES = 16 << 20
 NODE_WORDS = 8  # int32 words per ssm_node record
 
 
@@ -82,6 +83,7 @@ _SIGS = {
     "ssm_tree_layout_build": (ctypes.c_int, [_P, _I, _I, _I, _I, _P, _P]),
     "ssm_tree_verify": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P]),
     "ssm_tree_verify_workspace_size": (ctypes.c_size_t, [_P, _I, _I, _I]),
+    "ssm_tree_verify_noalloc": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_accept_path": (ctypes.c_int, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -204,6 +206,24 @@ def ssm_tree_verify(dims: Dims, params: dict, n_seq: int, n_nodes: int, max_dept
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
         _dev(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _opt_status(status), _stream(stream, h0)))
+
+
+def ssm_tree_verify_noalloc(dims: Dims, params: dict, n_seq: int, n_nodes: int, max_depth: int, layout, xBC, dt, h0,
+                            ring, ring_head, y, status=None, stream=None):
+    """ssm_tree_verify for callers that cannot allocate device memory: the scratch
+    is the library's own SSM_NOALLOC_WORKSPACE_BYTES array (shared by every call;
+    overlapping calls race).  Batches needing more raise SSMError(SSM_ERR_CAPACITY)."""
+    d, I, n = dims, n_seq * dims.n_layers, n_nodes
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    _check(lib().ssm_tree_verify_noalloc(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, max_depth,
+        _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+        _dev(h0, "h0", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+        _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
         _opt_status(status), _stream(stream, h0)))
 
 
