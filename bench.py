@@ -204,7 +204,7 @@ class OracleRunner:
         self.pool.join()
 
 
-def cpu_baseline(w, steps=3):
+def cpu_baseline(w, steps=8):
     r = OracleRunner(w)
     r.step()  # warm the workers (imports)
     units = secs = 0.0
@@ -403,6 +403,12 @@ def run_ours(args, w):
     if not args.no_e2e:
         e2e = run_e2e(args, w, b, dims, prm, h, ring, head, ws, dev, stream, world)
 
+    # ---- draft side (the draft model's own rounds) ----
+    draft = None
+    if not args.no_draft:
+        del y, ws
+        draft = run_draft(args, dev, stream, peak, world, rank)
+
     if status.item() != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
     if rank == 0:
@@ -415,12 +421,107 @@ def run_ours(args, w):
                 "roofline": roofline, "kernels": kernels, "step_GB/s": step_bytes / ms / 1e6,
                 "step_frac_of_hbm_peak": step_bytes / ms / 1e6 / peak,
                 "e2e": e2e, "gpu_launches": 4 * args.steps, "clocks": clk}
+        if draft is not None:
+            line["draft"] = draft
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def draft_step_bytes(H, P, N, n_inst, n_layers):
+    """Algorithmic bytes of one ssm_draft_step call: state read + write, the conv window
+    (3 ring rows) and the new row, dt, the ring write, the log row, y; params once per layer."""
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    per = (2 * H * P * N * 4 + 3 * conv_dim * 2 + conv_dim * 2 + H * 2 + conv_dim * 2 + (H + N + d_inner) * 4
+           + d_inner * 4 + 8)
+    return n_inst * per + n_layers * params_bytes_per_layer(H, P, N)
+
+
+def replay_bytes(H, P, N, n_inst, k_mean):
+    d_inner = H * P
+    return n_inst * (2 * H * P * N * 4 + k_mean * (H + N + d_inner) * 4 + 12)
+
+
+def run_draft(args, dev, stream, peak, world, rank):
+    """Draft rounds on the Mamba2-370M draft workload (48 layers, batch 1 per rank):
+    16 chained ssm_draft_step calls (one launch each, all layers batched), then
+    ssm_replay to the sampled accepted position.  Timed with CUDA events."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import Dims, ssm_draft_step, ssm_replay
+    from synth import draft_batch, workload
+    wd = workload(1)
+    seqs = shard_sequences(wd.batch, rank)
+    b = draft_batch(wd, seqs=seqs)
+    S, L, T = len(seqs), wd.n_layers, wd.draft_steps
+    H, P, N = wd.shape.H, wd.shape.P, wd.shape.N
+    I = S * L
+    dims = Dims(n_heads=H, n_layers=L, ring_cap=wd.ring_cap)
+    prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in b["params"].items()}
+    bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    xs = bf16(b["xBC"]).view(T, I, dims.conv_dim)
+    dts = bf16(b["dt"]).view(T, I, H)
+    h_ckpt0 = torch.from_numpy(b["h0"]).to(dev).view(I, H, P, N)
+    h_ckpt = h_ckpt0.clone()
+    h_work = torch.empty_like(h_ckpt)
+    ring0 = bf16(b["ring"]).view(I, wd.ring_cap, dims.conv_dim)
+    ring = ring0.clone()
+    head0 = torch.from_numpy(b["ring_head"]).to(dev).view(I)
+    head = head0.clone()
+    log_d = torch.zeros(I, T, H, device=dev)
+    log_b = torch.zeros(I, T, N, device=dev)
+    log_x = torch.zeros(I, T, dims.d_inner, device=dev)
+    log_len = torch.zeros(I, dtype=torch.int32, device=dev)
+    y = torch.empty(I, dims.d_inner, device=dev)
+    # replay every logged step (k = draft_steps): the synthetic accepted position can be 0,
+    # which would time bookkeeping only
+    k = torch.full((S,), T, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def round_(ev=None):
+        # each round restarts from the same checkpoint so every round does the same work
+        h_ckpt.copy_(h_ckpt0)
+        ring.copy_(ring0)
+        head.copy_(head0)
+        if ev is not None:
+            ev[0].record(stream)
+        for t in range(T):
+            ssm_draft_step(dims, prm, S, t, T, xs[t], dts[t], h_ckpt if t == 0 else h_work, h_work, ring, head,
+                           log_d, log_b, log_x, log_len, y, status)
+        if ev is not None:
+            ev[1].record(stream)
+        ssm_replay(dims, prm, S, T, k, log_d, log_b, log_x, log_len, h_ckpt, head, status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        round_()
+    torch.cuda.synchronize()
+    rounds = max(5, min(args.steps, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(rounds)]
+    for r in range(rounds):
+        round_(evs[r])
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the draft rounds")
+    step_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) / T
+    replay_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms = max_over_ranks(step_ms, world, dev)
+    replay_ms = max_over_ranks(replay_ms, world, dev)
+    sb = draft_step_bytes(H, P, N, I, L)
+    rb = replay_bytes(H, P, N, I, T)
+    state_mb = I * H * P * N * 4 / 1e6
+    return {"workload": wd.name, "sequences_per_gpu": S, "layers": L, "draft_steps": T,
+            "value": S * L * world / (step_ms / 1e3), "unit": "draft token-layer updates/s",
+            "ms_per_draft_step": step_ms, "ms_replay": replay_ms, "replay_k": T,
+            "draft_step": {"bytes": sb, "GB/s": sb / step_ms / 1e6, "frac_of_hbm_peak": sb / step_ms / 1e6 / peak},
+            "replay": {"bytes": rb, "GB/s": rb / replay_ms / 1e6, "frac_of_hbm_peak": rb / replay_ms / 1e6 / peak},
+            "note": f"the draft state ({state_mb:.0f} MB) fits in L2, so draft steps run from L2; "
+                    "a fraction above 1 of the HBM peak is possible and expected"}
 
 
 def run_e2e(args, w, b, dims, prm, h, ring, head, ws, dev, stream, world):
@@ -497,6 +598,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-draft", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

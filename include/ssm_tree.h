@@ -64,8 +64,9 @@ extern "C" {
                                  /* of that call are invalid)                   */
 
 /* Limits of this build (checked on the host; larger inputs get SSM_ERR_CAPACITY). */
-#define SSM_MAX_NODES 64         /* nodes per tree for ssm_tree_verify          */
-#define SSM_MAX_DEPTH 15         /* deepest node below the root                 */
+#define SSM_MAX_NODES 64         /* nodes per branching tree (ssm_tree_verify)  */
+#define SSM_MAX_DEPTH 15         /* deepest node below the root (branching)     */
+#define SSM_MAX_CHAIN_NODES 4096 /* nodes of a chain (parent[v] = v-1)          */
 #define SSM_MAX_PATH 256         /* accept / commit path length                 */
 
 typedef struct ssm_dims {
@@ -124,7 +125,10 @@ int ssm_tree_layout_build(const int32_t *parent, int32_t n_seq, int32_t n_nodes,
  * h_v is the state after the node's root-to-node path applied to h0.  The
  * per-node states never reach memory; only h0, the inputs and y do.
  *   layout     device ssm_node [S][n] (from ssm_tree_layout_build), max_depth
- *              = its deepest node (<= SSM_MAX_DEPTH); n <= SSM_MAX_NODES.
+ *              = its deepest node.  Branching trees: n <= SSM_MAX_NODES and
+ *              max_depth <= SSM_MAX_DEPTH.  A tree with max_depth = n-1 is a
+ *              chain; chains up to SSM_MAX_CHAIN_NODES are verified by walking
+ *              them with the state on chip (no workspace needed).
  *   xBC        device bf16 [I][n][conv_dim]  pre-conv rows of the tree nodes
  *   dt         device bf16 [I][n][H]         raw dt
  *   h0         device fp32 [I][H][P][N]      committed state (read only)

@@ -32,6 +32,7 @@ SSM_STATUS_TIMEOUT = 16
 SSM_MAX_NODES = 64
 SSM_MAX_DEPTH = 15
 SSM_MAX_PATH = 256
+SSM_MAX_CHAIN_NODES = 4096
 SSM_NOALLOC_WORKSPACE_BYTES = 16 << 20
 NODE_WORDS = 8  # int32 words per ssm_node record
 

@@ -19,7 +19,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "layout.cpp"]
+SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "layout.cpp"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(INCLUDE, "ssm_tree.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 LIBNAME = "libssmtree.so"

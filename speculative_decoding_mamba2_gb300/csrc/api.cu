@@ -65,12 +65,21 @@ extern "C" int32_t ssm_version(void) { return 100; }
 extern "C" const char* ssm_last_error(void) { return g_error.c_str(); }
 
 namespace {
+// A tree whose deepest node sits at depth n-1 is a chain; long chains take the chain kernel.
+bool long_chain(int32_t n_nodes, int32_t max_depth) {
+  return max_depth == n_nodes - 1 && max_depth > SSM_MAX_DEPTH;
+}
+
 int check_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_seq, int32_t n_nodes, int32_t max_depth) {
   if (int rc = check_dims(fn, dims, false, nullptr)) return rc;
   if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
   if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
-  if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
   if (max_depth < 0 || max_depth >= n_nodes) return fail(SSM_ERR_RANGE, fn, "max_depth must be in [0, n_nodes)");
+  if (long_chain(n_nodes, max_depth)) {
+    if (n_nodes > SSM_MAX_CHAIN_NODES) return fail(SSM_ERR_CAPACITY, fn, "chain longer than SSM_MAX_CHAIN_NODES");
+    return SSM_OK;
+  }
+  if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
   if (max_depth > SSM_MAX_DEPTH) return fail(SSM_ERR_CAPACITY, fn, "max_depth exceeds SSM_MAX_DEPTH");
   if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads) == 0 ||
       verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads) > 232448)
@@ -84,6 +93,7 @@ extern "C" size_t ssm_tree_verify_workspace_size(const ssm_dims* dims, int32_t n
   const char* fn = "ssm_tree_verify_workspace_size";
   if (check_verify_shape(fn, dims, n_seq, n_nodes, max_depth) != SSM_OK) return 0;
   g_error.clear();
+  if (long_chain(n_nodes, max_depth)) return 16;  // the chain kernel needs no workspace
   const size_t b = verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers);
   return b ? b : 16;
 }
@@ -100,7 +110,9 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
   if (((uintptr_t)xBC | (uintptr_t)h0 | (uintptr_t)ring | (uintptr_t)layout | (uintptr_t)workspace) & 15)
     return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h0, ring, layout and workspace must be 16-byte aligned");
-  if (workspace_bytes < verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers))
+  const bool chain = long_chain(n_nodes, max_depth);
+  if (!chain &&
+      workspace_bytes < verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers))
     return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_tree_verify_workspace_size()");
   VerifyArgs a;
   a.gpc = 1;
@@ -123,7 +135,8 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   a.ring_head = ring_head;
   a.y = y;
   a.status = dev_status;
-  return finish(fn, launch_verify(a, workspace, (cudaStream_t)stream));
+  return finish(fn, chain ? launch_chain_verify(a, (cudaStream_t)stream)
+                         : launch_verify(a, workspace, (cudaStream_t)stream));
 }
 
 extern "C" int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node* layout,
@@ -162,6 +175,8 @@ extern "C" int ssm_commit(const ssm_dims* dims, const ssm_params* prm, int32_t n
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!layout || !path || !path_len || !xBC || !dt || !h || !ring || !ring_head)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)xBC | (uintptr_t)h | (uintptr_t)ring) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h and ring must be 16-byte aligned");
   CommitArgs a;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
@@ -199,6 +214,7 @@ extern "C" int ssm_draft_step(const ssm_dims* dims, const ssm_params* prm, int32
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!xBC_t || !dt_t || !h_in || !h_out || !ring || !ring_head || !log_delta || !log_B || !log_x || !log_len || !y)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)h_in | (uintptr_t)h_out) & 15) return fail(SSM_ERR_INVALID_ARG, fn, "h_in and h_out must be 16-byte aligned");
   DraftArgs a;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
@@ -237,6 +253,7 @@ extern "C" int ssm_replay(const ssm_dims* dims, const ssm_params* prm, int32_t n
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!k || !log_delta || !log_B || !log_x || !log_len || !h_ckpt || !ring_head)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if ((uintptr_t)h_ckpt & 15) return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt must be 16-byte aligned");
   ReplayArgs a;
   a.H = dims->n_heads;
   a.L = dims->n_layers;

@@ -240,7 +240,10 @@ __global__ void ring_advance_kernel(CommitArgs a) {
     const int v = nodes3[j];
     if (v < 0) continue;
     const int pos = ring_pos(s_head, s_len - 3 + j, a.R);
-    for (int c = threadIdx.x; c < conv_dim; c += blockDim.x) ring[(size_t)pos * conv_dim + c] = xbc[(size_t)v * conv_dim + c];
+    // rows are conv_dim * 2 bytes = 16-byte multiples (conv_dim = 64*H + 256)
+    const uint4* src = reinterpret_cast<const uint4*>(xbc + (size_t)v * conv_dim);
+    uint4* dst = reinterpret_cast<uint4*>(ring + (size_t)pos * conv_dim);
+    for (int c = threadIdx.x; c < conv_dim / 8; c += blockDim.x) dst[c] = src[c];
   }
   __syncthreads();
   if (threadIdx.x == 0) a.ring_head[inst] = s_head + s_len;

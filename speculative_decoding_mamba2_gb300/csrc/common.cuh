@@ -201,6 +201,7 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst);
 int verify_heads_per_group(int n, int max_depth, int H);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H);
+cudaError_t launch_chain_verify(const VerifyArgs& a, cudaStream_t s);
 
 struct AcceptArgs {
   int n_seq, n, max_path;

@@ -154,6 +154,40 @@ def test_chain_accept_and_commit_256():
             assert int(head[i * 2 + j]) == head_ref
 
 
+def _chain_reference(b, i, j):
+    """Oracle outputs of a chain by sequential one-token steps (pinned equal to the
+    oracle's chain verify in test_oracle_pins.test_draft_chain_equals_chain_verify)."""
+    prm = params_at(b["params"], j)
+    h = b["h0"][i, j].astype(np.float64)
+    ring = f64(b["ring"][i, j])
+    head = int(b["ring_head"][i, j])
+    xs, dts = f64(b["xBC"][i, j]), f64(b["dt"][i, j])
+    ys = []
+    for t in range(len(xs)):
+        h, y, ring, _ = oracle.draft_step(prm, xs[t], dts[t], h, ring, head, t)
+        ys.append(y)
+    return np.stack(ys)
+
+
+@pytest.mark.parametrize("n", [17, 40])
+def test_chain_kernel_small(n):
+    # chains deeper than the branching-tree limit take the on-chip walk
+    w = Workload(56, "chain", Shape(H=5), n_layers=2, batch=2, trees=(("chain", n),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w), max_path=n)
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
+def test_config4_chain_256_sampled():
+    w = workload(4)
+    b = batch(w, seqs=[0, 63], layers=[0, 47], tree=1)
+    out = run_tree_step(upload_tree_batch(b, w), max_path=256, commit=False)
+    for i, j in [(0, 0), (1, 1)]:
+        ref = _chain_reference(b, i, j)
+        assert rel_err(out["y"][i * 2 + j].double().cpu().numpy(), ref) <= TOL, (i, j)
+    assert torch.isfinite(out["y"]).all()
+
+
 def test_delta_zero_keeps_state_exactly():
     w = Workload(53, "dt=-inf", Shape(H=4), n_layers=1, batch=2, trees=(("random", 16, 3, 4),))
     b = batch(w)
