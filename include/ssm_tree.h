@@ -188,6 +188,41 @@ int ssm_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
                void *stream);
 
 /*
+ * ssm_commit_verify -- ssm_commit of the previous step's accepted path
+ * followed by ssm_tree_verify of the next tree, in one pass over the state.
+ * SpecMamba page §3.1 (selective recomputation of the accepted path) and §3.2
+ * (FIFO tree verification): the commit is a rank-len update of h, so it is
+ * applied to each state chunk as the verify streams it in; h is read once and
+ * written once, where the separate calls read it twice and write it once.
+ * Results equal ssm_commit(prev...) then ssm_tree_verify(next...) up to fp32
+ * rounding order.  The pages describe the two steps, not this schedule.
+ *   prev_n_nodes, prev_layout       the previous tree (n' nodes): ssm_node [S][n']
+ *   prev_max_path                   row stride of prev_path, 1 <= .. <= SSM_MAX_DEPTH+1
+ *   prev_path, prev_path_len        device int32 [S][prev_max_path], [S] (ssm_accept_path)
+ *   prev_xBC, prev_dt               device bf16 [I][n'][conv_dim], [I][n'][H]: the previous
+ *                                   tree's inputs (only the accepted path's rows are read)
+ *   n_nodes .. dt                   the next tree, as for ssm_tree_verify (max_depth <= 15)
+ *   h                               device fp32 [I][H][P][N]: in the state before the
+ *                                   commit, out the committed state (the state the next
+ *                                   tree was verified from)
+ *   ring, ring_head                 device, updated as ssm_commit updates them
+ *   y                               device fp32 [I][n][d_inner], the next tree's outputs
+ *   workspace                       ssm_commit_verify_workspace_size() bytes
+ * A path entry that is not the root followed by children in order ends the
+ * path there and sets SSM_STATUS_PATH_RANGE (as ssm_commit does).  Returns
+ * SSM_ERR_CAPACITY for chain trees beyond SSM_MAX_DEPTH (they take the
+ * separate calls) or a too-small workspace.
+ */
+size_t ssm_commit_verify_workspace_size(const ssm_dims *dims, int32_t n_seq, int32_t n_nodes, int32_t max_depth,
+                                        int32_t prev_max_path);
+int ssm_commit_verify(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t prev_n_nodes,
+                      const ssm_node *prev_layout, int32_t prev_max_path, const int32_t *prev_path,
+                      const int32_t *prev_path_len, const uint16_t *prev_xBC, const uint16_t *prev_dt,
+                      int32_t n_nodes, int32_t max_depth, const ssm_node *layout, const uint16_t *xBC,
+                      const uint16_t *dt, float *h, uint16_t *ring, int32_t *ring_head, float *y, void *workspace,
+                      size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * ssm_draft_step -- one draft token per instance (a one-node tree), SpecMamba
  * page §3.1 (the draft logs only Δ, A, B, X).  Position = ring_head + step:
  * the token's pre-conv row is written to that ring position, the conv window

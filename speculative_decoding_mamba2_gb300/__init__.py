@@ -11,6 +11,8 @@ from .binding import (  # noqa: F401
     library_path,
     ssm_accept_path,
     ssm_commit,
+    ssm_commit_verify,
+    ssm_commit_verify_workspace_size,
     ssm_draft_step,
     ssm_last_error,
     ssm_replay,

@@ -87,6 +87,9 @@ _SIGS = {
     "ssm_tree_verify_noalloc": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_accept_path": (ctypes.c_int, [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_commit_verify_workspace_size": (ctypes.c_size_t, [_P, _I, _I, _I, _I]),
+    "ssm_commit_verify": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                         _P, ctypes.c_size_t, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_replay": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
@@ -250,6 +253,38 @@ def ssm_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, layout, max_p
         _dev(h, "h", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h)))
+
+
+def ssm_commit_verify_workspace_size(dims: Dims, n_seq: int, n_nodes: int, max_depth: int, prev_max_path: int) -> int:
+    cd = dims.c()
+    b = lib().ssm_commit_verify_workspace_size(ctypes.byref(cd), n_seq, n_nodes, max_depth, prev_max_path)
+    if b == 0:
+        raise SSMError(SSM_ERR_CAPACITY, ssm_last_error())
+    return int(b)
+
+
+def ssm_commit_verify(dims: Dims, params: dict, n_seq: int, prev_n_nodes: int, prev_layout, prev_max_path: int,
+                      prev_path, prev_path_len, prev_xBC, prev_dt, n_nodes: int, max_depth: int, layout, xBC, dt, h,
+                      ring, ring_head, y, workspace, status=None, stream=None):
+    """ssm_commit of the previous tree's accepted path, then ssm_tree_verify of the
+    next tree from the committed state, with one read and one write of h."""
+    d, I, n, pn = dims, n_seq * dims.n_layers, n_nodes, prev_n_nodes
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    _check(lib().ssm_commit_verify(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, pn,
+        _dev(prev_layout, "prev_layout", torch.int32, n_seq * pn * NODE_WORDS), prev_max_path,
+        _dev(prev_path, "prev_path", torch.int32, n_seq * prev_max_path),
+        _dev(prev_path_len, "prev_path_len", torch.int32, n_seq),
+        _dev(prev_xBC, "prev_xBC", torch.bfloat16, I * pn * d.conv_dim),
+        _dev(prev_dt, "prev_dt", torch.bfloat16, I * pn * d.n_heads),
+        n, max_depth, _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+        _dev(h, "h", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+        _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
+        _dev(workspace, "workspace", torch.uint8), ctypes.c_size_t(workspace.numel()),
+        _opt_status(status), _stream(stream, h)))
 
 
 def ssm_draft_step(dims: Dims, params: dict, n_seq: int, step: int, log_cap: int, xBC_t, dt_t, h_in, h_out, ring,

@@ -114,7 +114,7 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   if (!chain &&
       workspace_bytes < verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers))
     return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_tree_verify_workspace_size()");
-  VerifyArgs a;
+  VerifyArgs a{};
   a.gpc = 1;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
@@ -137,6 +137,86 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   a.status = dev_status;
   return finish(fn, chain ? launch_chain_verify(a, (cudaStream_t)stream)
                          : launch_verify(a, workspace, (cudaStream_t)stream));
+}
+
+namespace {
+int check_commit_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_seq, int32_t prev_n_nodes,
+                              int32_t prev_max_path, int32_t n_nodes, int32_t max_depth) {
+  if (int rc = check_verify_shape(fn, dims, n_seq, n_nodes, max_depth)) return rc;
+  if (long_chain(n_nodes, max_depth))
+    return fail(SSM_ERR_CAPACITY, fn, "chain trees deeper than SSM_MAX_DEPTH take ssm_commit + ssm_tree_verify");
+  if (prev_n_nodes < 1 || prev_n_nodes > SSM_MAX_NODES)
+    return fail(SSM_ERR_RANGE, fn, "prev_n_nodes must be in [1, SSM_MAX_NODES]");
+  if (prev_max_path < 1 || prev_max_path > SSM_MAX_DEPTH + 1)
+    return fail(SSM_ERR_RANGE, fn, "prev_max_path must be in [1, SSM_MAX_DEPTH + 1]");
+  if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads, prev_max_path) == 0 ||
+      verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads, prev_max_path) > 232448)
+    return fail(SSM_ERR_CAPACITY, fn, "tree and path too large for the shared-memory plan of this build");
+  return SSM_OK;
+}
+}  // namespace
+
+extern "C" size_t ssm_commit_verify_workspace_size(const ssm_dims* dims, int32_t n_seq, int32_t n_nodes,
+                                                   int32_t max_depth, int32_t prev_max_path) {
+  const char* fn = "ssm_commit_verify_workspace_size";
+  if (check_commit_verify_shape(fn, dims, n_seq, 1, prev_max_path, n_nodes, max_depth) != SSM_OK) return 0;
+  g_error.clear();
+  const size_t b =
+      verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers, prev_max_path);
+  return b ? b : 16;
+}
+
+extern "C" int ssm_commit_verify(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t prev_n_nodes,
+                                 const ssm_node* prev_layout, int32_t prev_max_path, const int32_t* prev_path,
+                                 const int32_t* prev_path_len, const uint16_t* prev_xBC, const uint16_t* prev_dt,
+                                 int32_t n_nodes, int32_t max_depth, const ssm_node* layout, const uint16_t* xBC,
+                                 const uint16_t* dt, float* h, uint16_t* ring, int32_t* ring_head, float* y,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_commit_verify";
+  if (int rc = check_commit_verify_shape(fn, dims, n_seq, prev_n_nodes, prev_max_path, n_nodes, max_depth)) return rc;
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!prev_layout || !prev_path || !prev_path_len || !prev_xBC || !prev_dt || !layout || !xBC || !dt || !h || !ring ||
+      !ring_head || !y || !workspace)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)prev_xBC | (uintptr_t)xBC | (uintptr_t)h | (uintptr_t)ring | (uintptr_t)layout |
+       (uintptr_t)workspace) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "prev_xBC, xBC, h, ring, layout and workspace must be 16-byte aligned");
+  if (workspace_bytes <
+      verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers, prev_max_path))
+    return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_commit_verify_workspace_size()");
+  VerifyArgs a{};
+  a.gpc = 1;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.max_depth = max_depth;
+  a.conv_w = prm->conv_w;
+  a.conv_b = prm->conv_b;
+  a.dt_bias = prm->dt_bias;
+  a.A_log = prm->A_log;
+  a.D = prm->D;
+  a.layout = layout;
+  a.xBC = xBC;
+  a.dt = dt;
+  a.ring = ring;
+  a.h0 = h;
+  a.ring_head = ring_head;
+  a.y = y;
+  a.status = dev_status;
+  a.LP = prev_max_path;
+  a.prev_n = prev_n_nodes;
+  a.prev_layout = prev_layout;
+  a.prev_path = prev_path;
+  a.prev_path_len = prev_path_len;
+  a.prev_xBC = prev_xBC;
+  a.prev_dt = prev_dt;
+  a.h_w = h;
+  a.ring_w = ring;
+  a.head_w = ring_head;
+  return finish(fn, launch_verify(a, workspace, (cudaStream_t)stream));
 }
 
 extern "C" int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node* layout,

@@ -196,11 +196,20 @@ struct VerifyArgs {
   const int32_t* ring_head;
   float* y;
   int32_t* status;
+  // commit of the previous step's accepted path folded into this verify (LP = 0: plain verify).
+  // LP bounds the path length; h_w / ring_w / head_w are the writable views of h0 / ring / ring_head.
+  int LP, prev_n;
+  const ssm_node* prev_layout;
+  const int32_t *prev_path, *prev_path_len;
+  const uint16_t *prev_xBC, *prev_dt;
+  float* h_w;
+  uint16_t* ring_w;
+  int32_t* head_w;
 };
 cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
-size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst);
-int verify_heads_per_group(int n, int max_depth, int H);  // 0: the plan does not fit in shared memory
-int verify_prep_smem_bytes(int n, int max_depth, int H);
+size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
+int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
+int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
 cudaError_t launch_chain_verify(const VerifyArgs& a, cudaStream_t s);
 
 struct AcceptArgs {

@@ -28,6 +28,18 @@
 //    producer) and contracts each chunk against C on the tensor cores
 //    (mma m16n8k8 TF32 with a 3-term hi/lo split, fp32 accumulate: fp32-level
 //    accuracy), and the epilogue adds the path terms and D·x and writes y.
+//
+// Commit folded into verify (LP > 0).  The selective recompute of the previous
+// step's accepted path m_0..m_{len-1} (SpecMamba page §3.1) is, by the same
+// linearity, a rank-len update of the state:
+//     h' = E·h + Σ_j u_j ⊗ B_j,   E = Π_j a_j,   u_j = Δ_j·(Π_{i>j} a_i)·x_j,
+// with a_j = exp(Δ_j·A) and x_j, B_j the post-conv rows of path node j.  The
+// prep kernel also computes E, u_j and B_j (conv over [the ring rows before the
+// path ‖ the path rows]), writes the path's last rows into the conv ring and
+// advances its head; the main kernel rewrites every h chunk it streams in as
+// h' (in shared memory), stores it back over h, and contracts C against h'.
+// The state is read once and written once per speculative step, instead of
+// read by verify and read + written again by a separate commit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdlib.h>
@@ -41,7 +53,8 @@ namespace {
 constexpr int NT = 16;           // nodes per tile
 constexpr int KC = 16;           // d_state columns per pipeline stage
 constexpr int KCH = kN / KC;     // stages per node tile
-constexpr int STAGES = 4;
+constexpr int STAGES_PLAIN = 4;  // h0 pipeline depth of the plain kernel
+constexpr int STAGES_FUSED = 3;  // ... and of the commit-folding kernel (its extra tables need the room)
 constexpr int SROW = KC;         // stage row: 64 B, 16-byte pieces swizzled by the copy engine
 constexpr int THREADS = 256;
 constexpr int DMAX = SSM_MAX_DEPTH + 1;
@@ -55,14 +68,14 @@ static_assert(2 * kN == THREADS, "one thread per B|C channel");
 // per-instance workspace written by the prep kernel (byte offsets)
 // ---------------------------------------------------------------------------
 struct Ws {
-  int NP;  // n rounded up to 4
+  int NP;  // n rounded up to 4 (n + 1 with a folded commit: column n holds E_h)
   int PP;  // path pairs n*(max_depth+1) rounded up to 4
-  size_t C, eS, coef, pathn, pairs, stride;
+  size_t C, eS, coef, pathn, pairs, BP, uP, meta, stride;
 };
 
-__host__ __device__ inline Ws ws_layout(int n, int max_depth, int H) {
+__host__ __device__ inline Ws ws_layout(int n, int max_depth, int H, int LP = 0) {
   Ws w;
-  w.NP = (n + 3) & ~3;
+  w.NP = (n + (LP > 0 ? 1 : 0) + 3) & ~3;
   w.PP = (n * (max_depth + 1) + 3) & ~3;
   size_t o = 0;
   auto take = [&](size_t b) {
@@ -75,6 +88,9 @@ __host__ __device__ inline Ws ws_layout(int n, int max_depth, int H) {
   w.coef = take((size_t)H * w.PP * 4);     // coef [H][PP] in pair order
   w.pathn = take((size_t)n * DMAX * 4);    // ancestor of v at depth j [n][DMAX]
   w.pairs = take((size_t)(w.PP + 4) * 4);  // [count, v*DMAX+j ...]
+  w.BP = take((size_t)LP * kN * 4);         // committed path: post-conv B_j [LP][N]
+  w.uP = take((size_t)LP * H * kP * 4);     // committed path: u_j = w_{j,h}·x_j [LP][d_inner]
+  w.meta = take(LP > 0 ? 16 : 0);           // committed path length
   w.stride = o;
   return w;
 }
@@ -113,10 +129,10 @@ __device__ __forceinline__ int4 tap_rows(const ssm_node& r, int v) {
 // prep kernel: everything per instance that does not depend on the head group
 // ---------------------------------------------------------------------------
 struct PrepSmem {
-  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, total;
+  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, total;
 };
 
-__host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP) {
+__host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0) {
   PrepSmem s;
   int o = 0;
   auto take = [&](int b) {
@@ -133,6 +149,9 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP) {
   s.Gm = take(n * DMAX * 4);
   s.dl = take(n * H * 4);
   s.S = take(n * H * 4);
+  s.pp = take(LP > 0 ? 20 * 4 : 0);  // committed path nodes [16], its length, the ring head before it
+  s.wP = take(LP * H * 4);           // Δ_j, then Δ_j·Π_{i>j} a_i  [LP][H]
+  s.aP = take(LP * H * 4);           // a_j = exp(Δ_j·A)          [LP][H]
   s.total = o;
   return s;
 }
@@ -140,8 +159,9 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP) {
 __global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n, H = a.H;
-  const Ws W = ws_layout(n, a.max_depth, H);
-  const PrepSmem L = prep_layout(n, H, W.PP);
+  const bool fuse = a.LP > 0;
+  const Ws W = ws_layout(n, a.max_depth, H, a.LP);
+  const PrepSmem L = prep_layout(n, H, W.PP, a.LP);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
   int* pairs = reinterpret_cast<int*>(smem + L.pairs);
@@ -158,13 +178,54 @@ __global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsign
   const int d_inner = H * kP, conv_dim = d_inner + 2 * kN, R = a.R;
   const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
   const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
-  const int head = a.ring_head[inst];
   unsigned char* ws = ws_base + (size_t)inst * W.stride;
+  int* pp = reinterpret_cast<int*>(smem + L.pp);
+  const uint16_t* prev_xbc = fuse ? a.prev_xBC + (size_t)inst * a.prev_n * conv_dim : nullptr;
 
-  // B|C input rows (ring rows above the root, then the nodes) in flight first
+  if (fuse) {
+    // the committed path, checked as the stand-alone commit checks it: root first, then each
+    // node a child of the one before; it ends at the first bad entry (a bad root commits node 0)
+    if (tid < 32) {
+      const int lane = tid;
+      const int32_t* pth = a.prev_path + (size_t)seq * a.LP;
+      int len = a.prev_path_len[seq];
+      const bool bad_len = len < 1 || len > a.LP;
+      len = len < 1 ? 1 : (len > a.LP ? a.LP : len);
+      const int v = lane < len ? pth[lane] : 0;
+      const int before = __shfl_up_sync(0xffffffffu, v, 1);
+      bool ok = true;
+      if (lane < len)
+        ok = lane == 0 ? v == 0
+                       : (v > before && v >= 1 && v < a.prev_n &&
+                          a.prev_layout[(size_t)seq * a.prev_n + v].parent == before);
+      const unsigned badm = __ballot_sync(0xffffffffu, lane < len && !ok);
+      const int good = badm ? __ffs(badm) - 1 : len;
+      if (lane < good) pp[lane] = v;
+      if (lane == 0) {
+        if (good == 0) pp[0] = 0;
+        pp[16] = good < 1 ? 1 : good;
+        pp[17] = a.ring_head[inst];
+        if (bad_len || badm) flag(a.status, SSM_STATUS_PATH_RANGE);
+      }
+    }
+    __syncthreads();
+  }
+  const int lenP = fuse ? pp[16] : 0;
+  const int head_old = fuse ? pp[17] : a.ring_head[inst];  // ring head before the committed path
+
+  // B|C input rows (the three rows before the root, then the nodes) in flight first.  The rows
+  // before the root are those of the conv ring after the commit: the path's last rows, then
+  // the ring rows that preceded the path.
   for (int i = tid; i < (n + 3) * 32; i += THREADS) {
     const int r = i >> 5, pc = i & 31;
-    const uint16_t* src = r < 3 ? ring + (size_t)ring_pos(head, r - 3, R) * conv_dim : xbc + (size_t)(r - 3) * conv_dim;
+    const uint16_t* src;
+    if (r >= 3) {
+      src = xbc + (size_t)(r - 3) * conv_dim;
+    } else {
+      const int k = 3 - r;  // k-th row before the root
+      src = k <= lenP ? prev_xbc + (size_t)pp[lenP - k] * conv_dim
+                      : ring + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim;
+    }
     cp_async16(xin + r * XW + pc * 8, src + d_inner + pc * 8);
   }
   cp_async_commit();
@@ -262,18 +323,78 @@ __global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsign
     const int v = pr / DMAX, m = pathn[pr];
     wc[h * W.PP + k] = expf(Sv[v * H + h] - Sv[m * H + h]) * dl[m * H + h] * Gm[pr];
   }
+  if (!fuse) return;
+
+  // ---- the committed path: Δ_j and a_j per head, then u_j = Δ_j·Π_{i>j} a_i·x_j, B_j, E ----
+  float* wP = reinterpret_cast<float*>(smem + L.wP);
+  float* aP = reinterpret_cast<float*>(smem + L.aP);
+  for (int i = tid; i < lenP * H; i += THREADS) {
+    const int j = i / H, h = i - j * H;
+    const float d = softplus_f(bf16f(a.prev_dt[((size_t)inst * a.prev_n + pp[j]) * H + h]) +
+                               a.dt_bias[(size_t)layer * H + h]);
+    wP[i] = d;
+    aP[i] = decay_of(d, neg_exp(a.A_log[(size_t)layer * H + h]));
+  }
+  __syncthreads();
+  for (int h = tid; h < H; h += THREADS) {
+    float run = 1.f;
+    for (int j = lenP - 1; j >= 0; --j) {
+      wP[j * H + h] *= run;
+      run *= aP[j * H + h];
+    }
+    reinterpret_cast<float*>(ws + W.eS)[h * W.NP + n] = run;  // E_h
+  }
+  __syncthreads();
+  {  // conv + SiLU of the path's x and B channels over [ring rows before the path ‖ path rows]
+    float* uP = reinterpret_cast<float*>(ws + W.uP);
+    float* BP = reinterpret_cast<float*>(ws + W.BP);
+    const uint16_t* q0 = ring + (size_t)ring_pos(head_old, -3, R) * conv_dim;
+    const uint16_t* q1 = ring + (size_t)ring_pos(head_old, -2, R) * conv_dim;
+    const uint16_t* q2 = ring + (size_t)ring_pos(head_old, -1, R) * conv_dim;
+    const float* cbias = a.conv_b + (size_t)layer * conv_dim;
+    for (int c = tid; c < d_inner + kN; c += THREADS) {
+      const float4 wk = cw[c];
+      const float bk = cbias[c];
+      float r0 = bf16f(q0[c]), r1 = bf16f(q1[c]), r2 = bf16f(q2[c]);
+      for (int j = 0; j < lenP; ++j) {
+        const float r3 = bf16f(prev_xbc[(size_t)pp[j] * conv_dim + c]);
+        const float post = silu_f(conv4_acc(wk, bk, r0, r1, r2, r3));
+        if (c < d_inner)
+          uP[(size_t)j * d_inner + c] = wP[j * H + c / kP] * post;
+        else
+          BP[j * kN + (c - d_inner)] = post;
+        r0 = r1;
+        r1 = r2;
+        r2 = r3;
+      }
+    }
+  }
+  __syncthreads();  // every read of the old ring rows is done
+  {  // conv ring: the path's last min(len, 3) rows go to positions head+len-3 .. head+len-1
+    uint16_t* rw = a.ring_w + (size_t)inst * R * conv_dim;
+    for (int j = lenP > 3 ? lenP - 3 : 0; j < lenP; ++j) {
+      const uint4* src = reinterpret_cast<const uint4*>(prev_xbc + (size_t)pp[j] * conv_dim);
+      uint4* dst = reinterpret_cast<uint4*>(rw + (size_t)ring_pos(head_old, j, R) * conv_dim);
+      for (int c = tid; c < conv_dim / 8; c += THREADS) dst[c] = src[c];
+    }
+  }
+  if (tid == 0) {
+    a.head_w[inst] = head_old + lenP;
+    reinterpret_cast<int*>(ws + W.meta)[0] = lenP;
+  }
 }
 
 // ---------------------------------------------------------------------------
 // main kernel
 // ---------------------------------------------------------------------------
 struct Smem {
-  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, pD, total;
+  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, pD, BPs, uPs, meta, total;
 };
 
-template <int G>
-__host__ __device__ inline Smem smem_layout(int n, int PP, int NP) {
+template <int G, bool FUSE>
+__host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   constexpr int ROWS = G * kP;
+  constexpr int ST = FUSE ? STAGES_FUSED : STAGES_PLAIN;
   Smem s;
   int o = 0;
   auto take = [&](int bytes) {
@@ -281,9 +402,9 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP) {
     o += (bytes + 15) & ~15;
     return r;
   };
-  s.bars = take((2 * STAGES + 2) * 8 + 16);  // full[], empty[], prologue, group inputs; abort flag
-  o = (o + 127) & ~127;                      // swizzled copies need 128-byte alignment
-  s.stage = take(STAGES * ROWS * SROW * 4);
+  s.bars = take((2 * ST + 2) * 8 + 16);  // full[], empty[], prologue, group inputs; abort flag
+  o = (o + 127) & ~127;                  // swizzled copies need 128-byte alignment
+  s.stage = take(ST * ROWS * SROW * 4);
   s.nodes = take(n * (int)sizeof(ssm_node));
   s.rowidx = take(n * 16);
   s.poff = take(n * 4);
@@ -295,18 +416,23 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP) {
   s.eSg = take(2 * G * NP * 4);    // two groups in flight: the next group's inputs land
   s.coefg = take(2 * G * PP * 4);  // before the current group's epilogue
   s.pD = take(MAX_GPC * G * 4);
+  s.BPs = take(FUSE ? LP * kN * 4 : 0);        // committed path B_j
+  s.uPs = take(FUSE ? 2 * LP * ROWS * 4 : 0);  // committed path u_j rows of a group (two groups in flight)
+  s.meta = take(FUSE ? 16 : 0);
   s.total = o;
   return s;
 }
 
-template <int G>
+template <int G, bool FUSE>
 __global__ void __launch_bounds__(THREADS, 2)
     tree_verify_kernel(VerifyArgs a, const unsigned char* __restrict__ ws_base, const __grid_constant__ CUtensorMap tmap) {
   constexpr int ROWS = G * kP;
+  constexpr int STAGES = FUSE ? STAGES_FUSED : STAGES_PLAIN;
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n;
-  const Ws W = ws_layout(n, a.max_depth, a.H);
-  const Smem L = smem_layout<G>(n, W.PP, W.NP);
+  const int LP = FUSE ? a.LP : 0;
+  const Ws W = ws_layout(n, a.max_depth, a.H, LP);
+  const Smem L = smem_layout<G, FUSE>(n, W.PP, W.NP, LP);
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int4* rowidx = reinterpret_cast<int4*>(smem + L.rowidx);
@@ -319,6 +445,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   float* eSg = reinterpret_cast<float*>(smem + L.eSg);
   float* coefg = reinterpret_cast<float*>(smem + L.coefg);
   float* pD = reinterpret_cast<float*>(smem + L.pD);
+  float* BPs = reinterpret_cast<float*>(smem + L.BPs);
+  float* uPs = reinterpret_cast<float*>(smem + L.uPs);
+  const int* s_meta = reinterpret_cast<const int*>(smem + L.meta);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NG = (a.H + G - 1) / G;
@@ -373,7 +502,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         const int heads = min(G, a.H - hb);
         const uint32_t xb = (uint32_t)heads * kP * 2;
         const int buf = pf_g & 1;
-        if (lane == 0) mbar_arrive_expect_tx(x_bar, xb * (n + 3) + (uint32_t)heads * (W.NP + W.PP) * 4);
+        const uint32_t ub = FUSE ? (uint32_t)LP * heads * kP * 4 : 0u;
+        if (lane == 0) mbar_arrive_expect_tx(x_bar, xb * (n + 3) + (uint32_t)heads * (W.NP + W.PP) * 4 + ub);
         __syncwarp();
         for (int r = lane; r < n + 3; r += 32) {
           const uint16_t* src =
@@ -384,6 +514,11 @@ __global__ void __launch_bounds__(THREADS, 2)
           bulk_load(smem_u32(eSg + buf * G * W.NP), ws + W.eS + (size_t)hb * W.NP * 4, heads * W.NP * 4, x_bar);
         if (lane == 1)
           bulk_load(smem_u32(coefg + buf * G * W.PP), ws + W.coef + (size_t)hb * W.PP * 4, heads * W.PP * 4, x_bar);
+        if (FUSE && lane >= 2 && lane < 2 + LP) {
+          const int j = lane - 2;
+          bulk_load(smem_u32(uPs + (buf * LP + j) * ROWS), ws + W.uP + ((size_t)j * d_inner + (size_t)hb * kP) * 4,
+                    heads * kP * 4, x_bar);
+        }
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(full_bar(slot), ROWS * SROW * 4);
@@ -418,11 +553,16 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(pro_bar, 1);
       mbar_init(x_bar, 1);
       fence_barrier_init();
-      mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4);
+      mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4 +
+                                         (FUSE ? (uint32_t)LP * kN * 4 + 16 : 0u));
       bulk_load(smem_u32(nodes), a.layout + (size_t)seq * n, n * (uint32_t)sizeof(ssm_node), pro_bar);
       bulk_load(smem_u32(Cs), ws + W.C, n * CSTR * 4, pro_bar);
       bulk_load(smem_u32(pathn), ws + W.pathn, n * DMAX * 4, pro_bar);
       bulk_load(smem_u32(pairs), ws + W.pairs, (W.PP + 4) * 4, pro_bar);
+      if (FUSE) {
+        bulk_load(smem_u32(BPs), ws + W.BP, LP * kN * 4, pro_bar);
+        bulk_load(smem_u32(s_meta), ws + W.meta, 16, pro_bar);
+      }
     }
     __syncwarp();
     produce(STAGES);
@@ -438,6 +578,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   __syncthreads();  // barriers initialised
   wait_or_abort(pro_bar, 0);
+  const int lenP = FUSE ? min(max(s_meta[0], 1), LP) : 0;
   for (int v = tid; v < n; v += THREADS) {
     // the prep kernel checked and reported the layout; clamp again so no index leaves its table
     ssm_node r = nodes[v];
@@ -460,7 +601,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int wrow = warp * 16 * MT;          // first state row of this warp within the group
   const int whead = wrow / kP;              // every row of a warp belongs to one head
   float acc[MT][2][4];
-  int q = 0;  // chunk index
+  float Ew = 1.f;  // decay of the whole committed path for this warp's head
+  int q = 0;       // chunk index
   for (int gi = 0; gi < g_count; ++gi) {
     const int hb = hc_begin + gi * G, heads = min(G, a.H - hb);
     const int hl = gi * G;
@@ -498,6 +640,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                                                  bf16f(xi[t.z * XW]), bf16f(xi[t.w * XW])));
             }
           }
+          if (FUSE) Ew = eSg[((gi & 1) * G + min(whead, heads - 1)) * W.NP + n];
           if (gi + 1 < g_count) {  // prefetch the next group's x conv weights
             const int hn = hb + G;
             if (tid < min(G, a.H - hn) * kP) {
@@ -519,7 +662,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         wait_or_abort(full_bar(slot), (q / STAGES) & 1);
         // A fragment rows of this lane: wrow + 16*mt + fg (+8); the copy engine's 64-byte
         // swizzle XORs the 16-byte piece index with shared-address bits 7..8
-        const unsigned char* st = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
+        unsigned char* st = reinterpret_cast<unsigned char*>(stage + slot * ROWS * SROW);
 #pragma unroll
         for (int ks = 0; ks < KC / 8; ++ks) {
           uint32_t bhi[2][2], blo[2][2];
@@ -531,14 +674,40 @@ __global__ void __launch_bounds__(THREADS, 2)
           }
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            const unsigned char* r0 = st + (wrow + mt * 16 + fg) * (SROW * 4);
+            unsigned char* r0 = st + (wrow + mt * 16 + fg) * (SROW * 4);
             const int swz = (smem_u32(r0) >> 7) & 3;  // rows r0 and r0+8 (512 B apart) share it
             const int o0 = (((2 * ks) ^ swz) << 4) + ft * 4, o1 = (((2 * ks + 1) ^ swz) << 4) + ft * 4;
+            float* p0 = reinterpret_cast<float*>(r0 + o0);
+            float* p1 = reinterpret_cast<float*>(r0 + 8 * SROW * 4 + o0);
+            float* p2 = reinterpret_cast<float*>(r0 + o1);
+            float* p3 = reinterpret_cast<float*>(r0 + 8 * SROW * 4 + o1);
+            float v0 = *p0, v1 = *p1, v2 = *p2, v3 = *p3;
+            if (FUSE) {
+              // h' = E·h + Σ_j u_j[row]·B_j[col] for the four elements of this lane's fragment
+              const int col = kc * KC + ks * 8 + ft;
+              const float* ur = uPs + (gi & 1) * LP * ROWS + wrow + mt * 16 + fg;
+              v0 *= Ew;
+              v1 *= Ew;
+              v2 *= Ew;
+              v3 *= Ew;
+              for (int j = 0; j < lenP; ++j) {
+                const float u0 = ur[j * ROWS], u1 = ur[j * ROWS + 8];
+                const float b0 = BPs[j * kN + col], b1 = BPs[j * kN + col + 4];
+                v0 = fmaf(u0, b0, v0);
+                v1 = fmaf(u1, b0, v1);
+                v2 = fmaf(u0, b1, v2);
+                v3 = fmaf(u1, b1, v3);
+              }
+              *p0 = v0;
+              *p1 = v1;
+              *p2 = v2;
+              *p3 = v3;
+            }
             uint32_t ahi[4], alo[4];
-            split_tf32(*reinterpret_cast<const float*>(r0 + o0), ahi[0], alo[0]);
-            split_tf32(*reinterpret_cast<const float*>(r0 + 8 * SROW * 4 + o0), ahi[1], alo[1]);
-            split_tf32(*reinterpret_cast<const float*>(r0 + o1), ahi[2], alo[2]);
-            split_tf32(*reinterpret_cast<const float*>(r0 + 8 * SROW * 4 + o1), ahi[3], alo[3]);
+            split_tf32(v0, ahi[0], alo[0]);
+            split_tf32(v1, ahi[1], alo[1]);
+            split_tf32(v2, ahi[2], alo[2]);
+            split_tf32(v3, ahi[3], alo[3]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
               mma_tf32(acc[mt][nt], alo, bhi[nt]);
@@ -548,6 +717,20 @@ __global__ void __launch_bounds__(THREADS, 2)
           }
         }
         __syncwarp();
+        if (FUSE && whead < heads) {
+          // store this warp's rows of the rewritten chunk over h: 16*MT rows x 64 bytes
+          const unsigned char* sb = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
+          float* gdst = a.h_w + ((size_t)(inst * a.H + hb) * kP + wrow) * kN + kc * KC;
+#pragma unroll
+          for (int t = 0; t < 2 * MT; ++t) {
+            const int idx = lane + 32 * t, row = idx >> 2, pc = idx & 3;
+            const unsigned char* rp = sb + (wrow + row) * (SROW * 4);
+            const int swz = (smem_u32(rp) >> 7) & 3;
+            *reinterpret_cast<float4*>(gdst + (size_t)row * kN + pc * 4) =
+                *reinterpret_cast<const float4*>(rp + ((pc ^ swz) << 4));
+          }
+          __syncwarp();
+        }
         if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
         if (kc == KCH - 1 && whead < heads) {
           // ---- epilogue: y = e^{S_v}·Z + Σ_path coef·x_m + D·x_v ----
@@ -597,7 +780,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 int g_sms[64] = {0};
-int g_configured[3][64] = {{0}};
+int g_configured[5][64] = {{0}};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -623,12 +806,13 @@ cudaError_t ensure_smem(K kernel, int idx, int dev, int bytes) {
   return cudaSuccess;
 }
 
-template <int G>
+template <int G, bool FUSE>
 cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStream_t s, int dev) {
   VerifyArgs a = a0;
-  const Ws W = ws_layout(a.n, a.max_depth, a.H);
-  const Smem L = smem_layout<G>(a.n, W.PP, W.NP);
-  cudaError_t e = ensure_smem(tree_verify_kernel<G>, G == 4 ? 0 : 1, dev, L.total);
+  const int LP = FUSE ? a.LP : 0;
+  const Ws W = ws_layout(a.n, a.max_depth, a.H, LP);
+  const Smem L = smem_layout<G, FUSE>(a.n, W.PP, W.NP, LP);
+  cudaError_t e = ensure_smem(tree_verify_kernel<G, FUSE>, (G == 4 ? 0 : 1) + (FUSE ? 2 : 0), dev, L.total);
   if (e != cudaSuccess) return e;
   int sms = dev < 64 ? g_sms[dev] : 0;
   if (sms == 0) {
@@ -666,27 +850,32 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  tree_verify_kernel<G><<<(unsigned)blocks, THREADS, L.total, s>>>(a, ws, tmap);
+  tree_verify_kernel<G, FUSE><<<(unsigned)blocks, THREADS, L.total, s>>>(a, ws, tmap);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst) {
-  return ws_layout(n, max_depth, H).stride * (size_t)n_inst;
+size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP) {
+  return ws_layout(n, max_depth, H, LP).stride * (size_t)n_inst;
 }
 
 // heads per group used for n nodes (4 while the shared-memory plan fits, else 2; 0 if neither fits)
-int verify_heads_per_group(int n, int max_depth, int H) {
-  const Ws W = ws_layout(n, max_depth, H);
-  if (smem_layout<4>(n, W.PP, W.NP).total <= SMEM_LIMIT) return 4;
-  if (smem_layout<2>(n, W.PP, W.NP).total <= SMEM_LIMIT) return 2;
+int verify_heads_per_group(int n, int max_depth, int H, int LP) {
+  const Ws W = ws_layout(n, max_depth, H, LP);
+  if (LP > 0) {
+    if (smem_layout<4, true>(n, W.PP, W.NP, LP).total <= SMEM_LIMIT) return 4;
+    if (smem_layout<2, true>(n, W.PP, W.NP, LP).total <= SMEM_LIMIT) return 2;
+    return 0;
+  }
+  if (smem_layout<4, false>(n, W.PP, W.NP, 0).total <= SMEM_LIMIT) return 4;
+  if (smem_layout<2, false>(n, W.PP, W.NP, 0).total <= SMEM_LIMIT) return 2;
   return 0;
 }
 
-int verify_prep_smem_bytes(int n, int max_depth, int H) {
-  const Ws W = ws_layout(n, max_depth, H);
-  return prep_layout(n, H, W.PP).total;
+int verify_prep_smem_bytes(int n, int max_depth, int H, int LP) {
+  const Ws W = ws_layout(n, max_depth, H, LP);
+  return prep_layout(n, H, W.PP, LP).total;
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s) {
@@ -695,16 +884,17 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   const long long inst = (long long)a.n_seq * a.L;
   if (inst == 0) return cudaSuccess;
-  const int G = verify_heads_per_group(a.n, a.max_depth, a.H);
+  const int G = verify_heads_per_group(a.n, a.max_depth, a.H, a.LP);
   if (G == 0) return cudaErrorInvalidValue;
-  const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H);
-  e = ensure_smem(tree_prep_kernel, 2, dev, prep_bytes);
+  const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H, a.LP);
+  e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);
   if (e != cudaSuccess) return e;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   tree_prep_kernel<<<(unsigned)inst, THREADS, prep_bytes, s>>>(a, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  return G == 4 ? launch_main<4>(a, ws, s, dev) : launch_main<2>(a, ws, s, dev);
+  if (a.LP > 0) return G == 4 ? launch_main<4, true>(a, ws, s, dev) : launch_main<2, true>(a, ws, s, dev);
+  return G == 4 ? launch_main<4, false>(a, ws, s, dev) : launch_main<2, false>(a, ws, s, dev);
 }
 
 }  // namespace ssmtree

@@ -141,6 +141,34 @@ def test_verify_validation(L):
         B.ssm_tree_verify_workspace_size(B.Dims(n_heads=4, n_layers=2), 1, 65, 4)
 
 
+def _commit_verify(L, dims, prm, n_seq=1, prev_n=16, lp=5, n=16, depth=4, ptr=FAKE, ws_bytes=1 << 30):
+    return L.ssm_commit_verify(ctypes.byref(dims), ctypes.byref(prm) if prm is not None else None, n_seq, prev_n,
+                               ptr, lp, ptr, ptr, ptr, ptr, n, depth, ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr,
+                               ctypes.c_size_t(ws_bytes), None, None)
+
+
+def test_commit_verify_validation(L):
+    d, p = _dims(), _prm()
+    assert _commit_verify(L, d, p, n_seq=0, ptr=None) == B.SSM_OK
+    assert _commit_verify(L, d, None) == B.SSM_ERR_INVALID_ARG
+    assert _commit_verify(L, d, p, ptr=None) == B.SSM_ERR_INVALID_ARG
+    assert _commit_verify(L, d, p, lp=0) == B.SSM_ERR_RANGE
+    assert _commit_verify(L, d, p, lp=17) == B.SSM_ERR_RANGE  # paths of trees the tree kernel verifies
+    assert _commit_verify(L, d, p, prev_n=0) == B.SSM_ERR_RANGE
+    assert _commit_verify(L, d, p, prev_n=65) == B.SSM_ERR_RANGE
+    assert _commit_verify(L, d, p, n=256, depth=255) == B.SSM_ERR_CAPACITY  # long chains: separate calls
+    assert "chain" in B.ssm_last_error()
+    assert _commit_verify(L, d, p, n=8, depth=8) == B.SSM_ERR_RANGE
+    assert _commit_verify(L, d, p, ptr=ctypes.c_void_p(24)) == B.SSM_ERR_INVALID_ARG
+    dims = B.Dims(n_heads=4, n_layers=2)
+    need = B.ssm_commit_verify_workspace_size(dims, 1, 16, 4, 5)
+    assert need % 16 == 0 and need > B.ssm_tree_verify_workspace_size(dims, 1, 16, 4)
+    assert B.ssm_commit_verify_workspace_size(dims, 3, 16, 4, 5) == 3 * need
+    assert _commit_verify(L, d, p, ws_bytes=need - 16) == B.SSM_ERR_CAPACITY
+    with pytest.raises(B.SSMError):
+        B.ssm_commit_verify_workspace_size(dims, 1, 16, 4, 17)
+
+
 def test_accept_commit_draft_replay_validation(L):
     P = FAKE
     assert L.ssm_accept_path(1, 16, 0, P, P, P, P, P, P, None, None) == B.SSM_ERR_RANGE
