@@ -59,7 +59,7 @@ constexpr int SROW = KC;         // stage row: 64 B, 16-byte pieces swizzled by 
 constexpr int THREADS = 256;
 constexpr int DMAX = SSM_MAX_DEPTH + 1;
 constexpr int XW = 256;          // channels per staged input row
-constexpr int CSTR = kN + 4;     // padded row of the C table (conflict-free B fragments)
+constexpr int CSTR = kN + 16;    // padded row of the C table (conflict-free 16-byte B-fragment loads)
 constexpr int MAX_GPC = 8;       // head groups per CTA
 constexpr int SMEM_LIMIT = 232448;
 static_assert(2 * kN == THREADS, "one thread per B|C channel");
@@ -156,7 +156,7 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0
   return s;
 }
 
-__global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
+__global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n, H = a.H;
   const bool fuse = a.LP > 0;
@@ -345,27 +345,55 @@ __global__ void __launch_bounds__(THREADS) tree_prep_kernel(VerifyArgs a, unsign
     reinterpret_cast<float*>(ws + W.eS)[h * W.NP + n] = run;  // E_h
   }
   __syncthreads();
-  {  // conv + SiLU of the path's x and B channels over [ring rows before the path ‖ path rows]
+  {  // conv + SiLU of the path's x and B channels over [ring rows before the path ‖ path rows]:
+     // 4 channels per thread, 8-byte loads, up to 5 path rows per pass with all 8 window rows
+     // in flight before the first is used
     float* uP = reinterpret_cast<float*>(ws + W.uP);
     float* BP = reinterpret_cast<float*>(ws + W.BP);
-    const uint16_t* q0 = ring + (size_t)ring_pos(head_old, -3, R) * conv_dim;
-    const uint16_t* q1 = ring + (size_t)ring_pos(head_old, -2, R) * conv_dim;
-    const uint16_t* q2 = ring + (size_t)ring_pos(head_old, -1, R) * conv_dim;
     const float* cbias = a.conv_b + (size_t)layer * conv_dim;
-    for (int c = tid; c < d_inner + kN; c += THREADS) {
-      const float4 wk = cw[c];
-      const float bk = cbias[c];
-      float r0 = bf16f(q0[c]), r1 = bf16f(q1[c]), r2 = bf16f(q2[c]);
-      for (int j = 0; j < lenP; ++j) {
-        const float r3 = bf16f(prev_xbc[(size_t)pp[j] * conv_dim + c]);
-        const float post = silu_f(conv4_acc(wk, bk, r0, r1, r2, r3));
-        if (c < d_inner)
-          uP[(size_t)j * d_inner + c] = wP[j * H + c / kP] * post;
-        else
-          BP[j * kN + (c - d_inner)] = post;
-        r0 = r1;
-        r1 = r2;
-        r2 = r3;
+    auto window_row = [&](int t) -> const uint16_t* {  // t < 3: ring rows before the path
+      return t < 3 ? ring + (size_t)ring_pos(head_old, t - 3, R) * conv_dim : prev_xbc + (size_t)pp[t - 3] * conv_dim;
+    };
+    for (int i = tid; i < (d_inner + kN) / 4; i += THREADS) {
+      const int c0 = i * 4;
+      float4 wk[4];
+      float bk[4];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        wk[cc] = cw[c0 + cc];
+        bk[cc] = cbias[c0 + cc];
+      }
+      for (int j0 = 0; j0 < lenP; j0 += 5) {
+        const int cnt = min(5, lenP - j0);
+        uint2 raw[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          if (t < cnt + 3) raw[t] = *reinterpret_cast<const uint2*>(window_row(j0 + t) + c0);
+#pragma unroll
+        for (int jj = 0; jj < 5; ++jj) {
+          if (jj >= cnt) break;
+          const int j = j0 + jj;
+          float out[4];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            float r[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t word = (cc >> 1) == 0 ? raw[jj + k].x : raw[jj + k].y;
+              r[k] = bf16f((uint16_t)((cc & 1) ? (word >> 16) : (word & 0xffffu)));
+            }
+            out[cc] = silu_f(conv4_acc(wk[cc], bk[cc], r[0], r[1], r[2], r[3]));
+          }
+          float4* dst;
+          float sc = 1.f;
+          if (c0 < d_inner) {
+            dst = reinterpret_cast<float4*>(uP + (size_t)j * d_inner + c0);
+            sc = wP[j * H + c0 / kP];
+          } else {
+            dst = reinterpret_cast<float4*>(BP + j * kN + (c0 - d_inner));
+          }
+          *dst = make_float4(sc * out[0], sc * out[1], sc * out[2], sc * out[3]);
+        }
       }
     }
   }
@@ -660,54 +688,70 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
         const int slot = q % STAGES;
         wait_or_abort(full_bar(slot), (q / STAGES) & 1);
-        // A fragment rows of this lane: wrow + 16*mt + fg (+8); the copy engine's 64-byte
-        // swizzle XORs the 16-byte piece index with shared-address bits 7..8
-        unsigned char* st = reinterpret_cast<unsigned char*>(stage + slot * ROWS * SROW);
+        // Contraction order within the 16-column chunk: k-step s (0, 1) takes columns
+        // 4t+2s (k = t) and 4t+2s+1 (k = t+4), t = 0..3, so lane (fg, ft) needs exactly the
+        // 16-byte piece ft of each of its rows wrow + 16*mt + fg (+8), and of each C row.
+        // The copy engine's 64-byte swizzle XORs the piece index with address bits 7..8.
+        const unsigned char* st = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
+        float4 ra[MT], rb[MT];  // rows fg and fg+8 of each m-tile, columns 4*ft .. 4*ft+3
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const unsigned char* r0 = st + (wrow + mt * 16 + fg) * (SROW * 4);
+          const int off = (ft ^ ((smem_u32(r0) >> 7) & 3)) << 4;  // rows r0 and r0+8 (512 B apart) share it
+          ra[mt] = *reinterpret_cast<const float4*>(r0 + off);
+          rb[mt] = *reinterpret_cast<const float4*>(r0 + 8 * SROW * 4 + off);
+        }
+        if (FUSE) {
+          // h' = E·h + Σ_j u_j[row]·B_j[col] on this lane's 4 x 2*MT elements, then h' over h
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            ra[mt].x *= Ew; ra[mt].y *= Ew; ra[mt].z *= Ew; ra[mt].w *= Ew;
+            rb[mt].x *= Ew; rb[mt].y *= Ew; rb[mt].z *= Ew; rb[mt].w *= Ew;
+          }
+          const float* ur = uPs + (gi & 1) * LP * ROWS + wrow + fg;
+          const float* br = BPs + kc * KC + 4 * ft;
+          for (int j = 0; j < lenP; ++j) {
+            const float4 bj = *reinterpret_cast<const float4*>(br + j * kN);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const float u0 = ur[j * ROWS + mt * 16], u1 = ur[j * ROWS + mt * 16 + 8];
+              ra[mt].x = fmaf(u0, bj.x, ra[mt].x);
+              ra[mt].y = fmaf(u0, bj.y, ra[mt].y);
+              ra[mt].z = fmaf(u0, bj.z, ra[mt].z);
+              ra[mt].w = fmaf(u0, bj.w, ra[mt].w);
+              rb[mt].x = fmaf(u1, bj.x, rb[mt].x);
+              rb[mt].y = fmaf(u1, bj.y, rb[mt].y);
+              rb[mt].z = fmaf(u1, bj.z, rb[mt].z);
+              rb[mt].w = fmaf(u1, bj.w, rb[mt].w);
+            }
+          }
+          if (whead < heads) {
+            float* g0 = a.h_w + ((size_t)(inst * a.H + hb) * kP + wrow + fg) * kN + kc * KC + 4 * ft;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              *reinterpret_cast<float4*>(g0 + (size_t)(mt * 16) * kN) = ra[mt];
+              *reinterpret_cast<float4*>(g0 + (size_t)(mt * 16 + 8) * kN) = rb[mt];
+            }
+          }
+        }
+        float4 cv[2];  // C rows of this lane's two B-fragment nodes, columns 4*ft .. 4*ft+3
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) cv[nt] = *reinterpret_cast<const float4*>(Cs + brow[nt] + kc * KC + 4 * ft);
 #pragma unroll
         for (int ks = 0; ks < KC / 8; ++ks) {
           uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            const float* cb0 = Cs + brow[nt] + kc * KC + ks * 8 + ft;
-            split_tf32(cb0[0], bhi[nt][0], blo[nt][0]);
-            split_tf32(cb0[4], bhi[nt][1], blo[nt][1]);
+            split_tf32(ks ? cv[nt].z : cv[nt].x, bhi[nt][0], blo[nt][0]);
+            split_tf32(ks ? cv[nt].w : cv[nt].y, bhi[nt][1], blo[nt][1]);
           }
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            unsigned char* r0 = st + (wrow + mt * 16 + fg) * (SROW * 4);
-            const int swz = (smem_u32(r0) >> 7) & 3;  // rows r0 and r0+8 (512 B apart) share it
-            const int o0 = (((2 * ks) ^ swz) << 4) + ft * 4, o1 = (((2 * ks + 1) ^ swz) << 4) + ft * 4;
-            float* p0 = reinterpret_cast<float*>(r0 + o0);
-            float* p1 = reinterpret_cast<float*>(r0 + 8 * SROW * 4 + o0);
-            float* p2 = reinterpret_cast<float*>(r0 + o1);
-            float* p3 = reinterpret_cast<float*>(r0 + 8 * SROW * 4 + o1);
-            float v0 = *p0, v1 = *p1, v2 = *p2, v3 = *p3;
-            if (FUSE) {
-              // h' = E·h + Σ_j u_j[row]·B_j[col] for the four elements of this lane's fragment
-              const int col = kc * KC + ks * 8 + ft;
-              const float* ur = uPs + (gi & 1) * LP * ROWS + wrow + mt * 16 + fg;
-              v0 *= Ew;
-              v1 *= Ew;
-              v2 *= Ew;
-              v3 *= Ew;
-              for (int j = 0; j < lenP; ++j) {
-                const float u0 = ur[j * ROWS], u1 = ur[j * ROWS + 8];
-                const float b0 = BPs[j * kN + col], b1 = BPs[j * kN + col + 4];
-                v0 = fmaf(u0, b0, v0);
-                v1 = fmaf(u1, b0, v1);
-                v2 = fmaf(u0, b1, v2);
-                v3 = fmaf(u1, b1, v3);
-              }
-              *p0 = v0;
-              *p1 = v1;
-              *p2 = v2;
-              *p3 = v3;
-            }
             uint32_t ahi[4], alo[4];
-            split_tf32(v0, ahi[0], alo[0]);
-            split_tf32(v1, ahi[1], alo[1]);
-            split_tf32(v2, ahi[2], alo[2]);
-            split_tf32(v3, ahi[3], alo[3]);
+            split_tf32(ks ? ra[mt].z : ra[mt].x, ahi[0], alo[0]);
+            split_tf32(ks ? rb[mt].z : rb[mt].x, ahi[1], alo[1]);
+            split_tf32(ks ? ra[mt].w : ra[mt].y, ahi[2], alo[2]);
+            split_tf32(ks ? rb[mt].w : rb[mt].y, ahi[3], alo[3]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
               mma_tf32(acc[mt][nt], alo, bhi[nt]);
@@ -717,20 +761,6 @@ __global__ void __launch_bounds__(THREADS, 2)
           }
         }
         __syncwarp();
-        if (FUSE && whead < heads) {
-          // store this warp's rows of the rewritten chunk over h: 16*MT rows x 64 bytes
-          const unsigned char* sb = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
-          float* gdst = a.h_w + ((size_t)(inst * a.H + hb) * kP + wrow) * kN + kc * KC;
-#pragma unroll
-          for (int t = 0; t < 2 * MT; ++t) {
-            const int idx = lane + 32 * t, row = idx >> 2, pc = idx & 3;
-            const unsigned char* rp = sb + (wrow + row) * (SROW * 4);
-            const int swz = (smem_u32(rp) >> 7) & 3;
-            *reinterpret_cast<float4*>(gdst + (size_t)row * kN + pc * 4) =
-                *reinterpret_cast<const float4*>(rp + ((pc ^ swz) << 4));
-          }
-          __syncwarp();
-        }
         if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
         if (kc == KCH - 1 && whead < heads) {
           // ---- epilogue: y = e^{S_v}·Z + Σ_path coef·x_m + D·x_v ----
