@@ -205,7 +205,8 @@ int ssm_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
  *   h                               device fp32 [I][H][P][N]: in the state before the
  *                                   commit, out the committed state (the state the next
  *                                   tree was verified from)
- *   ring, ring_head                 device, updated as ssm_commit updates them
+ *   ring, ring_head                 device, updated as ssm_commit updates them;
+ *                                   ring_cap >= prev_max_path + 3
  *   y                               device fp32 [I][n][d_inner], the next tree's outputs
  *   workspace                       ssm_commit_verify_workspace_size() bytes
  * A path entry that is not the root followed by children in order ends the

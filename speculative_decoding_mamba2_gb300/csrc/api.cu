@@ -149,6 +149,8 @@ int check_commit_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_se
     return fail(SSM_ERR_RANGE, fn, "prev_n_nodes must be in [1, SSM_MAX_NODES]");
   if (prev_max_path < 1 || prev_max_path > SSM_MAX_DEPTH + 1)
     return fail(SSM_ERR_RANGE, fn, "prev_max_path must be in [1, SSM_MAX_DEPTH + 1]");
+  if (dims->ring_cap < prev_max_path + 3)
+    return fail(SSM_ERR_CAPACITY, fn, "ring_cap must be >= prev_max_path + 3 (the rows before the path are read after the path is written)");
   if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads, prev_max_path) == 0 ||
       verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads, prev_max_path) > 232448)
     return fail(SSM_ERR_CAPACITY, fn, "tree and path too large for the shared-memory plan of this build");

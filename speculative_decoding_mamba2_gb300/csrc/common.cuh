@@ -16,6 +16,10 @@ constexpr int kW = 4;
 // bf16 bit pattern -> fp32 (exact).
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
 
+// The two bf16 values of a 32-bit word (low half = lower channel) -> fp32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
 
 // SiLU with the fast exp/divide intrinsics (relative error ~1e-6 on the

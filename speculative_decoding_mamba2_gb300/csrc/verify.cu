@@ -10,8 +10,8 @@
 //     h_v = e^{S_v}·h0 + Σ_{m ∈ path(v)} e^{S_v - S_m}·Δ_m·(x_m ⊗ B_m),
 //     S_v = Σ_{m ∈ path(v)} Δ_m·A,
 // and y_v = C_v·h_v + D·x_v becomes
-//     y_v[p] = e^{S_v}·(C_v·h0[p,:]) + Σ_{m ∈ path(v)} coef[v,m]·x_m[p] + D·x_v[p],
-//     coef[v,m] = e^{S_v - S_m}·Δ_m·(C_v·B_m).
+//     y_v[p] = e^{S_v}·(C_v·h0[p,:] + Σ_{m ∈ path(v)} coef[v,m]·x_m[p]),
+//     coef[v,m] = e^{-S_m}·Δ_m·(C_v·B_m)  (+ D·e^{-S_v} for m = v, the D·x term).
 // The per-node states are never formed (the extreme of "release after the
 // children are done"); h0 is read from HBM exactly once.
 //
@@ -27,17 +27,20 @@
 //    tensor copies with 64-byte swizzle, full/empty mbarriers, warp 0 as
 //    producer) and contracts each chunk against C on the tensor cores
 //    (mma m16n8k8 TF32 with a 3-term hi/lo split, fp32 accumulate: fp32-level
-//    accuracy), and the epilogue adds the path terms and D·x and writes y.
+//    accuracy).  The path terms are a small (rows x nodes) · (nodes x nodes)
+//    product that starts each node tile's accumulator, on the same tensor
+//    cores; the epilogue only scales by e^{S_v} and writes y.
 //
 // Commit folded into verify (LP > 0).  The selective recompute of the previous
 // step's accepted path m_0..m_{len-1} (SpecMamba page §3.1) is, by the same
 // linearity, a rank-len update of the state:
-//     h' = E·h + Σ_j u_j ⊗ B_j,   E = Π_j a_j,   u_j = Δ_j·(Π_{i>j} a_i)·x_j,
-// with a_j = exp(Δ_j·A) and x_j, B_j the post-conv rows of path node j.  The
-// prep kernel also computes E, u_j and B_j (conv over [the ring rows before the
-// path ‖ the path rows]), writes the path's last rows into the conv ring and
-// advances its head; the main kernel rewrites every h chunk it streams in as
-// h' (in shared memory), stores it back over h, and contracts C against h'.
+//     h' = E·h + Σ_j u_j ⊗ B_j,   E = Π_j a_j,   u_j = w_j·x_j,   w_j = Δ_j·Π_{i>j} a_i,
+// with a_j = exp(Δ_j·A) and x_j, B_j the post-conv rows of path node j (conv over
+// [the ring rows before the path ‖ the path rows]).  The prep kernel computes
+// E, w_j and B_j, writes the path's last rows into the conv ring and advances
+// its head; the main kernel computes its heads' u_j next to the tree's x conv,
+// rewrites every h chunk it streams in as h', stores it over h, and contracts
+// C against h'.
 // The state is read once and written once per speculative step, instead of
 // read by verify and read + written again by a separate commit.
 #include <cuda.h>
@@ -62,20 +65,21 @@ constexpr int XW = 256;          // channels per staged input row
 constexpr int CSTR = kN + 16;    // padded row of the C table (conflict-free 16-byte B-fragment loads)
 constexpr int MAX_GPC = 8;       // head groups per CTA
 constexpr int SMEM_LIMIT = 232448;
+constexpr int kMetaInts = 20;    // folded-commit record: [0] path length, [1] ring head before it, [4..19] nodes
 static_assert(2 * kN == THREADS, "one thread per B|C channel");
 
 // ---------------------------------------------------------------------------
 // per-instance workspace written by the prep kernel (byte offsets)
 // ---------------------------------------------------------------------------
 struct Ws {
-  int NP;  // n rounded up to 4 (n + 1 with a folded commit: column n holds E_h)
+  int NP;  // e^S row: n nodes (+ E_h at column n and w_{j,h} at n+1+j with a folded commit), padded to 4
   int PP;  // path pairs n*(max_depth+1) rounded up to 4
-  size_t C, eS, coef, pathn, pairs, BP, uP, meta, stride;
+  size_t C, eS, coef, pathn, pairs, BP, meta, stride;
 };
 
 __host__ __device__ inline Ws ws_layout(int n, int max_depth, int H, int LP = 0) {
   Ws w;
-  w.NP = (n + (LP > 0 ? 1 : 0) + 3) & ~3;
+  w.NP = (n + (LP > 0 ? 1 + LP : 0) + 3) & ~3;
   w.PP = (n * (max_depth + 1) + 3) & ~3;
   size_t o = 0;
   auto take = [&](size_t b) {
@@ -88,9 +92,8 @@ __host__ __device__ inline Ws ws_layout(int n, int max_depth, int H, int LP = 0)
   w.coef = take((size_t)H * w.PP * 4);     // coef [H][PP] in pair order
   w.pathn = take((size_t)n * DMAX * 4);    // ancestor of v at depth j [n][DMAX]
   w.pairs = take((size_t)(w.PP + 4) * 4);  // [count, v*DMAX+j ...]
-  w.BP = take((size_t)LP * kN * 4);         // committed path: post-conv B_j [LP][N]
-  w.uP = take((size_t)LP * H * kP * 4);     // committed path: u_j = w_{j,h}·x_j [LP][d_inner]
-  w.meta = take(LP > 0 ? 16 : 0);           // committed path length
+  w.BP = take((size_t)LP * kN * 4);           // committed path: post-conv B_j [LP][N]
+  w.meta = take(LP > 0 ? kMetaInts * 4 : 0);  // committed path: length, old ring head, nodes
   w.stride = o;
   return w;
 }
@@ -182,6 +185,11 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   int* pp = reinterpret_cast<int*>(smem + L.pp);
   const uint16_t* prev_xbc = fuse ? a.prev_xBC + (size_t)inst * a.prev_n * conv_dim : nullptr;
 
+  // B|C input rows of the tree's nodes in flight first (rows 3..n+2; rows 0..2 follow below)
+  for (int i = tid; i < n * 32; i += THREADS) {
+    const int r = 3 + (i >> 5), pc = i & 31;
+    cp_async16(xin + r * XW + pc * 8, xbc + (size_t)(r - 3) * conv_dim + d_inner + pc * 8);
+  }
   if (fuse) {
     // the committed path, checked as the stand-alone commit checks it: root first, then each
     // node a child of the one before; it ends at the first bad entry (a bad root commits node 0)
@@ -213,19 +221,13 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   const int lenP = fuse ? pp[16] : 0;
   const int head_old = fuse ? pp[17] : a.ring_head[inst];  // ring head before the committed path
 
-  // B|C input rows (the three rows before the root, then the nodes) in flight first.  The rows
-  // before the root are those of the conv ring after the commit: the path's last rows, then
-  // the ring rows that preceded the path.
-  for (int i = tid; i < (n + 3) * 32; i += THREADS) {
+  // the three rows before the root: those of the conv ring after the commit, i.e. the path's
+  // last rows, then the ring rows that preceded the path
+  for (int i = tid; i < 3 * 32; i += THREADS) {
     const int r = i >> 5, pc = i & 31;
-    const uint16_t* src;
-    if (r >= 3) {
-      src = xbc + (size_t)(r - 3) * conv_dim;
-    } else {
-      const int k = 3 - r;  // k-th row before the root
-      src = k <= lenP ? prev_xbc + (size_t)pp[lenP - k] * conv_dim
-                      : ring + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim;
-    }
+    const int k = 3 - r;  // k-th row before the root
+    const uint16_t* src = k <= lenP ? prev_xbc + (size_t)pp[lenP - k] * conv_dim
+                                    : ring + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim;
     cp_async16(xin + r * XW + pc * 8, src + d_inner + pc * 8);
   }
   cp_async_commit();
@@ -315,17 +317,20 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     for (int i = tid; i < W.PP + 4; i += THREADS) dq[i] = i <= n_pairs ? pairs[i] : 0;
   }
   __syncthreads();
-  // coef[h][k] = e^{S_v - S_m}·Δ_m·(C_v·B_m) for pair k = (v, depth-j ancestor m)
+  // coef[h][k] = e^{-S_m}·Δ_m·(C_v·B_m) for pair k = (v, depth-j ancestor m), plus D·e^{-S_v}
+  // on the node's own pair: the path terms and D·x of y_v, divided by e^{S_v}
   float* wc = reinterpret_cast<float*>(ws + W.coef);
   for (int i = tid; i < n_pairs * H; i += THREADS) {
     const int k = i / H, h = i - k * H;
     const int pr = pairs[1 + k];
     const int v = pr / DMAX, m = pathn[pr];
-    wc[h * W.PP + k] = expf(Sv[v * H + h] - Sv[m * H + h]) * dl[m * H + h] * Gm[pr];
+    float c = expf(-Sv[m * H + h]) * dl[m * H + h] * Gm[pr];
+    if (m == v) c = fmaf(a.D[(size_t)layer * H + h], expf(-Sv[v * H + h]), c);
+    wc[h * W.PP + k] = c;
   }
   if (!fuse) return;
 
-  // ---- the committed path: Δ_j and a_j per head, then u_j = Δ_j·Π_{i>j} a_i·x_j, B_j, E ----
+  // ---- the committed path: Δ_j and a_j per head, then w_j = Δ_j·Π_{i>j} a_i, E = Π_j a_j, B_j ----
   float* wP = reinterpret_cast<float*>(smem + L.wP);
   float* aP = reinterpret_cast<float*>(smem + L.aP);
   for (int i = tid; i < lenP * H; i += THREADS) {
@@ -337,25 +342,25 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   }
   __syncthreads();
   for (int h = tid; h < H; h += THREADS) {
+    float* eh = reinterpret_cast<float*>(ws + W.eS) + h * W.NP;
     float run = 1.f;
     for (int j = lenP - 1; j >= 0; --j) {
-      wP[j * H + h] *= run;
+      eh[n + 1 + j] = wP[j * H + h] * run;  // w_{j,h}
       run *= aP[j * H + h];
     }
-    reinterpret_cast<float*>(ws + W.eS)[h * W.NP + n] = run;  // E_h
+    eh[n] = run;  // E_h
   }
-  __syncthreads();
-  {  // conv + SiLU of the path's x and B channels over [ring rows before the path ‖ path rows]:
+  {  // conv + SiLU of the path's B channels over [ring rows before the path ‖ path rows]:
      // 4 channels per thread, 8-byte loads, up to 5 path rows per pass with all 8 window rows
-     // in flight before the first is used
-    float* uP = reinterpret_cast<float*>(ws + W.uP);
+     // in flight before the first is used (the x channels are done per head group by the
+     // main kernel)
     float* BP = reinterpret_cast<float*>(ws + W.BP);
     const float* cbias = a.conv_b + (size_t)layer * conv_dim;
     auto window_row = [&](int t) -> const uint16_t* {  // t < 3: ring rows before the path
       return t < 3 ? ring + (size_t)ring_pos(head_old, t - 3, R) * conv_dim : prev_xbc + (size_t)pp[t - 3] * conv_dim;
     };
-    for (int i = tid; i < (d_inner + kN) / 4; i += THREADS) {
-      const int c0 = i * 4;
+    for (int i = tid; i < kN / 4; i += THREADS) {
+      const int c0 = d_inner + i * 4;
       float4 wk[4];
       float bk[4];
 #pragma unroll
@@ -384,15 +389,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
             }
             out[cc] = silu_f(conv4_acc(wk[cc], bk[cc], r[0], r[1], r[2], r[3]));
           }
-          float4* dst;
-          float sc = 1.f;
-          if (c0 < d_inner) {
-            dst = reinterpret_cast<float4*>(uP + (size_t)j * d_inner + c0);
-            sc = wP[j * H + c0 / kP];
-          } else {
-            dst = reinterpret_cast<float4*>(BP + j * kN + (c0 - d_inner));
-          }
-          *dst = make_float4(sc * out[0], sc * out[1], sc * out[2], sc * out[3]);
+          *reinterpret_cast<float4*>(BP + j * kN + (c0 - d_inner)) = make_float4(out[0], out[1], out[2], out[3]);
         }
       }
     }
@@ -406,9 +403,12 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
       for (int c = tid; c < conv_dim / 8; c += THREADS) dst[c] = src[c];
     }
   }
+  int* meta = reinterpret_cast<int*>(ws + W.meta);
+  if (tid < 16) meta[4 + tid] = tid < lenP ? pp[tid] : 0;
   if (tid == 0) {
+    meta[0] = lenP;
+    meta[1] = head_old;
     a.head_w[inst] = head_old + lenP;
-    reinterpret_cast<int*>(ws + W.meta)[0] = lenP;
   }
 }
 
@@ -416,8 +416,13 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
 // main kernel
 // ---------------------------------------------------------------------------
 struct Smem {
-  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, pD, BPs, uPs, meta, total;
+  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
 };
+
+// x rows of a group: node v at xs[v * xs_stride<G>()], rows padded by 8 floats so that the
+// path-term A fragments (8 rows x 4 nodes per load) hit 32 different banks; nodes padded to 8
+template <int G>
+__host__ __device__ constexpr int xs_stride() { return G * kP + 8; }
 
 template <int G, bool FUSE>
 __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
@@ -439,14 +444,13 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   s.pathn = take(n * DMAX * 4);
   s.pairs = take((PP + 4) * 4);
   s.Cs = take(n * CSTR * 4);
-  s.xs = take(n * ROWS * 4);
-  s.xinX = take((n + 3) * XW * 2);
+  s.xs = take(((n + 7) & ~7) * xs_stride<G>() * 4);
+  s.xinX = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows before the path ‖ path rows][tree rows]
   s.eSg = take(2 * G * NP * 4);    // two groups in flight: the next group's inputs land
   s.coefg = take(2 * G * PP * 4);  // before the current group's epilogue
-  s.pD = take(MAX_GPC * G * 4);
   s.BPs = take(FUSE ? LP * kN * 4 : 0);        // committed path B_j
-  s.uPs = take(FUSE ? 2 * LP * ROWS * 4 : 0);  // committed path u_j rows of a group (two groups in flight)
-  s.meta = take(FUSE ? 16 : 0);
+  s.uPs = take(FUSE ? LP * ROWS * 4 : 0);  // committed path u_j of the group's rows
+  s.meta = take(FUSE ? kMetaInts * 4 : 0);
   s.total = o;
   return s;
 }
@@ -472,10 +476,9 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint16_t* xinX = reinterpret_cast<uint16_t*>(smem + L.xinX);
   float* eSg = reinterpret_cast<float*>(smem + L.eSg);
   float* coefg = reinterpret_cast<float*>(smem + L.coefg);
-  float* pD = reinterpret_cast<float*>(smem + L.pD);
   float* BPs = reinterpret_cast<float*>(smem + L.BPs);
   float* uPs = reinterpret_cast<float*>(smem + L.uPs);
-  const int* s_meta = reinterpret_cast<const int*>(smem + L.meta);
+  int* s_meta = reinterpret_cast<int*>(smem + L.meta);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NG = (a.H + G - 1) / G;
@@ -485,7 +488,6 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int g_first = part * a.gpc;
   const int g_count = min(a.gpc, NG - g_first);
   const int hc_begin = g_first * G;
-  const int hc_count = min(g_count * G, a.H - hc_begin);
   const int seq = inst / a.L;
   const int layer = inst % a.L;
   const int d_inner = a.H * kP;
@@ -510,13 +512,39 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
 
-  // Producer = warp 0.  Chunk c goes to stage c % STAGES; the first chunk of a group also
-  // brings the group's inputs (x rows for the conv, e^S and coef of its heads) on x_bar.
-  // A group's x_bar phase completes before the next group's inputs are issued: those go
-  // out with the next group's first chunk, after every warp has released a stage of this
-  // group, i.e. after every warp has waited on this phase.
+  // Producer = warp 0.  Chunk c goes to stage c % STAGES.  A group's inputs (x rows for the
+  // conv, e^S and coef of its heads) come on x_bar: group 0's once the prologue tables are in
+  // (the folded commit's record names the rows), group g's with its first chunk.  A group's
+  // x_bar phase completes before the next group's inputs are issued: those go out with the
+  // next group's first chunk, after every warp has released a stage of this group, i.e.
+  // after every warp has waited on this phase.
+  // x rows, oldest first: the window (the three ring rows before the committed path, then
+  // the path's rows; without a folded commit, the three ring rows before the root), then the
+  // tree's nodes.
   int pf_g = 0, pf_t = 0, pf_k = 0, pf_n = 0;
-  const int head = a.ring_head[inst];
+  int win = 3, head_old = 0;  // window rows, ring head before the window's path (warp 0)
+  auto issue_inputs = [&](int g) {  // warp 0, all lanes
+    const int hb = hc_begin + g * G;
+    const int heads = min(G, a.H - hb);
+    const uint32_t xb = (uint32_t)heads * kP * 2;
+    const int buf = g & 1;
+    if (lane == 0) mbar_arrive_expect_tx(x_bar, xb * (win + n) + (uint32_t)heads * (W.NP + W.PP) * 4);
+    __syncwarp();
+    for (int r = lane; r < win + n; r += 32) {
+      const uint16_t* src;
+      if (r < 3)
+        src = ring + (size_t)ring_pos(head_old, r - 3, R) * conv_dim;
+      else if (r < win)
+        src = a.prev_xBC + ((size_t)inst * a.prev_n + s_meta[4 + r - 3]) * conv_dim;
+      else
+        src = xbc + (size_t)(r - win) * conv_dim;
+      bulk_load(smem_u32(xinX + r * XW), src + hb * kP, xb, x_bar);
+    }
+    if (lane == 0)
+      bulk_load(smem_u32(eSg + buf * G * W.NP), ws + W.eS + (size_t)hb * W.NP * 4, heads * W.NP * 4, x_bar);
+    if (lane == 1)
+      bulk_load(smem_u32(coefg + buf * G * W.PP), ws + W.coef + (size_t)hb * W.PP * 4, heads * W.PP * 4, x_bar);
+  };
   auto produce = [&](int upto) {  // warp 0, all lanes
     while (pf_n < upto && pf_n < total) {
       const int slot = pf_n % STAGES;
@@ -526,28 +554,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         return;
       }
       const int hb = hc_begin + pf_g * G;
-      if (pf_t == 0 && pf_k == 0) {
-        const int heads = min(G, a.H - hb);
-        const uint32_t xb = (uint32_t)heads * kP * 2;
-        const int buf = pf_g & 1;
-        const uint32_t ub = FUSE ? (uint32_t)LP * heads * kP * 4 : 0u;
-        if (lane == 0) mbar_arrive_expect_tx(x_bar, xb * (n + 3) + (uint32_t)heads * (W.NP + W.PP) * 4 + ub);
-        __syncwarp();
-        for (int r = lane; r < n + 3; r += 32) {
-          const uint16_t* src =
-              r < 3 ? ring + (size_t)ring_pos(head, r - 3, R) * conv_dim : xbc + (size_t)(r - 3) * conv_dim;
-          bulk_load(smem_u32(xinX + r * XW), src + hb * kP, xb, x_bar);
-        }
-        if (lane == 0)
-          bulk_load(smem_u32(eSg + buf * G * W.NP), ws + W.eS + (size_t)hb * W.NP * 4, heads * W.NP * 4, x_bar);
-        if (lane == 1)
-          bulk_load(smem_u32(coefg + buf * G * W.PP), ws + W.coef + (size_t)hb * W.PP * 4, heads * W.PP * 4, x_bar);
-        if (FUSE && lane >= 2 && lane < 2 + LP) {
-          const int j = lane - 2;
-          bulk_load(smem_u32(uPs + (buf * LP + j) * ROWS), ws + W.uP + ((size_t)j * d_inner + (size_t)hb * kP) * 4,
-                    heads * kP * 4, x_bar);
-        }
-      }
+      if (pf_t == 0 && pf_k == 0 && pf_g > 0) issue_inputs(pf_g);
       if (lane == 0) {
         mbar_arrive_expect_tx(full_bar(slot), ROWS * SROW * 4);
         tma_load_2d(smem_u32(stage + slot * ROWS * SROW), &tmap, pf_k * KC, (inst * a.H + hb) * kP, full_bar(slot));
@@ -582,27 +589,48 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_init(x_bar, 1);
       fence_barrier_init();
       mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4 +
-                                         (FUSE ? (uint32_t)LP * kN * 4 + 16 : 0u));
+                                         (FUSE ? (uint32_t)LP * kN * 4 + kMetaInts * 4 : 0u));
       bulk_load(smem_u32(nodes), a.layout + (size_t)seq * n, n * (uint32_t)sizeof(ssm_node), pro_bar);
       bulk_load(smem_u32(Cs), ws + W.C, n * CSTR * 4, pro_bar);
       bulk_load(smem_u32(pathn), ws + W.pathn, n * DMAX * 4, pro_bar);
       bulk_load(smem_u32(pairs), ws + W.pairs, (W.PP + 4) * 4, pro_bar);
       if (FUSE) {
         bulk_load(smem_u32(BPs), ws + W.BP, LP * kN * 4, pro_bar);
-        bulk_load(smem_u32(s_meta), ws + W.meta, 16, pro_bar);
+        bulk_load(smem_u32(s_meta), ws + W.meta, kMetaInts * 4, pro_bar);
       }
     }
     __syncwarp();
     produce(STAGES);
+    if (FUSE) {
+      if (!mbar_wait(pro_bar, 0)) {
+        flag(a.status, SSM_STATUS_TIMEOUT);
+        s_abort = 1;
+      } else {
+        win = 3 + min(max(s_meta[0], 1), LP);
+        head_old = s_meta[1];
+      }
+    } else {
+      head_old = a.ring_head[inst];
+    }
+    if (!s_abort) issue_inputs(0);
   }
-  if (tid < hc_count) pD[tid] = a.D[(size_t)layer * a.H + hc_begin + tid];
+  // x conv: two channels per thread (2*cp, 2*cp+1), the nodes split between PARTS threads
+  constexpr int XSTR = xs_stride<G>();
+  constexpr int PAIRS = ROWS / 2;
+  constexpr int PARTS = THREADS / PAIRS;
+  const int NX = (n + 7) & ~7;
+  for (int i = tid; i < (NX - n) * XSTR; i += THREADS) xs[n * XSTR + i] = 0.f;  // padding nodes
+  const int cp = tid % PAIRS, cpart = tid / PAIRS;
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float* cb = a.conv_b + (size_t)layer * conv_dim;
-  float4 wx = make_float4(0.f, 0.f, 0.f, 0.f);  // x conv weights of the next group
-  float bx = 0.f;
-  if (tid < min(G, a.H - hc_begin) * kP) {
-    wx = cw[hc_begin * kP + tid];
-    bx = cb[hc_begin * kP + tid];
+  float4 wx0 = make_float4(0.f, 0.f, 0.f, 0.f), wx1 = wx0;  // x conv weights of the next group
+  float bx0 = 0.f, bx1 = 0.f;
+  if (2 * cp < min(G, a.H - hc_begin) * kP) {
+    const int c = hc_begin * kP + 2 * cp;
+    wx0 = cw[c];
+    wx1 = cw[c + 1];
+    bx0 = cb[c];
+    bx1 = cb[c + 1];
   }
   __syncthreads();  // barriers initialised
   wait_or_abort(pro_bar, 0);
@@ -614,7 +642,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (r.tap[d] >= v || r.tap[d] < -3) r.tap[d] = -1;
     r.depth = v == 0 ? 0 : min(max(r.depth, 0), a.max_depth);
     nodes[v] = r;
-    rowidx[v] = tap_rows(r, v);
+    const int4 t = tap_rows(r, v);  // rows counted from the last three window rows
+    rowidx[v] = make_int4(t.x + lenP, t.y + lenP, t.z + lenP, t.w + lenP);
   }
   __syncthreads();
   for (int v = tid; v < n; v += THREADS) {
@@ -622,6 +651,14 @@ __global__ void __launch_bounds__(THREADS, 2)
     for (int u = 0; u < v; ++u) off += nodes[u].depth + 1;
     poff[v] = off;
   }
+
+  // coef[v,m] of the tree (this warp's head) for nodes v and m: zero unless m is on v's path
+  auto path_coef = [&](const float* chd, int v, int m) -> float {
+    if (v >= n || m > v) return 0.f;
+    const int dm = nodes[m].depth;
+    if (dm > nodes[v].depth || pathn[v * DMAX + dm] != m) return 0.f;
+    return chd[poff[v] + dm];
+  };
 
   // Z tile of a group: 8 warps x (MT m16 tiles) rows x 16 nodes, mma m16n8k8 (TF32, split 3x)
   constexpr int MT = G / 2;
@@ -633,7 +670,6 @@ __global__ void __launch_bounds__(THREADS, 2)
   int q = 0;       // chunk index
   for (int gi = 0; gi < g_count; ++gi) {
     const int hb = hc_begin + gi * G, heads = min(G, a.H - hb);
-    const int hl = gi * G;
     for (int tile = 0; tile < n_tiles; ++tile) {
       int brow[2];
 #pragma unroll
@@ -641,50 +677,100 @@ __global__ void __launch_bounds__(THREADS, 2)
       for (int kc = 0; kc < KCH; ++kc, ++q) {
         if (warp == 0) produce(q + STAGES);  // refill the stage chunk q-1 used
         if (tile == 0 && kc == 0) {
-          // ---- group set-up: x conv + SiLU (four nodes at a time for ILP) ----
+          // ---- group set-up: x conv + SiLU of the tree's nodes (and the committed path's u_j) ----
           __syncthreads();  // every warp is past the previous group's epilogue
           wait_or_abort(x_bar, gi & 1);
-          if (tid < heads * kP) {
-            const uint16_t* __restrict__ xi = xinX + tid;
-            float* __restrict__ xo = xs + tid;
-            int v = 0;
-            for (; v + 4 <= n; v += 4) {
-              float r[4][4];
+          if (2 * cp < heads * kP) {
+            const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
+            float2* __restrict__ xo = reinterpret_cast<float2*>(xs) + cp;                     // node v: xo[v * XSTR/2]
+            const int per = (n + PARTS - 1) / PARTS;
+            const int v1 = min(n, (cpart + 1) * per);
+            int v = cpart * per;
+            for (; v + 4 <= v1; v += 4) {  // four nodes at a time: 16 loads in flight
+              uint32_t r[4][4];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int4 t = rowidx[v + u];
-                r[u][0] = bf16f(xi[t.x * XW]);
-                r[u][1] = bf16f(xi[t.y * XW]);
-                r[u][2] = bf16f(xi[t.z * XW]);
-                r[u][3] = bf16f(xi[t.w * XW]);
+                r[u][0] = xi[t.x * (XW / 2)];
+                r[u][1] = xi[t.y * (XW / 2)];
+                r[u][2] = xi[t.z * (XW / 2)];
+                r[u][3] = xi[t.w * (XW / 2)];
               }
 #pragma unroll
               for (int u = 0; u < 4; ++u)
-                xo[(v + u) * ROWS] = silu_fast(conv4_acc(wx, bx, r[u][0], r[u][1], r[u][2], r[u][3]));
+                xo[(v + u) * (XSTR / 2)] =
+                    make_float2(silu_fast(conv4_acc(wx0, bx0, bf16_lo(r[u][0]), bf16_lo(r[u][1]), bf16_lo(r[u][2]),
+                                                    bf16_lo(r[u][3]))),
+                                silu_fast(conv4_acc(wx1, bx1, bf16_hi(r[u][0]), bf16_hi(r[u][1]), bf16_hi(r[u][2]),
+                                                    bf16_hi(r[u][3]))));
             }
-            for (; v < n; ++v) {
+            for (; v < v1; ++v) {
               const int4 t = rowidx[v];
-              xo[v * ROWS] = silu_fast(conv4_acc(wx, bx, bf16f(xi[t.x * XW]), bf16f(xi[t.y * XW]),
-                                                 bf16f(xi[t.z * XW]), bf16f(xi[t.w * XW])));
+              const uint32_t r0 = xi[t.x * (XW / 2)], r1 = xi[t.y * (XW / 2)], r2 = xi[t.z * (XW / 2)],
+                             r3 = xi[t.w * (XW / 2)];
+              xo[v * (XSTR / 2)] =
+                  make_float2(silu_fast(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
+                              silu_fast(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
+            }
+            if (FUSE) {  // u_j = w_{j,h}·x_j of the committed path (window rows j .. j+3)
+              const float* wj = eSg + ((gi & 1) * G + (2 * cp) / kP) * W.NP + n + 1;
+              for (int j = cpart; j < lenP; j += PARTS) {
+                const uint32_t r0 = xi[j * (XW / 2)], r1 = xi[(j + 1) * (XW / 2)], r2 = xi[(j + 2) * (XW / 2)],
+                               r3 = xi[(j + 3) * (XW / 2)];
+                *reinterpret_cast<float2*>(uPs + j * ROWS + 2 * cp) = make_float2(
+                    wj[j] * silu_fast(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
+                    wj[j] * silu_fast(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
+              }
             }
           }
           if (FUSE) Ew = eSg[((gi & 1) * G + min(whead, heads - 1)) * W.NP + n];
           if (gi + 1 < g_count) {  // prefetch the next group's x conv weights
             const int hn = hb + G;
-            if (tid < min(G, a.H - hn) * kP) {
-              wx = cw[hn * kP + tid];
-              bx = cb[hn * kP + tid];
+            if (2 * cp < min(G, a.H - hn) * kP) {
+              const int c = hn * kP + 2 * cp;
+              wx0 = cw[c];
+              wx1 = cw[c + 1];
+              bx0 = cb[c];
+              bx1 = cb[c + 1];
             }
           }
           __syncthreads();
         }
         if (kc == 0) {
+          // the tile's accumulator starts at Σ_m coef[v,m]·x_m[p] (path terms and D·x over e^{S_v}):
+          // A = x rows of the nodes m (K), B = coef of node v (N; zero off v's path)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
+          const float* chd = coefg + ((gi & 1) * G + min(whead, heads - 1)) * W.PP;
+          const int ksteps = min(2 * (tile + 1), NX / 8);  // ancestors precede their nodes
+          for (int k8 = 0; k8 < ksteps; ++k8) {
+            uint32_t bhi[2][2], blo[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              const int v = tile * NT + nt * 8 + fg;
+              split_tf32(path_coef(chd, v, k8 * 8 + ft), bhi[nt][0], blo[nt][0]);
+              split_tf32(path_coef(chd, v, k8 * 8 + ft + 4), bhi[nt][1], blo[nt][1]);
+            }
+            const float* xa = xs + (k8 * 8 + ft) * XSTR + wrow + fg;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              uint32_t ahi[4], alo[4];
+              split_tf32(xa[mt * 16], ahi[0], alo[0]);
+              split_tf32(xa[mt * 16 + 8], ahi[1], alo[1]);
+              split_tf32(xa[4 * XSTR + mt * 16], ahi[2], alo[2]);
+              split_tf32(xa[4 * XSTR + mt * 16 + 8], ahi[3], alo[3]);
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt) {
+                mma_tf32(acc[mt][nt], alo, bhi[nt]);
+                mma_tf32(acc[mt][nt], ahi, blo[nt]);
+                mma_tf32(acc[mt][nt], ahi, bhi[nt]);
+              }
+            }
+          }
         }
         const int slot = q % STAGES;
         wait_or_abort(full_bar(slot), (q / STAGES) & 1);
@@ -708,7 +794,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             ra[mt].x *= Ew; ra[mt].y *= Ew; ra[mt].z *= Ew; ra[mt].w *= Ew;
             rb[mt].x *= Ew; rb[mt].y *= Ew; rb[mt].z *= Ew; rb[mt].w *= Ew;
           }
-          const float* ur = uPs + (gi & 1) * LP * ROWS + wrow + fg;
+          const float* ur = uPs + wrow + fg;
           const float* br = BPs + kc * KC + 4 * ft;
           for (int j = 0; j < lenP; ++j) {
             const float4 bj = *reinterpret_cast<const float4*>(br + j * kN);
@@ -763,10 +849,8 @@ __global__ void __launch_bounds__(THREADS, 2)
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
         if (kc == KCH - 1 && whead < heads) {
-          // ---- epilogue: y = e^{S_v}·Z + Σ_path coef·x_m + D·x_v ----
-          const float Dh = pD[hl + whead];
+          // ---- epilogue: y = e^{S_v}·acc ----
           const float* eh = eSg + ((gi & 1) * G + whead) * W.NP;
-          const float* chd = coefg + ((gi & 1) * G + whead) * W.PP;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -774,29 +858,11 @@ __global__ void __launch_bounds__(THREADS, 2)
               const int v = tile * NT + nt * 8 + 2 * ft + c;
               if (v >= n) continue;
               const float es = eh[v];
-              float yv[MT][2];
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                yv[mt][0] = es * acc[mt][nt][c];
-                yv[mt][1] = es * acc[mt][nt][2 + c];
-              }
-              const int dv = nodes[v].depth;
-              const int pb = poff[v];
-              for (int jj = 0; jj <= dv; ++jj) {
-                const float cf = chd[pb + jj];
-                const float* xm = xs + pathn[v * DMAX + jj] * ROWS + wrow + fg;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                  yv[mt][0] = fmaf(cf, xm[mt * 16], yv[mt][0]);
-                  yv[mt][1] = fmaf(cf, xm[mt * 16 + 8], yv[mt][1]);
-                }
-              }
-              const float* xv = xs + v * ROWS + wrow + fg;
               float* yrow = a.y + ((size_t)inst * n + v) * d_inner + hb * kP + wrow + fg;
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
-                yrow[mt * 16] = fmaf(Dh, xv[mt * 16], yv[mt][0]);
-                yrow[mt * 16 + 8] = fmaf(Dh, xv[mt * 16 + 8], yv[mt][1]);
+                yrow[mt * 16] = es * acc[mt][nt][c];
+                yrow[mt * 16 + 8] = es * acc[mt][nt][2 + c];
               }
             }
         }

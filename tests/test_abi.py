@@ -156,6 +156,7 @@ def test_commit_verify_validation(L):
     assert _commit_verify(L, d, p, lp=17) == B.SSM_ERR_RANGE  # paths of trees the tree kernel verifies
     assert _commit_verify(L, d, p, prev_n=0) == B.SSM_ERR_RANGE
     assert _commit_verify(L, d, p, prev_n=65) == B.SSM_ERR_RANGE
+    assert _commit_verify(L, _dims(ring_cap=7), p, lp=5) == B.SSM_ERR_CAPACITY  # rows before the path kept
     assert _commit_verify(L, d, p, n=256, depth=255) == B.SSM_ERR_CAPACITY  # long chains: separate calls
     assert "chain" in B.ssm_last_error()
     assert _commit_verify(L, d, p, n=8, depth=8) == B.SSM_ERR_RANGE
