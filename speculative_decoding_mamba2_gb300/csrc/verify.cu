@@ -26,8 +26,9 @@
 //    group's h0 slice through a 4-stage ring of 16-column chunks (2-D bulk
 //    tensor copies with 64-byte swizzle, full/empty mbarriers, warp 0 as
 //    producer) and contracts each chunk against C on the tensor cores
-//    (mma m16n8k8 TF32 with a 3-term hi/lo split, fp32 accumulate: fp32-level
-//    accuracy).  The path terms are a small (rows x nodes) · (nodes x nodes)
+//    (mma m16n8k16 on bf16 hi/lo splits of both operands, three products
+//    hi·hi + hi·lo + lo·hi, fp32 accumulate: each product to ~2^-17
+//    relative, far inside the 1e-3 output bound).  The path terms are a small (rows x nodes) · (nodes x nodes)
 //    product that starts each node tile's accumulator, on the same tensor
 //    cores; the epilogue only scales by e^{S_v} and writes y.
 //
@@ -62,7 +63,8 @@ constexpr int SROW = KC;         // stage row: 64 B, 16-byte pieces swizzled by 
 constexpr int THREADS = 256;
 constexpr int DMAX = SSM_MAX_DEPTH + 1;
 constexpr int XW = 256;          // channels per staged input row
-constexpr int CSTR = kN + 16;    // padded row of the C table (conflict-free 16-byte B-fragment loads)
+constexpr int CSTR = kN + 16;    // padded row of the C tables: fp32 in the prep, bf16 hi/lo in the workspace
+                                 // (288-byte bf16 rows: conflict-free 8-byte B-fragment loads)
 constexpr int MAX_GPC = 8;       // head groups per CTA
 constexpr int SMEM_LIMIT = 232448;
 constexpr int kMetaInts = 20;    // folded-commit record: [0] path length, [1] ring head before it, [4..19] nodes
@@ -87,7 +89,7 @@ __host__ __device__ inline Ws ws_layout(int n, int max_depth, int H, int LP = 0)
     o += (b + 15) & ~size_t(15);
     return r;
   };
-  w.C = take((size_t)n * CSTR * 4);        // post-conv C [n][CSTR]
+  w.C = take((size_t)n * CSTR * 4);        // post-conv C as bf16 hi [n][CSTR], then bf16 lo [n][CSTR]
   w.eS = take((size_t)H * w.NP * 4);       // e^{S_v} [H][NP]
   w.coef = take((size_t)H * w.PP * 4);     // coef [H][PP] in pair order
   w.pathn = take((size_t)n * DMAX * 4);    // ancestor of v at depth j [n][DMAX]
@@ -308,9 +310,16 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     }
   }
   {  // workspace: C table, path tables
-    const float4* src = reinterpret_cast<const float4*>(Cs);
-    float4* dstC = reinterpret_cast<float4*>(ws + W.C);
-    for (int i = tid; i < n * CSTR / 4; i += THREADS) dstC[i] = src[i];
+    // C split once for the tensor cores: C = hi + lo (bf16 pairs, 2^-18 relative)
+    uint32_t* dhi = reinterpret_cast<uint32_t*>(ws + W.C);
+    uint32_t* dlo = dhi + n * CSTR / 2;
+    for (int i = tid; i < n * CSTR / 2; i += THREADS) {
+      const int v = i / (CSTR / 2), k = 2 * (i - v * (CSTR / 2));
+      uint32_t hi = 0, lo = 0;
+      if (k < kN) split_bf16x2(Cs[v * CSTR + k], Cs[v * CSTR + k + 1], hi, lo);
+      dhi[i] = hi;
+      dlo[i] = lo;
+    }
     int* dp = reinterpret_cast<int*>(ws + W.pathn);
     for (int i = tid; i < n * DMAX; i += THREADS) dp[i] = pathn[i];
     int* dq = reinterpret_cast<int*>(ws + W.pairs);
@@ -419,10 +428,11 @@ struct Smem {
   int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
 };
 
-// x rows of a group: node v at xs[v * xs_stride<G>()], rows padded by 8 floats so that the
-// path-term A fragments (8 rows x 4 nodes per load) hit 32 different banks; nodes padded to 8
+// x rows of a group: node v at xs[v * xs_stride<G>()], rows padded by 4 floats so that the
+// path-term A fragments (8 rows x 4 node pairs per load) hit 32 different banks; nodes
+// padded to 16 (one k-step of the path-term product)
 template <int G>
-__host__ __device__ constexpr int xs_stride() { return G * kP + 8; }
+__host__ __device__ constexpr int xs_stride() { return G * kP + 4; }
 
 template <int G, bool FUSE>
 __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
@@ -444,7 +454,7 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   s.pathn = take(n * DMAX * 4);
   s.pairs = take((PP + 4) * 4);
   s.Cs = take(n * CSTR * 4);
-  s.xs = take(((n + 7) & ~7) * xs_stride<G>() * 4);
+  s.xs = take(((n + 15) & ~15) * xs_stride<G>() * 4);
   s.xinX = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows before the path ‖ path rows][tree rows]
   s.eSg = take(2 * G * NP * 4);    // two groups in flight: the next group's inputs land
   s.coefg = take(2 * G * PP * 4);  // before the current group's epilogue
@@ -471,7 +481,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   int* poff = reinterpret_cast<int*>(smem + L.poff);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
   int* pairs = reinterpret_cast<int*>(smem + L.pairs);
-  float* Cs = reinterpret_cast<float*>(smem + L.Cs);
+  const uint16_t* Chi = reinterpret_cast<const uint16_t*>(smem + L.Cs);  // bf16 [n][CSTR]
+  const uint16_t* Clo = Chi + n * CSTR;                                   // bf16 [n][CSTR]
   float* xs = reinterpret_cast<float*>(smem + L.xs);
   uint16_t* xinX = reinterpret_cast<uint16_t*>(smem + L.xinX);
   float* eSg = reinterpret_cast<float*>(smem + L.eSg);
@@ -591,7 +602,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4 +
                                          (FUSE ? (uint32_t)LP * kN * 4 + kMetaInts * 4 : 0u));
       bulk_load(smem_u32(nodes), a.layout + (size_t)seq * n, n * (uint32_t)sizeof(ssm_node), pro_bar);
-      bulk_load(smem_u32(Cs), ws + W.C, n * CSTR * 4, pro_bar);
+      bulk_load(smem_u32(smem + L.Cs), ws + W.C, n * CSTR * 4, pro_bar);
       bulk_load(smem_u32(pathn), ws + W.pathn, n * DMAX * 4, pro_bar);
       bulk_load(smem_u32(pairs), ws + W.pairs, (W.PP + 4) * 4, pro_bar);
       if (FUSE) {
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   constexpr int XSTR = xs_stride<G>();
   constexpr int PAIRS = ROWS / 2;
   constexpr int PARTS = THREADS / PAIRS;
-  const int NX = (n + 7) & ~7;
+  const int NX = (n + 15) & ~15;
   for (int i = tid; i < (NX - n) * XSTR; i += THREADS) xs[n * XSTR + i] = 0.f;  // padding nodes
   const int cp = tid % PAIRS, cpart = tid / PAIRS;
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
@@ -660,7 +671,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     return chd[poff[v] + dm];
   };
 
-  // Z tile of a group: 8 warps x (MT m16 tiles) rows x 16 nodes, mma m16n8k8 (TF32, split 3x)
+  // Z tile of a group: 8 warps x (MT m16 tiles) rows x 16 nodes, mma m16n8k16 (bf16 hi/lo, 3 products)
   constexpr int MT = G / 2;
   const int fg = lane >> 2, ft = lane & 3;  // fragment row group / thread-in-group
   const int wrow = warp * 16 * MT;          // first state row of this warp within the group
@@ -746,36 +757,39 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
               for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
           const float* chd = coefg + ((gi & 1) * G + min(whead, heads - 1)) * W.PP;
-          const int ksteps = min(2 * (tile + 1), NX / 8);  // ancestors precede their nodes
-          for (int k8 = 0; k8 < ksteps; ++k8) {
+          const int ksteps = min(tile + 1, NX / 16);  // ancestors precede their nodes
+          for (int k16 = 0; k16 < ksteps; ++k16) {
+            // k = node m: lane (fg, ft) holds m = 2ft, 2ft+1 and 2ft+8, 2ft+9 of the k-step
+            const int m0 = k16 * 16 + 2 * ft;
             uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
               const int v = tile * NT + nt * 8 + fg;
-              split_tf32(path_coef(chd, v, k8 * 8 + ft), bhi[nt][0], blo[nt][0]);
-              split_tf32(path_coef(chd, v, k8 * 8 + ft + 4), bhi[nt][1], blo[nt][1]);
+              split_bf16x2(path_coef(chd, v, m0), path_coef(chd, v, m0 + 1), bhi[nt][0], blo[nt][0]);
+              split_bf16x2(path_coef(chd, v, m0 + 8), path_coef(chd, v, m0 + 9), bhi[nt][1], blo[nt][1]);
             }
-            const float* xa = xs + (k8 * 8 + ft) * XSTR + wrow + fg;
+            const float* xa = xs + m0 * XSTR + wrow + fg;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
+              const float* x0 = xa + mt * 16;
               uint32_t ahi[4], alo[4];
-              split_tf32(xa[mt * 16], ahi[0], alo[0]);
-              split_tf32(xa[mt * 16 + 8], ahi[1], alo[1]);
-              split_tf32(xa[4 * XSTR + mt * 16], ahi[2], alo[2]);
-              split_tf32(xa[4 * XSTR + mt * 16 + 8], ahi[3], alo[3]);
+              split_bf16x2(x0[0], x0[XSTR], ahi[0], alo[0]);
+              split_bf16x2(x0[8], x0[XSTR + 8], ahi[1], alo[1]);
+              split_bf16x2(x0[8 * XSTR], x0[9 * XSTR], ahi[2], alo[2]);
+              split_bf16x2(x0[8 * XSTR + 8], x0[9 * XSTR + 8], ahi[3], alo[3]);
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
-                mma_tf32(acc[mt][nt], alo, bhi[nt]);
-                mma_tf32(acc[mt][nt], ahi, blo[nt]);
-                mma_tf32(acc[mt][nt], ahi, bhi[nt]);
+                mma_bf16(acc[mt][nt], alo, bhi[nt]);
+                mma_bf16(acc[mt][nt], ahi, blo[nt]);
+                mma_bf16(acc[mt][nt], ahi, bhi[nt]);
               }
             }
           }
         }
         const int slot = q % STAGES;
         wait_or_abort(full_bar(slot), (q / STAGES) & 1);
-        // Contraction order within the 16-column chunk: k-step s (0, 1) takes columns
-        // 4t+2s (k = t) and 4t+2s+1 (k = t+4), t = 0..3, so lane (fg, ft) needs exactly the
+        // Contraction order within the 16-column chunk (one m16n8k16 k-step): k = 2t, 2t+1,
+        // 2t+8, 2t+9 take columns 4t .. 4t+3, t = 0..3, so lane (fg, ft) needs exactly the
         // 16-byte piece ft of each of its rows wrow + 16*mt + fg (+8), and of each C row.
         // The copy engine's 64-byte swizzle XORs the piece index with address bits 7..8.
         const unsigned char* st = reinterpret_cast<const unsigned char*>(stage + slot * ROWS * SROW);
@@ -820,30 +834,28 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
           }
         }
-        float4 cv[2];  // C rows of this lane's two B-fragment nodes, columns 4*ft .. 4*ft+3
+        uint32_t bhi[2][2], blo[2][2];  // C of this lane's two B-fragment nodes, columns 4*ft .. 4*ft+3
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) cv[nt] = *reinterpret_cast<const float4*>(Cs + brow[nt] + kc * KC + 4 * ft);
+        for (int nt = 0; nt < 2; ++nt) {
+          const uint2 h2 = *reinterpret_cast<const uint2*>(Chi + brow[nt] + kc * KC + 4 * ft);
+          const uint2 l2 = *reinterpret_cast<const uint2*>(Clo + brow[nt] + kc * KC + 4 * ft);
+          bhi[nt][0] = h2.x;
+          bhi[nt][1] = h2.y;
+          blo[nt][0] = l2.x;
+          blo[nt][1] = l2.y;
+        }
 #pragma unroll
-        for (int ks = 0; ks < KC / 8; ++ks) {
-          uint32_t bhi[2][2], blo[2][2];
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t ahi[4], alo[4];
+          split_bf16x2(ra[mt].x, ra[mt].y, ahi[0], alo[0]);
+          split_bf16x2(rb[mt].x, rb[mt].y, ahi[1], alo[1]);
+          split_bf16x2(ra[mt].z, ra[mt].w, ahi[2], alo[2]);
+          split_bf16x2(rb[mt].z, rb[mt].w, ahi[3], alo[3]);
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt) {
-            split_tf32(ks ? cv[nt].z : cv[nt].x, bhi[nt][0], blo[nt][0]);
-            split_tf32(ks ? cv[nt].w : cv[nt].y, bhi[nt][1], blo[nt][1]);
-          }
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            uint32_t ahi[4], alo[4];
-            split_tf32(ks ? ra[mt].z : ra[mt].x, ahi[0], alo[0]);
-            split_tf32(ks ? rb[mt].z : rb[mt].x, ahi[1], alo[1]);
-            split_tf32(ks ? ra[mt].w : ra[mt].y, ahi[2], alo[2]);
-            split_tf32(ks ? rb[mt].w : rb[mt].y, ahi[3], alo[3]);
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              mma_tf32(acc[mt][nt], alo, bhi[nt]);
-              mma_tf32(acc[mt][nt], ahi, blo[nt]);
-              mma_tf32(acc[mt][nt], ahi, bhi[nt]);
-            }
+            mma_bf16(acc[mt][nt], alo, bhi[nt]);
+            mma_bf16(acc[mt][nt], ahi, blo[nt]);
+            mma_bf16(acc[mt][nt], ahi, bhi[nt]);
           }
         }
         __syncwarp();
