@@ -192,6 +192,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+// Programmatic dependent launch: the primary grid lets its dependent grid be scheduled;
+// the dependent waits until the primary grid has completed and its writes are visible
+// (a no-op when the kernel was not launched as a dependent).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 // 2-D tiled bulk tensor copy global -> shared, completion counted on `bar`
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {
   asm volatile(
