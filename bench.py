@@ -215,7 +215,7 @@ class OracleRunner:
         self.pool.join()
 
 
-def cpu_baseline(w, steps=8):
+def cpu_baseline(w, steps=64):
     r = OracleRunner(w)
     r.step()  # warm the workers (imports)
     units = secs = 0.0
@@ -584,10 +584,11 @@ def run_draft(args, dev, stream, peak, world, rank):
 
 def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     """Same rounds through the public API with each round's inputs in pinned host
-    memory: host layout build, H2D of xBC/dt/layout/tokens into one of two device
-    buffers, ssm_commit_verify (the previous round's path, this round's tree),
-    ssm_accept_path, D2H of the accepted paths and bonus tokens, all inside the
-    timed region (wall clock, synchronised every round)."""
+    memory.  Per round, inside the timed region: the host layout build; the H2D of
+    xBC/dt/layout/tokens into one of two device buffers, in four chunks of sequences on
+    a copy stream; per chunk, as soon as it has landed, ssm_commit_verify (the previous
+    round's path, this round's tree) and ssm_accept_path on the compute stream; then the
+    D2H of the accepted paths and bonus tokens and a synchronize."""
     import numpy as np
     import torch
 
@@ -596,8 +597,8 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     S, L, n = len(b["seqs"]), w.n_layers, w.n_nodes()
     I = S * L
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    xBC_h = pin(b["xBC"].view(np.int16))
-    dt_h = pin(b["dt"].view(np.int16))
+    xBC_h = pin(b["xBC"].view(np.int16)).view(S, L * n * dims.conv_dim)
+    dt_h = pin(b["dt"].view(np.int16)).view(S, L * n * dims.n_heads)
     par_h = np.ascontiguousarray(b["parent"])
     tok_h, tgt_h = pin(b["tok"]), pin(b["tgt"])
     xBC_d = [torch.empty(xBC_h.shape, dtype=torch.int16, device=dev) for _ in range(2)]
@@ -605,7 +606,11 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     lay_d = [torch.empty((S, n, 8), dtype=torch.int32, device=dev) for _ in range(2)]
     tok_d = torch.empty(tok_h.shape, dtype=torch.int32, device=dev)
     tgt_d = torch.empty(tgt_h.shape, dtype=torch.int32, device=dev)
-    y = torch.empty((I, n, dims.d_inner), device=dev)
+    y = torch.empty((S, L * n * dims.d_inner), device=dev)
+    hv = h.view(S, -1)
+    ringv = ring.view(S, -1)
+    headv = head.view(S, L)
+    wsv = ws_f.view(S, -1)  # the workspace is per instance, sequence-major
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     steps = max(3, min(args.steps, args.e2e_steps))
     lay0, depth = ssm_tree_layout_build(par_h, max_branches=3, max_depth=4)
@@ -614,25 +619,35 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     plen = torch.empty(S, dtype=torch.int32, device=dev)
     bonus = torch.empty(S, dtype=torch.int32, device=dev)
     out = torch.empty((S, max_path + 2), dtype=torch.int32).pin_memory()
+    lay_pin = torch.empty((S, n, 8), dtype=torch.int32).pin_memory()
+    copy_stream = torch.cuda.Stream(dev)
+    n_chunks = 4 if S % 4 == 0 else 1
+    per = S // n_chunks
     state = {"r": 0, "depth": depth}
-
-    def upload(buf):
-        lay, dp = ssm_tree_layout_build(par_h, max_branches=3, max_depth=4)
-        lay_d[buf].copy_(torch.from_numpy(lay).pin_memory(), non_blocking=True)
-        xBC_d[buf].copy_(xBC_h, non_blocking=True)
-        dt_d[buf].copy_(dt_h, non_blocking=True)
-        tok_d.copy_(tok_h, non_blocking=True)
-        tgt_d.copy_(tgt_h, non_blocking=True)
-        return dp
 
     def one():
         cur, prev = (state["r"] + 1) % 2, state["r"] % 2
         state["r"] += 1
-        dp = upload(cur)
-        ssm_commit_verify(dims, prm, S, n, lay_d[prev], state["depth"] + 1, path, plen, xBC_d[prev].view(torch.bfloat16),
-                          dt_d[prev].view(torch.bfloat16), n, dp, lay_d[cur], xBC_d[cur].view(torch.bfloat16),
-                          dt_d[cur].view(torch.bfloat16), h, ring, head, y, ws_f, status)
-        ssm_accept_path(S, n, dp + 1, lay_d[cur], tok_d, tgt_d, path, plen, bonus, status)
+        lay, dp = ssm_tree_layout_build(par_h, max_branches=3, max_depth=4)
+        lay_pin.numpy()[...] = lay
+        copy_stream.wait_stream(stream)  # the previous round is finished with both buffers
+        for c in range(n_chunks):
+            q = slice(c * per, (c + 1) * per)
+            with torch.cuda.stream(copy_stream):
+                lay_d[cur][q].copy_(lay_pin[q], non_blocking=True)
+                xBC_d[cur][q].copy_(xBC_h[q], non_blocking=True)
+                dt_d[cur][q].copy_(dt_h[q], non_blocking=True)
+                tok_d[q].copy_(tok_h[q], non_blocking=True)
+                tgt_d[q].copy_(tgt_h[q], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(copy_stream)
+            stream.wait_event(landed)
+            ssm_commit_verify(dims, prm, per, n, lay_d[prev][q], state["depth"] + 1, path[q], plen[q],
+                              xBC_d[prev][q].view(torch.bfloat16), dt_d[prev][q].view(torch.bfloat16), n, dp,
+                              lay_d[cur][q], xBC_d[cur][q].view(torch.bfloat16), dt_d[cur][q].view(torch.bfloat16),
+                              hv[q], ringv[q], headv[q], y[q], wsv[q], status, stream)
+            ssm_accept_path(per, n, dp + 1, lay_d[cur][q], tok_d[q], tgt_d[q], path[q], plen[q], bonus[q], status,
+                            stream)
         state["depth"] = dp
         out[:, :max_path].copy_(path, non_blocking=True)
         out[:, max_path].copy_(plen, non_blocking=True)
@@ -642,7 +657,11 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
 
     # the first round needs an accepted path to commit: accept the tree of buffer 0 (the
     # state it would be verified from is the one the device holds)
-    upload(0)
+    lay_d[0].copy_(torch.from_numpy(lay0))
+    xBC_d[0].copy_(xBC_h)
+    dt_d[0].copy_(dt_h)
+    tok_d.copy_(tok_h)
+    tgt_d.copy_(tgt_h)
     ssm_accept_path(S, n, max_path, lay_d[0], tok_d, tgt_d, path, plen, bonus, status)
     for _ in range(2):
         one()
@@ -663,7 +682,9 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     d2h = S * (max_path + 2) * 4
     return {"value": n * L * S * world / secs, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": secs * 1e3,
-            "calls": "ssm_tree_layout_build, ssm_commit_verify, ssm_accept_path"}
+            "calls": "ssm_tree_layout_build, ssm_commit_verify, ssm_accept_path",
+            "overlap": f"H2D in {n_chunks} chunks of sequences on a copy stream; each chunk's calls start when "
+                       "its inputs have landed"}
 
 
 def main():
