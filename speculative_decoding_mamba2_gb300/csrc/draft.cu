@@ -93,12 +93,19 @@ __global__ void __launch_bounds__(DTHREADS) draft_step_kernel(DraftArgs a) {
   const float* hin = a.h_in + ((size_t)inst * a.H + h_begin) * kP * kN;
   float* hout = a.h_out + ((size_t)inst * a.H + h_begin) * kP * kN;
   const int rows = heads * kP;
-  constexpr int U = 4;
-  for (int r0w = warp * U; r0w < rows; r0w += (DTHREADS / 32) * U) {
+  constexpr int U = 4;                       // rows per step of a warp
+  constexpr int STRIDE = (DTHREADS / 32) * U;
+  float4 nx[U];                              // the warp's next U rows, loaded one step ahead
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (warp * U + u < rows) nx[u] = reinterpret_cast<const float4*>(hin + (size_t)(warp * U + u) * kN)[lane];
+  for (int r0w = warp * U; r0w < rows; r0w += STRIDE) {
     float4 hv[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (r0w + u < rows) hv[u] = reinterpret_cast<const float4*>(hin + (size_t)(r0w + u) * kN)[lane];
+    for (int u = 0; u < U; ++u) {
+      hv[u] = nx[u];
+      if (r0w + STRIDE + u < rows) nx[u] = reinterpret_cast<const float4*>(hin + (size_t)(r0w + STRIDE + u) * kN)[lane];
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int row = r0w + u;
@@ -123,12 +130,16 @@ __global__ void __launch_bounds__(DTHREADS) draft_step_kernel(DraftArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// replay
+// replay: one warp per state row at a time (lane = 4 columns); a pass covers up to RT
+// logged steps, whose B columns each lane keeps in registers and whose u = Δ·x sit in
+// shared memory (one value per step and row); the update uses packed pairs with the same
+// two roundings per element as the draft step: h = fma(a, h, u·b)
 // ---------------------------------------------------------------------------
-constexpr int RG = 4;
-constexpr int RROWS = RG * kP;
-constexpr int RT = 16;  // log rows per sweep
-constexpr int RTHREADS = 256;
+constexpr int RW = 8;               // warps per CTA
+constexpr int RTHREADS = RW * 32;
+constexpr int RH = 2;               // heads per CTA
+constexpr int RROWS = RH * kP;      // 128 state rows, 16 per warp
+constexpr int RT = 16;              // logged steps per pass
 
 __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool report) {
   const int seq = inst / a.L;
@@ -141,70 +152,101 @@ __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool repo
   return k;
 }
 
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long p) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __global__ void __launch_bounds__(RTHREADS) replay_kernel(ReplayArgs a) {
-  __shared__ __align__(16) float Bs[RT][kN];
-  __shared__ float xs[RT][RROWS];
-  __shared__ float dls[RT][RG], decs[RT][RG];
-  const int tid = threadIdx.x;
-  const int n_groups = (a.H + RG - 1) / RG;
+  __shared__ float us[RT][RROWS];  // u = Δ_t·x_t[row]
+  __shared__ float decs[RT][RH];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n_groups = (a.H + RH - 1) / RH;
   const int grp = blockIdx.x % n_groups;
   const int inst = blockIdx.x / n_groups;
   const int layer = inst % a.L;
-  const int h_begin = grp * RG;
-  const int heads = min(RG, a.H - h_begin);
+  const int h_begin = grp * RH;
+  const int heads = min(RH, a.H - h_begin);
+  const int rows = heads * kP;
   const int d_inner = a.H * kP;
   const int k = replay_k(a, inst, grp == 0 && tid == 0);
   float* hs = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
-  const int n4 = heads * kP * kN / 4;
+  const int row0 = warp * (RROWS / RW);  // this warp's 16 rows, all of one head
+  const int g = row0 / kP;
 
   for (int t0 = 0; t0 < k; t0 += RT) {
     const int cnt = min(RT, k - t0);
-    if (t0 > 0) __syncthreads();
-    for (int i = tid; i < cnt * kN; i += RTHREADS) {
-      const int t = i / kN, nn = i % kN;
-      Bs[t][nn] = a.log_B[((size_t)inst * a.log_cap + t0 + t) * kN + nn];
-    }
+    if (t0 > 0) __syncthreads();  // the previous pass is done with us / decs
     for (int i = tid; i < cnt * RROWS; i += RTHREADS) {
-      const int t = i / RROWS, r = i % RROWS;
-      xs[t][r] = r < heads * kP ? a.log_x[((size_t)inst * a.log_cap + t0 + t) * d_inner + h_begin * kP + r] : 0.f;
-    }
-    if (tid < cnt * RG) {
-      const int t = tid / RG, g = tid % RG;
-      float d = 0.f, e = 1.f;
-      if (g < heads) {
-        const int h = h_begin + g;
-        d = a.log_delta[((size_t)inst * a.log_cap + t0 + t) * a.H + h];
-        e = decay_of(d, neg_exp(a.A_log[(size_t)layer * a.H + h]));
+      const int t = i / RROWS, r = i - t * RROWS;
+      float u = 0.f;
+      if (r < rows) {
+        const size_t lrow = (size_t)inst * a.log_cap + t0 + t;
+        u = __fmul_rn(a.log_delta[lrow * a.H + h_begin + r / kP], a.log_x[lrow * d_inner + h_begin * kP + r]);
       }
-      dls[t][g] = d;
-      decs[t][g] = e;
+      us[t][r] = u;
+    }
+    if (tid < cnt * RH) {
+      const int t = tid / RH, gg = tid - t * RH;
+      float e = 1.f;
+      if (gg < heads) {
+        const int h = h_begin + gg;
+        e = decay_of(a.log_delta[((size_t)inst * a.log_cap + t0 + t) * a.H + h],
+                     neg_exp(a.A_log[(size_t)layer * a.H + h]));
+      }
+      decs[t][gg] = e;
+    }
+    // this lane's B columns 4*lane .. 4*lane+3 for the pass's steps, as packed pairs
+    unsigned long long b01[RT], b23[RT];
+#pragma unroll
+    for (int t = 0; t < RT; ++t) {
+      float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < cnt) bv = reinterpret_cast<const float4*>(a.log_B + ((size_t)inst * a.log_cap + t0 + t) * kN)[lane];
+      b01[t] = pack2(bv.x, bv.y);
+      b23[t] = pack2(bv.z, bv.w);
     }
     __syncthreads();
-    for (int e0 = tid; e0 < n4; e0 += RTHREADS * 4) {
-      float4 hv[4];
+    if (g < heads) {
+      unsigned long long dec2[RT];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * RTHREADS;
-        if (e < n4) hv[u] = reinterpret_cast<const float4*>(hs)[e];
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int e = e0 + u * RTHREADS;
-        if (e >= n4) continue;
-        const int row = e / (kN / 4);
-        const int g = row / kP;
-        const int nn = (e % (kN / 4)) * 4;
-        float4 h4 = hv[u];
-        for (int t = 0; t < cnt; ++t) {
-          const float uu = __fmul_rn(dls[t][g], xs[t][row]);
-          const float dec = decs[t][g];
-          const float4 b4 = *reinterpret_cast<const float4*>(&Bs[t][nn]);
-          h4.x = ssm_update(dec, h4.x, uu, b4.x);
-          h4.y = ssm_update(dec, h4.y, uu, b4.y);
-          h4.z = ssm_update(dec, h4.z, uu, b4.z);
-          h4.w = ssm_update(dec, h4.w, uu, b4.w);
+      for (int t = 0; t < RT; ++t) dec2[t] = pack2(decs[t][g], decs[t][g]);
+      const int row_end = row0 + RROWS / RW;
+      float4 n0 = reinterpret_cast<const float4*>(hs + (size_t)row0 * kN)[lane];
+      float4 n1 = reinterpret_cast<const float4*>(hs + (size_t)(row0 + 1) * kN)[lane];
+      for (int r = row0; r < row_end; r += 2) {  // two rows in work, the next two in flight
+        float4* p0 = reinterpret_cast<float4*>(hs + (size_t)r * kN) + lane;
+        float4* p1 = reinterpret_cast<float4*>(hs + (size_t)(r + 1) * kN) + lane;
+        const float4 h0 = n0, h1 = n1;
+        if (r + 2 < row_end) {
+          n0 = reinterpret_cast<const float4*>(hs + (size_t)(r + 2) * kN)[lane];
+          n1 = reinterpret_cast<const float4*>(hs + (size_t)(r + 3) * kN)[lane];
         }
-        reinterpret_cast<float4*>(hs)[e] = h4;
+        unsigned long long a01 = pack2(h0.x, h0.y), a23 = pack2(h0.z, h0.w);
+        unsigned long long c01 = pack2(h1.x, h1.y), c23 = pack2(h1.z, h1.w);
+#pragma unroll
+        for (int t = 0; t < RT; ++t) {
+          if (t < cnt) {
+            const unsigned long long u0 = pack2(us[t][r], us[t][r]), u1 = pack2(us[t][r + 1], us[t][r + 1]);
+            a01 = ffma2(dec2[t], a01, fmul2(u0, b01[t]));
+            a23 = ffma2(dec2[t], a23, fmul2(u0, b23[t]));
+            c01 = ffma2(dec2[t], c01, fmul2(u1, b01[t]));
+            c23 = ffma2(dec2[t], c23, fmul2(u1, b23[t]));
+          }
+        }
+        const float2 x01 = unpack2(a01), x23 = unpack2(a23), y01 = unpack2(c01), y23 = unpack2(c23);
+        *p0 = make_float4(x01.x, x01.y, x23.x, x23.y);
+        *p1 = make_float4(y01.x, y01.y, y23.x, y23.y);
       }
     }
   }
@@ -230,7 +272,7 @@ cudaError_t launch_draft_step(const DraftArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_replay(const ReplayArgs& a, cudaStream_t s) {
-  const int n_groups = (a.H + RG - 1) / RG;
+  const int n_groups = (a.H + RH - 1) / RH;
   const long long inst = (long long)a.n_seq * a.L;
   if (inst == 0) return cudaSuccess;
   replay_kernel<<<(unsigned)(n_groups * inst), RTHREADS, 0, s>>>(a);

@@ -144,3 +144,20 @@ def test_config4_shape_draft_replay_16():
             h_or, _ = oracle.replay(b["params"]["A_log"][j].astype(np.float64), log, ks[i],
                                     b["h0"][i, j].astype(np.float64), 3)
             assert rel_err(h[inst].double().cpu().numpy(), h_or) <= TOL
+
+
+def test_replay_longer_than_one_pass_and_ragged_heads():
+    # 40 logged steps (several passes of the replay's register-held B rows) and H = 5 (the
+    # last head group of the replay is ragged): replay(k) equals the stepped state bit for bit
+    w = Workload(62, "draft long", Shape(H=5), n_layers=2, batch=2, trees=(), draft_steps=40, ring_cap=48)
+    b = draft_batch(w)
+    r = run_draft(b, w, 40)
+    ks = [40, 23]
+    h, head, ll, st = replay(r, 2, ks)
+    assert st == 0
+    for i in range(2):
+        for j in range(2):
+            inst = i * 2 + j
+            assert torch.equal(h[inst], r["states"][ks[i] - 1][inst])
+    assert head.cpu().tolist() == [3 + 40, 3 + 40, 3 + 23, 3 + 23]
+    assert ll.cpu().tolist() == [0, 0, 0, 0]
