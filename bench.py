@@ -468,6 +468,11 @@ def run_ours(args, w):
         del y, ws_f, xBC, dt
         draft = run_draft(args, dev, stream, peak, world, rank)
 
+    # ---- the stress workload's chain tree (chain kernel) ----
+    chain = None
+    if not args.no_chain:
+        chain = run_chain(args, dev, stream, world, rank)
+
     if status.item() != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
     if rank == 0:
@@ -481,12 +486,78 @@ def run_ours(args, w):
                 "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk}
         if draft is not None:
             line["draft"] = draft
+        if chain is not None:
+            line["chain"] = chain
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM, the ALU roofline of the chain kernel
+
+
+def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
+    """The stress workload's 256-node chain tree (Mamba2-780M shape, 48 layers) through
+    ssm_tree_verify, which takes the chain kernel: every node's state is formed in
+    registers, so it is bound by the FP32 pipe (3 ops per state element per node: the
+    update's multiply and fma, and the fma of C·h).  A bounded sample of the batch-64
+    workload: `seqs_per_rank` sequences x 48 layers."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import Dims, ssm_tree_layout_build, ssm_tree_verify
+    from synth import batch, workload
+    w = workload(4)
+    seqs = list(range(rank * seqs_per_rank, (rank + 1) * seqs_per_rank))
+    b = batch(w, seqs=seqs, tree=1)
+    S, L, n = len(seqs), w.n_layers, b["n_nodes"]
+    H, P, N = w.shape.H, w.shape.P, w.shape.N
+    I = S * L
+    dims = Dims(n_heads=H, n_layers=L, ring_cap=w.ring_cap)
+    bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    lay, depth = ssm_tree_layout_build(b["parent"])
+    prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in b["params"].items()}
+    layout = torch.from_numpy(lay).to(dev)
+    xBC, dt = bf16(b["xBC"]), bf16(b["dt"])
+    h0 = torch.from_numpy(b["h0"]).to(dev)
+    ring = bf16(b["ring"])
+    head = torch.from_numpy(b["ring_head"]).to(dev)
+    y = torch.empty((I, n, H * P), device=dev)
+    ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    del b
+
+    def call(k, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ssm_tree_verify(dims, prm, S, n, depth, layout, xBC, dt, h0, ring, head, y, ws, status)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for k in range(3):
+        call(k)
+    torch.cuda.synchronize()
+    steps = max(5, min(args.steps, 20))
+    ms, evs = _timed(steps, call, world, stream, 2)
+    ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the chain verify")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ops = 3.0 * n * H * P * N * I
+    clk = 2.07e9
+    peak = sms * FP32_LANES_PER_SM * clk
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    by = I * (H * P * N * 4 + n * conv_dim * 2 + n * H * 2 + 3 * conv_dim * 2 + n * d_inner * 4)
+    return {"workload": w.name + f" (chain tree; a sample of {S} sequences x {L} layers per GPU)",
+            "nodes": n, "instances_per_gpu": I, "ms": ms,
+            "value": n * I * world / (ms / 1e3), "unit": "verified tree-node SSM updates/s",
+            "roofline": {"bound": "alu", "achieved": ops / (ms / 1e3) / 1e12, "peak": peak / 1e12,
+                         "unit": "T FP32 lane-ops/s", "frac": ops / (ms / 1e3) / peak,
+                         "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2.07 GHz (maximum SM clock)"},
+            "bytes": by, "GB/s": by / ms / 1e6}
 
 
 def draft_step_bytes(H, P, N, n_inst, n_layers):
@@ -698,6 +769,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true")
+    ap.add_argument("--no-chain", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

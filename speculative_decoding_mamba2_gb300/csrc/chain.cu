@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(CT) chain_verify_kernel(VerifyArgs a) {
       const float u = __fmul_rn(dls[j], xv);
       const float4* b4 = reinterpret_cast<const float4*>(&Bs[j][qq * (QS + 4)]);
       const float4* c4 = reinterpret_cast<const float4*>(&Cs[j][qq * (QS + 4)]);
-      float acc = 0.f;
+      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // four independent partial sums
 #pragma unroll
       for (int i = 0; i < QS / 4; ++i) {
         const float4 bv = b4[i], cv = c4[i];
@@ -116,11 +116,12 @@ __global__ void __launch_bounds__(CT) chain_verify_kernel(VerifyArgs a) {
         st[4 * i + 1] = ssm_update(dec, st[4 * i + 1], u, bv.y);
         st[4 * i + 2] = ssm_update(dec, st[4 * i + 2], u, bv.z);
         st[4 * i + 3] = ssm_update(dec, st[4 * i + 3], u, bv.w);
-        acc = fmaf(cv.x, st[4 * i], acc);
-        acc = fmaf(cv.y, st[4 * i + 1], acc);
-        acc = fmaf(cv.z, st[4 * i + 2], acc);
-        acc = fmaf(cv.w, st[4 * i + 3], acc);
+        acc0 = fmaf(cv.x, st[4 * i], acc0);
+        acc1 = fmaf(cv.y, st[4 * i + 1], acc1);
+        acc2 = fmaf(cv.z, st[4 * i + 2], acc2);
+        acc3 = fmaf(cv.w, st[4 * i + 3], acc3);
       }
+      float acc = (acc0 + acc1) + (acc2 + acc3);
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
       if (qq == 0) a.y[((size_t)inst * n + s0 + j) * d_inner + h * kP + p] = fmaf(Dh, xv, acc);

@@ -152,22 +152,6 @@ __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool repo
   return k;
 }
 
-__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float2 unpack2(unsigned long long p) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ unsigned long long fmul2(unsigned long long a, unsigned long long b) {
-  unsigned long long d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-
 __global__ void __launch_bounds__(RTHREADS) replay_kernel(ReplayArgs a) {
   __shared__ float us[RT][RROWS];  // u = Δ_t·x_t[row]
   __shared__ float decs[RT][RH];
