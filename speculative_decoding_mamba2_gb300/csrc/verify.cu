@@ -18,19 +18,23 @@
 // Two kernels per call:
 //  * tree_prep_kernel, one CTA per (layer, sequence) instance: B and C conv +
 //    SiLU for every node, the path tables, C_v·B_m along every path, Δ, S,
-//    e^S and coef[v,m] for every head, written to a caller-provided workspace
-//    (tens of KB per instance, L2-sized).
+//    e^S and coef[v,m] for every head, and C split into bf16 hi + lo, written
+//    to a caller-provided workspace (tens of KB per instance, L2-sized).  It
+//    lets the main kernel be scheduled while its last CTAs run (programmatic
+//    dependent launch).
 //  * tree_verify_kernel, one CTA (256 threads) per (instance, run of head
-//    groups of G heads): its prologue is a handful of bulk copies from the
-//    workspace; per head group it runs the x conv + SiLU, then streams the
-//    group's h0 slice through a 4-stage ring of 16-column chunks (2-D bulk
-//    tensor copies with 64-byte swizzle, full/empty mbarriers, warp 0 as
-//    producer) and contracts each chunk against C on the tensor cores
-//    (mma m16n8k16 on bf16 hi/lo splits of both operands, three products
-//    hi·hi + hi·lo + lo·hi, fp32 accumulate: each product to ~2^-17
-//    relative, far inside the 1e-3 output bound).  The path terms are a small (rows x nodes) · (nodes x nodes)
-//    product that starts each node tile's accumulator, on the same tensor
-//    cores; the epilogue only scales by e^{S_v} and writes y.
+//    groups of G heads).  Warp 0 is the producer: it streams the group's h0
+//    slice through a ring of 16-column chunks (4 stages, 3 with a folded commit;
+//    2-D bulk tensor copies with 64-byte swizzle, full/empty mbarriers) -- the
+//    first chunks go out before the kernel waits for the prep grid -- and brings
+//    each group's inputs (x rows, e^S, coef) on a second barrier.  The x conv +
+//    SiLU of group g+1 runs between group g's chunks.  Each node tile's
+//    accumulator starts at the path terms, a (rows x nodes)·(nodes x nodes)
+//    product on the tensor cores; each chunk is contracted against C on the
+//    tensor cores (mma m16n8k16 on bf16 hi/lo splits of both operands, three
+//    products hi·hi + hi·lo + lo·hi, fp32 accumulate: each product to ~2^-17
+//    relative, far inside the 1e-3 output bound); the epilogue scales by
+//    e^{S_v} and writes y.
 //
 // Commit folded into verify (LP > 0).  The selective recompute of the previous
 // step's accepted path m_0..m_{len-1} (SpecMamba page §3.1) is, by the same
