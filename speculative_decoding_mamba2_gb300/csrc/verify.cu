@@ -862,7 +862,9 @@ __global__ void __launch_bounds__(THREADS, 2)
               rb[mt].w = fmaf(u1, bj.w, rb[mt].w);
             }
           }
-          if (whead < heads) {
+          // every node tile streams the same h and rebuilds h' in registers; only the last
+          // tile stores it, so no tile can read back a chunk that is already committed
+          if (whead < heads && tile == n_tiles - 1) {
             float* g0 = a.h_w + ((size_t)(inst * a.H + hb) * kP + wrow + fg) * kN + kc * KC + 4 * ft;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {

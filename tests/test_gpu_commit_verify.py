@@ -203,3 +203,27 @@ def test_config3_full_size_sampled():
     assert out["status"] == 0 and out["sep_status"] == 0
     check_oracle(b0, b1, out, [(0, 0), (15, 63), (7, 40), (3, 5)])
     check_separate(out)
+
+
+@pytest.mark.parametrize("nxt", [("full", 3, 3), ("random", 64, 4, 15)])
+def test_next_tree_of_several_node_tiles(nxt):
+    # 40- and 64-node next trees: several node tiles per head group (the next group's x conv
+    # runs in the last tile; the path-term product spans several k-steps), depth up to 15
+    w0 = Workload(70, "tiles", Shape(H=8), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
+    w1 = next_workload(w0, 71, nxt)
+    b0, b1 = batch(w0), batch(w1)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
+    check_separate(out)
+
+
+def test_stress_shape_ternary_next_tree_sampled():
+    # the stress workload's shape (48 heads) and its 40-node ternary tree after a committed path
+    w0 = workload(4)
+    w1 = next_workload(w0, 72, ("full", 3, 3))
+    b0, b1 = batch(w0, seqs=[0, 21, 63], tree=0), batch(w1, seqs=[0, 21, 63])
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(0, 0), (1, 24), (2, 47)])
+    check_separate(out)
