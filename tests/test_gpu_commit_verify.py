@@ -227,3 +227,30 @@ def test_stress_shape_ternary_next_tree_sampled():
     assert out["status"] == 0 and out["sep_status"] == 0
     check_oracle(b0, b1, out, [(0, 0), (1, 24), (2, 47)])
     check_separate(out)
+
+
+@pytest.mark.parametrize("gpc", ["2", "3"])
+def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
+    # several head groups per CTA (H = 10: the last one ragged) with a 40-node next tree
+    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    w0 = Workload(73, "groups x tiles", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),),
+                  p_accept=0.9)
+    w1 = next_workload(w0, 74, ("full", 3, 3))
+    b0, b1 = batch(w0), batch(w1)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
+    check_separate(out)
+
+
+def test_ring_positions_wrap_around():
+    # ring heads just below the ring size and far beyond it: the committed rows and the
+    # rows before the next root wrap around the 20-row ring
+    w0 = Workload(75, "wrap", Shape(H=8), n_layers=2, batch=2, trees=(("chain", 8),), p_accept=1.0)
+    w1 = next_workload(w0, 76, ("random", 16, 3, 4))
+    b0, b1 = batch(w0), batch(w1)
+    b0["ring_head"][:] = np.array([[18, 19], [37, 1000001]], np.int32)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
+    check_separate(out)

@@ -90,6 +90,17 @@ def test_several_head_groups_per_cta(gpc, monkeypatch):
     check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
 
 
+@pytest.mark.parametrize("gpc", ["2", "3"])
+def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
+    # several head groups per CTA (the last one ragged) with a 40-node tree (three node
+    # tiles): the next group's x conv runs inside the last tile of the current group
+    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    w = Workload(56, "groups x tiles", Shape(H=10), n_layers=2, batch=2, trees=(("full", 3, 3),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
 def test_single_node_tree():
     w = Workload(52, "root only", Shape(H=4), n_layers=3, batch=2, trees=(("chain", 1),))
     b = batch(w)
