@@ -496,15 +496,13 @@ def run_ours(args, w):
     return 0
 
 
-FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM, the ALU roofline of the chain kernel
-
-
 def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
     """The stress workload's 256-node chain tree (Mamba2-780M shape, 48 layers) through
-    ssm_tree_verify, which takes the chain kernel: every node's state is formed in
-    registers, so it is bound by the FP32 pipe (3 ops per state element per node: the
-    update's multiply and fma, and the fma of C·h).  A bounded sample of the batch-64
-    workload: `seqs_per_rank` sequences x 48 layers."""
+    ssm_tree_verify, which takes the chain kernel: 16-node chunks, each a tree verify
+    from the chunk's entry state plus the commit of the whole chunk, all on the tensor
+    cores with the state in registers.  Roofline: HBM (h0 read once, the inputs, y),
+    which binds before the tensor pipe.  A bounded sample of the batch-64 workload:
+    `seqs_per_rank` sequences x 48 layers."""
     import numpy as np
     import torch
 
@@ -545,19 +543,16 @@ def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
     ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the chain verify")
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    ops = 3.0 * n * H * P * N * I
-    clk = 2.07e9
-    peak = sms * FP32_LANES_PER_SM * clk
+    peak, peak_kind = measured_peaks()
     d_inner, conv_dim = H * P, H * P + 2 * N
     by = I * (H * P * N * 4 + n * conv_dim * 2 + n * H * 2 + 3 * conv_dim * 2 + n * d_inner * 4)
+    flops = 4.0 * n * H * P * N * I  # C·h and u·B over the state, 2 FLOP each per element and node
     return {"workload": w.name + f" (chain tree; a sample of {S} sequences x {L} layers per GPU)",
             "nodes": n, "instances_per_gpu": I, "ms": ms,
             "value": n * I * world / (ms / 1e3), "unit": "verified tree-node SSM updates/s",
-            "roofline": {"bound": "alu", "achieved": ops / (ms / 1e3) / 1e12, "peak": peak / 1e12,
-                         "unit": "T FP32 lane-ops/s", "frac": ops / (ms / 1e3) / peak,
-                         "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2.07 GHz (maximum SM clock)"},
-            "bytes": by, "GB/s": by / ms / 1e6}
+            "roofline": {"bound": "hbm", "achieved": by / ms / 1e6, "peak": peak, "unit": "GB/s",
+                         "frac": by / ms / 1e6 / peak, "peak_source": peak_kind},
+            "bytes": by, "state_TFLOP/s": flops / (ms / 1e3) / 1e12}
 
 
 def draft_step_bytes(H, P, N, n_inst, n_layers):

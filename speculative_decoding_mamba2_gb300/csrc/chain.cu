@@ -1,130 +1,320 @@
 // Verification of a chain-shaped draft tree (parent[v] = v - 1), of any length.
 //
 // SpecMamba page ("FPGA加速Mamba推理：SpecMamba方案与优化实践") §3.2: the tree
-// is walked in order, each node updated from its parent's state, the parent's
-// state released once its child is done.  For a chain that walk needs exactly
-// one live state, so one CTA per (instance, head) keeps its 64 x 128 state slice
-// in registers (256 threads, 32 elements each: row p = thread/4, columns
-// 32*(thread%4) .. +32) for the whole chain.  The nodes stream through shared
-// memory in segments of 16: conv + SiLU of the segment's x (this head) and B, C
-// channels from the pre-conv rows (the three rows before the segment come from
-// the previous nodes, or from the conv ring for the first segment), Δ and the
-// decay exp(Δ·A); then, node by node,
-//     h = exp(Δ_v·A)·h + (Δ_v·x_v[p])·B_v[k],   y_v[p] = Σ_k C_v[k]·h[p][k] + D·x_v[p]
-// with the four partial sums of a row combined by quad shuffles.  h0 is read
-// once, no per-node state touches memory.
+// is walked in order, each node updated from its parent's state.  For a chain
+// the walk is a plain scan, cut here into chunks of Q = 16 nodes.  With h the
+// state before a chunk (h0 for the first), S_v = Σ_{m ≤ v in the chunk} Δ_m·A
+// and the update linear in h (LightMamba page, "为什么 Mamba 难加速"), every
+// node of the chunk and the state after it are, exactly,
+//     y_v[p] = e^{S_v}·(C_v·h[p,:] + Σ_{m ≤ v} coef[v,m]·x_m[p]),
+//     coef[v,m] = e^{-S_m}·Δ_m·(C_v·B_m)  (+ D·e^{-S_v} for m = v),
+//     h'[p,:] = E·h[p,:] + Σ_m u_m[p]·B_m,   E = e^{S_last},  u_m = Δ_m·e^{S_last - S_m}·x_m,
+// i.e. a 16-node tree verify from h followed by the commit of all 16 nodes
+// (the same dual form as the tree kernels), and all three sums are small
+// dense products on the tensor cores.
+//
+// One CTA (8 warps) per (instance, pair of heads); warp w owns 16 state rows of
+// head w / 4, kept in registers in the mma accumulator layout for the whole
+// chain: that layout is also the A-operand layout of the C·h product over the
+// state columns, so the state never goes through shared memory; h0 is read
+// once, y is the only output.  Per chunk: the pre-conv rows (prefetched with
+// cp.async one chunk ahead) are convolved + SiLU'd into x (both heads), B and
+// C; Δ, S, E, the Gram C_v·B_m and the coefficients follow; every product uses
+// bf16 hi/lo splits of both operands and three mma (hi·hi + hi·lo + lo·hi).
 #include "common.cuh"
 
 namespace ssmtree {
 namespace {
 
-constexpr int CT = 256;          // threads: 64 rows x 4 column quarters
-constexpr int SEG = 16;          // nodes per segment
-constexpr int QS = kN / 4;       // 32 columns per thread
-constexpr int BSTR = kN + 16;    // B/C rows padded so the four quarters hit different banks
+constexpr int Q = 16;                    // chain nodes per chunk (one mma k-step)
+constexpr int CHG = 2;                   // heads per CTA
+constexpr int CROWS = CHG * kP;          // 128 state rows
+constexpr int CTHREADS = 256;            // 8 warps, 16 rows each
+constexpr int RAWR = Q + 3;              // pre-conv rows of a chunk (3 before it)
+constexpr int RAWC = CHG * kP + 2 * kN;  // staged channels: the pair's x, then B | C (384)
+constexpr int PS = 12;                   // row stride (u32) of the node-pair tables: conflict-free
+constexpr int CPS = kN / 2 + 4;          // row stride (u32) of the C pair table: conflict-free
 
-__device__ __forceinline__ int bc_col(int k) { return k + (k / QS) * 4; }
+struct ChainSmem {
+  uint16_t raw[2][RAWR][RAWC];               // pre-conv rows, double-buffered across chunks
+  float xf[Q][CROWS];                        // post-conv x of the chunk's nodes
+  float bf[Q][kN], cf[Q][kN];                // post-conv B, C
+  uint32_t chi[Q][CPS], clo[Q][CPS];         // C as bf16 pairs along the state columns (B of C·h)
+  uint32_t bhi[kN][PS], blo[kN][PS];         // B as bf16 pairs along the nodes (B of the update)
+  uint32_t xhi[CROWS][PS], xlo[CROWS][PS];   // x as bf16 pairs along the nodes (A of the path terms)
+  uint32_t uhi[CROWS][PS], ulo[CROWS][PS];   // u = w·x likewise (A of the update)
+  uint32_t khi[CHG][Q][PS], klo[CHG][Q][PS]; // coef[v][m] pairs along m (B of the path terms)
+  float gram[Q][Q];                          // C_v·B_m
+  float dl[CHG][Q], S[CHG][Q], eS[CHG][Q], emS[CHG][Q], w[CHG][Q];
+  float E[CHG];
+};
 
-__global__ void __launch_bounds__(CT) chain_verify_kernel(VerifyArgs a) {
-  __shared__ __align__(16) float Bs[SEG][BSTR];
-  __shared__ __align__(16) float Cs[SEG][BSTR];
-  __shared__ float xs[SEG][kP];
-  __shared__ float dls[SEG], decs[SEG];
-
-  const int tid = threadIdx.x;
-  const int h = blockIdx.x % a.H;
-  const int inst = blockIdx.x / a.H;
+__global__ void __launch_bounds__(CTHREADS, 2) chain_verify_kernel(VerifyArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ChainSmem& sm = *reinterpret_cast<ChainSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int fg = lane >> 2, ft = lane & 3;
+  const int n_pairs = (a.H + CHG - 1) / CHG;
+  const int hp = blockIdx.x % n_pairs;
+  const int inst = blockIdx.x / n_pairs;
   const int layer = inst % a.L;
-  const int n = a.n;
-  const int d_inner = a.H * kP, conv_dim = d_inner + 2 * kN, R = a.R;
-  const int p = tid >> 2, qq = tid & 3;
+  const int h_begin = hp * CHG;
+  const int heads = min(CHG, a.H - h_begin);
+  const int n = a.n, R = a.R;
+  const int d_inner = a.H * kP, conv_dim = d_inner + 2 * kN;
   const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
   const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
   const int head = a.ring_head[inst];
-  const float A = neg_exp(a.A_log[(size_t)layer * a.H + h]);
-  const float bias = a.dt_bias[(size_t)layer * a.H + h];
-  const float Dh = a.D[(size_t)layer * a.H + h];
+  const int hh = warp / 4;                      // this warp's head within the pair
+  const int rbase = hh * kP + (warp % 4) * 16;  // its first state row within the pair
+  const bool live = hh < heads;
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float* cb = a.conv_b + (size_t)layer * conv_dim;
 
-  // this thread's state: row p of head h, columns 32*qq .. 32*qq+31
-  float st[QS];
+  // pre-conv rows of the chunk starting at c0 into raw buffer `buf`: row r = chain position
+  // c0 - 3 + r (negative: the conv ring), channels [the pair's x | B | C]; rows past the
+  // chain and channels past the last head are zero
+  auto stage = [&](int c0, int buf) {
+    constexpr int XP = (CHG * kP) / 8;  // 16-byte pieces of x per row
+    constexpr int PIECES = RAWC / 8;
+    for (int i = tid; i < RAWR * PIECES; i += CTHREADS) {
+      const int r = i / PIECES, pc = i - r * PIECES;
+      const int pos = c0 - 3 + r;
+      uint16_t* dst = &sm.raw[buf][r][pc * 8];
+      const int ch = pc < XP ? h_begin * kP + pc * 8 : d_inner + (pc - XP) * 8;
+      if (pos >= n || (pc < XP && ch >= d_inner)) {
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        continue;
+      }
+      const uint16_t* row = pos >= 0 ? xbc + (size_t)pos * conv_dim : ring + (size_t)ring_pos(head, pos, R) * conv_dim;
+      cp_async16(dst, row + ch);
+    }
+    cp_async_commit();
+  };
+
+  // this warp's state rows rbase + fg (+8), columns 8j + 2ft (+1): the accumulator layout
+  float st[kN / 8][4];
   {
-    const float4* src =
-        reinterpret_cast<const float4*>(a.h0 + (((size_t)inst * a.H + h) * kP + p) * kN + qq * QS);
+    const float* h0 = a.h0 + ((size_t)inst * a.H + h_begin) * kP * kN;
 #pragma unroll
-    for (int i = 0; i < QS / 4; ++i) {
-      const float4 v = src[i];
-      st[4 * i] = v.x;
-      st[4 * i + 1] = v.y;
-      st[4 * i + 2] = v.z;
-      st[4 * i + 3] = v.w;
+    for (int j = 0; j < kN / 8; ++j) {
+      float2 lo = make_float2(0.f, 0.f), hi = lo;
+      if (live) {
+        lo = *reinterpret_cast<const float2*>(h0 + (size_t)(rbase + fg) * kN + 8 * j + 2 * ft);
+        hi = *reinterpret_cast<const float2*>(h0 + (size_t)(rbase + fg + 8) * kN + 8 * j + 2 * ft);
+      }
+      st[j][0] = lo.x;
+      st[j][1] = lo.y;
+      st[j][2] = hi.x;
+      st[j][3] = hi.y;
     }
   }
-  // pre-conv value of channel c at chain position j (j < 0: ring position head + j)
-  auto pre = [&](int j, int c) -> float {
-    if (j >= 0) return bf16f(xbc[(size_t)j * conv_dim + c]);
-    return bf16f(ring[(size_t)ring_pos(head, j, R) * conv_dim + c]);
-  };
-  // conv jobs of a segment: x channels of this head (64) and B, C (256), one channel per thread
-  const int c_x = h * kP + (tid & (kP - 1));  // threads 0..63 do x
-  const int c_bc = d_inner + tid;              // every thread does one B|C channel
-  const float4 wx = cw[c_x], wbc = cw[c_bc];
-  const float bx = cb[c_x], bbc = cb[c_bc];
 
-  for (int s0 = 0; s0 < n; s0 += SEG) {
-    const int cnt = min(SEG, n - s0);
-    __syncthreads();  // previous segment's tables consumed
-    {
-      float r0 = pre(s0 - 3, c_bc), r1 = pre(s0 - 2, c_bc), r2 = pre(s0 - 1, c_bc);
-      float* dst = tid < kN ? &Bs[0][bc_col(tid)] : &Cs[0][bc_col(tid - kN)];
-      for (int j = 0; j < cnt; ++j) {
-        const float r3 = pre(s0 + j, c_bc);
-        dst[j * BSTR] = silu_f(conv4_acc(wbc, bbc, r0, r1, r2, r3));
-        r0 = r1;
-        r1 = r2;
-        r2 = r3;
-      }
-    }
-    if (tid < kP) {
-      float r0 = pre(s0 - 3, c_x), r1 = pre(s0 - 2, c_x), r2 = pre(s0 - 1, c_x);
-      for (int j = 0; j < cnt; ++j) {
-        const float r3 = pre(s0 + j, c_x);
-        xs[j][tid] = silu_f(conv4_acc(wx, bx, r0, r1, r2, r3));
-        r0 = r1;
-        r1 = r2;
-        r2 = r3;
-      }
-    } else if (tid < kP + cnt) {
-      const int j = tid - kP;
-      const float d = softplus_f(bf16f(a.dt[((size_t)inst * n + s0 + j) * a.H + h]) + bias);
-      dls[j] = d;
-      decs[j] = decay_of(d, A);
+  stage(0, 0);
+  const int n_chunks = (n + Q - 1) / Q;
+  for (int ci = 0; ci < n_chunks; ++ci) {
+    const int c0 = ci * Q, cnt = min(Q, n - c0), buf = ci & 1;
+    __syncthreads();  // the previous chunk's tables and the other raw buffer are no longer read
+    if (ci + 1 < n_chunks) {
+      stage(c0 + Q, buf ^ 1);  // the next chunk's rows stay in flight during this chunk
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    for (int j = 0; j < cnt; ++j) {
-      const float dec = decs[j];
-      const float xv = xs[j][p];
-      const float u = __fmul_rn(dls[j], xv);
-      const float4* b4 = reinterpret_cast<const float4*>(&Bs[j][qq * (QS + 4)]);
-      const float4* c4 = reinterpret_cast<const float4*>(&Cs[j][qq * (QS + 4)]);
-      float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;  // four independent partial sums
-#pragma unroll
-      for (int i = 0; i < QS / 4; ++i) {
-        const float4 bv = b4[i], cv = c4[i];
-        st[4 * i] = ssm_update(dec, st[4 * i], u, bv.x);
-        st[4 * i + 1] = ssm_update(dec, st[4 * i + 1], u, bv.y);
-        st[4 * i + 2] = ssm_update(dec, st[4 * i + 2], u, bv.z);
-        st[4 * i + 3] = ssm_update(dec, st[4 * i + 3], u, bv.w);
-        acc0 = fmaf(cv.x, st[4 * i], acc0);
-        acc1 = fmaf(cv.y, st[4 * i + 1], acc1);
-        acc2 = fmaf(cv.z, st[4 * i + 2], acc2);
-        acc3 = fmaf(cv.w, st[4 * i + 3], acc3);
+
+    // ---- conv + SiLU: B | C (thread = channel), x of both heads (threads 0..127), Δ ----
+    {
+      const int c = tid;
+      const float4 wk = cw[d_inner + c];
+      const float bk = cb[d_inner + c];
+      float r0 = bf16f(sm.raw[buf][0][CROWS + c]), r1 = bf16f(sm.raw[buf][1][CROWS + c]),
+            r2 = bf16f(sm.raw[buf][2][CROWS + c]);
+      float* dst = c < kN ? &sm.bf[0][c] : &sm.cf[0][c - kN];
+      for (int v = 0; v < Q; ++v) {
+        const float r3 = bf16f(sm.raw[buf][v + 3][CROWS + c]);
+        dst[v * kN] = v < cnt ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
+        r0 = r1;
+        r1 = r2;
+        r2 = r3;
       }
-      float acc = (acc0 + acc1) + (acc2 + acc3);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (qq == 0) a.y[((size_t)inst * n + s0 + j) * d_inner + h * kP + p] = fmaf(Dh, xv, acc);
+    }
+    if (tid < CROWS) {
+      const int hx = tid / kP;
+      float4 wk = make_float4(0.f, 0.f, 0.f, 0.f);
+      float bk = 0.f;
+      if (hx < heads) {
+        const int c = (h_begin + hx) * kP + (tid - hx * kP);
+        wk = cw[c];
+        bk = cb[c];
+      }
+      float r0 = bf16f(sm.raw[buf][0][tid]), r1 = bf16f(sm.raw[buf][1][tid]), r2 = bf16f(sm.raw[buf][2][tid]);
+      for (int v = 0; v < Q; ++v) {
+        const float r3 = bf16f(sm.raw[buf][v + 3][tid]);
+        sm.xf[v][tid] = (v < cnt && hx < heads) ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
+        r0 = r1;
+        r1 = r2;
+        r2 = r3;
+      }
+    } else if (tid < CROWS + CHG * Q) {
+      const int k = tid - CROWS, hx = k / Q, v = k - hx * Q;
+      float d = 0.f;
+      if (hx < heads && v < cnt) {
+        const int h = h_begin + hx;
+        d = softplus_f(bf16f(a.dt[((size_t)inst * n + c0 + v) * a.H + h]) + a.dt_bias[(size_t)layer * a.H + h]);
+      }
+      sm.dl[hx][v] = d;  // Δ = 0 past the chain: no decay, no input
+    }
+    __syncthreads();
+
+    // ---- S, e^{±S}, E, w per head; the Gram C_v·B_m; C, B and x as bf16 pairs ----
+    if (tid < CHG * Q) {  // warp 0: lane = (head, node); S by a shuffle scan over the 16 nodes
+      const int hx = tid / Q, v = tid - hx * Q;
+      const float A = hx < heads ? neg_exp(a.A_log[(size_t)layer * a.H + h_begin + hx]) : 0.f;
+      const float d = sm.dl[hx][v];
+      float s = d * A;
+#pragma unroll
+      for (int off = 1; off < Q; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, s, off, Q);
+        if (v >= off) s += o;
+      }
+      const float s_last = __shfl_sync(0xffffffffu, s, Q - 1, Q);
+      sm.S[hx][v] = s;
+      sm.eS[hx][v] = expf(s);
+      sm.emS[hx][v] = expf(-s);
+      sm.w[hx][v] = d * expf(s_last - s);
+      if (v == Q - 1) sm.E[hx] = expf(s_last);
+    }
+    {  // Gram: thread (v, m) = tid (256 = Q x Q), the k loop staggered by m against conflicts
+      const int v = tid / Q, m = tid - v * Q;
+      const float4* cr = reinterpret_cast<const float4*>(sm.cf[v]);
+      const float4* br = reinterpret_cast<const float4*>(sm.bf[m]);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+      for (int i = 0; i < kN / 4; ++i) {
+        const int k = (i + m) & (kN / 4 - 1);
+        const float4 c4 = cr[k], b4 = br[k];
+        s0 = fmaf(c4.x, b4.x, s0);
+        s1 = fmaf(c4.y, b4.y, s1);
+        s0 = fmaf(c4.z, b4.z, s0);
+        s1 = fmaf(c4.w, b4.w, s1);
+      }
+      sm.gram[v][m] = s0 + s1;
+    }
+    for (int i = tid; i < Q * (kN / 2); i += CTHREADS) {  // C pairs along the state columns
+      const int v = i / (kN / 2), k = i - v * (kN / 2);
+      split_bf16x2(sm.cf[v][2 * k], sm.cf[v][2 * k + 1], sm.chi[v][k], sm.clo[v][k]);
+    }
+    for (int i = tid; i < kN * (Q / 2); i += CTHREADS) {  // B pairs along the nodes
+      const int col = i / (Q / 2), k = i - col * (Q / 2);
+      split_bf16x2(sm.bf[2 * k][col], sm.bf[2 * k + 1][col], sm.bhi[col][k], sm.blo[col][k]);
+    }
+    for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // x pairs along the nodes
+      const int r = i / (Q / 2), k = i - r * (Q / 2);
+      split_bf16x2(sm.xf[2 * k][r], sm.xf[2 * k + 1][r], sm.xhi[r][k], sm.xlo[r][k]);
+    }
+    __syncthreads();
+    for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // u = w·x pairs
+      const int r = i / (Q / 2), k = i - r * (Q / 2), hx = r / kP;
+      split_bf16x2(sm.w[hx][2 * k] * sm.xf[2 * k][r], sm.w[hx][2 * k + 1] * sm.xf[2 * k + 1][r], sm.uhi[r][k],
+                   sm.ulo[r][k]);
+    }
+    for (int i = tid; i < CHG * Q * (Q / 2); i += CTHREADS) {  // coef pairs along m
+      const int hx = i / (Q * (Q / 2)), rest = i - hx * (Q * (Q / 2)), v = rest / (Q / 2), k = rest - v * (Q / 2);
+      const float Dh = hx < heads ? a.D[(size_t)layer * a.H + h_begin + hx] : 0.f;
+      float cm[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int m = 2 * k + e;
+        float c = m <= v ? sm.emS[hx][m] * sm.dl[hx][m] * sm.gram[v][m] : 0.f;
+        if (m == v) c = fmaf(Dh, sm.emS[hx][v], c);
+        cm[e] = c;
+      }
+      split_bf16x2(cm[0], cm[1], sm.khi[hx][v][k], sm.klo[hx][v][k]);
+    }
+    __syncthreads();
+
+    // ---- this warp: the chunk's y and the state after it ----
+    if (live) {
+      float acc[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+      {  // path terms: A = x (rows x nodes m), B = coef (nodes m x nodes v)
+        uint32_t ahi[4], alo[4];
+        ahi[0] = sm.xhi[rbase + fg][ft];
+        alo[0] = sm.xlo[rbase + fg][ft];
+        ahi[1] = sm.xhi[rbase + fg + 8][ft];
+        alo[1] = sm.xlo[rbase + fg + 8][ft];
+        ahi[2] = sm.xhi[rbase + fg][ft + 4];
+        alo[2] = sm.xlo[rbase + fg][ft + 4];
+        ahi[3] = sm.xhi[rbase + fg + 8][ft + 4];
+        alo[3] = sm.xlo[rbase + fg + 8][ft + 4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int v = nt * 8 + fg;
+          const uint32_t bh[2] = {sm.khi[hh][v][ft], sm.khi[hh][v][ft + 4]};
+          const uint32_t bl[2] = {sm.klo[hh][v][ft], sm.klo[hh][v][ft + 4]};
+          mma_bf16(acc[nt], alo, bh);
+          mma_bf16(acc[nt], ahi, bl);
+          mma_bf16(acc[nt], ahi, bh);
+        }
+      }
+      // C·h: A = the state in registers (rows x state columns), B = C (columns x nodes)
+#pragma unroll
+      for (int ks = 0; ks < kN / 16; ++ks) {
+        uint32_t ahi[4], alo[4];
+        split_bf16x2(st[2 * ks][0], st[2 * ks][1], ahi[0], alo[0]);
+        split_bf16x2(st[2 * ks][2], st[2 * ks][3], ahi[1], alo[1]);
+        split_bf16x2(st[2 * ks + 1][0], st[2 * ks + 1][1], ahi[2], alo[2]);
+        split_bf16x2(st[2 * ks + 1][2], st[2 * ks + 1][3], ahi[3], alo[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int v = nt * 8 + fg;
+          const uint32_t bh[2] = {sm.chi[v][8 * ks + ft], sm.chi[v][8 * ks + ft + 4]};
+          const uint32_t bl[2] = {sm.clo[v][8 * ks + ft], sm.clo[v][8 * ks + ft + 4]};
+          mma_bf16(acc[nt], alo, bh);
+          mma_bf16(acc[nt], ahi, bl);
+          mma_bf16(acc[nt], ahi, bh);
+        }
+      }
+      // y_v[p] = e^{S_v}·acc
+      float* yb = a.y + (size_t)inst * n * d_inner + (size_t)(h_begin * kP + rbase + fg);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int v = nt * 8 + 2 * ft + c;
+          if (v < cnt) {
+            const float es = sm.eS[hh][v];
+            float* yr = yb + (size_t)(c0 + v) * d_inner;
+            yr[0] = es * acc[nt][c];
+            yr[8] = es * acc[nt][2 + c];
+          }
+        }
+      // h' = E·h + u·B: A = u (rows x nodes), B = B (nodes x state columns), accumulator = the state
+      uint32_t uhi[4], ulo[4];
+      uhi[0] = sm.uhi[rbase + fg][ft];
+      ulo[0] = sm.ulo[rbase + fg][ft];
+      uhi[1] = sm.uhi[rbase + fg + 8][ft];
+      ulo[1] = sm.ulo[rbase + fg + 8][ft];
+      uhi[2] = sm.uhi[rbase + fg][ft + 4];
+      ulo[2] = sm.ulo[rbase + fg][ft + 4];
+      uhi[3] = sm.uhi[rbase + fg + 8][ft + 4];
+      ulo[3] = sm.ulo[rbase + fg + 8][ft + 4];
+      const float E = sm.E[hh];
+#pragma unroll
+      for (int j = 0; j < kN / 8; ++j) {
+        const int col = 8 * j + fg;
+        const uint32_t bh[2] = {sm.bhi[col][ft], sm.bhi[col][ft + 4]};
+        const uint32_t bl[2] = {sm.blo[col][ft], sm.blo[col][ft + 4]};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) st[j][e] *= E;
+        mma_bf16(st[j], ulo, bh);
+        mma_bf16(st[j], uhi, bl);
+        mma_bf16(st[j], uhi, bh);
+      }
     }
   }
 }
@@ -132,9 +322,19 @@ __global__ void __launch_bounds__(CT) chain_verify_kernel(VerifyArgs a) {
 }  // namespace
 
 cudaError_t launch_chain_verify(const VerifyArgs& a, cudaStream_t s) {
-  const long long blocks = (long long)a.n_seq * a.L * a.H;
+  const long long blocks = (long long)a.n_seq * a.L * ((a.H + CHG - 1) / CHG);
   if (blocks == 0) return cudaSuccess;
-  chain_verify_kernel<<<(unsigned)blocks, CT, 0, s>>>(a);
+  const int bytes = (int)sizeof(ChainSmem);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(chain_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) configured[dev] = 1;
+  }
+  chain_verify_kernel<<<(unsigned)blocks, CTHREADS, bytes, s>>>(a);
   return cudaGetLastError();
 }
 
