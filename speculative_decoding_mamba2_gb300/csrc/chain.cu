@@ -201,21 +201,23 @@ __global__ void __launch_bounds__(CTHREADS, 2) chain_verify_kernel(VerifyArgs a)
       }
       sm.gram[v][m] = s0 + s1;
     }
+    // (lanes run along the fp32 tables' rows: conflict-free reads)
     for (int i = tid; i < Q * (kN / 2); i += CTHREADS) {  // C pairs along the state columns
       const int v = i / (kN / 2), k = i - v * (kN / 2);
-      split_bf16x2(sm.cf[v][2 * k], sm.cf[v][2 * k + 1], sm.chi[v][k], sm.clo[v][k]);
+      const float2 c2 = reinterpret_cast<const float2*>(sm.cf[v])[k];
+      split_bf16x2(c2.x, c2.y, sm.chi[v][k], sm.clo[v][k]);
     }
     for (int i = tid; i < kN * (Q / 2); i += CTHREADS) {  // B pairs along the nodes
-      const int col = i / (Q / 2), k = i - col * (Q / 2);
+      const int k = i / kN, col = i - k * kN;
       split_bf16x2(sm.bf[2 * k][col], sm.bf[2 * k + 1][col], sm.bhi[col][k], sm.blo[col][k]);
     }
     for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // x pairs along the nodes
-      const int r = i / (Q / 2), k = i - r * (Q / 2);
+      const int k = i / CROWS, r = i - k * CROWS;
       split_bf16x2(sm.xf[2 * k][r], sm.xf[2 * k + 1][r], sm.xhi[r][k], sm.xlo[r][k]);
     }
     __syncthreads();
     for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // u = w·x pairs
-      const int r = i / (Q / 2), k = i - r * (Q / 2), hx = r / kP;
+      const int k = i / CROWS, r = i - k * CROWS, hx = r / kP;
       split_bf16x2(sm.w[hx][2 * k] * sm.xf[2 * k][r], sm.w[hx][2 * k + 1] * sm.xf[2 * k + 1][r], sm.uhi[r][k],
                    sm.ulo[r][k]);
     }
