@@ -18,9 +18,11 @@
 // chain: that layout is also the A-operand layout of the C·h product over the
 // state columns, so the state never goes through shared memory; h0 is read
 // once, y is the only output.  Per chunk: the pre-conv rows (prefetched with
-// cp.async one chunk ahead) are convolved + SiLU'd into x (both heads), B and
-// C; Δ, S, E, the Gram C_v·B_m and the coefficients follow; every product uses
-// bf16 hi/lo splits of both operands and three mma (hi·hi + hi·lo + lo·hi).
+// cp.async one chunk ahead, dt in registers) are convolved + SiLU'd straight into
+// the bf16 hi/lo pair tables the mma fragments read (x and u = w·x of both heads,
+// B and C); Δ, S, E (a shuffle scan), the Gram C_v·B_m (mma) and the coefficients
+// follow.  Every product uses bf16 hi/lo splits of both operands and three mma
+// (hi·hi + hi·lo + lo·hi).
 #include "common.cuh"
 
 namespace ssmtree {
@@ -35,11 +37,14 @@ constexpr int RAWC = CHG * kP + 2 * kN;  // staged channels: the pair's x, then 
 constexpr int PS = 12;                   // row stride (u32) of the node-pair tables: conflict-free
 constexpr int CPS = kN / 2 + 4;          // row stride (u32) of the C pair table: conflict-free
 
+static_assert(CHG * Q * (Q / 2) == CTHREADS, "one coefficient pair per thread");
+static_assert(2 * kN == CTHREADS, "one B | C channel per thread");
+static_assert(CHG * Q == 32, "one warp for Δ and S of the head pair");
+
 struct ChainSmem {
   uint16_t raw[2][RAWR][RAWC];               // pre-conv rows, double-buffered across chunks
-  float xf[Q][CROWS];                        // post-conv x of the chunk's nodes
-  float bf[Q][kN], cf[Q][kN];                // post-conv B, C
-  uint32_t chi[Q][CPS], clo[Q][CPS];         // C as bf16 pairs along the state columns (B of C·h)
+  uint32_t chi[Q][CPS], clo[Q][CPS];         // C as bf16 pairs along the state columns (B of C·h, A of the Gram)
+  uint32_t bchi[Q][CPS], bclo[Q][CPS];       // B as bf16 pairs along the state columns (B of the Gram)
   uint32_t bhi[kN][PS], blo[kN][PS];         // B as bf16 pairs along the nodes (B of the update)
   uint32_t xhi[CROWS][PS], xlo[CROWS][PS];   // x as bf16 pairs along the nodes (A of the path terms)
   uint32_t uhi[CROWS][PS], ulo[CROWS][PS];   // u = w·x likewise (A of the update)
@@ -110,35 +115,86 @@ __global__ void __launch_bounds__(CTHREADS, 2) chain_verify_kernel(VerifyArgs a)
     }
   }
 
+  // dt of a chunk for warp 0's lanes (lane = head * Q + node), one chunk ahead
+  auto load_dt = [&](int c0) -> float {
+    const int hx = lane / Q, v = lane - hx * Q;
+    if (warp != 0 || hx >= heads || c0 + v >= n) return 0.f;
+    return bf16f(a.dt[((size_t)inst * n + c0 + v) * a.H + h_begin + hx]);
+  };
   stage(0, 0);
+  float dt_next = load_dt(0);
   const int n_chunks = (n + Q - 1) / Q;
   for (int ci = 0; ci < n_chunks; ++ci) {
     const int c0 = ci * Q, cnt = min(Q, n - c0), buf = ci & 1;
+    const float dt_cur = dt_next;
     __syncthreads();  // the previous chunk's tables and the other raw buffer are no longer read
     if (ci + 1 < n_chunks) {
       stage(c0 + Q, buf ^ 1);  // the next chunk's rows stay in flight during this chunk
+      dt_next = load_dt(c0 + Q);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
 
-    // ---- conv + SiLU: B | C (thread = channel), x of both heads (threads 0..127), Δ ----
-    {
+    // ---- phase 1: Δ, S, e^{±S}, E, w (warp 0, shuffle scan); B | C conv + SiLU into pairs ----
+    if (warp == 0) {
+      const int hx = lane / Q, v = lane - hx * Q;
+      float d = 0.f, A = 0.f;
+      if (hx < heads) {
+        A = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + hx]);
+        if (v < cnt) d = softplus_f(dt_cur + a.dt_bias[(size_t)layer * a.H + h_begin + hx]);
+      }
+      float s = d * A;  // Δ = 0 past the chain: no decay, no input
+#pragma unroll
+      for (int off = 1; off < Q; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, s, off, Q);
+        if (v >= off) s += o;
+      }
+      const float s_last = __shfl_sync(0xffffffffu, s, Q - 1, Q);
+      sm.dl[hx][v] = d;
+      sm.S[hx][v] = s;
+      sm.eS[hx][v] = expf(s);
+      sm.emS[hx][v] = expf(-s);
+      sm.w[hx][v] = d * expf(s_last - s);
+      if (v == Q - 1) sm.E[hx] = expf(s_last);
+    }
+    {  // thread = B | C channel: 16 nodes, then the pair tables (neighbour column by shuffle)
       const int c = tid;
       const float4 wk = cw[d_inner + c];
       const float bk = cb[d_inner + c];
+      float val[Q];
       float r0 = bf16f(sm.raw[buf][0][CROWS + c]), r1 = bf16f(sm.raw[buf][1][CROWS + c]),
             r2 = bf16f(sm.raw[buf][2][CROWS + c]);
-      float* dst = c < kN ? &sm.bf[0][c] : &sm.cf[0][c - kN];
+#pragma unroll
       for (int v = 0; v < Q; ++v) {
         const float r3 = bf16f(sm.raw[buf][v + 3][CROWS + c]);
-        dst[v * kN] = v < cnt ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
+        val[v] = v < cnt ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
         r0 = r1;
         r1 = r2;
         r2 = r3;
       }
+      const int col = c & (kN - 1), odd = c & 1;
+      if (c < kN) {  // B: pairs along the nodes for the update
+#pragma unroll
+        for (int k = 0; k < Q / 2; ++k) split_bf16x2(val[2 * k], val[2 * k + 1], sm.bhi[col][k], sm.blo[col][k]);
+      }
+      // pairs along the columns (B for the Gram, C for C·h and the Gram): even lanes nodes 0..7,
+      // odd lanes nodes 8..15, each pair = (even column, odd column)
+      uint32_t(*phi)[CPS] = c < kN ? sm.bchi : sm.chi;
+      uint32_t(*plo)[CPS] = c < kN ? sm.bclo : sm.clo;
+#pragma unroll
+      for (int v = 0; v < Q; ++v) {
+        const float nb = __shfl_xor_sync(0xffffffffu, val[v], 1);
+        if ((v < Q / 2) != (odd != 0)) {
+          const float e0 = odd ? nb : val[v], e1 = odd ? val[v] : nb;
+          split_bf16x2(e0, e1, phi[v][col >> 1], plo[v][col >> 1]);
+        }
+      }
     }
+    __syncthreads();
+
+    // ---- phase 2: x conv + SiLU into x and u = w·x pairs (threads 0..127); the Gram (warps 4, 5) ----
     if (tid < CROWS) {
       const int hx = tid / kP;
       float4 wk = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -148,81 +204,49 @@ __global__ void __launch_bounds__(CTHREADS, 2) chain_verify_kernel(VerifyArgs a)
         wk = cw[c];
         bk = cb[c];
       }
+      float val[Q];
       float r0 = bf16f(sm.raw[buf][0][tid]), r1 = bf16f(sm.raw[buf][1][tid]), r2 = bf16f(sm.raw[buf][2][tid]);
+#pragma unroll
       for (int v = 0; v < Q; ++v) {
         const float r3 = bf16f(sm.raw[buf][v + 3][tid]);
-        sm.xf[v][tid] = (v < cnt && hx < heads) ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
+        val[v] = (v < cnt && hx < heads) ? silu_fast(conv4_acc(wk, bk, r0, r1, r2, r3)) : 0.f;
         r0 = r1;
         r1 = r2;
         r2 = r3;
       }
-    } else if (tid < CROWS + CHG * Q) {
-      const int k = tid - CROWS, hx = k / Q, v = k - hx * Q;
-      float d = 0.f;
-      if (hx < heads && v < cnt) {
-        const int h = h_begin + hx;
-        d = softplus_f(bf16f(a.dt[((size_t)inst * n + c0 + v) * a.H + h]) + a.dt_bias[(size_t)layer * a.H + h]);
+#pragma unroll
+      for (int k = 0; k < Q / 2; ++k) {
+        split_bf16x2(val[2 * k], val[2 * k + 1], sm.xhi[tid][k], sm.xlo[tid][k]);
+        split_bf16x2(sm.w[hx][2 * k] * val[2 * k], sm.w[hx][2 * k + 1] * val[2 * k + 1], sm.uhi[tid][k],
+                     sm.ulo[tid][k]);
       }
-      sm.dl[hx][v] = d;  // Δ = 0 past the chain: no decay, no input
+    } else if (warp == 4 || warp == 5) {
+      // Gram[v][m] = C_v·B_m: M = 16 nodes v, N = 8 nodes m of this warp, K = the 128 columns
+      const int nt = warp - 4;
+      float g4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < kN / 16; ++ks) {
+        const int kk = 8 * ks + ft;
+        const uint32_t ahi[4] = {sm.chi[fg][kk], sm.chi[fg + 8][kk], sm.chi[fg][kk + 4], sm.chi[fg + 8][kk + 4]};
+        const uint32_t alo[4] = {sm.clo[fg][kk], sm.clo[fg + 8][kk], sm.clo[fg][kk + 4], sm.clo[fg + 8][kk + 4]};
+        const int m = nt * 8 + fg;
+        const uint32_t bh[2] = {sm.bchi[m][kk], sm.bchi[m][kk + 4]};
+        const uint32_t bl[2] = {sm.bclo[m][kk], sm.bclo[m][kk + 4]};
+        mma_bf16(g4, alo, bh);
+        mma_bf16(g4, ahi, bl);
+        mma_bf16(g4, ahi, bh);
+      }
+      const int m = nt * 8 + 2 * ft;
+      sm.gram[fg][m] = g4[0];
+      sm.gram[fg][m + 1] = g4[1];
+      sm.gram[fg + 8][m] = g4[2];
+      sm.gram[fg + 8][m + 1] = g4[3];
     }
     __syncthreads();
 
-    // ---- S, e^{±S}, E, w per head; the Gram C_v·B_m; C, B and x as bf16 pairs ----
-    if (tid < CHG * Q) {  // warp 0: lane = (head, node); S by a shuffle scan over the 16 nodes
-      const int hx = tid / Q, v = tid - hx * Q;
-      const float A = hx < heads ? neg_exp(a.A_log[(size_t)layer * a.H + h_begin + hx]) : 0.f;
-      const float d = sm.dl[hx][v];
-      float s = d * A;
-#pragma unroll
-      for (int off = 1; off < Q; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, s, off, Q);
-        if (v >= off) s += o;
-      }
-      const float s_last = __shfl_sync(0xffffffffu, s, Q - 1, Q);
-      sm.S[hx][v] = s;
-      sm.eS[hx][v] = expf(s);
-      sm.emS[hx][v] = expf(-s);
-      sm.w[hx][v] = d * expf(s_last - s);
-      if (v == Q - 1) sm.E[hx] = expf(s_last);
-    }
-    {  // Gram: thread (v, m) = tid (256 = Q x Q), the k loop staggered by m against conflicts
-      const int v = tid / Q, m = tid - v * Q;
-      const float4* cr = reinterpret_cast<const float4*>(sm.cf[v]);
-      const float4* br = reinterpret_cast<const float4*>(sm.bf[m]);
-      float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-      for (int i = 0; i < kN / 4; ++i) {
-        const int k = (i + m) & (kN / 4 - 1);
-        const float4 c4 = cr[k], b4 = br[k];
-        s0 = fmaf(c4.x, b4.x, s0);
-        s1 = fmaf(c4.y, b4.y, s1);
-        s0 = fmaf(c4.z, b4.z, s0);
-        s1 = fmaf(c4.w, b4.w, s1);
-      }
-      sm.gram[v][m] = s0 + s1;
-    }
-    // (lanes run along the fp32 tables' rows: conflict-free reads)
-    for (int i = tid; i < Q * (kN / 2); i += CTHREADS) {  // C pairs along the state columns
-      const int v = i / (kN / 2), k = i - v * (kN / 2);
-      const float2 c2 = reinterpret_cast<const float2*>(sm.cf[v])[k];
-      split_bf16x2(c2.x, c2.y, sm.chi[v][k], sm.clo[v][k]);
-    }
-    for (int i = tid; i < kN * (Q / 2); i += CTHREADS) {  // B pairs along the nodes
-      const int k = i / kN, col = i - k * kN;
-      split_bf16x2(sm.bf[2 * k][col], sm.bf[2 * k + 1][col], sm.bhi[col][k], sm.blo[col][k]);
-    }
-    for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // x pairs along the nodes
-      const int k = i / CROWS, r = i - k * CROWS;
-      split_bf16x2(sm.xf[2 * k][r], sm.xf[2 * k + 1][r], sm.xhi[r][k], sm.xlo[r][k]);
-    }
-    __syncthreads();
-    for (int i = tid; i < CROWS * (Q / 2); i += CTHREADS) {  // u = w·x pairs
-      const int k = i / CROWS, r = i - k * CROWS, hx = r / kP;
-      split_bf16x2(sm.w[hx][2 * k] * sm.xf[2 * k][r], sm.w[hx][2 * k + 1] * sm.xf[2 * k + 1][r], sm.uhi[r][k],
-                   sm.ulo[r][k]);
-    }
-    for (int i = tid; i < CHG * Q * (Q / 2); i += CTHREADS) {  // coef pairs along m
-      const int hx = i / (Q * (Q / 2)), rest = i - hx * (Q * (Q / 2)), v = rest / (Q / 2), k = rest - v * (Q / 2);
+    // ---- phase 3: coef pairs along m (thread = head, node v, pair k) ----
+    {
+      const int hx = tid / (Q * (Q / 2)), rest = tid - hx * (Q * (Q / 2)), v = rest / (Q / 2), k = rest - v * (Q / 2);
       const float Dh = hx < heads ? a.D[(size_t)layer * a.H + h_begin + hx] : 0.f;
       float cm[2];
 #pragma unroll
