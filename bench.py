@@ -687,7 +687,7 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     out = torch.empty((S, max_path + 2), dtype=torch.int32).pin_memory()
     lay_pin = torch.empty((S, n, 8), dtype=torch.int32).pin_memory()
     copy_stream = torch.cuda.Stream(dev)
-    n_chunks = 4 if S % 4 == 0 else 1
+    n_chunks = args.e2e_chunks if S % args.e2e_chunks == 0 else 1
     per = S // n_chunks
     state = {"r": 0, "depth": depth}
 
@@ -761,6 +761,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[2, 3])
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="sequence chunks the e2e round's copies are cut into")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true")

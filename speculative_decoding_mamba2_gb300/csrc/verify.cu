@@ -138,7 +138,7 @@ __device__ __forceinline__ int4 tap_rows(const ssm_node& r, int v) {
 // prep kernel: everything per instance that does not depend on the head group
 // ---------------------------------------------------------------------------
 struct PrepSmem {
-  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, total;
+  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, hp, total;
 };
 
 __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0) {
@@ -161,6 +161,7 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0
   s.pp = take(LP > 0 ? 20 * 4 : 0);  // committed path nodes [16], its length, the ring head before it
   s.wP = take(LP * H * 4);           // Δ_j, then Δ_j·Π_{i>j} a_i  [LP][H]
   s.aP = take(LP * H * 4);           // a_j = exp(Δ_j·A)          [LP][H]
+  s.hp = take(3 * H * 4);            // per head: A = -exp(A_log), dt_bias, D
   s.total = o;
   return s;
 }
@@ -192,6 +193,9 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
   unsigned char* ws = ws_base + (size_t)inst * W.stride;
   int* pp = reinterpret_cast<int*>(smem + L.pp);
+  float* hA = reinterpret_cast<float*>(smem + L.hp);  // per head: A, then dt_bias, then D
+  float* hBias = hA + H;
+  float* hD = hA + 2 * H;
   const uint16_t* prev_xbc = fuse ? a.prev_xBC + (size_t)inst * a.prev_n * conv_dim : nullptr;
 
   // B|C input rows of the tree's nodes in flight first (rows 3..n+2; rows 0..2 follow below)
@@ -202,6 +206,11 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   // warp 0 checks the committed path while the other warps load the node records and Δ
   const ssm_node* lay = a.layout + (size_t)seq * n;
   const int t0 = fuse ? 32 : 0;
+  for (int h = tid; h < H; h += THREADS) {
+    hA[h] = neg_exp(a.A_log[(size_t)layer * H + h]);
+    hBias[h] = a.dt_bias[(size_t)layer * H + h];
+    hD[h] = a.D[(size_t)layer * H + h];
+  }
   if (tid >= t0) {
     for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, a.status);
     for (int i = tid - t0; i < n * H; i += THREADS - t0) {
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   // contiguous stores), Δ_v·e^{-S_v} kept for the coefficients
   for (int i = tid; i < n * H; i += THREADS) {
     const int h = i / n, v = i - h * n;
-    const float A = neg_exp(a.A_log[(size_t)layer * H + h]);
+    const float A = hA[h];
     float s = 0.f;
     const int dv = nodes[v].depth;
     for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * H + h], A, s);
@@ -347,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     const int pr = pairs[1 + k];
     const int v = pr / DMAX, m = pathn[pr];
     float c = emS[m * H + h] * dl[m * H + h] * Gm[pr];
-    if (m == v) c = fmaf(a.D[(size_t)layer * H + h], emS[v * H + h], c);
+    if (m == v) c = fmaf(hD[h], emS[v * H + h], c);
     wc[h * W.PP + k] = c;
   }
   if (!fuse) return;
@@ -357,10 +366,9 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   float* aP = reinterpret_cast<float*>(smem + L.aP);
   for (int i = tid; i < lenP * H; i += THREADS) {
     const int j = i / H, h = i - j * H;
-    const float d = softplus_f(bf16f(a.prev_dt[((size_t)inst * a.prev_n + pp[j]) * H + h]) +
-                               a.dt_bias[(size_t)layer * H + h]);
+    const float d = softplus_f(bf16f(a.prev_dt[((size_t)inst * a.prev_n + pp[j]) * H + h]) + hBias[h]);
     wP[i] = d;
-    aP[i] = decay_of(d, neg_exp(a.A_log[(size_t)layer * H + h]));
+    aP[i] = decay_of(d, hA[h]);
   }
   __syncthreads();
   for (int h = tid; h < H; h += THREADS) {
@@ -416,26 +424,16 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
       }
     }
   }
-  __syncthreads();  // every read of the old ring rows is done
-  {  // conv ring: the path's last min(len, 3) rows go to positions head+len-3 .. head+len-1,
-     // 16-byte pieces, every load of a pass in flight before its stores
+  {  // conv ring, B | C channels: the three rows before the new root (staged in xin rows 0..2)
+     // that are path rows go to their ring positions head+j (the main kernel writes the x
+     // channels of the same rows from its staged window); rows of the old ring stay where they are
     uint16_t* rw = a.ring_w + (size_t)inst * R * conv_dim;
-    const int j0 = lenP > 3 ? lenP - 3 : 0;
-    const int c8 = conv_dim / 8, total = (lenP - j0) * c8;
-    for (int base = 0; base < total; base += 8 * THREADS) {
-      uint4 buf[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * THREADS + tid;
-        if (idx < total)
-          buf[u] = reinterpret_cast<const uint4*>(prev_xbc + (size_t)pp[j0 + idx / c8] * conv_dim)[idx % c8];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int idx = base + u * THREADS + tid;
-        if (idx < total)
-          reinterpret_cast<uint4*>(rw + (size_t)ring_pos(head_old, j0 + idx / c8, R) * conv_dim)[idx % c8] = buf[u];
-      }
+    for (int i = tid; i < 3 * 32; i += THREADS) {
+      const int r = i >> 5, pc = i & 31;
+      const int k = 3 - r;  // k-th row before the new root = path row lenP - k
+      if (k > lenP) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(xin + r * XW + pc * 8);
+      *reinterpret_cast<uint4*>(rw + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim + d_inner + pc * 8) = v;
     }
   }
   int* meta = reinterpret_cast<int*>(ws + W.meta);
@@ -706,6 +704,17 @@ __global__ void __launch_bounds__(THREADS, 2)
   auto xconv = [&](int g) {
     const int hb = hc_begin + g * G, heads = min(G, a.H - hb);
     wait_or_abort(x_bar, g & 1);
+    if (FUSE) {
+      // conv ring, this group's x channels: the committed path's last min(len, 3) rows (window
+      // rows 3 + j) go to ring positions head + j; the prep kernel writes their B | C channels
+      const int j0 = lenP > 3 ? lenP - 3 : 0, per_row = heads * kP / 8;
+      uint16_t* rw = a.ring_w + (size_t)inst * R * conv_dim + (size_t)hb * kP;
+      for (int i = tid; i < (lenP - j0) * per_row; i += THREADS) {
+        const int j = j0 + i / per_row, pc = i - (i / per_row) * per_row;
+        *reinterpret_cast<uint4*>(rw + (size_t)ring_pos(s_meta[1], j, R) * conv_dim + pc * 8) =
+            *reinterpret_cast<const uint4*>(xinX + (3 + j) * XW + pc * 8);
+      }
+    }
     if (2 * cp < heads * kP) {
       const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
       float2* __restrict__ xo = reinterpret_cast<float2*>(xs) + cp;                     // node v: xo[v * XSTR/2]
