@@ -269,15 +269,19 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def source_digest(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def source_digest(paths):
+    """sha256 prefix of the concatenated kernel sources a capture was taken on."""
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def ncu_traffic(call, units):
     """DRAM bytes of one call (all its launches) from a committed ncu summary
     (profiles/dram_traffic.txt), scaled to `units` instances; None if absent or
-    taken on other kernel source."""
+    taken on other kernel source (`source=` lists the files, joined by '+')."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -287,8 +291,9 @@ def ncu_traffic(call, units):
         kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
         if kv.get("call") != call:
             continue
-        src = os.path.join(ROOT, "speculative_decoding_mamba2_gb300", "csrc", kv.get("source", ""))
-        if not os.path.exists(src) or source_digest(src) != kv.get("sha"):
+        srcs = [os.path.join(ROOT, "speculative_decoding_mamba2_gb300", "csrc", f)
+                for f in kv.get("source", "").split("+") if f]
+        if not srcs or not all(os.path.exists(s) for s in srcs) or source_digest(srcs) != kv.get("sha"):
             return None
         return float(kv["bytes_per_unit"]) * units
     return None

@@ -28,6 +28,36 @@ __device__ __forceinline__ float silu_fast(float v) {
   return v < -80.0f ? 0.0f : __fdividef(v, 1.0f + __expf(-v));
 }
 
+// SiLU on the FMA pipe only (no special-function unit), for conv work that runs next to
+// tensor-core work: v / (1 + 2^t), t = -v·log2(e).
+//  * 2^t: Cody-Waite range reduction -- n = round(t) by adding and subtracting 1.5·2^23,
+//    f = t - n in [-1/2, 1/2] -- then the degree-6 Taylor series of 2^f = e^{f·ln 2}
+//    (coefficients (ln 2)^k / k!, remainder about 1e-7 on that interval), scaled by 2^n
+//    through the exponent field; t is clamped to [-126, 126] (v beyond ±87 gives v or 0).
+//  * 1 / d: Newton-Raphson r <- r·(2 - d·r), three steps from the linear bit-pattern guess
+//    0x7F000000 - bits(d) (relative error below 1/8, then 2^-6, 2^-12, 2^-24).
+// Relative error of the result about 4e-6, like the special-function version above.
+__device__ __forceinline__ float exp2_poly(float t) {
+  t = fminf(fmaxf(t, -126.0f), 126.0f);
+  const float m = t + 12582912.0f;  // 1.5·2^23: m's low mantissa bits hold round(t)
+  const float f = t - (m - 12582912.0f);
+  float p = 1.5403530393381608e-4f;
+  p = fmaf(p, f, 1.3333558146428443e-3f);
+  p = fmaf(p, f, 9.618129107628477e-3f);
+  p = fmaf(p, f, 5.550410866482158e-2f);
+  p = fmaf(p, f, 2.402265069591007e-1f);
+  p = fmaf(p, f, 6.931471805599453e-1f);
+  p = fmaf(p, f, 1.0f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(m) - 0x4B400000) * (1 << 23));
+}
+__device__ __forceinline__ float recip_nr(float d) {
+  float r = __int_as_float(0x7F000000 - __float_as_int(d));
+#pragma unroll
+  for (int i = 0; i < 3; ++i) r = fmaf(r, fmaf(-d, r, 1.0f), r);
+  return r;
+}
+__device__ __forceinline__ float silu_fma(float v) { return v * recip_nr(1.0f + exp2_poly(-1.4426950408889634f * v)); }
+
 // softplus(v) = log(1 + e^v); above 20 it equals v to fp32 precision.
 __device__ __forceinline__ float softplus_f(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
 
