@@ -269,6 +269,9 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12  # GB300 FP32 CUDA-core peak at the 2070 MHz maximum SM clock
+
+
 def source_digest(paths):
     """sha256 prefix of the concatenated kernel sources a capture was taken on."""
     h = hashlib.sha256()
@@ -511,7 +514,8 @@ def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
     import numpy as np
     import torch
 
-    from speculative_decoding_mamba2_gb300 import Dims, ssm_tree_layout_build, ssm_tree_verify
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_tree_layout_build, ssm_tree_verify,
+                                                   ssm_tree_verify_workspace_size)
     from synth import batch, workload
     w = workload(4)
     seqs = list(range(rank * seqs_per_rank, (rank + 1) * seqs_per_rank))
@@ -529,7 +533,7 @@ def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
     ring = bf16(b["ring"])
     head = torch.from_numpy(b["ring_head"]).to(dev)
     y = torch.empty((I, n, H * P), device=dev)
-    ws = torch.empty(16, dtype=torch.uint8, device=dev)
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, depth), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     del b
 
@@ -552,12 +556,17 @@ def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
     d_inner, conv_dim = H * P, H * P + 2 * N
     by = I * (H * P * N * 4 + n * conv_dim * 2 + n * H * 2 + 3 * conv_dim * 2 + n * d_inner * 4)
     flops = 4.0 * n * H * P * N * I  # C·h and u·B over the state, 2 FLOP each per element and node
+    tf = flops / (ms / 1e3) / 1e12
     return {"workload": w.name + f" (chain tree; a sample of {S} sequences x {L} layers per GPU)",
             "nodes": n, "instances_per_gpu": I, "ms": ms,
             "value": n * I * world / (ms / 1e3), "unit": "verified tree-node SSM updates/s",
             "roofline": {"bound": "hbm", "achieved": by / ms / 1e6, "peak": peak, "unit": "GB/s",
-                         "frac": by / ms / 1e6 / peak, "peak_source": peak_kind},
-            "bytes": by, "state_TFLOP/s": flops / (ms / 1e3) / 1e12}
+                         "frac": by / ms / 1e6 / peak, "peak_source": peak_kind,
+                         "traffic": ncu_traffic("ssm_tree_verify_chain", I)},
+            "bytes": by, "state_TFLOP/s": tf,
+            # the same state FLOPs against the FP32 CUDA-core peak (152 SMs x 128 lanes x 2 FLOP
+            # x 2.07 GHz): the bound of a plain recurrence, which these tensor-core products lift
+            "fp32_alu": {"achieved": tf, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS}}
 
 
 def draft_step_bytes(H, P, N, n_inst, n_layers):

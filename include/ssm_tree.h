@@ -128,7 +128,9 @@ int ssm_tree_layout_build(const int32_t *parent, int32_t n_seq, int32_t n_nodes,
  *              = its deepest node.  Branching trees: n <= SSM_MAX_NODES and
  *              max_depth <= SSM_MAX_DEPTH.  A tree with max_depth = n-1 is a
  *              chain; chains up to SSM_MAX_CHAIN_NODES are verified by walking
- *              them with the state on chip (no workspace needed).
+ *              them in 16-node chunks with the state on chip (the workspace
+ *              then holds each chunk's B | C tables, 17 KB per instance and
+ *              chunk).
  *   xBC        device bf16 [I][n][conv_dim]  pre-conv rows of the tree nodes
  *   dt         device bf16 [I][n][H]         raw dt
  *   h0         device fp32 [I][H][P][N]      committed state (read only)

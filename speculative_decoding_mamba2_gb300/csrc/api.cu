@@ -93,8 +93,9 @@ extern "C" size_t ssm_tree_verify_workspace_size(const ssm_dims* dims, int32_t n
   const char* fn = "ssm_tree_verify_workspace_size";
   if (check_verify_shape(fn, dims, n_seq, n_nodes, max_depth) != SSM_OK) return 0;
   g_error.clear();
-  if (long_chain(n_nodes, max_depth)) return 16;  // the chain kernel needs no workspace
-  const size_t b = verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers);
+  const size_t b = long_chain(n_nodes, max_depth)
+                       ? chain_workspace_bytes(n_nodes, dims->n_heads, (long long)n_seq * dims->n_layers)
+                       : verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers);
   return b ? b : 16;
 }
 
@@ -111,8 +112,9 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   if (((uintptr_t)xBC | (uintptr_t)h0 | (uintptr_t)ring | (uintptr_t)layout | (uintptr_t)workspace) & 15)
     return fail(SSM_ERR_INVALID_ARG, fn, "xBC, h0, ring, layout and workspace must be 16-byte aligned");
   const bool chain = long_chain(n_nodes, max_depth);
-  if (!chain &&
-      workspace_bytes < verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, (long long)n_seq * dims->n_layers))
+  const long long n_inst = (long long)n_seq * dims->n_layers;
+  if (workspace_bytes < (chain ? chain_workspace_bytes(n_nodes, dims->n_heads, n_inst)
+                               : verify_workspace_bytes(n_nodes, max_depth, dims->n_heads, n_inst)))
     return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_tree_verify_workspace_size()");
   VerifyArgs a{};
   a.gpc = 1;
@@ -135,7 +137,7 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   a.ring_head = ring_head;
   a.y = y;
   a.status = dev_status;
-  return finish(fn, chain ? launch_chain_verify(a, (cudaStream_t)stream)
+  return finish(fn, chain ? launch_chain_verify(a, workspace, (cudaStream_t)stream)
                          : launch_verify(a, workspace, (cudaStream_t)stream));
 }
 

@@ -286,7 +286,9 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
 int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
-cudaError_t launch_chain_verify(const VerifyArgs& a, cudaStream_t s);
+// Chain trees: workspace bytes (one record per instance and 16-node chunk) and the launch.
+size_t chain_workspace_bytes(int n, int H, long long n_inst);
+cudaError_t launch_chain_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
 
 struct AcceptArgs {
   int n_seq, n, max_path;

@@ -189,6 +189,27 @@ def test_chain_kernel_small(n):
     check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
 
 
+def test_chain_kernel_longest_chain():
+    # 4095 nodes, one below SSM_MAX_CHAIN_NODES: 256 chunks, the last one 15 nodes; an odd
+    # head count (a CTA with one head); two layers
+    from speculative_decoding_mamba2_gb300 import ssm_tree_verify, ssm_tree_verify_workspace_size
+    n = 4095
+    w = Workload(57, "longest chain", Shape(H=3), n_layers=2, batch=1, trees=(("chain", n),))
+    b = batch(w)
+    d = upload_tree_batch(b, w)
+    dims, S = d["dims"], d["n_seq"]
+    y = torch.full((S * 2, n, dims.d_inner), float("nan"), device="cuda")
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, d["depth"]), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ssm_tree_verify(dims, d["params"], S, n, d["depth"], d["layout"], d["xBC"], d["dt"], d["h0"], d["ring"],
+                    d["ring_head"], y, ws, status)
+    torch.cuda.synchronize()
+    assert int(status) == 0
+    for j in range(2):
+        ref = _chain_reference(b, 0, j)
+        assert rel_err(y[j].double().cpu().numpy(), ref) <= TOL, j
+
+
 def test_config4_chain_256_sampled():
     w = workload(4)
     b = batch(w, seqs=[0, 63], layers=[0, 47], tree=1)
