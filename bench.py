@@ -698,42 +698,97 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     path = torch.empty((S, max_path), dtype=torch.int32, device=dev)
     plen = torch.empty(S, dtype=torch.int32, device=dev)
     bonus = torch.empty(S, dtype=torch.int32, device=dev)
-    out = torch.empty((S, max_path + 2), dtype=torch.int32).pin_memory()
+    out_path = torch.empty((S, max_path), dtype=torch.int32).pin_memory()  # contiguous: graph-capturable D2H
+    out_len = torch.empty(S, dtype=torch.int32).pin_memory()
+    out_bonus = torch.empty(S, dtype=torch.int32).pin_memory()
     lay_pin = torch.empty((S, n, 8), dtype=torch.int32).pin_memory()
     copy_stream = torch.cuda.Stream(dev)
-    n_chunks = args.e2e_chunks if S % args.e2e_chunks == 0 else 1
-    per = S // n_chunks
+    if args.e2e_split == "ramp":  # 1, 1, 2, 3, ...: the first chunk lands early, later ones keep up
+        sizes, nxt = [1], 1
+        while sum(sizes) < S:
+            sizes.append(min(nxt, S - sum(sizes)))
+            nxt += 1
+        if len(sizes) > 2 and 2 * sizes[-1] < sizes[-2]:  # fold a small tail chunk into the one before
+            tail = sizes.pop()
+            sizes[-1] += tail
+    elif args.e2e_split:  # explicit chunk sizes in sequences, e.g. "2,2,4,8"
+        sizes = [int(v) for v in args.e2e_split.split(",")]
+        if sum(sizes) != S or min(sizes) < 1:
+            raise SystemExit(f"--e2e-split must be positive sizes summing to {S}")
+    else:
+        k = args.e2e_chunks if S % args.e2e_chunks == 0 else 1
+        sizes = [S // k] * k
+    bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
+    n_chunks = len(sizes)
     state = {"r": 0, "depth": depth}
+
+    computes = [torch.cuda.Stream(dev) for _ in range(max(0, args.e2e_streams - 1))]
+
+    def enqueue(cur, prev, dp, cs):
+        """One round's copies and calls: copies on copy_stream, chunk calls alternating between
+        compute stream `cs` and a second one (chunks touch disjoint sequences), so one
+        chunk's prep kernel overlaps the previous chunk's main kernel."""
+        copy_stream.wait_stream(cs)  # the previous round is finished with both buffers
+        streams = [cs] + computes
+        for x in computes:
+            x.wait_stream(cs)
+        with torch.cuda.stream(copy_stream):  # the small per-sequence inputs of all chunks first
+            lay_d[cur].copy_(lay_pin, non_blocking=True)
+            tok_d.copy_(tok_h, non_blocking=True)
+            tgt_d.copy_(tgt_h, non_blocking=True)
+        for c in range(n_chunks):
+            q = slice(bounds[c], bounds[c + 1])
+            per = sizes[c]
+            ccs = streams[c % len(streams)]
+            with torch.cuda.stream(copy_stream):
+                xBC_d[cur][q].copy_(xBC_h[q], non_blocking=True)
+                dt_d[cur][q].copy_(dt_h[q], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(copy_stream)
+            ccs.wait_event(landed)
+            ssm_commit_verify(dims, prm, per, n, lay_d[prev][q], state["depth"] + 1, path[q], plen[q],
+                              xBC_d[prev][q].view(torch.bfloat16), dt_d[prev][q].view(torch.bfloat16), n, dp,
+                              lay_d[cur][q], xBC_d[cur][q].view(torch.bfloat16), dt_d[cur][q].view(torch.bfloat16),
+                              hv[q], ringv[q], headv[q], y[q], wsv[q], status, ccs)
+            ssm_accept_path(per, n, dp + 1, lay_d[cur][q], tok_d[q], tgt_d[q], path[q], plen[q], bonus[q], status,
+                            ccs)
+        cs.wait_stream(copy_stream)
+        for x in computes:
+            cs.wait_stream(x)
+        with torch.cuda.stream(cs):
+            out_path.copy_(path, non_blocking=True)
+            out_len.copy_(plen, non_blocking=True)
+            out_bonus.copy_(bonus, non_blocking=True)
+
+    # With --e2e-graph each round's copies and calls are captured once per buffer parity into a
+    # CUDA graph (the tree shape, hence every size and depth, is the same each round) and
+    # replayed: the host then only builds the layout, fills the pinned layout buffer and
+    # launches one graph per round.
+    graphs = {}
 
     def one():
         cur, prev = (state["r"] + 1) % 2, state["r"] % 2
         state["r"] += 1
         lay, dp = ssm_tree_layout_build(par_h, max_branches=3, max_depth=4)
         lay_pin.numpy()[...] = lay
-        copy_stream.wait_stream(stream)  # the previous round is finished with both buffers
-        for c in range(n_chunks):
-            q = slice(c * per, (c + 1) * per)
-            with torch.cuda.stream(copy_stream):
-                lay_d[cur][q].copy_(lay_pin[q], non_blocking=True)
-                xBC_d[cur][q].copy_(xBC_h[q], non_blocking=True)
-                dt_d[cur][q].copy_(dt_h[q], non_blocking=True)
-                tok_d[q].copy_(tok_h[q], non_blocking=True)
-                tgt_d[q].copy_(tgt_h[q], non_blocking=True)
-                landed = torch.cuda.Event()
-                landed.record(copy_stream)
-            stream.wait_event(landed)
-            ssm_commit_verify(dims, prm, per, n, lay_d[prev][q], state["depth"] + 1, path[q], plen[q],
-                              xBC_d[prev][q].view(torch.bfloat16), dt_d[prev][q].view(torch.bfloat16), n, dp,
-                              lay_d[cur][q], xBC_d[cur][q].view(torch.bfloat16), dt_d[cur][q].view(torch.bfloat16),
-                              hv[q], ringv[q], headv[q], y[q], wsv[q], status, stream)
-            ssm_accept_path(per, n, dp + 1, lay_d[cur][q], tok_d[q], tgt_d[q], path[q], plen[q], bonus[q], status,
-                            stream)
+        if args.e2e_graph:
+            if dp != state["depth"]:
+                raise RuntimeError("the e2e graph replays one tree shape")
+            if cur not in graphs:
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream(dev)
+                side.wait_stream(stream)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    enqueue(cur, prev, dp, torch.cuda.current_stream())
+                graphs[cur] = g
+            with torch.cuda.stream(stream):
+                graphs[cur].replay()
+        else:
+            enqueue(cur, prev, dp, stream)
         state["depth"] = dp
-        out[:, :max_path].copy_(path, non_blocking=True)
-        out[:, max_path].copy_(plen, non_blocking=True)
-        out[:, max_path + 1].copy_(bonus, non_blocking=True)
         torch.cuda.synchronize()
-        return out
+        return out_path, out_len, out_bonus
 
     # the first round needs an accepted path to commit: accept the tree of buffer 0 (the
     # state it would be verified from is the one the device holds)
@@ -763,8 +818,9 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     return {"value": n * L * S * world / secs, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": steps, "ms_per_step": secs * 1e3,
             "calls": "ssm_tree_layout_build, ssm_commit_verify, ssm_accept_path",
-            "overlap": f"H2D in {n_chunks} chunks of sequences on a copy stream; each chunk's calls start when "
-                       "its inputs have landed"}
+            "overlap": f"H2D in {n_chunks} chunks of {sizes} sequences on a copy stream; each chunk's calls start when "
+                       f"its inputs have landed, alternating over {args.e2e_streams} compute stream(s)"
+                       + ("; each round replayed as one CUDA graph" if args.e2e_graph else "")}
 
 
 def main():
@@ -775,7 +831,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=[2, 3])
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--e2e-chunks", type=int, default=4, help="sequence chunks the e2e round's copies are cut into")
+    ap.add_argument("--e2e-chunks", type=int, default=4, help="equal sequence chunks of the e2e round (with --e2e-split '')")
+    ap.add_argument("--e2e-graph", type=int, default=1, help="replay each e2e round as a CUDA graph (1) or enqueue it (0)")
+    ap.add_argument("--e2e-streams", type=int, default=2, help="compute streams the e2e chunk calls alternate over")
+    ap.add_argument("--e2e-split", default="ramp",
+                    help="e2e chunk sizes in sequences: 'ramp' (1, 1, 2, 3, ...), a list such as '4,4,4,4', "
+                         "or '' for --e2e-chunks equal chunks")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true")
