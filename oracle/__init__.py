@@ -15,3 +15,10 @@ from .ssm_oracle import (  # noqa: F401
     draft_step,
     replay,
 )
+from .block_oracle import (  # noqa: F401
+    to_bf16,
+    linear,
+    rmsnorm,
+    gated_rmsnorm,
+    block_verify,
+)

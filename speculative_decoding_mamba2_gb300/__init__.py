@@ -1,8 +1,9 @@
 """SpecMamba-style tree verification for Mamba2 on GB300 (sm_103a).
 
 The compute path is libssmtree.so (hand-written CUDA, C ABI in
-include/ssm_tree.h); this package holds its sources (csrc/), its build step
-(build.py) and a thin ctypes binding (binding.py) with the same names.
+include/ssm_tree.h and include/ssm_layer.h); this package holds its sources
+(csrc/), its build step (build.py) and a thin ctypes binding (binding.py) with
+the same names.
 """
 from .binding import (  # noqa: F401
     Dims,
@@ -14,8 +15,12 @@ from .binding import (  # noqa: F401
     ssm_commit_verify,
     ssm_commit_verify_workspace_size,
     ssm_draft_step,
+    ssm_gated_rmsnorm,
     ssm_last_error,
+    ssm_linear,
+    ssm_linear_tile_cols,
     ssm_replay,
+    ssm_rmsnorm,
     ssm_tree_layout_build,
     ssm_tree_verify,
     ssm_tree_verify_noalloc,

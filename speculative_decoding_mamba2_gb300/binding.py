@@ -317,3 +317,83 @@ def ssm_replay(dims: Dims, params: dict, n_seq: int, log_cap: int, k, log_delta,
         _dev(log_x, "log_x", torch.float32, I * log_cap * d.d_inner), _dev(log_len, "log_len", torch.int32, I),
         _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
+
+
+# ---------------------------------------------------------------------------
+# the block's dense steps (include/ssm_layer.h)
+# ---------------------------------------------------------------------------
+class ssm_out_segment(ctypes.Structure):
+    _fields_ = [("col", ctypes.c_int32), ("f32", ctypes.c_int32), ("ld", ctypes.c_int64), ("ptr", ctypes.c_void_p)]
+
+
+_SIGS.update({
+    "ssm_linear": (ctypes.c_int, [_I, _I, _I, _P, ctypes.c_int64, _P, ctypes.c_int64, _I, _P, _P, ctypes.c_int64, _P,
+                                  _P]),
+    "ssm_linear_tile_cols": (_I, []),
+    "ssm_rmsnorm": (ctypes.c_int, [_I, _I, _P, ctypes.c_int64, _P, ctypes.c_float, _P, ctypes.c_int64, _P]),
+    "ssm_gated_rmsnorm": (ctypes.c_int, [_I, _I, _P, ctypes.c_int64, _P, ctypes.c_int64, _P, ctypes.c_float, _P,
+                                         ctypes.c_int64, _P]),
+})
+
+
+def _rows(t: torch.Tensor, name: str, dtype, cols: int | None = None):
+    """A 2-D CUDA tensor whose rows are contiguous (any row stride): (pointer, rows, row stride)."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if t.dim() != 2 or (t.size(1) > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name}: must be 2-D with contiguous rows")
+    if cols is not None and t.size(1) != cols:
+        raise ValueError(f"{name}: {t.size(1)} columns, expected {cols}")
+    return ctypes.c_void_p(t.data_ptr()), t.size(0), t.stride(0)
+
+
+def ssm_linear_tile_cols() -> int:
+    return int(lib().ssm_linear_tile_cols())
+
+
+def ssm_linear(A, W, segments, residual=None, status=None, stream=None):
+    """D = A · Wᵀ (+ residual) on the tensor cores.  A: bf16 [M, K], W: bf16 [N, K] (rows
+    contiguous, any row stride).  segments: [(first column, out)], out a bf16 or fp32
+    [M, width] view; the segments cover [0, N) in order.  residual: fp32 [M, N] or None
+    (it may be the output itself)."""
+    a, M, lda = _rows(A, "A", torch.bfloat16)
+    w, N, ldw = _rows(W, "W", torch.bfloat16, A.size(1))
+    K = A.size(1)
+    segs = (ssm_out_segment * len(segments))()
+    for i, (col, out) in enumerate(segments):
+        end = segments[i + 1][0] if i + 1 < len(segments) else N
+        p, rows, ld = _rows(out, f"segment {i}", out.dtype, end - col)
+        if out.dtype not in (torch.bfloat16, torch.float32) or rows != M:
+            raise ValueError(f"segment {i}: bf16 or fp32 with {M} rows")
+        segs[i] = ssm_out_segment(col, 1 if out.dtype == torch.float32 else 0, ld, p.value)
+    r, ldr = None, 0
+    if residual is not None:
+        r, rows, ldr = _rows(residual, "residual", torch.float32, N)
+        if rows != M:
+            raise ValueError("residual: M rows")
+    _check(lib().ssm_linear(M, N, K, a, lda, w, ldw, len(segments), segs, r, ldr, _opt_status(status),
+                            _stream(stream, A)))
+
+
+def ssm_rmsnorm(x, w, eps: float, out, stream=None):
+    """out (bf16) = w · x / sqrt(mean(x²) + eps) per row of x (fp32 [M, C])."""
+    px, M, ldx = _rows(x, "x", torch.float32)
+    C = x.size(1)
+    po, Mo, ldo = _rows(out, "out", torch.bfloat16, C)
+    if Mo != M:
+        raise ValueError("out: M rows")
+    _check(lib().ssm_rmsnorm(M, C, px, ldx, _dev(w, "w", torch.float32, C), float(eps), po, ldo, _stream(stream, x)))
+
+
+def ssm_gated_rmsnorm(y, z, w, eps: float, out, stream=None):
+    """out (bf16) = RMSNorm(y · SiLU(z)) · w per row; y fp32 [M, C], z bf16 [M, C]."""
+    py, M, ldy = _rows(y, "y", torch.float32)
+    C = y.size(1)
+    pz, Mz, ldz = _rows(z, "z", torch.bfloat16, C)
+    po, Mo, ldo = _rows(out, "out", torch.bfloat16, C)
+    if Mz != M or Mo != M:
+        raise ValueError("z, out: M rows")
+    _check(lib().ssm_gated_rmsnorm(M, C, py, ldy, pz, ldz, _dev(w, "w", torch.float32, C), float(eps), po, ldo,
+                                   _stream(stream, y)))

@@ -19,8 +19,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "layout.cpp"]
-HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(INCLUDE, "ssm_tree.h")]
+SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "gemm.cu", "norm.cu",
+           "layer_api.cu", "layout.cpp"]
+HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(INCLUDE, "ssm_tree.h"), os.path.join(INCLUDE, "ssm_layer.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 LIBNAME = "libssmtree.so"
 

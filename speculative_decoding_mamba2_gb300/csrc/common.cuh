@@ -286,6 +286,25 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
 int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
+// Projections (gemm.cu): D = A · Wᵀ (+ residual) with the output columns cut into segments.
+struct GemmArgs {
+  int M, N, K;
+  int n_seg;
+  int seg_col[4];         // first column of each segment (multiples of the tile width)
+  long long seg_ld[4];    // row stride of each segment's output, elements
+  int seg_f32[4];         // 1: fp32 output, 0: bf16
+  void* seg_ptr[4];
+  const float* residual;  // nullptr or fp32 [M][ldr], added to the accumulator
+  long long ldr;
+  int32_t* status;
+};
+int gemm_tile_cols();
+cudaError_t launch_gemm_bf16(const GemmArgs& g, const void* A, long long lda, const void* W, long long ldw,
+                             cudaStream_t s);
+// Row norms (norm.cu): RMSNorm of fp32 rows, and the gated form of y ⊙ SiLU(z).
+cudaError_t launch_rmsnorm(int M, int C, const float* x, long long ldx, const uint16_t* z, long long ldz,
+                           const float* w, float eps, uint16_t* out, long long ldo, cudaStream_t s);
+
 // Chain trees: workspace bytes (one record per instance and 16-node chunk) and the launch.
 size_t chain_workspace_bytes(int n, int H, long long n_inst);
 cudaError_t launch_chain_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);

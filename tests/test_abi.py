@@ -23,7 +23,7 @@ def L():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = open(HEADER).read() + open(os.path.join(os.path.dirname(HEADER), "ssm_layer.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(ssm_\w+)\s*\(", src)))
 
