@@ -481,6 +481,11 @@ def run_ours(args, w):
     if not args.no_chain:
         chain = run_chain(args, dev, stream, world, rank)
 
+    # ---- whole blocks: the dense steps either side of the SSM ----
+    block = None
+    if not args.no_block:
+        block = run_block(args, dev, stream, world, rank, peak)
+
     if status.item() != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
     if rank == 0:
@@ -496,6 +501,8 @@ def run_ours(args, w):
             line["draft"] = draft
         if chain is not None:
             line["chain"] = chain
+        if block is not None:
+            line["block"] = block
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -567,6 +574,145 @@ def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
             # the same state FLOPs against the FP32 CUDA-core peak (152 SMs x 128 lanes x 2 FLOP
             # x 2.07 GHz): the bound of a plain recurrence, which these tensor-core products lift
             "fp32_alu": {"achieved": tf, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS}}
+
+
+def run_block(args, dev, stream, world, rank, peak):
+    """Whole-model tree verify: the batched-verify trees (16 sequences x 16-node trees)
+    through all 64 blocks of the Mamba2-2.7B shape (d_model 2560) with synthetic weights.
+    Per block: RMSNorm -> input projection (tcgen05; z, x|B|C and dt written where the
+    next steps read them) -> ssm_commit_verify (the previous round's accepted path
+    committed, this round's tree verified) -> gated RMSNorm -> output projection added
+    to the residual stream; then the accept walk.  Each round is one CUDA graph of
+    those API calls.  The projections are also timed alone, 64 layers back to back."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_commit_verify,
+                                                   ssm_commit_verify_workspace_size, ssm_gated_rmsnorm,
+                                                   ssm_linear, ssm_rmsnorm, ssm_tree_layout_build)
+    from synth import batch, layer_params, workload
+    w = workload(3)
+    S, L, n = w.batch, w.n_layers, w.n_nodes()
+    H, P, N, R = w.shape.H, w.shape.P, w.shape.N, w.ring_cap
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    d_model = d_inner // 2
+    n_in = d_inner + conv_dim + H
+    T, eps = S * n, 1e-5
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242 + rank)
+
+    def bf16_randn(*shape, scale=1.0):
+        return (torch.randn(*shape, device=dev, generator=gen) * scale).to(torch.bfloat16)
+
+    W_in = [bf16_randn(n_in, d_model, scale=d_model ** -0.5) for _ in range(L)]
+    W_out = [bf16_randn(d_model, d_inner, scale=d_inner ** -0.5) for _ in range(L)]
+    norm_w = [1 + 0.1 * torch.randn(d_model, device=dev, generator=gen) for _ in range(L)]
+    gnorm_w = [1 + 0.1 * torch.randn(d_inner, device=dev, generator=gen) for _ in range(L)]
+    b = batch(w, layers=[0])  # the trees and tokens (the tree inputs come from the projections)
+    prm_all = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in layer_params(w).items()}
+    prm = [{k: v[l:l + 1] for k, v in prm_all.items()} for l in range(L)]
+    h = [torch.randn(S, H, P, N, device=dev, generator=gen) * 0.1 for _ in range(L)]
+    ring = [bf16_randn(S, R, conv_dim) for _ in range(L)]
+    head = [torch.full((S,), 3, dtype=torch.int32, device=dev) for _ in range(L)]
+    xbc = [[torch.empty(T, conv_dim, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(2)]
+    dtb = [[torch.empty(T, H, dtype=torch.bfloat16, device=dev) for _ in range(L)] for _ in range(2)]
+    x0 = torch.randn(T, d_model, device=dev, generator=gen)
+    x = torch.empty_like(x0)
+    u = torch.empty(T, d_model, dtype=torch.bfloat16, device=dev)
+    z = torch.empty(T, d_inner, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T, d_inner, device=dev)
+    gb = torch.empty(T, d_inner, dtype=torch.bfloat16, device=dev)
+    lay, depth = ssm_tree_layout_build(b["parent"], max_branches=3, max_depth=4)
+    layout = torch.from_numpy(lay).to(dev)
+    max_path = depth + 1
+    tok, tgt = torch.from_numpy(b["tok"]).to(dev), torch.from_numpy(b["tgt"]).to(dev)
+    path = torch.empty((S, max_path), dtype=torch.int32, device=dev)
+    plen = torch.empty(S, dtype=torch.int32, device=dev)
+    bonus = torch.empty(S, dtype=torch.int32, device=dev)
+    dims1 = Dims(n_heads=H, n_layers=1, ring_cap=R)
+    ws = torch.empty(ssm_commit_verify_workspace_size(dims1, S, n, depth, max_path), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def project_in(l, buf, cs):
+        ssm_rmsnorm(x, norm_w[l], eps, u, cs)
+        ssm_linear(u, W_in[l], [(0, z), (d_inner, xbc[buf][l]), (d_inner + conv_dim, dtb[buf][l])], status=status,
+                   stream=cs)
+
+    def one_round(cur, cs):
+        prev = 1 - cur
+        x.copy_(x0)
+        for l in range(L):
+            project_in(l, cur, cs)
+            ssm_commit_verify(dims1, prm[l], S, n, layout, max_path, path, plen, xbc[prev][l], dtb[prev][l], n, depth,
+                              layout, xbc[cur][l], dtb[cur][l], h[l], ring[l], head[l], y, ws, status, cs)
+            ssm_gated_rmsnorm(y, z, gnorm_w[l], eps, gb, cs)
+            ssm_linear(gb, W_out[l], [(0, x)], residual=x, status=status, stream=cs)
+        ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status, cs)
+
+    with torch.cuda.stream(stream):  # a first round's projections and accept, so every round has a path to commit
+        x.copy_(x0)
+        for l in range(L):
+            project_in(l, 1, stream)
+        ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status, stream)
+    torch.cuda.synchronize()
+    graphs = []
+    for cur in (0, 1):
+        gph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gph, stream=side):
+            one_round(cur, torch.cuda.current_stream())
+        graphs.append(gph)
+    r = [0]
+
+    def replay(ev=None):
+        with torch.cuda.stream(stream):
+            graphs[r[0] % 2].replay()
+        r[0] += 1
+
+    for _ in range(max(3, args.warmup)):
+        replay()
+    torch.cuda.synchronize()
+    steps = max(5, min(args.steps, 20))
+    ms, _ = _timed(steps, lambda k, ev=None: replay(), world, stream, 0)
+    ms = max_over_ranks(ms, world, dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the block rounds")
+
+    # the projections alone, 64 layers back to back (weights stream from HBM: 3.5 + 1.7 GB)
+    def proj_loop(which):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for l in range(L):
+                if which == "in":
+                    ssm_linear(u, W_in[l], [(0, z), (d_inner, xbc[0][l]), (d_inner + conv_dim, dtb[0][l])],
+                               stream=stream)
+                else:
+                    ssm_linear(gb, W_out[l], [(0, x)], residual=x, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / L
+    proj = {}
+    for which, (NN, KK) in (("in", (n_in, d_model)), ("out", (d_model, d_inner))):
+        proj_loop(which)
+        us = proj_loop(which) * 1e3
+        by = NN * KK * 2 + T * KK * 2 + T * NN * (2 if which == "in" else 8)
+        fl = 2.0 * T * NN * KK
+        proj[which] = {"shape_MNK": [T, NN, KK], "us": us, "GB/s": by / us / 1e3, "TFLOP/s": fl / us / 1e6,
+                       "frac_of_hbm_peak": by / us / 1e3 / peak}
+    weights = L * (n_in * d_model + d_model * d_inner) * 2
+    ssm_bytes = commit_verify_bytes_per_instance(H, P, N, n, float(plen.float().mean())) * S * L
+    total = weights + ssm_bytes
+    return {"workload": f"whole-model tree verify: {L} Mamba2-2.7B blocks (d_model {d_model}, synthetic weights), "
+                        f"batch {S}, {n}-node random trees",
+            "ms_per_round": ms, "value": n * S * L * world / (ms / 1e3), "unit": UNIT,
+            "tree_tokens_per_s": n * S * world / (ms / 1e3),
+            "bytes_per_round": total, "weights_bytes": weights,
+            "roofline": {"bound": "hbm", "achieved": total / ms / 1e6, "peak": peak, "unit": "GB/s",
+                         "frac": total / ms / 1e6 / peak},
+            "launches_per_round": L * 6 + 1, "projections": proj}
 
 
 def draft_step_bytes(H, P, N, n_inst, n_layers):
@@ -841,6 +987,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
+    ap.add_argument("--no-block", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
