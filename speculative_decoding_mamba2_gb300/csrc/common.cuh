@@ -297,10 +297,10 @@ struct GemmArgs {
   const float* residual;  // nullptr or fp32 [M][ldr], added to the accumulator
   long long ldr;
   int32_t* status;
+  int tn, cl, splits, kb_per_split, tmem_cols, stages;  // tile plan, set by launch_gemm_bf16
 };
 int gemm_tile_cols();
-cudaError_t launch_gemm_bf16(const GemmArgs& g, const void* A, long long lda, const void* W, long long ldw,
-                             cudaStream_t s);
+cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const void* W, long long ldw, cudaStream_t s);
 // Row norms (norm.cu): RMSNorm of fp32 rows, and the gated form of y ⊙ SiLU(z).
 cudaError_t launch_rmsnorm(int M, int C, const float* x, long long ldx, const uint16_t* z, long long ldz,
                            const float* w, float eps, uint16_t* out, long long ldo, cudaStream_t s);

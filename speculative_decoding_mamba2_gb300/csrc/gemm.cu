@@ -7,31 +7,46 @@
 //     D[t, o] = Σ_k A[t, k] · W[o, k]          (bf16 inputs, fp32 accumulation)
 // with W stored row-major [out features][in features] (K contiguous), A [tokens][K].
 //
-// gemm_bf16_kernel: one CTA (4 warps) per 128 x 128 output tile.  Thread 0 issues
-// tensor-map bulk copies (TMA, 128-byte swizzle) of 128 x 64 tiles of A and W into a
-// 4-stage shared-memory ring; thread 32 issues tcgen05.mma (M = 128, N = 128, K = 16,
-// both operands from shared memory through matrix descriptors) into one fp32 TMEM
-// accumulator and hands each stage back with tcgen05.commit; after the last k-block
-// all four warps read the accumulator (tcgen05.ld, each warp its 32 TMEM lanes = rows)
-// and store it.  The epilogue writes up to four column segments to separate outputs
-// (the input projection's z, x|B|C and dt land where the next kernels read them),
-// as bf16 or fp32, optionally adding an fp32 residual (the output projection updates
-// the residual stream in place).  Every wait on an mbarrier is bounded.
+// gemm_bf16_kernel is built for few tokens and wide weights (a decode/verify batch: a few
+// hundred tokens against megabytes of weights), where the weights must stream from HBM once:
+//  * the MMA computes Dᵀ = W · tokensᵀ: a CTA (4 warps) owns 128 output features (the MMA's
+//    M, TMEM lanes), all tokens of a chunk of up to 256 (the MMA's N) and one K-split, so
+//    each weight tile is read by exactly one CTA and each MMA does 128 x N x 16;
+//  * CTAs come in clusters of up to 4 along the features; every k-block's token tile is
+//    shared: each CTA loads 1/CL of its rows with a multicast bulk tensor copy (TMA) into
+//    the same shared-memory offset of every CTA in the cluster;
+//  * K-splits, chosen on the host to fill the SMs, accumulate into an fp32 output with
+//    vector reductions (used by the output projection, which adds into the residual
+//    stream anyway);
+//  * warp 0 feeds a ring of as many stages as shared memory holds (a stage is refilled once
+//    every CTA of the cluster has finished with it: the MMAs' completion is multicast to
+//    their `empty` barriers), warp 1 issues tcgen05.mma (operands from shared memory
+//    through 128-byte-swizzle matrix descriptors) and commits; after the last k-block all
+//    four warps read the accumulator (tcgen05.ld, warp w = TMEM lanes 32w..) into the now
+//    idle stage memory as a [token][feature] tile and write it out row by row with
+//    coalesced vector stores.
+// The epilogue writes up to four column segments to separate outputs (the input
+// projection's z, x|B|C and dt land where the next kernels read them), bf16 or fp32,
+// optionally adding an fp32 residual.  Every wait on an mbarrier is bounded and polled by one
+// thread while its warp (or the CTA) waits at a hardware barrier; the cluster meets at a
+// barrier before any copy and before any CTA leaves.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 
 namespace ssmtree {
 namespace {
 
-constexpr int GBM = 128, GBN = 128, GBK = 64, GSTAGES = 4, GTHREADS = 128;
-constexpr int A_STAGE = GBM * GBK * 2;  // 16 KB: 128 rows of 128 bytes
-constexpr int B_STAGE = GBN * GBK * 2;  // 16 KB
-constexpr int TMEM_COLS = GBN;          // one fp32 accumulator column per output column
-constexpr int GEMM_SMEM = GSTAGES * (A_STAGE + B_STAGE) + 1024 /* alignment */ + 256 /* barriers */;
-
-static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM is allocated in powers of two >= 32");
+constexpr int GBK = 64, GTHREADS = 128;
+constexpr int FM = 128;                            // output features per CTA (MMA M, TMEM lanes)
+constexpr int MAX_TN = 256;                        // tokens per CTA (MMA N)
+constexpr int MAX_STAGES = 8;
+constexpr int GEMM_SMEM = 227 * 1024;              // the stage ring takes what the tile plan fits in here
+constexpr int GEMM_RESERVED = 1024 /* alignment */ + 512 /* barriers */;
+constexpr int SEG_ALIGN = 16;                      // segment boundaries: multiples of the narrowest tile
 
 // ---- tcgen05 / TMEM helpers (inline PTX) ----
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -95,6 +110,53 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// arrive on `bar` (same shared-memory offset) in every CTA of `mask` once this thread's MMAs complete
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
+               ::"r"(bar), "h"(mask)
+               : "memory");
+}
+// 2-D bulk tensor copy into the same shared-memory offset (and barrier) of every CTA in `mask`
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+      "%3}], [%4], %5;\n" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
+      : "memory");
+}
+// Wait for phase `parity` of `bar` by polling the non-blocking test_wait from ONE thread (the
+// rest of its warp or CTA waits at a hardware barrier): a thread suspended in try_wait is not
+// always woken as soon as an asynchronous arrival (a bulk copy, an MMA commit) completes the
+// phase.  Gives up after about one second of global time and returns false.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_ns();
+  for (unsigned it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if ((it & 1023) == 1023 && global_ns() - t0 > 1000000000ull) return false;
+  }
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -105,128 +167,177 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tw, GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char* sa = smem;                              // [GSTAGES][A_STAGE]
-  unsigned char* sw = smem + GSTAGES * A_STAGE;          // [GSTAGES][B_STAGE]
-  unsigned long long* full = reinterpret_cast<unsigned long long*>(sw + GSTAGES * B_STAGE);
-  unsigned long long* empty = full + GSTAGES;
-  unsigned long long* acc_bar = empty + GSTAGES;
+  const int TN = g.tn, CL = g.cl, GSTAGES = g.stages;
+  const int w_stage = FM * GBK * 2, t_stage = TN * GBK * 2;  // both multiples of 1024
+  unsigned char* sw = smem;                      // [GSTAGES][w_stage]: weight rows (MMA operand A)
+  unsigned char* st = smem + GSTAGES * w_stage;  // [GSTAGES][t_stage]: token rows (MMA operand B)
+  unsigned long long* full = reinterpret_cast<unsigned long long*>(st + GSTAGES * t_stage);
+  unsigned long long* empty = full + MAX_STAGES;
+  unsigned long long* acc_bar = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * GBM, n0 = blockIdx.y * GBN;
+  const int f0 = blockIdx.x * FM, t0 = blockIdx.z * MAX_TN;
   const int KB = (g.K + GBK - 1) / GBK;
+  const int kb0 = blockIdx.y * g.kb_per_split, kb1 = min(KB, kb0 + g.kb_per_split);
+  const int rank = CL > 1 ? (int)cluster_rank() : 0;
+  const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
+  const int slice_rows = TN / CL;  // token rows this CTA loads for the whole cluster (a multiple of 8)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < GSTAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), CL);  // every CTA of the cluster hands the stage back
     }
     mbar_init(smem_u32(acc_bar), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), (uint32_t)g.tmem_cols);
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (threadIdx.x == 0) {  // producer: TMA tiles of A (tokens) and W (features)
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % GSTAGES, use = kb / GSTAGES;
-      if (use > 0 && !mbar_wait(smem_u32(&empty[s]), (use - 1) & 1)) {
-        *abort_flag = 1;
-        break;
+  // Warp 0 feeds the ring and warp 1 issues the MMAs; each whole warp runs its loop (every lane
+  // waits on the same barriers, lane 0 issues).
+  if (warp == 0) {  // producer: this CTA's weight tile and its share of the token tile (to the cluster)
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int i = kb - kb0, s = i % GSTAGES, use = i / GSTAGES;
+      int bad = 0;
+      if (lane == 0) {
+        if (use > 0 && !mbar_poll(smem_u32(&empty[s]), (use - 1) & 1)) {
+          *abort_flag = 1;
+          bad = 1;
+        } else {
+          mbar_arrive_expect_tx(smem_u32(&full[s]), (uint32_t)(w_stage + t_stage));
+          tma_load_2d(smem_u32(sw + s * w_stage), &tw, kb * GBK, f0, smem_u32(&full[s]));
+          const uint32_t tdst = smem_u32(st + s * t_stage + rank * slice_rows * GBK * 2);
+          if (CL > 1)
+            tma_load_2d_mc(tdst, &ta, kb * GBK, t0 + rank * slice_rows, smem_u32(&full[s]), cmask);
+          else
+            tma_load_2d(tdst, &ta, kb * GBK, t0, smem_u32(&full[s]));
+        }
       }
-      mbar_arrive_expect_tx(smem_u32(&full[s]), A_STAGE + B_STAGE);
-      tma_load_2d(smem_u32(sa + s * A_STAGE), &ta, kb * GBK, m0, smem_u32(&full[s]));
-      tma_load_2d(smem_u32(sw + s * B_STAGE), &tw, kb * GBK, n0, smem_u32(&full[s]));
+      if (__shfl_sync(0xffffffffu, bad, 0)) break;
     }
-  } else if (threadIdx.x == 32) {  // MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(GBM, GBN);
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % GSTAGES, use = kb / GSTAGES;
-      if (*abort_flag || !mbar_wait(smem_u32(&full[s]), use & 1)) {
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t ad = desc_sw128(smem_u32(sa + s * A_STAGE));
-      const uint64_t wd = desc_sw128(smem_u32(sw + s * B_STAGE));
+  } else if (warp == 1) {  // MMA issuer: D[128 features][TN tokens] += W · tokensᵀ
+    const uint32_t idesc = idesc_bf16_f32(FM, TN);
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int i = kb - kb0, s = i % GSTAGES, use = i / GSTAGES;
+      int bad = 0;
+      if (lane == 0) {
+        // no tcgen05 fence: the copies and the MMAs are both in the async proxy, and the
+        // barrier's completion already orders the stage's data before the MMAs that read it
+        if (*abort_flag || !mbar_poll(smem_u32(&full[s]), use & 1)) {
+          *abort_flag = 1;
+          bad = 1;
+        } else {
+          const uint64_t wd = desc_sw128(smem_u32(sw + s * w_stage));
+          const uint64_t td = desc_sw128(smem_u32(st + s * t_stage));
 #pragma unroll
-      for (int k = 0; k < GBK / 16; ++k)  // next 16 columns: 32 bytes further in the swizzled rows
-        umma_bf16(tmem, ad + 2 * k, wd + 2 * k, idesc, (kb | k) != 0);
-      umma_commit(smem_u32(&empty[s]));  // the stage is free once these have read it
+          for (int k = 0; k < GBK / 16; ++k)  // next 16 columns: 32 bytes further in the swizzled rows
+            umma_bf16(tmem, wd + 2 * k, td + 2 * k, idesc, (i | k) != 0);
+          if (CL > 1)
+            umma_commit_mc(smem_u32(&empty[s]), cmask);  // the stage is free in every CTA that shares it
+          else
+            umma_commit(smem_u32(&empty[s]));
+        }
+      }
+      if (__shfl_sync(0xffffffffu, bad, 0)) break;
     }
-    umma_commit(smem_u32(acc_bar));  // the accumulator is complete
+    if (lane == 0) umma_commit(smem_u32(acc_bar));  // the accumulator is complete
+    __syncwarp();
   }
 
-  // ---- epilogue: warp w holds rows m0 + 32w .. m0 + 32w + 31 (TMEM lanes 32w ..) ----
-  const bool ok = mbar_wait(smem_u32(acc_bar), 0);
-  __syncwarp();
+  // ---- epilogue: thread = one output feature (TMEM lane); 16 tokens per tcgen05.ld ----
+  // one thread watches the accumulator barrier; the CTA waits for it at a hardware barrier
+  if (threadIdx.x == 64 && !mbar_poll(smem_u32(acc_bar), 0)) *abort_flag = 1;
+  __syncthreads();
   tc_fence_after();
-  if (__any_sync(0xffffffffu, !ok || *abort_flag)) {  // warp-uniform: tcgen05.ld needs the whole warp
+  if (*abort_flag) {  // CTA-uniform after the barrier: tcgen05.ld needs whole warps
     if (threadIdx.x == 0) flag(g.status, SSM_STATUS_TIMEOUT);
   } else {
-    int seg = 0;
-    while (seg + 1 < g.n_seg && n0 >= g.seg_col[seg + 1]) ++seg;
-    const int seg_end = seg + 1 < g.n_seg ? g.seg_col[seg + 1] : g.N;
-    const int row = m0 + warp * 32 + lane;
-    const long long ld = g.seg_ld[seg];
-    const int c_base = n0 - g.seg_col[seg];  // column of this tile inside its segment
-    const int cols = min(GBN, seg_end - n0);
+    // (1) accumulator -> shared memory, [token][feature] fp32 (the stage ring is free now: the
+    //     last MMA has read it and every copy into it, a peer's multicast included, has landed)
+    float* tile = reinterpret_cast<float*>(smem);  // TN x FM fp32 <= 128 KB
+    const int fl = warp * 32 + lane;               // this thread's feature within the tile
 #pragma unroll 1
-    for (int c0 = 0; c0 < GBN; c0 += 16) {
+    for (int c0 = 0; c0 < TN; c0 += 16) {
       float v[16];
       __syncwarp();
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);  // warp-wide: every lane takes part
-      if (row >= g.M || c0 >= cols) continue;
-      const int nc = min(16, cols - c0);
-      if (g.residual) {
-        const float* rr = g.residual + (size_t)row * g.ldr + n0 + c0;
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);  // the whole warp takes part
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (i < nc) v[i] += rr[i];
-      }
-      if (g.seg_f32[seg]) {
-        float* d = static_cast<float*>(g.seg_ptr[seg]) + (size_t)row * ld + c_base + c0;
-        if (nc == 16) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) *reinterpret_cast<float4*>(d + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < nc) d[i] = v[i];
+      for (int i = 0; i < 16; ++i) tile[(c0 + i) * FM + fl] = v[i];  // lanes: consecutive words
+    }
+    __syncthreads();
+    // (2) token rows out: 32 threads per row, 4 features each; a thread keeps its group of 4
+    //     features (which lies in one segment) for every row, so the segment is resolved once
+    const bool accumulate = g.splits > 1;  // fp32 output holding the residual: add the partial sums
+    const int rows = min(TN, g.M - t0);
+    const int fg = 4 * (threadIdx.x & (FM / 4 - 1)), f = f0 + fg;
+    if (f < g.N) {
+      int seg = 0;
+      while (seg + 1 < g.n_seg && f >= g.seg_col[seg + 1]) ++seg;
+      const int seg_end = seg + 1 < g.n_seg ? g.seg_col[seg + 1] : g.N;
+      const int nc = min(4, seg_end - f);
+      const bool vec = nc == 4 && seg_end - g.seg_col[seg] >= 16;  // 16-byte row strides guaranteed
+      const long long ld = g.seg_ld[seg];
+      const bool f32 = g.seg_f32[seg] != 0;
+      unsigned char* base = static_cast<unsigned char*>(g.seg_ptr[seg]) +
+                            (size_t)(f - g.seg_col[seg]) * (f32 || accumulate ? 4 : 2);
+      const float* res = g.residual ? g.residual + f : nullptr;
+      const long long ldr = g.ldr;
+#pragma unroll 4
+      for (int tr = threadIdx.x / (FM / 4); tr < rows; tr += GTHREADS / (FM / 4)) {
+        const int t = t0 + tr;
+        float4 v = *reinterpret_cast<const float4*>(tile + tr * FM + fg);
+        if (accumulate) {
+          float* d = reinterpret_cast<float*>(base) + (size_t)t * ld;
+          if (vec) {
+            atomicAdd(reinterpret_cast<float4*>(d), v);
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < nc; ++i) atomicAdd(d + i, vv[i]);
+          }
+          continue;
         }
-      } else {
-        uint16_t* d = static_cast<uint16_t*>(g.seg_ptr[seg]) + (size_t)row * ld + c_base + c0;
-        if (nc == 16) {
-          uint4 p0, p1;
-          p0.x = pack_bf16(v[0], v[1]);
-          p0.y = pack_bf16(v[2], v[3]);
-          p0.z = pack_bf16(v[4], v[5]);
-          p0.w = pack_bf16(v[6], v[7]);
-          p1.x = pack_bf16(v[8], v[9]);
-          p1.y = pack_bf16(v[10], v[11]);
-          p1.z = pack_bf16(v[12], v[13]);
-          p1.w = pack_bf16(v[14], v[15]);
-          reinterpret_cast<uint4*>(d)[0] = p0;
-          reinterpret_cast<uint4*>(d)[1] = p1;
+        if (res) {
+          const float* rr = res + (size_t)t * ldr;
+          v.x += rr[0];
+          if (nc > 1) v.y += rr[1];
+          if (nc > 2) v.z += rr[2];
+          if (nc > 3) v.w += rr[3];
+        }
+        if (f32) {
+          float* d = reinterpret_cast<float*>(base) + (size_t)t * ld;
+          if (vec) {
+            *reinterpret_cast<float4*>(d) = v;
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < nc; ++i) d[i] = vv[i];
+          }
         } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < nc) d[i] = (uint16_t)(pack_bf16(v[i], 0.f) & 0xffffu);
+          uint16_t* d = reinterpret_cast<uint16_t*>(base) + (size_t)t * ld;
+          if (vec) {
+            *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < nc; ++i) d[i] = (uint16_t)(pack_bf16(vv[i], 0.f) & 0xffffu);
+          }
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still copy into it or arrive on its barriers
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc(tmem, (uint32_t)g.tmem_cols);
   }
 }
 
@@ -257,26 +368,103 @@ bool encode_bf16(CUtensorMap* m, const void* base, long long rows, long long col
 
 }  // namespace
 
-int gemm_tile_cols() { return GBN; }
+int gemm_tile_cols() { return SEG_ALIGN; }
 
-cudaError_t launch_gemm_bf16(const GemmArgs& g, const void* A, long long lda, const void* W, long long ldw,
-                             cudaStream_t s) {
+// Tile plan: 128 output features per CTA (the MMA's M), all tokens of a chunk of up to 256
+// (the MMA's N, rounded up to a multiple of 16 and of 8 rows per cluster CTA), clusters of up
+// to 4 CTAs sharing the token tiles, and K-splits (only when the output is an fp32
+// accumulator) so the grid fills the SMs with the least data per SM.
+void plan_gemm(GemmArgs& g, int sms, bool can_split) {
+  const int KB = (g.K + GBK - 1) / GBK;
+  const int tiles = (g.N + FM - 1) / FM;
+  g.cl = tiles >= 4 ? 4 : (tiles >= 2 ? 2 : 1);
+  const int chunk = g.M < MAX_TN ? g.M : MAX_TN;
+  const int q = 8 * g.cl > 16 ? 8 * g.cl : 16;
+  g.tn = (chunk + q - 1) / q * q;
+  const int tchunks = (g.M + MAX_TN - 1) / MAX_TN;
+  const int tiles_c = (tiles + g.cl - 1) / g.cl * g.cl;
+  double best = 1e300;
+  g.splits = 1;
+  g.kb_per_split = KB;
+  for (int sp = 1; sp <= (can_split ? 16 : 1); ++sp) {
+    const int kbp = (KB + sp - 1) / sp;
+    if ((sp - 1) * kbp >= KB) continue;  // every split gets at least one k-block
+    const long long ctas = (long long)tiles_c * sp * tchunks;
+    const long long waves = (ctas + sms - 1) / sms;
+    const double per_cta = (double)kbp * GBK * 2 * (FM + (double)g.tn / g.cl);
+    const double est = waves * per_cta * (1.0 + 0.02 * sp);  // small charge per split (reductions)
+    if (est < best * 0.999) {
+      best = est;
+      g.splits = sp;
+      g.kb_per_split = kbp;
+    }
+  }
+  if (const char* o = getenv("SSM_LINEAR_PLAN")) {  // tuning override: "cl,splits"
+    int cl = 0, sp = 0;
+    if (sscanf(o, "%d,%d", &cl, &sp) == 2 && (cl == 1 || cl == 2 || cl == 4) && cl <= tiles && sp >= 1 &&
+        (sp == 1 || can_split) && (sp - 1) * ((KB + sp - 1) / sp) < KB) {
+      g.cl = cl;
+      const int q2 = 8 * cl > 16 ? 8 * cl : 16;
+      g.tn = (chunk + q2 - 1) / q2 * q2;
+      g.splits = sp;
+      g.kb_per_split = (KB + sp - 1) / sp;
+    }
+  }
+  int cols = 32;
+  while (cols < g.tn) cols *= 2;
+  g.tmem_cols = cols;
+  const int stage_bytes = (FM + g.tn) * GBK * 2;
+  g.stages = (GEMM_SMEM - GEMM_RESERVED) / stage_bytes;
+  if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
+  // the epilogue stages the fp32 [token][feature] tile in the ring's memory
+  const int min_stages = (g.tn * FM * 4 + stage_bytes - 1) / stage_bytes;
+  if (const char* o = getenv("SSM_LINEAR_STAGES")) {  // tuning override
+    const int v = atoi(o);
+    if (v >= 2 && v >= min_stages && v < g.stages) g.stages = v;
+  }
+}
+
+cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const void* W, long long ldw, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
-  CUtensorMap ta, tw;
-  if (!encode_bf16(&ta, A, g.M, g.K, lda, GBM) || !encode_bf16(&tw, W, g.N, g.K, ldw, GBN))
-    return cudaErrorInvalidValue;
-  static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  static int configured[64] = {0};
+  static int sm_count[64] = {0};
   if (dev >= 64 || !configured[dev]) {
     e = cudaFuncSetAttribute(gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
     if (e != cudaSuccess) return e;
-    if (dev < 64) configured[dev] = 1;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) {
+      sm_count[dev] = sms;
+      configured[dev] = 1;
+    }
   }
-  const dim3 grid((unsigned)((g.M + GBM - 1) / GBM), (unsigned)((g.N + GBN - 1) / GBN));
-  gemm_bf16_kernel<<<grid, GTHREADS, GEMM_SMEM, s>>>(ta, tw, g);
-  return cudaGetLastError();
+  const int sms = dev < 64 ? sm_count[dev] : 148;
+  // K-splits add partial sums into the output: only for one fp32 segment that is its own residual
+  const bool can_split = g.n_seg == 1 && g.seg_f32[0] && g.residual == g.seg_ptr[0] && g.ldr == g.seg_ld[0];
+  plan_gemm(g, sms, can_split);
+  CUtensorMap ta, tw;
+  if (!encode_bf16(&ta, A, g.M, g.K, lda, g.tn / g.cl) || !encode_bf16(&tw, W, g.N, g.K, ldw, FM))
+    return cudaErrorInvalidValue;
+  const int tiles = (g.N + FM - 1) / FM;
+  const dim3 grid((unsigned)((tiles + g.cl - 1) / g.cl * g.cl), (unsigned)g.splits,
+                  (unsigned)((g.M + MAX_TN - 1) / MAX_TN));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(GTHREADS);
+  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)g.cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel, ta, tw, g);
 }
 
 }  // namespace ssmtree
