@@ -715,6 +715,72 @@ def run_block(args, dev, stream, world, rank, peak):
             "launches_per_round": L * 6 + 1, "projections": proj}
 
 
+def run_linear_only(args):
+    """The block's two projections alone at the Mamba2-2.7B shape (256 tree tokens: 16
+    sequences x 16 nodes): the input projection [256 x 2560] x [10576 x 2560]^T with its
+    z | x B C | dt segments, and the output projection [256 x 5120] x [2560 x 5120]^T added
+    into the fp32 residual stream.  Launches are captured in a CUDA graph (device time
+    only), the weights rotate over copies larger than L2.  torch.matmul (cuBLAS) on the
+    same product is timed beside it as context."""
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import ssm_linear
+    dev = torch.device("cuda")
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": None}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    T, d_model, d_inner, H = 256, 2560, 5120, 80
+    conv_dim = d_inner + 256
+    n_in = d_inner + conv_dim + H
+
+    def graph_us(fn, reps=20):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn(0, side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(reps):
+                fn(i, torch.cuda.current_stream(dev))
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    out = {}
+    A = (torch.randn(T, d_model, device=dev, generator=gen)).to(torch.bfloat16)
+    W = [(torch.randn(n_in, d_model, device=dev, generator=gen) * d_model ** -0.5).to(torch.bfloat16) for _ in range(4)]
+    z = torch.empty(T, d_inner, device=dev, dtype=torch.bfloat16)
+    xbc = torch.empty(T, conv_dim, device=dev, dtype=torch.bfloat16)
+    dt = torch.empty(T, H, device=dev, dtype=torch.bfloat16)
+    full = torch.empty(T, n_in, device=dev, dtype=torch.bfloat16)
+    us = graph_us(lambda i, s: ssm_linear(A, W[i % 4], [(0, z), (d_inner, xbc), (d_inner + conv_dim, dt)], stream=s))
+    ref = graph_us(lambda i, s: torch.matmul(A, W[i % 4].t(), out=full))
+    by, fl = n_in * d_model * 2 + T * d_model * 2 + T * n_in * 2, 2.0 * T * n_in * d_model
+    out["in"] = {"shape_MNK": [T, n_in, d_model], "us": us, "GB/s": by / us / 1e3, "TFLOP/s": fl / us / 1e6,
+                 "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "cublas_matmul_us": ref}
+    G = torch.randn(T, d_inner, device=dev, generator=gen).to(torch.bfloat16)
+    Wo = [(torch.randn(d_model, d_inner, device=dev, generator=gen) * d_inner ** -0.5).to(torch.bfloat16)
+          for _ in range(8)]
+    x = torch.randn(T, d_model, device=dev, generator=gen)
+    xo = torch.empty(T, d_model, device=dev, dtype=torch.bfloat16)
+    us = graph_us(lambda i, s: ssm_linear(G, Wo[i % 8], [(0, x)], residual=x, stream=s))
+    ref = graph_us(lambda i, s: torch.matmul(G, Wo[i % 8].t(), out=xo))
+    by, fl = d_model * d_inner * 2 + T * d_inner * 2 + T * d_model * 8, 2.0 * T * d_model * d_inner
+    out["out"] = {"shape_MNK": [T, d_model, d_inner], "us": us, "GB/s": by / us / 1e3, "TFLOP/s": fl / us / 1e6,
+                  "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "cublas_matmul_us": ref}
+    print(json.dumps({"metric": "projection time (Mamba2-2.7B block, 256 tokens)", "unit": "us",
+                      "higher_is_better": False, "data": "synthetic", "projections": out}), flush=True)
+    return 0
+
+
 def draft_step_bytes(H, P, N, n_inst, n_layers):
     """Algorithmic bytes of one ssm_draft_step call: state read + write, the conv window
     (3 ring rows) and the new row, dt, the ring write, the log row, y; params once per layer."""
@@ -988,6 +1054,8 @@ def main():
     ap.add_argument("--no-draft", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--no-block", action="store_true")
+    ap.add_argument("--only", choices=["linear"], default=None,
+                    help="run one measurement alone: 'linear' = the block's projections")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -995,6 +1063,8 @@ def main():
     w = workload(args.workload)
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.only == "linear":
+        return run_linear_only(args)
     return run_ours(args, w)
 
 
