@@ -226,6 +226,34 @@ int ssm_commit_verify(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq
                       size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * ssm_commit_verify_prep / ssm_commit_verify_main -- the two halves of
+ * ssm_commit_verify, same arguments.  Issued back to back on one stream they are
+ * exactly ssm_commit_verify.  They exist so that the SSM can start as soon as Δ, B
+ * and C exist: the LightMamba page ("计算重排序与细粒度分块融合") reorders the input
+ * projection to produce Δ, B, C first and starts the SSM while X and Z are still
+ * being produced.
+ *   _prep reads, of this step's tree, only the B | C channels of xBC and dt (plus
+ *         the previous path's rows, the ring, the layouts and the parameters); it
+ *         writes the workspace, the committed ring rows' B | C channels and ring_head.
+ *   _main reads the x channels of xBC, h and what _prep wrote; it must run after
+ *         _prep on the same workspace (same stream, or ordered by the caller) and
+ *         after the x channels are in place.  It writes h, the ring's x channels and y.
+ * Both validate every argument as ssm_commit_verify does.
+ */
+int ssm_commit_verify_prep(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t prev_n_nodes,
+                           const ssm_node *prev_layout, int32_t prev_max_path, const int32_t *prev_path,
+                           const int32_t *prev_path_len, const uint16_t *prev_xBC, const uint16_t *prev_dt,
+                           int32_t n_nodes, int32_t max_depth, const ssm_node *layout, const uint16_t *xBC,
+                           const uint16_t *dt, float *h, uint16_t *ring, int32_t *ring_head, float *y,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+int ssm_commit_verify_main(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t prev_n_nodes,
+                           const ssm_node *prev_layout, int32_t prev_max_path, const int32_t *prev_path,
+                           const int32_t *prev_path_len, const uint16_t *prev_xBC, const uint16_t *prev_dt,
+                           int32_t n_nodes, int32_t max_depth, const ssm_node *layout, const uint16_t *xBC,
+                           const uint16_t *dt, float *h, uint16_t *ring, int32_t *ring_head, float *y,
+                           void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
  * ssm_draft_step -- one draft token per instance (a one-node tree), SpecMamba
  * page §3.1 (the draft logs only Δ, A, B, X).  Position = ring_head + step:
  * the token's pre-conv row is written to that ring position, the conv window

@@ -90,6 +90,10 @@ _SIGS = {
     "ssm_commit_verify_workspace_size": (ctypes.c_size_t, [_P, _I, _I, _I, _I]),
     "ssm_commit_verify": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P,
                                          _P, ctypes.c_size_t, _P, _P]),
+    "ssm_commit_verify_prep": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, ctypes.c_size_t, _P, _P]),
+    "ssm_commit_verify_main": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, ctypes.c_size_t, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_replay": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
@@ -265,13 +269,16 @@ def ssm_commit_verify_workspace_size(dims: Dims, n_seq: int, n_nodes: int, max_d
 
 def ssm_commit_verify(dims: Dims, params: dict, n_seq: int, prev_n_nodes: int, prev_layout, prev_max_path: int,
                       prev_path, prev_path_len, prev_xBC, prev_dt, n_nodes: int, max_depth: int, layout, xBC, dt, h,
-                      ring, ring_head, y, workspace, status=None, stream=None):
+                      ring, ring_head, y, workspace, status=None, stream=None, part: str = "all"):
     """ssm_commit of the previous tree's accepted path, then ssm_tree_verify of the
-    next tree from the committed state, with one read and one write of h."""
+    next tree from the committed state, with one read and one write of h.
+    part="prep" / "main" issues only one half (ssm_commit_verify_prep / _main): the
+    prep needs only the tree's B|C channels and dt, the main the x channels too."""
     d, I, n, pn = dims, n_seq * dims.n_layers, n_nodes, prev_n_nodes
     cd = d.c()
     cp = _params(params, d, d.n_layers)
-    _check(lib().ssm_commit_verify(
+    entry = {"all": "ssm_commit_verify", "prep": "ssm_commit_verify_prep", "main": "ssm_commit_verify_main"}[part]
+    _check(getattr(lib(), entry)(
         ctypes.byref(cd), ctypes.byref(cp), n_seq, pn,
         _dev(prev_layout, "prev_layout", torch.int32, n_seq * pn * NODE_WORDS), prev_max_path,
         _dev(prev_path, "prev_path", torch.int32, n_seq * prev_max_path),

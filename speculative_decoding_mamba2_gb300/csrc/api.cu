@@ -138,7 +138,7 @@ extern "C" int ssm_tree_verify(const ssm_dims* dims, const ssm_params* prm, int3
   a.y = y;
   a.status = dev_status;
   return finish(fn, chain ? launch_chain_verify(a, workspace, (cudaStream_t)stream)
-                         : launch_verify(a, workspace, (cudaStream_t)stream));
+                         : launch_verify(a, workspace, (cudaStream_t)stream, 0));
 }
 
 namespace {
@@ -170,13 +170,14 @@ extern "C" size_t ssm_commit_verify_workspace_size(const ssm_dims* dims, int32_t
   return b ? b : 16;
 }
 
-extern "C" int ssm_commit_verify(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t prev_n_nodes,
-                                 const ssm_node* prev_layout, int32_t prev_max_path, const int32_t* prev_path,
-                                 const int32_t* prev_path_len, const uint16_t* prev_xBC, const uint16_t* prev_dt,
-                                 int32_t n_nodes, int32_t max_depth, const ssm_node* layout, const uint16_t* xBC,
-                                 const uint16_t* dt, float* h, uint16_t* ring, int32_t* ring_head, float* y,
-                                 void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
-  const char* fn = "ssm_commit_verify";
+namespace {
+// which: 0 = the whole folded call, 1 = its prep kernel only, 2 = its main kernel only
+int commit_verify_call(const char* fn, int which, const ssm_dims* dims, const ssm_params* prm, int32_t n_seq,
+                       int32_t prev_n_nodes, const ssm_node* prev_layout, int32_t prev_max_path,
+                       const int32_t* prev_path, const int32_t* prev_path_len, const uint16_t* prev_xBC,
+                       const uint16_t* prev_dt, int32_t n_nodes, int32_t max_depth, const ssm_node* layout,
+                       const uint16_t* xBC, const uint16_t* dt, float* h, uint16_t* ring, int32_t* ring_head, float* y,
+                       void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (int rc = check_commit_verify_shape(fn, dims, n_seq, prev_n_nodes, prev_max_path, n_nodes, max_depth)) return rc;
   if (int rc = check_dims(fn, dims, true, prm)) return rc;
   if (n_seq == 0) return finish(fn, cudaSuccess);
@@ -220,7 +221,28 @@ extern "C" int ssm_commit_verify(const ssm_dims* dims, const ssm_params* prm, in
   a.h_w = h;
   a.ring_w = ring;
   a.head_w = ring_head;
-  return finish(fn, launch_verify(a, workspace, (cudaStream_t)stream));
+  return finish(fn, launch_verify(a, workspace, (cudaStream_t)stream, which));
+}
+}  // namespace
+
+#define SSM_COMMIT_VERIFY_ARGS                                                                                      \
+  const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t prev_n_nodes, const ssm_node *prev_layout,   \
+      int32_t prev_max_path, const int32_t *prev_path, const int32_t *prev_path_len, const uint16_t *prev_xBC,     \
+      const uint16_t *prev_dt, int32_t n_nodes, int32_t max_depth, const ssm_node *layout, const uint16_t *xBC,     \
+      const uint16_t *dt, float *h, uint16_t *ring, int32_t *ring_head, float *y, void *workspace,                 \
+      size_t workspace_bytes, int32_t *dev_status, void *stream
+#define SSM_COMMIT_VERIFY_PASS                                                                                      \
+  dims, prm, n_seq, prev_n_nodes, prev_layout, prev_max_path, prev_path, prev_path_len, prev_xBC, prev_dt, n_nodes, \
+      max_depth, layout, xBC, dt, h, ring, ring_head, y, workspace, workspace_bytes, dev_status, stream
+
+extern "C" int ssm_commit_verify(SSM_COMMIT_VERIFY_ARGS) {
+  return commit_verify_call("ssm_commit_verify", 0, SSM_COMMIT_VERIFY_PASS);
+}
+extern "C" int ssm_commit_verify_prep(SSM_COMMIT_VERIFY_ARGS) {
+  return commit_verify_call("ssm_commit_verify_prep", 1, SSM_COMMIT_VERIFY_PASS);
+}
+extern "C" int ssm_commit_verify_main(SSM_COMMIT_VERIFY_ARGS) {
+  return commit_verify_call("ssm_commit_verify_main", 2, SSM_COMMIT_VERIFY_PASS);
 }
 
 extern "C" int ssm_accept_path(int32_t n_seq, int32_t n_nodes, int32_t max_path, const ssm_node* layout,

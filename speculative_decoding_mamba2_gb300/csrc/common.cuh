@@ -282,7 +282,8 @@ struct VerifyArgs {
   uint16_t* ring_w;
   int32_t* head_w;
 };
-cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s);
+// which: 0 = prep + main, 1 = prep only, 2 = main only (after a prep on the same workspace)
+cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, int which);
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
 int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
@@ -297,7 +298,7 @@ struct GemmArgs {
   const float* residual;  // nullptr or fp32 [M][ldr], added to the accumulator
   long long ldr;
   int32_t* status;
-  int tn, cl, splits, kb_per_split, tmem_cols, stages;  // tile plan, set by launch_gemm_bf16
+  int tn, tchunk, cl, splits, kb_per_split, tmem_cols, stages;  // tile plan, set by launch_gemm_bf16
 };
 int gemm_tile_cols();
 cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const void* W, long long ldw, cudaStream_t s);

@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int f0 = blockIdx.x * FM, t0 = blockIdx.z * MAX_TN;
+  const int f0 = blockIdx.x * FM, t0 = blockIdx.z * g.tchunk;
   const int KB = (g.K + GBK - 1) / GBK;
   const int kb0 = blockIdx.y * g.kb_per_split, kb1 = min(KB, kb0 + g.kb_per_split);
   const int rank = CL > 1 ? (int)cluster_rank() : 0;
@@ -378,11 +378,17 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
   const int KB = (g.K + GBK - 1) / GBK;
   const int tiles = (g.N + FM - 1) / FM;
   g.cl = tiles >= 4 ? 4 : (tiles >= 2 ? 2 : 1);
-  const int chunk = g.M < MAX_TN ? g.M : MAX_TN;
+  const int tiles_c = (tiles + g.cl - 1) / g.cl * g.cl;
+  // few feature tiles (a narrow projection) and no K-splits (a bf16 output): cut the tokens into
+  // smaller chunks so more CTAs, each with a deeper ring of smaller stages, share the work
+  g.tchunk = MAX_TN;
+  while (!can_split && g.tchunk > 64 && g.M > g.tchunk / 2 &&
+         (long long)tiles_c * ((g.M + g.tchunk / 2 - 1) / (g.tchunk / 2)) <= sms / 2)
+    g.tchunk /= 2;
+  const int chunk = g.M < g.tchunk ? g.M : g.tchunk;
   const int q = 8 * g.cl > 16 ? 8 * g.cl : 16;
   g.tn = (chunk + q - 1) / q * q;
-  const int tchunks = (g.M + MAX_TN - 1) / MAX_TN;
-  const int tiles_c = (tiles + g.cl - 1) / g.cl * g.cl;
+  const int tchunks = (g.M + g.tchunk - 1) / g.tchunk;
   double best = 1e300;
   g.splits = 1;
   g.kb_per_split = KB;
@@ -451,7 +457,7 @@ cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const voi
     return cudaErrorInvalidValue;
   const int tiles = (g.N + FM - 1) / FM;
   const dim3 grid((unsigned)((tiles + g.cl - 1) / g.cl * g.cl), (unsigned)g.splits,
-                  (unsigned)((g.M + MAX_TN - 1) / MAX_TN));
+                  (unsigned)((g.M + g.tchunk - 1) / g.tchunk));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(GTHREADS);

@@ -1050,7 +1050,7 @@ int verify_prep_smem_bytes(int n, int max_depth, int H, int LP) {
   return prep_layout(n, H, W.PP, LP).total;
 }
 
-cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s) {
+cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, int which) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1062,9 +1062,11 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s) 
   e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);
   if (e != cudaSuccess) return e;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  tree_prep_kernel<<<(unsigned)inst, THREADS, prep_bytes, s>>>(a, ws);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (which != 2) {
+    tree_prep_kernel<<<(unsigned)inst, THREADS, prep_bytes, s>>>(a, ws);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || which == 1) return e;
+  }
   if (a.LP > 0) return G == 4 ? launch_main<4, true>(a, ws, s, dev) : launch_main<2, true>(a, ws, s, dev);
   return G == 4 ? launch_main<4, false>(a, ws, s, dev) : launch_main<2, false>(a, ws, s, dev);
 }

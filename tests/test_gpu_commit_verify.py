@@ -254,3 +254,51 @@ def test_ring_positions_wrap_around():
     assert out["status"] == 0 and out["sep_status"] == 0
     check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
     check_separate(out)
+
+
+def test_split_prep_then_main_is_the_folded_call():
+    """ssm_commit_verify_prep, then ssm_commit_verify_main on the same workspace, equals the
+    one folded call bit for bit -- also when the x channels of the new tree's rows only
+    arrive between the two (the prep reads B | C and dt only)."""
+    from speculative_decoding_mamba2_gb300 import (ssm_accept_path, ssm_commit_verify, ssm_commit_verify_workspace_size,
+                                                   ssm_tree_layout_build)
+    w0 = Workload(91, "split", Shape(H=6), n_layers=2, batch=3, trees=(("random", 16, 3, 4),), p_accept=0.9)
+    b0, b1 = batch(w0), batch(Workload(92, "split next", Shape(H=6), n_layers=2, batch=3,
+                                       trees=(("random", 16, 3, 4),)))
+    d0 = upload_tree_batch(b0, w0)
+    dims, S, n0 = d0["dims"], d0["n_seq"], d0["n"]
+    I = S * dims.n_layers
+    mp = d0["depth"] + 1
+    path = torch.empty((S, mp), dtype=torch.int32, device="cuda")
+    plen = torch.empty(S, dtype=torch.int32, device="cuda")
+    bonus = torch.empty(S, dtype=torch.int32, device="cuda")
+    ssm_accept_path(S, n0, mp, d0["layout"], d0["tok"], d0["tgt"], path, plen, bonus)
+    n1 = b1["n_nodes"]
+    lay1_h, depth1 = ssm_tree_layout_build(b1["parent"])
+    lay1 = dev(lay1_h)
+    xBC1 = bf16_dev(b1["xBC"]).view(I, n1, dims.conv_dim)
+    dt1 = bf16_dev(b1["dt"]).view(I, n1, dims.n_heads)
+    outs = []
+    for mode in ("all", "split", "late x"):
+        h, ring, head = d0["h0"].clone(), d0["ring"].clone(), d0["ring_head"].clone()
+        y = torch.full((I, n1, dims.d_inner), float("nan"), device="cuda")
+        ws = torch.empty(ssm_commit_verify_workspace_size(dims, S, n1, depth1, mp), dtype=torch.uint8, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        args = (dims, d0["params"], S, n0, d0["layout"], mp, path, plen, d0["xBC"], d0["dt"], n1, depth1, lay1)
+        x_in = xBC1.clone()
+        if mode == "late x":
+            x_in[..., :dims.d_inner] = float("nan")  # the x channels land after the prep
+        if mode == "all":
+            ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status)
+        else:
+            ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status, part="prep")
+            if mode == "late x":
+                x_in[..., :dims.d_inner] = xBC1[..., :dims.d_inner]
+            ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status, part="main")
+        torch.cuda.synchronize()
+        assert int(status) == 0
+        outs.append((y.cpu(), h.cpu(), ring.cpu(), head.cpu()))
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
+                               b.view(torch.int32) if b.dtype == torch.float32 else b)
