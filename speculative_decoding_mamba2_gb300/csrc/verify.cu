@@ -1056,8 +1056,21 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
   if (e != cudaSuccess) return e;
   const long long inst = (long long)a.n_seq * a.L;
   if (inst == 0) return cudaSuccess;
-  const int G = verify_heads_per_group(a.n, a.max_depth, a.H, a.LP);
+  int G = verify_heads_per_group(a.n, a.max_depth, a.H, a.LP);
   if (G == 0) return cudaErrorInvalidValue;
+  if (G == 4) {  // few instances: groups of 2 heads when they fill the SMs' two CTA slots in fewer rounds
+    int sms = dev < 64 ? g_sms[dev] : 0;
+    if (sms == 0) {
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) g_sms[dev] = sms;
+    }
+    const long long slots = 2LL * sms, c4 = inst * ((a.H + 3) / 4), c2 = inst * ((a.H + 1) / 2);
+    const Ws W2 = ws_layout(a.n, a.max_depth, a.H, a.LP);
+    const bool fits2 = a.LP > 0 ? smem_layout<2, true>(a.n, W2.PP, W2.NP, a.LP).total <= SMEM_LIMIT
+                                : smem_layout<2, false>(a.n, W2.PP, W2.NP, 0).total <= SMEM_LIMIT;
+    if (fits2 && c4 < 4 * slots && ((c2 + slots - 1) / slots) * 2 < ((c4 + slots - 1) / slots) * 4) G = 2;
+  }
   const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H, a.LP);
   e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);
   if (e != cudaSuccess) return e;
