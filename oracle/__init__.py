@@ -14,6 +14,8 @@ from .ssm_oracle import (  # noqa: F401
     commit,
     draft_step,
     replay,
+    draft_tree_level,
+    draft_tree_commit,
 )
 from .block_oracle import (  # noqa: F401
     to_bf16,

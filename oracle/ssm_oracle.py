@@ -33,7 +33,9 @@ shared by all heads (ngroups = 1); node 0 is the last committed token and is
 processed with h_parent(root) = h0 and the conv ring holding the positions
 before it; softplus is exact log1p(exp(v)); the greedy accept walk takes, at
 each node, the first child in breadth-first order whose draft token equals the
-target's token after that node.
+target's token after that node; a draft tree is processed one depth level at a
+time, each node from its branch state, which is the committed state followed by
+its ancestors' logged (Δ, B, x) updates.
 
 Every function here has a pin in ``tests/test_oracle_pins.py`` that checks it
 against something other than itself (a library routine, a closed form, an
@@ -267,3 +269,63 @@ def replay(A_log, log_rows, k, h_ckpt, head):
         delta, B, x = log_rows[t]
         h = ssm_step(h, np.asarray(delta), A, np.asarray(x).reshape(H, P), np.asarray(B))
     return h, head + int(k)
+
+
+# ---------------------------------------------------------------------------
+# draft-side tree drafting: branch states recovered from the light log
+# ---------------------------------------------------------------------------
+def draft_tree_level(params, parent, level, xBC, dt, h_ckpt, ring, head, log):
+    """Process the nodes of depth `level` of a draft tree (the tree the target verifies next).
+
+    The draft keeps one committed state h_ckpt and, for each node it has processed, only the
+    light log row (Δ [H], B [N], x [H*P]), post-conv (SpecMamba page §3.1: the small
+    intermediates recover the state).  A node's branch state is h_ckpt followed by the logged
+    updates of its ancestors, root first, then the node's own update; it is never stored.
+    xBC [n][conv_dim] holds the pre-conv rows of every node of depth <= level (a node's conv
+    window runs over its ancestors, then the conv ring, as in verify); dt [n][H] raw.
+    log: dict node -> (Δ, B, x) for every node of depth < level.
+    Returns (ys, rows): dicts node -> y [H*P] and node -> (Δ, B, x) for the level's nodes.
+    """
+    H, P, N = h_ckpt.shape
+    lay = tree_layout(parent)
+    A = -np.exp(np.asarray(params["A_log"], np.float64))
+    ys, rows = {}, {}
+    for v in range(lay["n"]):
+        if lay["depth"][v] != level:
+            continue
+        post = conv_silu(node_window(lay, v, xBC, ring, head), params["conv_w"], params["conv_b"])
+        x, B, C = split_xbc(post, H, P, N)
+        delta = softplus(dt[v] + params["dt_bias"])
+        h = np.array(h_ckpt, np.float64)
+        for m in lay["path"][v][:-1]:  # the ancestors' logged updates, root first
+            dm, Bm, xm = log[m]
+            h = ssm_step(h, np.asarray(dm), A, np.asarray(xm).reshape(H, P), np.asarray(Bm))
+        h = ssm_step(h, delta, A, x, B)
+        ys[v] = ssm_out(h, C, params["D"], x).reshape(H * P)
+        rows[v] = (delta, B, x.reshape(H * P))
+    return ys, rows
+
+
+def draft_tree_commit(A_log, parent, path, log, xBC, h_ckpt, ring, head):
+    """Move the draft's committed state along the path the target accepted (root..last,
+    node indices): h <- the path's logged updates applied in order (no conv, no input
+    re-read); the path's pre-conv rows go to ring positions head .. head+len-1 and the head
+    advances by len.  Returns (h, ring_new, head_new)."""
+    lay = tree_layout(parent)
+    path = [int(v) for v in path]
+    if not path or path[0] != 0:
+        raise ValueError("path must start at the root")
+    for a, b in zip(path, path[1:]):
+        if lay["parent"][b] != a:
+            raise ValueError("path is not a root-to-node chain")
+    H, P, N = h_ckpt.shape
+    A = -np.exp(np.asarray(A_log, np.float64))
+    h = np.array(h_ckpt, np.float64)
+    for m in path:
+        dm, Bm, xm = log[m]
+        h = ssm_step(h, np.asarray(dm), A, np.asarray(xm).reshape(H, P), np.asarray(Bm))
+    ring_new = np.array(ring, copy=True)
+    R = ring.shape[0]
+    for j, m in enumerate(path):
+        ring_new[(head + j) % R] = xBC[m]
+    return h, ring_new, head + len(path)
