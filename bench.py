@@ -476,6 +476,11 @@ def run_ours(args, w):
         del y, ws_f, xBC, dt
         draft = run_draft(args, dev, stream, peak, world, rank)
 
+    # ---- draft-side tree drafting (branch states from the log) ----
+    draft_tree = None
+    if not args.no_draft:
+        draft_tree = run_draft_tree(args, dev, stream, peak, world, rank)
+
     # ---- the stress workload's chain tree (chain kernel) ----
     chain = None
     if not args.no_chain:
@@ -499,6 +504,8 @@ def run_ours(args, w):
                 "e2e": e2e, "gpu_launches": 3 * args.steps, "clocks": clk}
         if draft is not None:
             line["draft"] = draft
+        if draft_tree is not None:
+            line["draft_tree"] = draft_tree
         if chain is not None:
             line["chain"] = chain
         if block is not None:
@@ -896,6 +903,169 @@ def run_draft(args, dev, stream, peak, world, rank):
             "replay": {"bytes": rb, "GB/s": rb / replay_ms / 1e6, "frac_of_hbm_peak": rb / replay_ms / 1e6 / peak},
             "note": f"the draft state ({state_mb:.0f} MB) fits in L2, so draft steps run from L2; "
                     "a fraction above 1 of the HBM peak is possible and expected"}
+
+
+def draft_tree_level_bytes(H, P, N, n_inst, n_layers, frontier, ancestors):
+    """Algorithmic bytes of one ssm_draft_tree_level call: the committed state read once;
+    per frontier node its pre-conv row, three tap rows and dt, its log row and y written;
+    the log rows (Δ, B, x) of the distinct ancestors on the frontier's paths read; params
+    once per layer."""
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    log_row = (H + N + d_inner) * 4
+    per = (H * P * N * 4 + frontier * (4 * conv_dim * 2 + H * 2 + log_row + d_inner * 4) + ancestors * log_row)
+    return n_inst * per + n_layers * params_bytes_per_layer(H, P, N)
+
+
+def draft_tree_commit_bytes(H, P, N, n_inst, path_len):
+    """State read + write, the path's log rows, its last three pre-conv rows into the ring."""
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    rows = min(3, path_len)
+    return n_inst * (2 * H * P * N * 4 + path_len * (H + N + d_inner) * 4 + rows * conv_dim * 2 * 2 + 8)
+
+
+def run_draft_tree(args, dev, stream, peak, world, rank):
+    """Draft-side tree drafting on the Mamba2-370M draft shape (48 layers, batch 1 per rank):
+    the 16-node random tree (3 branches, depth 4) drafted one depth level per
+    ssm_draft_tree_level call, every branch from the one committed state and the log, then
+    ssm_draft_tree_commit of the accepted path; and a 16-node chain the same way (one level
+    per token: the state is read, never written, until the commit).  The draft state
+    (50 MB) fits in L2, but between two levels the draft model's other layers run, so each
+    level is timed after a write of 256 MB (L2 flushed): "cold" is the figure against the
+    HBM roofline; "warm" (levels back to back) is given beside it."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_draft_tree_commit,
+                                                   ssm_draft_tree_level, ssm_tree_layout_build)
+    from synth import Workload, batch, workload
+    out = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    w5 = workload(5)
+    chain = Workload(w5.index, "draft chain drafted level by level, Mamba2-370M shape, 48 layers, batch 1, "
+                     "16 tokens", w5.shape, n_layers=w5.n_layers, batch=w5.batch, trees=(("chain", 16),))
+    for key, w in (("tree", w5), ("chain", chain)):
+        seqs = shard_sequences(w.batch, rank)
+        b = batch(w, seqs=seqs)
+        S, L, n = len(seqs), w.n_layers, b["n_nodes"]
+        H, P, N = w.shape.H, w.shape.P, w.shape.N
+        I = S * L
+        dims = Dims(n_heads=H, n_layers=L, ring_cap=w.ring_cap)
+        layout_h, depth = ssm_tree_layout_build(b["parent"])
+        layout = torch.from_numpy(layout_h).to(dev)
+        prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in b["params"].items()}
+        bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+        xBC = bf16(b["xBC"]).view(I, n, dims.conv_dim)
+        dt = bf16(b["dt"]).view(I, n, H)
+        h0 = torch.from_numpy(b["h0"]).to(dev).view(I, H, P, N)
+        h = h0.clone()
+        ring0 = bf16(b["ring"]).view(I, w.ring_cap, dims.conv_dim)
+        ring = ring0.clone()
+        head0 = torch.from_numpy(b["ring_head"]).to(dev).view(I)
+        head = head0.clone()
+        log_d = torch.zeros(I, n, H, device=dev)
+        log_b = torch.zeros(I, n, N, device=dev)
+        log_x = torch.zeros(I, n, dims.d_inner, device=dev)
+        y = torch.empty(I, n, dims.d_inner, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        max_path = depth + 1
+        path = torch.empty(S, max_path, dtype=torch.int32, device=dev)
+        plen = torch.empty(S, dtype=torch.int32, device=dev)
+        bonus = torch.empty(S, dtype=torch.int32, device=dev)
+        if key == "tree":
+            ssm_accept_path(S, n, max_path, layout, torch.from_numpy(b["tok"]).to(dev),
+                            torch.from_numpy(b["tgt"]).to(dev), path, plen, bonus, status)
+        else:  # the whole chain is accepted
+            path.copy_(torch.arange(n, dtype=torch.int32, device=dev).expand(S, n))
+            plen.fill_(n)
+        levels = list(range(depth + 1))
+
+        def round_(ev=None, cold=True):
+            h.copy_(h0)
+            ring.copy_(ring0)
+            head.copy_(head0)
+            for i, lv in enumerate(levels):
+                if cold:
+                    flush.fill_(i & 1)
+                if ev is not None:
+                    ev[2 * i].record(stream)
+                ssm_draft_tree_level(dims, prm, S, n, lv, layout, xBC, dt, h, ring, head, log_d, log_b, log_x, y,
+                                     status)
+                if ev is not None:
+                    ev[2 * i + 1].record(stream)
+            if cold:
+                flush.fill_(7)
+            if ev is not None:
+                ev[-2].record(stream)
+            ssm_draft_tree_commit(dims, prm, S, n, layout, max_path, path, plen, log_d, log_b, log_x, xBC, h, ring,
+                                  head, status)
+            if ev is not None:
+                ev[-1].record(stream)
+
+        for _ in range(args.warmup):
+            round_()
+        torch.cuda.synchronize()
+        rounds = max(5, min(args.steps, 30))
+        res = {}
+        for mode in ("cold", "warm"):
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(levels) + 2)] for _ in range(rounds)]
+            for r in range(rounds):
+                round_(evs[r], cold=(mode == "cold"))
+            torch.cuda.synchronize()
+            lv_ms = [statistics.mean(e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs) for i in range(len(levels))]
+            cm_ms = statistics.mean(e[-2].elapsed_time(e[-1]) for e in evs)
+            lv_ms = [max_over_ranks(t, world, dev) for t in lv_ms]
+            cm_ms = max_over_ranks(cm_ms, world, dev)
+            res[mode] = (lv_ms, cm_ms)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} in the draft-tree rounds")
+        lay = [oracle_free_depths(b["parent"][i]) for i in range(S)]
+        plens = plen.cpu().numpy()
+        entry = {"workload": w.name, "sequences_per_gpu": S, "layers": L, "nodes": n, "levels": len(levels),
+                 "mean_accepted_path": float(plens.mean())}
+        for mode, (lv_ms, cm_ms) in res.items():
+            per_level = []
+            tot_b = 0
+            for i, lv in enumerate(levels):
+                fr = int(np.mean([sum(1 for d in dep if d == lv) for dep in lay]))
+                anc = int(np.mean([len(ancestors_at(b["parent"][q], dep, lv)) for q, dep in enumerate(lay)]))
+                lb = draft_tree_level_bytes(H, P, N, I, L, fr, anc)
+                tot_b += lb
+                per_level.append({"level": lv, "nodes": fr, "ms": lv_ms[i], "GB/s": lb / lv_ms[i] / 1e6,
+                                  "frac_of_hbm_peak": lb / lv_ms[i] / 1e6 / peak})
+            cb = draft_tree_commit_bytes(H, P, N, I, int(round(float(plens.mean()))))
+            tree_ms = sum(lv_ms) + cm_ms
+            entry[mode] = {"ms_per_tree": tree_ms, "ms_levels": sum(lv_ms), "ms_commit": cm_ms,
+                           "levels": per_level,
+                           "level_GB/s": tot_b / sum(lv_ms) / 1e6,
+                           "level_frac_of_hbm_peak": tot_b / sum(lv_ms) / 1e6 / peak,
+                           "commit": {"bytes": cb, "GB/s": cb / cm_ms / 1e6, "frac_of_hbm_peak": cb / cm_ms / 1e6 / peak},
+                           "value": S * L * n * world / (tree_ms / 1e3)}
+        entry["unit"] = "drafted node-layer updates/s (value)"
+        out[key] = entry
+        del xBC, dt, h0, h, ring0, ring, log_d, log_b, log_x, y
+    out["note"] = ("cold: a 256 MB write before every level and before the commit, so the state comes from HBM; "
+                   "warm: levels back to back with the 50 MB state in L2")
+    return out
+
+
+def oracle_free_depths(parent):
+    """Depth of every node of a breadth-first parent[] (host bookkeeping for the byte counts)."""
+    dep = [0] * len(parent)
+    for v in range(1, len(parent)):
+        dep[v] = dep[int(parent[v])] + 1
+    return dep
+
+
+def ancestors_at(parent, dep, level):
+    """Distinct proper ancestors of the nodes of depth `level`."""
+    out = set()
+    for v in range(len(parent)):
+        if dep[v] == level:
+            u = int(parent[v])
+            while u >= 0:
+                out.add(u)
+                u = int(parent[u])
+    return out
 
 
 def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):

@@ -288,6 +288,60 @@ int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
                int32_t *ring_head, int32_t *dev_status, void *stream);
 
 /*
+ * ssm_draft_tree_level -- draft-side tree drafting, one depth level per call.
+ * SpecMamba page §3.1 (the draft keeps only the light intermediates Δ, A, B, X
+ * and recovers states from them) and §3.2 (a node's children continue from the
+ * node's state).  A draft tree grows one depth at a time: the tokens of depth
+ * level+1 come from the outputs of depth `level`.  For every node v of depth
+ * `level` (in every instance): its pre-conv row goes through the tree conv
+ * (taps over its ancestors, then the conv ring) and SiLU, Δ = softplus(dt +
+ * dt_bias), and
+ *     y_v = C_v·h_v + D·x_v,  h_v = h_ckpt followed by the logged updates of
+ *     v's ancestors (root first) and then v's own update.
+ * h_v is never formed: the call reads h_ckpt once and the ancestors' log rows,
+ * and writes v's log row {Δ [H], B [N], x [d_inner]} (fp32, post-conv) and y_v.
+ * No state is written, so every branch shares the one committed state.
+ *   n_nodes    1..SSM_MAX_NODES;  level 0..SSM_MAX_DEPTH (a level with no
+ *              node is a no-op)
+ *   layout     device ssm_node [S][n] (ssm_tree_layout_build of the draft tree)
+ *   xBC, dt    device bf16 [I][n][conv_dim], [I][n][H]: rows of the nodes of
+ *              depth <= level must be written (read only)
+ *   h_ckpt     device fp32 [I][H][P][N], 16-byte aligned (read only)
+ *   ring, ring_head  as for ssm_tree_verify (read only)
+ *   log_delta  device fp32 [I][n][H]; log_B [I][n][N] (16-byte aligned);
+ *   log_x      [I][n][d_inner]: rows of depth < level are read (the earlier
+ *              levels' calls wrote them), rows of depth == level are written
+ *   y          device fp32 [I][n][d_inner]: rows of depth == level written
+ * A layout record that points outside its tree sets SSM_STATUS_BAD_LAYOUT and
+ * the instance writes nothing.
+ */
+int ssm_draft_tree_level(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
+                         int32_t level, const ssm_node *layout, const uint16_t *xBC, const uint16_t *dt,
+                         const float *h_ckpt, const uint16_t *ring, const int32_t *ring_head, float *log_delta,
+                         float *log_B, float *log_x, float *y, int32_t *dev_status, void *stream);
+
+/*
+ * ssm_draft_tree_commit -- after the target accepts a path of the draft tree
+ * (ssm_accept_path), move the draft's committed state along it from the log:
+ * h_ckpt <- the logged updates of path[0 .. path_len) applied in order (no conv,
+ * no input re-read; the same fp32 operations as ssm_draft_step, so on a chain
+ * the result equals the stepped state bit for bit), the path's pre-conv rows
+ * appended to the conv ring (the last three are written) and ring_head +=
+ * path_len.  Every node on the path must have been drafted (its log row written).
+ *   path       device int32 [S][max_path]: path[0] = 0, each entry a child of
+ *              the one before; path_len device int32 [S], 0..max_path.  A bad
+ *              entry sets SSM_STATUS_PATH_RANGE and only the valid prefix commits.
+ *   log_*      as written by ssm_draft_tree_level (log_B 16-byte aligned)
+ *   xBC        device bf16 [I][n][conv_dim] (16-byte aligned)
+ *   h_ckpt     device fp32 [I][H][P][N], in/out, 16-byte aligned
+ *   ring       device bf16 [I][R][conv_dim] (16-byte aligned), ring_head [I]
+ */
+int ssm_draft_tree_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
+                          const ssm_node *layout, int32_t max_path, const int32_t *path, const int32_t *path_len,
+                          const float *log_delta, const float *log_B, const float *log_x, const uint16_t *xBC,
+                          float *h_ckpt, uint16_t *ring, int32_t *ring_head, int32_t *dev_status, void *stream);
+
+/*
  * ssm_tree_verify_noalloc -- ssm_tree_verify for callers that cannot allocate
  * device memory (a runtime that gives a plugin only the current op's tensors
  * and owns all other device memory, an embedding with allocation forbidden

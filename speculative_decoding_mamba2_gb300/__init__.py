@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     ssm_commit_verify,
     ssm_commit_verify_workspace_size,
     ssm_draft_step,
+    ssm_draft_tree_commit,
+    ssm_draft_tree_level,
     ssm_gated_rmsnorm,
     ssm_last_error,
     ssm_linear,

@@ -96,6 +96,8 @@ _SIGS = {
                                               _P, _P, ctypes.c_size_t, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_replay": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_draft_tree_level": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_draft_tree_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -323,6 +325,42 @@ def ssm_replay(dims: Dims, params: dict, n_seq: int, log_cap: int, k, log_delta,
         _dev(log_B, "log_B", torch.float32, I * log_cap * d.d_state),
         _dev(log_x, "log_x", torch.float32, I * log_cap * d.d_inner), _dev(log_len, "log_len", torch.int32, I),
         _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
+
+
+def ssm_draft_tree_level(dims: Dims, params: dict, n_seq: int, n_nodes: int, level: int, layout, xBC, dt, h_ckpt,
+                         ring, ring_head, log_delta, log_B, log_x, y, status=None, stream=None):
+    """One depth level of the draft tree: y and log rows of the nodes of depth `level`."""
+    d, I, n = dims, n_seq * dims.n_layers, n_nodes
+    cd = d.c()
+    cp = _params(params, d, d.n_layers)
+    _check(lib().ssm_draft_tree_level(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, level,
+        _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+        _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim), _dev(ring_head, "ring_head", torch.int32, I),
+        _dev(log_delta, "log_delta", torch.float32, I * n * d.n_heads),
+        _dev(log_B, "log_B", torch.float32, I * n * d.d_state),
+        _dev(log_x, "log_x", torch.float32, I * n * d.d_inner),
+        _dev(y, "y", torch.float32, I * n * d.d_inner), _opt_status(status), _stream(stream, y)))
+
+
+def ssm_draft_tree_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, layout, max_path: int, path, path_len,
+                          log_delta, log_B, log_x, xBC, h_ckpt, ring, ring_head, status=None, stream=None):
+    """The accepted path's logged updates into h_ckpt, its rows into the ring, head += path_len."""
+    d, I, n = dims, n_seq * dims.n_layers, n_nodes
+    cd = d.c()
+    cp = ssm_params(None, None, None, _ptr(params["A_log"], "A_log", torch.float32, d.n_layers * d.n_heads), None)
+    _check(lib().ssm_draft_tree_commit(
+        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+        max_path, _dev(path, "path", torch.int32, n_seq * max_path), _dev(path_len, "path_len", torch.int32, n_seq),
+        _dev(log_delta, "log_delta", torch.float32, I * n * d.n_heads),
+        _dev(log_B, "log_B", torch.float32, I * n * d.d_state),
+        _dev(log_x, "log_x", torch.float32, I * n * d.d_inner),
+        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim),
+        _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
 
 

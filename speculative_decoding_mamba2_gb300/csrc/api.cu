@@ -8,6 +8,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "draft_tree.cuh"
 
 namespace ssmtree {
 
@@ -375,4 +376,85 @@ extern "C" int ssm_replay(const ssm_dims* dims, const ssm_params* prm, int32_t n
   a.ring_head = ring_head;
   a.status = dev_status;
   return finish(fn, launch_replay(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_draft_tree_level(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
+                                    int32_t level, const ssm_node* layout, const uint16_t* xBC, const uint16_t* dt,
+                                    const float* h_ckpt, const uint16_t* ring, const int32_t* ring_head,
+                                    float* log_delta, float* log_B, float* log_x, float* y, int32_t* dev_status,
+                                    void* stream) {
+  const char* fn = "ssm_draft_tree_level";
+  if (int rc = check_dims(fn, dims, true, prm)) return rc;
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
+  if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
+  if (level < 0 || level > SSM_MAX_DEPTH) return fail(SSM_ERR_RANGE, fn, "level must be in [0, SSM_MAX_DEPTH]");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!layout || !xBC || !dt || !h_ckpt || !ring || !ring_head || !log_delta || !log_B || !log_x || !y)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)h_ckpt | (uintptr_t)log_B | (uintptr_t)prm->conv_w) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt, log_B and params->conv_w must be 16-byte aligned");
+  DraftTreeArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.level = level;
+  a.conv_w = prm->conv_w;
+  a.conv_b = prm->conv_b;
+  a.dt_bias = prm->dt_bias;
+  a.A_log = prm->A_log;
+  a.D = prm->D;
+  a.layout = layout;
+  a.xBC = xBC;
+  a.dt = dt;
+  a.h = h_ckpt;
+  a.ring = ring;
+  a.ring_head = ring_head;
+  a.log_delta = log_delta;
+  a.log_B = log_B;
+  a.log_x = log_x;
+  a.y = y;
+  a.status = dev_status;
+  return finish(fn, launch_draft_tree_level(a, (cudaStream_t)stream));
+}
+
+extern "C" int ssm_draft_tree_commit(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
+                                     const ssm_node* layout, int32_t max_path, const int32_t* path,
+                                     const int32_t* path_len, const float* log_delta, const float* log_B,
+                                     const float* log_x, const uint16_t* xBC, float* h_ckpt, uint16_t* ring,
+                                     int32_t* ring_head, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_draft_tree_commit";
+  if (int rc = check_dims(fn, dims, false, nullptr)) return rc;
+  if (!prm || !prm->A_log) return fail(SSM_ERR_INVALID_ARG, fn, "params->A_log is NULL");
+  if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
+  if (n_nodes < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_nodes must be >= 1");
+  if (n_nodes > SSM_MAX_NODES) return fail(SSM_ERR_CAPACITY, fn, "n_nodes exceeds SSM_MAX_NODES");
+  if (max_path < 1 || max_path > SSM_MAX_PATH) return fail(SSM_ERR_RANGE, fn, "max_path must be in [1, SSM_MAX_PATH]");
+  if (n_seq == 0) return finish(fn, cudaSuccess);
+  if (!layout || !path || !path_len || !log_delta || !log_B || !log_x || !xBC || !h_ckpt || !ring || !ring_head)
+    return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
+  if (((uintptr_t)h_ckpt | (uintptr_t)log_B | (uintptr_t)xBC | (uintptr_t)ring) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt, log_B, xBC and ring must be 16-byte aligned");
+  DraftTreeCommitArgs a;
+  a.H = dims->n_heads;
+  a.L = dims->n_layers;
+  a.R = dims->ring_cap;
+  a.n_seq = n_seq;
+  a.n = n_nodes;
+  a.max_path = max_path;
+  a.A_log = prm->A_log;
+  a.layout = layout;
+  a.path = path;
+  a.path_len = path_len;
+  a.log_delta = log_delta;
+  a.log_B = log_B;
+  a.log_x = log_x;
+  a.xBC = xBC;
+  a.h = h_ckpt;
+  a.ring = ring;
+  a.ring_head = ring_head;
+  a.status = dev_status;
+  return finish(fn, launch_draft_tree_commit(a, (cudaStream_t)stream));
 }

@@ -95,6 +95,8 @@ WORKLOADS = {
     4: Workload(4, "stress, Mamba2-780M shape, 48 layers, batch 64, 40-node ternary tree + 256-node chain",
                 Shape(H=48), n_layers=48, batch=64, trees=(("full", 3, 3), ("chain", 256)),
                 p_accept=0.9, draft_steps=16),
+    5: Workload(5, "draft tree, Mamba2-370M shape, 48 layers, batch 1, 16-node random tree drafted level by level",
+                Shape(H=32), n_layers=48, batch=1, trees=(("random", 16, 3, 4),)),
 }
 
 
