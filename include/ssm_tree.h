@@ -280,8 +280,8 @@ int ssm_draft_step(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, i
  * re-read; the same fp32 operations as ssm_draft_step, so the result equals
  * the state that step k left, bit for bit); ring_head += k; log_len = 0.
  *   k          device int32 [S], 0 <= k <= log_len (else clamped + status bit)
- *   log_*      as written by ssm_draft_step
- *   h_ckpt     device fp32 [I][H][P][N], in/out
+ *   log_*      as written by ssm_draft_step (log_B 16-byte aligned)
+ *   h_ckpt     device fp32 [I][H][P][N], in/out, 16-byte aligned
  */
 int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t log_cap, const int32_t *k,
                const float *log_delta, const float *log_B, const float *log_x, int32_t *log_len, float *h_ckpt,
@@ -312,13 +312,26 @@ int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
  *   log_x      [I][n][d_inner]: rows of depth < level are read (the earlier
  *              levels' calls wrote them), rows of depth == level are written
  *   y          device fp32 [I][n][d_inner]: rows of depth == level written
+ *   workspace  device, 16-byte aligned, >= ssm_draft_tree_workspace_size()
+ *              bytes, caller-owned scratch (per level node: C, e^{S_v} per
+ *              head and the path sums of every row, written and read within
+ *              the call); calls that overlap on the GPU must not share one
  * A layout record that points outside its tree sets SSM_STATUS_BAD_LAYOUT and
  * the instance writes nothing.
  */
 int ssm_draft_tree_level(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,
                          int32_t level, const ssm_node *layout, const uint16_t *xBC, const uint16_t *dt,
                          const float *h_ckpt, const uint16_t *ring, const int32_t *ring_head, float *log_delta,
-                         float *log_B, float *log_x, float *y, int32_t *dev_status, void *stream);
+                         float *log_B, float *log_x, float *y, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, void *stream);
+
+/*
+ * ssm_draft_tree_workspace_size -- host-only.  Bytes of device workspace
+ * ssm_draft_tree_level needs: about n_nodes * (N + H + d_inner) * 4 per
+ * instance (each part padded to 128 bytes); 0 if the shape is rejected
+ * (reason in ssm_last_error()).
+ */
+size_t ssm_draft_tree_workspace_size(const ssm_dims *dims, int32_t n_seq, int32_t n_nodes);
 
 /*
  * ssm_draft_tree_commit -- after the target accepts a path of the draft tree

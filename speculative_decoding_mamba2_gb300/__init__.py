@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     ssm_draft_step,
     ssm_draft_tree_commit,
     ssm_draft_tree_level,
+    ssm_draft_tree_workspace_size,
     ssm_gated_rmsnorm,
     ssm_last_error,
     ssm_linear,

@@ -96,7 +96,9 @@ _SIGS = {
                                               _P, _P, ctypes.c_size_t, _P, _P]),
     "ssm_draft_step": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "ssm_replay": (ctypes.c_int, [_P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "ssm_draft_tree_level": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "ssm_draft_tree_level": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                            ctypes.c_size_t, _P, _P]),
+    "ssm_draft_tree_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
     "ssm_draft_tree_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -328,8 +330,17 @@ def ssm_replay(dims: Dims, params: dict, n_seq: int, log_cap: int, k, log_delta,
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
 
 
+def ssm_draft_tree_workspace_size(dims: Dims, n_seq: int, n_nodes: int) -> int:
+    """Bytes of device workspace ssm_draft_tree_level needs (host call)."""
+    cd = dims.c()
+    b = lib().ssm_draft_tree_workspace_size(ctypes.byref(cd), n_seq, n_nodes)
+    if b == 0:
+        raise SSMError(SSM_ERR_INVALID_ARG, ssm_last_error())
+    return int(b)
+
+
 def ssm_draft_tree_level(dims: Dims, params: dict, n_seq: int, n_nodes: int, level: int, layout, xBC, dt, h_ckpt,
-                         ring, ring_head, log_delta, log_B, log_x, y, status=None, stream=None):
+                         ring, ring_head, log_delta, log_B, log_x, y, workspace, status=None, stream=None):
     """One depth level of the draft tree: y and log rows of the nodes of depth `level`."""
     d, I, n = dims, n_seq * dims.n_layers, n_nodes
     cd = d.c()
@@ -343,7 +354,8 @@ def ssm_draft_tree_level(dims: Dims, params: dict, n_seq: int, n_nodes: int, lev
         _dev(log_delta, "log_delta", torch.float32, I * n * d.n_heads),
         _dev(log_B, "log_B", torch.float32, I * n * d.d_state),
         _dev(log_x, "log_x", torch.float32, I * n * d.d_inner),
-        _dev(y, "y", torch.float32, I * n * d.d_inner), _opt_status(status), _stream(stream, y)))
+        _dev(y, "y", torch.float32, I * n * d.d_inner), _dev(workspace, "workspace", torch.uint8),
+        ctypes.c_size_t(workspace.numel()), _opt_status(status), _stream(stream, y)))
 
 
 def ssm_draft_tree_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, layout, max_path: int, path, path_len,

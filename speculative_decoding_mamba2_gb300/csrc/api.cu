@@ -360,7 +360,8 @@ extern "C" int ssm_replay(const ssm_dims* dims, const ssm_params* prm, int32_t n
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!k || !log_delta || !log_B || !log_x || !log_len || !h_ckpt || !ring_head)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
-  if ((uintptr_t)h_ckpt & 15) return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt must be 16-byte aligned");
+  if (((uintptr_t)h_ckpt | (uintptr_t)log_B) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt and log_B must be 16-byte aligned");
   ReplayArgs a;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
@@ -381,8 +382,8 @@ extern "C" int ssm_replay(const ssm_dims* dims, const ssm_params* prm, int32_t n
 extern "C" int ssm_draft_tree_level(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,
                                     int32_t level, const ssm_node* layout, const uint16_t* xBC, const uint16_t* dt,
                                     const float* h_ckpt, const uint16_t* ring, const int32_t* ring_head,
-                                    float* log_delta, float* log_B, float* log_x, float* y, int32_t* dev_status,
-                                    void* stream) {
+                                    float* log_delta, float* log_B, float* log_x, float* y, void* workspace,
+                                    size_t workspace_bytes, int32_t* dev_status, void* stream) {
   const char* fn = "ssm_draft_tree_level";
   if (int rc = check_dims(fn, dims, true, prm)) return rc;
   if (n_seq < 0) return fail(SSM_ERR_INVALID_ARG, fn, "n_seq must be >= 0");
@@ -392,8 +393,11 @@ extern "C" int ssm_draft_tree_level(const ssm_dims* dims, const ssm_params* prm,
   if (n_seq == 0) return finish(fn, cudaSuccess);
   if (!layout || !xBC || !dt || !h_ckpt || !ring || !ring_head || !log_delta || !log_B || !log_x || !y)
     return fail(SSM_ERR_INVALID_ARG, fn, "a tensor pointer is NULL");
-  if (((uintptr_t)h_ckpt | (uintptr_t)log_B | (uintptr_t)prm->conv_w) & 15)
-    return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt, log_B and params->conv_w must be 16-byte aligned");
+  if (!workspace) return fail(SSM_ERR_INVALID_ARG, fn, "workspace is NULL");
+  if (((uintptr_t)h_ckpt | (uintptr_t)log_B | (uintptr_t)prm->conv_w | (uintptr_t)workspace) & 15)
+    return fail(SSM_ERR_INVALID_ARG, fn, "h_ckpt, log_B, params->conv_w and workspace must be 16-byte aligned");
+  if (workspace_bytes < draft_tree_workspace_bytes(n_nodes, dims->n_heads, (long long)n_seq * dims->n_layers))
+    return fail(SSM_ERR_CAPACITY, fn, "workspace smaller than ssm_draft_tree_workspace_size()");
   DraftTreeArgs a;
   a.H = dims->n_heads;
   a.L = dims->n_layers;
@@ -417,7 +421,18 @@ extern "C" int ssm_draft_tree_level(const ssm_dims* dims, const ssm_params* prm,
   a.log_x = log_x;
   a.y = y;
   a.status = dev_status;
-  return finish(fn, launch_draft_tree_level(a, (cudaStream_t)stream));
+  return finish(fn, launch_draft_tree_level(a, workspace, (cudaStream_t)stream));
+}
+
+extern "C" size_t ssm_draft_tree_workspace_size(const ssm_dims* dims, int32_t n_seq, int32_t n_nodes) {
+  const char* fn = "ssm_draft_tree_workspace_size";
+  if (check_dims(fn, dims, false, nullptr)) return 0;
+  if (n_seq < 0 || n_nodes < 1 || n_nodes > SSM_MAX_NODES) {
+    fail(SSM_ERR_INVALID_ARG, fn, "need n_seq >= 0 and 1 <= n_nodes <= SSM_MAX_NODES");
+    return 0;
+  }
+  const size_t b = draft_tree_workspace_bytes(n_nodes, dims->n_heads, (long long)n_seq * dims->n_layers);
+  return b ? b : 16;
 }
 
 extern "C" int ssm_draft_tree_commit(const ssm_dims* dims, const ssm_params* prm, int32_t n_seq, int32_t n_nodes,

@@ -8,6 +8,7 @@
 // exact fp32 operation sequence of the step kernel (decay_of, __fmul_rn,
 // ssm_update), so it reproduces the stepped state bit for bit.
 #include "common.cuh"
+#include "log_apply.cuh"
 
 namespace ssmtree {
 namespace {
@@ -130,10 +131,11 @@ __global__ void __launch_bounds__(DTHREADS) draft_step_kernel(DraftArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// replay: one warp per state row at a time (lane = 4 columns); a pass covers up to RT
-// logged steps, whose B columns each lane keeps in registers and whose u = Δ·x sit in
-// shared memory (one value per step and row); the update uses packed pairs with the same
-// two roundings per element as the draft step: h = fma(a, h, u·b)
+// replay: each warp holds 16 state rows of one head in registers (a float4 of 4 columns
+// per lane and row, all 16 loads in flight while the log is staged); a pass stages up to
+// RT logged steps in shared memory (u = Δ·x per step and row, the decay per step and
+// head, B per step) and applies them with the draft step's operations
+// (apply_logged_updates)
 // ---------------------------------------------------------------------------
 constexpr int RW = 8;               // warps per CTA
 constexpr int RTHREADS = RW * 32;
@@ -152,9 +154,10 @@ __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool repo
   return k;
 }
 
-__global__ void __launch_bounds__(RTHREADS) replay_kernel(ReplayArgs a) {
+__global__ void __launch_bounds__(RTHREADS, 2) replay_kernel(ReplayArgs a) {
   __shared__ float us[RT][RROWS];  // u = Δ_t·x_t[row]
   __shared__ float decs[RT][RH];
+  __shared__ __align__(16) float Bs[RT][kN];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_groups = (a.H + RH - 1) / RH;
   const int grp = blockIdx.x % n_groups;
@@ -165,74 +168,62 @@ __global__ void __launch_bounds__(RTHREADS) replay_kernel(ReplayArgs a) {
   const int rows = heads * kP;
   const int d_inner = a.H * kP;
   const int k = replay_k(a, inst, grp == 0 && tid == 0);
+  if (k == 0) return;
   float* hs = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
   const int row0 = warp * (RROWS / RW);  // this warp's 16 rows, all of one head
   const int g = row0 / kP;
-
+  const bool mine = g < heads;
+  float4 hr[16];
+  if (mine) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) hr[r] = reinterpret_cast<const float4*>(hs + (size_t)(row0 + r) * kN)[lane];
+  }
+  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid & 1, heads - 1)]);
   for (int t0 = 0; t0 < k; t0 += RT) {
     const int cnt = min(RT, k - t0);
-    if (t0 > 0) __syncthreads();  // the previous pass is done with us / decs
-    for (int i = tid; i < cnt * RROWS; i += RTHREADS) {
-      const int t = i / RROWS, r = i - t * RROWS;
-      float u = 0.f;
-      if (r < rows) {
+    if (t0 > 0) __syncthreads();  // the previous pass is done with us, decs, Bs
+    // every log value of the pass in flight at once: Δ and x for (row, step) pairs, B rows,
+    // then the products and decays into shared memory
+    const int r = tid & (RROWS - 1), th = tid >> 7;
+    float dl[RT / 2], xv[RT / 2];
+#pragma unroll
+    for (int j = 0; j < RT / 2; ++j) {
+      const int t = th + 2 * j;
+      dl[j] = 0.f;
+      xv[j] = 0.f;
+      if (t < cnt && r < rows) {
         const size_t lrow = (size_t)inst * a.log_cap + t0 + t;
-        u = __fmul_rn(a.log_delta[lrow * a.H + h_begin + r / kP], a.log_x[lrow * d_inner + h_begin * kP + r]);
+        dl[j] = a.log_delta[lrow * a.H + h_begin + r / kP];
+        xv[j] = a.log_x[lrow * d_inner + h_begin * kP + r];
       }
-      us[t][r] = u;
     }
-    if (tid < cnt * RH) {
-      const int t = tid / RH, gg = tid - t * RH;
-      float e = 1.f;
-      if (gg < heads) {
-        const int h = h_begin + gg;
-        e = decay_of(a.log_delta[((size_t)inst * a.log_cap + t0 + t) * a.H + h],
-                     neg_exp(a.A_log[(size_t)layer * a.H + h]));
-      }
-      decs[t][gg] = e;
-    }
-    // this lane's B columns 4*lane .. 4*lane+3 for the pass's steps, as packed pairs
-    unsigned long long b01[RT], b23[RT];
+    float4 bv[RT * (kN / 4) / RTHREADS];
 #pragma unroll
-    for (int t = 0; t < RT; ++t) {
-      float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (t < cnt) bv = reinterpret_cast<const float4*>(a.log_B + ((size_t)inst * a.log_cap + t0 + t) * kN)[lane];
-      b01[t] = pack2(bv.x, bv.y);
-      b23[t] = pack2(bv.z, bv.w);
+    for (int q = 0; q < RT * (kN / 4) / RTHREADS; ++q) {
+      const int i = tid + q * RTHREADS, t = i / (kN / 4), c4 = i - t * (kN / 4);
+      bv[q] = t < cnt ? reinterpret_cast<const float4*>(a.log_B + ((size_t)inst * a.log_cap + t0 + t) * kN)[c4]
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    const int dt_ = tid / RH, dg = tid - dt_ * RH;
+    float dd = 0.f;
+    if (tid < cnt * RH && dg < heads) dd = a.log_delta[((size_t)inst * a.log_cap + t0 + dt_) * a.H + h_begin + dg];
+#pragma unroll
+    for (int j = 0; j < RT / 2; ++j) {
+      const int t = th + 2 * j;
+      if (t < cnt) us[t][r] = __fmul_rn(dl[j], xv[j]);
+    }
+#pragma unroll
+    for (int q = 0; q < RT * (kN / 4) / RTHREADS; ++q) {
+      const int i = tid + q * RTHREADS, t = i / (kN / 4), c4 = i - t * (kN / 4);
+      reinterpret_cast<float4*>(Bs[t])[c4] = bv[q];
+    }
+    if (tid < cnt * RH) decs[dt_][dg] = dg < heads ? decay_of(dd, A_g) : 1.f;
     __syncthreads();
-    if (g < heads) {
-      unsigned long long dec2[RT];
+    if (mine) apply_logged_updates(hr, cnt, &us[0][0], RROWS, row0, &Bs[0][0], &decs[0][g], RH, lane);
+  }
+  if (mine) {
 #pragma unroll
-      for (int t = 0; t < RT; ++t) dec2[t] = pack2(decs[t][g], decs[t][g]);
-      const int row_end = row0 + RROWS / RW;
-      float4 n0 = reinterpret_cast<const float4*>(hs + (size_t)row0 * kN)[lane];
-      float4 n1 = reinterpret_cast<const float4*>(hs + (size_t)(row0 + 1) * kN)[lane];
-      for (int r = row0; r < row_end; r += 2) {  // two rows in work, the next two in flight
-        float4* p0 = reinterpret_cast<float4*>(hs + (size_t)r * kN) + lane;
-        float4* p1 = reinterpret_cast<float4*>(hs + (size_t)(r + 1) * kN) + lane;
-        const float4 h0 = n0, h1 = n1;
-        if (r + 2 < row_end) {
-          n0 = reinterpret_cast<const float4*>(hs + (size_t)(r + 2) * kN)[lane];
-          n1 = reinterpret_cast<const float4*>(hs + (size_t)(r + 3) * kN)[lane];
-        }
-        unsigned long long a01 = pack2(h0.x, h0.y), a23 = pack2(h0.z, h0.w);
-        unsigned long long c01 = pack2(h1.x, h1.y), c23 = pack2(h1.z, h1.w);
-#pragma unroll
-        for (int t = 0; t < RT; ++t) {
-          if (t < cnt) {
-            const unsigned long long u0 = pack2(us[t][r], us[t][r]), u1 = pack2(us[t][r + 1], us[t][r + 1]);
-            a01 = ffma2(dec2[t], a01, fmul2(u0, b01[t]));
-            a23 = ffma2(dec2[t], a23, fmul2(u0, b23[t]));
-            c01 = ffma2(dec2[t], c01, fmul2(u1, b01[t]));
-            c23 = ffma2(dec2[t], c23, fmul2(u1, b23[t]));
-          }
-        }
-        const float2 x01 = unpack2(a01), x23 = unpack2(a23), y01 = unpack2(c01), y23 = unpack2(c23);
-        *p0 = make_float4(x01.x, x01.y, x23.x, x23.y);
-        *p1 = make_float4(y01.x, y01.y, y23.x, y23.y);
-      }
-    }
+    for (int r = 0; r < 16; ++r) reinterpret_cast<float4*>(hs + (size_t)(row0 + r) * kN)[lane] = hr[r];
   }
 }
 

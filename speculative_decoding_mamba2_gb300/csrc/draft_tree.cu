@@ -11,22 +11,27 @@
 // which reads the committed state once per level, whatever the number of branches, and
 // writes no state.  The ancestors' Δ, B, x are the log rows their own level wrote.
 //
-// draft_tree_level_kernel: one CTA per (instance, pair of heads).  Each thread loads its
-// share of the pair's 128 state rows (8 lanes per row, 16 columns each) into registers
-// first, so the loads are in flight while the CTA sets up the level: the frontier list
-// and the union of the frontier's paths (shared memory), the ancestors' logged x and Δ,
-// the frontier's conv + SiLU (x of the pair's channels, B, C), Δ and their log rows, the
-// cumulative log-decays S, the B·C products along each path (one warp per pair) and
-// the per-row path sums.  The C_v · h contraction then runs from registers, FB = 8 nodes
-// per pass; the 8 lanes of a row end with one node's sum each after a 7-shuffle
-// reduce-scatter.
+// draft_tree_prep_kernel (one CTA per instance and block of 4 heads): one warp finds the
+// level's nodes and the nodes on their paths; then every input is loaded in one batch: x of
+// the block's 256 channels and B for every node on the paths (the ancestors' from the log,
+// the level's through the tree conv + SiLU, logged here), C of the level's nodes and Δ.  S,
+// the B·C products and the path coefficients follow in shared memory, and the CTA writes
+// to the workspace, per level node: e^{S_v} for its heads and the path sum
+// Σ_k e^{S_v − S_{m_k}} Δ_{m_k} (B_{m_k} · C_v) x_{m_k} + D·x_v for its rows (and C_v, from the
+// first block).
+// draft_tree_level_kernel (one CTA per instance and pair of heads, launched to overlap the
+// prep): each thread loads its share of the pair's 128 committed state rows into registers
+// (8 lanes per row, 16 columns each) and waits for the prep grid; the C_v · h contraction
+// then runs from registers, 8 nodes per pass, the 8 lanes of a row ending with one node's
+// sum each after a 7-shuffle reduce-scatter: y_v = e^{S_v} (C_v · h) + path sum.
 //
-// draft_tree_commit_kernel: one CTA per (instance, pair of heads), one warp per state row at
-// a time (4 columns per lane), the path's updates applied in path order with the same fp32
-// operations as the one-token draft step, so on a chain it reproduces the stepped state bit
-// for bit.  draft_tree_ring_kernel then writes the path's last three pre-conv rows into the
-// ring and advances the head.
+// draft_tree_commit_kernel (one CTA per instance and pair of heads): each warp holds 16 state
+// rows in registers (16 loads in flight per lane) and applies the path's logged updates in
+// path order with the one-token draft step's fp32 operations (apply_logged_updates), so on a
+// chain it reproduces the stepped state bit for bit.  draft_tree_ring_kernel then writes the
+// path's last three pre-conv rows into the ring and advances the head.
 #include "draft_tree.cuh"
+#include "log_apply.cuh"
 
 namespace ssmtree {
 namespace {
@@ -35,25 +40,96 @@ constexpr int TG = 2;                            // heads per CTA
 constexpr int TROWS = TG * kP;                   // 128 state rows
 constexpr int TTHREADS = 256;                    // 8 lanes per row: 32 rows per sweep
 constexpr int TSWEEPS = TROWS / (TTHREADS / 8);  // 4
-constexpr int FB = 8;                            // frontier nodes per pass
+constexpr int FB = 8;                            // level nodes per pass
 constexpr int MAXN = SSM_MAX_NODES;              // 64
 constexpr int MAXP = SSM_MAX_DEPTH + 1;          // 16 nodes on a root-to-node path
+static_assert(MAXN <= 64, "level_setup covers 64 nodes with one warp");
 
-struct LevelSmem {
-  int par[MAXN], dep[MAXN], tap[MAXN][3], slot[MAXN], front[MAXN];
-  int nf;
-  int pslot[FB][MAXP], pnode[FB][MAXP], plen[FB];
-  float A[TG], Dh[TG];
-  float du[MAXN][TG];        // Δ of every node on a frontier path (by slot)
-  float su[MAXN][TG];        // S: cumulative Δ·A from the root to the node, inclusive
-  float coef[FB][MAXP][TG];  // e^{S_v − S_m} Δ_m (B_m · C_v)
-  float E[FB][TG];           // e^{S_v}
-  float bc[FB][MAXP];        // B_m · C_v
-  __align__(16) float Cf[FB][kN];
-  __align__(16) float Bf[FB][kN];
-  float base[FB][TROWS];     // Σ_k coef·x_{m_k}[row] + D·x_v[row]
-  float xu[MAXN][TROWS];     // post-conv x of the pair's channels, by slot
+// The level's nodes and every node on their root-to-node paths, for one sequence.
+struct LevelSetup {
+  int par[MAXN], dep[MAXN], tap[MAXN][3];
+  int slot[MAXN];   // node -> position among the nodes on the level's paths (node order), or -1
+  int snode[MAXN];  // slot -> node
+  int front[MAXN];  // the level's nodes, in node order
+  int nf, nu;
 };
+
+// One warp: loads the records, checks that every parent and tap is an earlier node and the
+// depths agree, and lists the level's nodes and the nodes on their paths.  A record that
+// fails leaves nf = 0 (and sets SSM_STATUS_BAD_LAYOUT when `report`).
+__device__ void level_setup(LevelSetup& s, const ssm_node* lay, int n, int level, int32_t* status, bool report) {
+  const int lane = threadIdx.x & 31;
+  const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int v = lane + 32 * k;
+    if (v < n) {
+      const ssm_node r = lay[v];
+      s.par[v] = r.parent;
+      s.dep[v] = r.depth;
+      s.slot[v] = -1;
+      ok = ok && (v == 0 ? (r.parent == -1 && r.depth == 0) : (r.parent >= 0 && r.parent < v));
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        s.tap[v][t] = r.tap[t];
+        ok = ok && r.tap[t] < v && r.tap[t] >= -3;
+      }
+    }
+  }
+  ok = __all_sync(full, ok);
+  __syncwarp();
+  if (ok) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int v = lane + 32 * k;
+      if (v < n && v > 0) ok = ok && s.dep[v] == s.dep[s.par[v]] + 1;
+    }
+    ok = __all_sync(full, ok);
+  }
+  if (!ok) {
+    if (lane == 0) {
+      if (report) flag(status, SSM_STATUS_BAD_LAYOUT);
+      s.nf = 0;
+      s.nu = 0;
+    }
+    return;
+  }
+  const unsigned m0 = __ballot_sync(full, lane < n && s.dep[lane] == level);
+  const unsigned m1 = __ballot_sync(full, lane + 32 < n && s.dep[lane + 32] == level);
+  if ((m0 >> lane) & 1u) s.front[__popc(m0 & lt)] = lane;
+  if ((m1 >> lane) & 1u) s.front[__popc(m0) + __popc(m1 & lt)] = lane + 32;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int v = lane + 32 * k;
+    if (v < n && s.dep[v] == level)
+      for (int u = v; u >= 0; u = s.par[u]) s.slot[u] = 0;  // same value from every lane
+  }
+  __syncwarp();
+  const unsigned p0 = __ballot_sync(full, lane < n && s.slot[lane] >= 0);
+  const unsigned p1 = __ballot_sync(full, lane + 32 < n && s.slot[lane + 32] >= 0);
+  if ((p0 >> lane) & 1u) {
+    const int sl = __popc(p0 & lt);
+    s.slot[lane] = sl;
+    s.snode[sl] = lane;
+  }
+  if ((p1 >> lane) & 1u) {
+    const int sl = __popc(p0) + __popc(p1 & lt);
+    s.slot[lane + 32] = sl;
+    s.snode[sl] = lane + 32;
+  }
+  if (lane == 0) {
+    s.nf = __popc(m0) + __popc(m1);
+    s.nu = __popc(p0) + __popc(p1);
+  }
+}
+
+// Pre-conv value of channel c at tap source src of this instance (node row or ring row).
+__device__ __forceinline__ float tap_ldg(const uint16_t* xbc, const uint16_t* ring, int head, int R, int conv_dim,
+                                         int src, int c) {
+  const uint16_t* p = src >= 0 ? xbc + (size_t)src * conv_dim : ring + (size_t)ring_pos(head, src, R) * conv_dim;
+  return bf16f(__ldg(p + c));
+}
 
 // 8 partial sums per lane, over the 8 lanes o = 0..7 of an aligned lane group: returns
 // the full sum of value o (recursive halving: 4 + 2 + 1 shuffles).
@@ -77,248 +153,332 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[FB], int o) {
   return keep + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
-__global__ void __launch_bounds__(TTHREADS, 2) draft_tree_level_kernel(DraftTreeArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  LevelSmem& s = *reinterpret_cast<LevelSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, o = tid & 7, rsub = tid >> 3;
-  const int n_groups = (a.H + TG - 1) / TG;
-  const int grp = blockIdx.x % n_groups;
-  const long long inst = blockIdx.x / n_groups;
+constexpr int PG = 4;             // heads per prep CTA
+constexpr int PROWS = PG * kP;    // 256 channels (x rows) per prep CTA
+
+// Workspace of one instance (floats): C rows [n][kN], e^{S_v} [n][H], path sums [n][d_inner],
+// indexed by node; only the level's nodes are written.  Each section (and so each instance)
+// starts on a 128-byte boundary, for the 16-byte vector accesses.
+__host__ __device__ inline size_t ws_pad(size_t f) { return (f + 31) & ~(size_t)31; }
+__host__ __device__ inline size_t ws_E_off(int n) { return ws_pad((size_t)n * kN); }
+__host__ __device__ inline size_t ws_P_off(int n, int H) { return ws_E_off(n) + ws_pad((size_t)n * H); }
+__host__ __device__ inline size_t ws_floats_per_inst(int n, int H) {
+  return ws_P_off(n, H) + ws_pad((size_t)n * H * kP);
+}
+
+struct PrepFixed {
+  LevelSetup ls;
+  const uint16_t* tp[MAXN][3];  // the pre-conv rows of each node's taps (node row or ring row)
+  float A[PG], Dh[PG];
+};
+
+// Shared-memory layout of draft_tree_prep_kernel for trees of n nodes (byte offsets, each a
+// multiple of 128).  Slots index the nodes on the level's paths, positions the level's nodes.
+struct PrepLayout {
+  int xu, Bu, Cf, coef, du, su, pslot, plen, total;
+};
+__host__ __device__ inline PrepLayout prep_layout(int n) {
+  auto up = [](int b) { return (b + 127) & ~127; };
+  PrepLayout L;
+  int o = up((int)sizeof(PrepFixed));
+  L.xu = o;    o += up(n * PROWS * 4);       // x of the block's channels, by slot
+  L.Bu = o;    o += up(n * kN * 4);          // B, by slot
+  L.Cf = o;    o += up(n * kN * 4);          // C, by position
+  L.coef = o;  o += up(n * MAXP * PG * 4);   // e^{S_v − S_m} Δ_m (B_m · C_v), by position and path index
+  L.du = o;    o += up(n * PG * 4);          // Δ, by slot
+  L.su = o;    o += up(n * PG * 4);          // S = Σ Δ·A from the root, inclusive, by slot
+  L.pslot = o; o += up(n * MAXP * 4);        // path slots, root first, by position
+  L.plen = o;  o += up(n * 4);
+  L.total = o;
+  return L;
+}
+
+__global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeArgs a, float* ws) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  PrepFixed& s = *reinterpret_cast<PrepFixed*>(smem);
+  const int n = a.n;
+  const PrepLayout Lo = prep_layout(n);
+  float* xu = reinterpret_cast<float*>(smem + Lo.xu);
+  float* Bu = reinterpret_cast<float*>(smem + Lo.Bu);
+  float* Cf = reinterpret_cast<float*>(smem + Lo.Cf);
+  float* coef = reinterpret_cast<float*>(smem + Lo.coef);
+  float* du = reinterpret_cast<float*>(smem + Lo.du);
+  float* su = reinterpret_cast<float*>(smem + Lo.su);
+  int* pslot = reinterpret_cast<int*>(smem + Lo.pslot);
+  int* plen = reinterpret_cast<int*>(smem + Lo.plen);
+  // the level kernel may be scheduled once every prep CTA runs; it waits for this grid's
+  // completion before it reads anything written here
+  launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_blocks = (a.H + PG - 1) / PG;
+  const int blk = blockIdx.x % n_blocks;
+  const long long inst = blockIdx.x / n_blocks;
   const int seq = (int)(inst / a.L), layer = (int)(inst % a.L);
-  const int h_begin = grp * TG, heads = min(TG, a.H - h_begin), rows = heads * kP;
-  const int n = a.n, d_inner = a.H * kP, conv_dim = d_inner + 2 * kN;
-  const size_t node0 = (size_t)inst * n;  // first node row of this instance (xBC, dt, log, y)
+  const int h_begin = blk * PG, heads = min(PG, a.H - h_begin), rows = heads * kP;
+  const int H = a.H, d_inner = H * kP, conv_dim = d_inner + 2 * kN;
+  const size_t node0 = (size_t)inst * n;
 
-  // this thread's state values: rows rsub + 32 i, columns 4 o + 32 j
-  const float* hb = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
-  float4 hv[TSWEEPS][4];
-#pragma unroll
-  for (int i = 0; i < TSWEEPS; ++i) {
-    const int row = rsub + 32 * i;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      hv[i][j] = row < rows ? __ldg(reinterpret_cast<const float4*>(hb + (size_t)row * kN) + o + 8 * j)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
-  const ssm_node* lay = a.layout + (size_t)seq * n;
-  for (int v = tid; v < n; v += TTHREADS) {
-    const ssm_node r = lay[v];
-    s.par[v] = r.parent;
-    s.dep[v] = r.depth;
-    s.tap[v][0] = r.tap[0];
-    s.tap[v][1] = r.tap[1];
-    s.tap[v][2] = r.tap[2];
-    s.slot[v] = -1;
-  }
-  if (tid < TG) {
-    const bool on = tid < heads;
-    s.A[tid] = on ? neg_exp(a.A_log[(size_t)layer * a.H + h_begin + tid]) : 0.f;
-    s.Dh[tid] = on ? a.D[(size_t)layer * a.H + h_begin + tid] : 0.f;
+  if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, blk == 0);
+  if (warp == 1 && lane < PG) {
+    const bool on = lane < heads;
+    s.A[lane] = on ? neg_exp(a.A_log[(size_t)layer * H + h_begin + lane]) : 0.f;
+    s.Dh[lane] = on ? a.D[(size_t)layer * H + h_begin + lane] : 0.f;
   }
   __syncthreads();
-  if (tid == 0) {
-    // records in range (parents and taps earlier nodes, depths consistent), the level's
-    // nodes in node order, and every node on their paths numbered in node order
-    bool ok = s.par[0] == -1 && s.dep[0] == 0;
-    int nf = 0;
-    for (int v = 0; v < n && ok; ++v) {
-      const int p = s.par[v];
-      if (v > 0 && (p < 0 || p >= v || s.dep[v] != s.dep[p] + 1)) ok = false;
-      for (int t = 0; t < 3; ++t) {
-        const int src = s.tap[v][t];
-        if (src >= v || src < -3) ok = false;
-      }
-      if (ok && s.dep[v] == a.level) s.front[nf++] = v;
-    }
-    if (ok) {
-      for (int f = 0; f < nf; ++f)
-        for (int v = s.front[f]; v >= 0; v = s.par[v]) s.slot[v] = 0;
-      int nu = 0;
-      for (int v = 0; v < n; ++v)
-        if (s.slot[v] >= 0) s.slot[v] = nu++;
-    } else {
-      flag(a.status, SSM_STATUS_BAD_LAYOUT);
-    }
-    s.nf = ok ? nf : 0;
-  }
-  __syncthreads();
-  const int nf = s.nf;
+  const int nf = s.ls.nf, nu = s.ls.nu;
   if (nf == 0) return;
-
-  // ancestors on the frontier's paths: their logged x (this pair's channels) and Δ
-  for (int i = tid; i < n * TROWS; i += TTHREADS) {
-    const int v = i / TROWS, r = i - v * TROWS;
-    const int sl = s.slot[v];
-    if (sl < 0 || s.dep[v] >= a.level) continue;
-    s.xu[sl][r] = r < rows ? a.log_x[(node0 + v) * d_inner + h_begin * kP + r] : 0.f;
-  }
-  for (int i = tid; i < n * TG; i += TTHREADS) {
-    const int v = i / TG, g = i - v * TG;
-    const int sl = s.slot[v];
-    if (sl < 0 || s.dep[v] >= a.level) continue;
-    s.du[sl][g] = g < heads ? a.log_delta[(node0 + v) * a.H + h_begin + g] : 0.f;
+  const uint16_t* xbc = a.xBC + node0 * conv_dim;
+  if (tid < nf * 3) {  // tap rows of the level's nodes, ring positions resolved once
+    const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
+    const int v = s.ls.front[tid / 3], t = tid % 3, src = s.ls.tap[v][t];
+    s.tp[v][t] = src >= 0 ? xbc + (size_t)src * conv_dim
+                          : ring + (size_t)ring_pos(a.ring_head[inst], src, a.R) * conv_dim;
   }
   __syncthreads();
-  if (tid < TG) {  // S of the ancestors, parents first
-    for (int v = 0; v < n; ++v) {
-      const int sl = s.slot[v];
-      if (sl < 0 || s.dep[v] >= a.level) continue;
-      const int p = s.par[v];
-      s.su[sl][tid] = (p >= 0 ? s.su[s.slot[p]][tid] : 0.f) + s.du[sl][tid] * s.A[tid];
+
+  // ---- every input in one batch: x (the block's channels) and B for each slot, C for each
+  // level node, Δ for each slot; the level's own values through the conv, and logged ----
+  {
+    const float4* cw4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
+    const float* cbv = a.conv_b + (size_t)layer * conv_dim;
+    const bool live = tid < rows;
+    const int cx = h_begin * kP + tid;  // x channel of this thread
+    const int cb = d_inner + tid;       // B (tid < kN) or C channel of this thread
+    const float4 wx = live ? cw4[cx] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float bx = live ? cbv[cx] : 0.f;
+    const float4 wb = cw4[cb];
+    const float bb = cbv[cb];
+    float dval = 0.f;  // Δ: one (slot, head) per thread
+    int d_sl = -1, d_g = 0;
+    bool d_conv = false;
+    if (tid < nu * PG) {
+      d_sl = tid / PG;
+      d_g = tid - d_sl * PG;
+      const int v = s.ls.snode[d_sl];
+      if (d_g < heads) {
+        const int h = h_begin + d_g;
+        if (s.ls.dep[v] < a.level) {
+          dval = __ldg(a.log_delta + (node0 + v) * H + h);
+        } else {
+          d_conv = true;
+          dval = bf16f(__ldg(a.dt + (node0 + v) * H + h)) + a.dt_bias[(size_t)layer * H + h];
+        }
+      }
+    }
+    const int nbj = tid < kN ? nu : nf;  // B jobs: every slot; C jobs: every level node
+    for (int j0 = 0; j0 < nu || j0 < nbj; j0 += 4) {
+      float rx[4][4], rb[4][4];
+      bool xcv[4], bcv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xcv[i] = false;
+        bcv[i] = false;
+        const int j = j0 + i;
+        if (j < nu && live) {
+          const int v = s.ls.snode[j];
+          if (s.ls.dep[v] < a.level) {
+            rx[i][0] = __ldg(a.log_x + (node0 + v) * d_inner + cx);
+          } else {
+            xcv[i] = true;
+            rx[i][0] = bf16f(__ldg(s.tp[v][2] + cx));
+            rx[i][1] = bf16f(__ldg(s.tp[v][1] + cx));
+            rx[i][2] = bf16f(__ldg(s.tp[v][0] + cx));
+            rx[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cx));
+          }
+        }
+        if (j < nbj) {
+          const int v = tid < kN ? s.ls.snode[j] : s.ls.front[j];
+          if (tid < kN && s.ls.dep[v] < a.level) {
+            rb[i][0] = __ldg(a.log_B + (node0 + v) * kN + tid);
+          } else {
+            bcv[i] = true;
+            rb[i][0] = bf16f(__ldg(s.tp[v][2] + cb));
+            rb[i][1] = bf16f(__ldg(s.tp[v][1] + cb));
+            rb[i][2] = bf16f(__ldg(s.tp[v][0] + cb));
+            rb[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cb));
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = j0 + i;
+        if (j < nu) {
+          float x = 0.f;
+          if (live) {
+            x = rx[i][0];
+            if (xcv[i]) {
+              x = conv4_silu(wx, bx, rx[i][0], rx[i][1], rx[i][2], rx[i][3]);
+              a.log_x[(node0 + s.ls.snode[j]) * d_inner + cx] = x;
+            }
+          }
+          xu[j * PROWS + tid] = x;
+        }
+        if (j < nbj) {
+          float val = rb[i][0];
+          if (bcv[i]) val = conv4_silu(wb, bb, rb[i][0], rb[i][1], rb[i][2], rb[i][3]);
+          if (tid < kN) {
+            Bu[j * kN + tid] = val;
+            if (bcv[i] && blk == 0) a.log_B[(node0 + s.ls.snode[j]) * kN + tid] = val;
+          } else {
+            Cf[j * kN + tid - kN] = val;
+          }
+        }
+      }
+    }
+    if (d_sl >= 0) {
+      if (d_conv) {
+        dval = softplus_f(dval);
+        a.log_delta[(node0 + s.ls.snode[d_sl]) * H + h_begin + d_g] = dval;
+      }
+      du[d_sl * PG + d_g] = dval;
     }
   }
-
-  const uint16_t* xbc = a.xBC + node0 * conv_dim;
-  const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
-  const int head = a.ring_head[inst];
-  const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
-  const float* cb = a.conv_b + (size_t)layer * conv_dim;
-  constexpr int JOBS = TROWS + 2 * kN;  // per node: the pair's x channels, then B and C
-
-  for (int f0 = 0; f0 < nf; f0 += FB) {
-    const int fc = min(FB, nf - f0);
-    // conv + SiLU of the pass's nodes, their Δ, and their log rows
-    for (int job = tid; job < FB * JOBS; job += TTHREADS) {
-      const int f = job / JOBS, cl = job - f * JOBS;
-      if (f >= fc) {
-        if (cl >= TROWS + kN) s.Cf[f][cl - TROWS - kN] = 0.f;
-        continue;
-      }
-      const int v = s.front[f0 + f];
-      int c;
-      if (cl < TROWS) {
-        if (cl >= rows) {
-          s.xu[s.slot[v]][cl] = 0.f;
-          continue;
-        }
-        c = h_begin * kP + cl;
-      } else {
-        c = d_inner + (cl - TROWS);
-      }
-      const float post = node_conv(xbc, ring, head, a.R, conv_dim, s.tap[v], v, c, cw[c], cb[c]);
-      if (cl < TROWS) {
-        s.xu[s.slot[v]][cl] = post;
-        a.log_x[(node0 + v) * d_inner + c] = post;
-      } else {
-        const int j = cl - TROWS;
-        if (j < kN) {
-          s.Bf[f][j] = post;
-          if (grp == 0) a.log_B[(node0 + v) * kN + j] = post;
-        } else {
-          s.Cf[f][j - kN] = post;
-        }
-      }
+  __syncthreads();
+  // S of every slot (walking its path to the root) and each level node's path as slots
+  for (int i = tid; i < nu * PG; i += TTHREADS) {
+    const int sl = i / PG, g = i - sl * PG;
+    float acc = 0.f;
+    for (int u = s.ls.snode[sl]; u >= 0; u = s.ls.par[u]) acc = fmaf(du[s.ls.slot[u] * PG + g], s.A[g], acc);
+    su[sl * PG + g] = acc;
+  }
+  for (int f = tid; f < nf; f += TTHREADS) {
+    int u = s.ls.front[f];
+    const int len = s.ls.dep[u] + 1;
+    for (int k = len - 1; k >= 0; --k) {
+      pslot[f * MAXP + k] = s.ls.slot[u];
+      u = s.ls.par[u];
     }
-    if (tid < FB * TG) {
-      const int f = tid / TG, g = tid - f * TG;
-      if (f < fc) {
-        const int v = s.front[f0 + f];
-        float d = 0.f;
-        if (g < heads) {
-          const int h = h_begin + g;
-          d = softplus_f(bf16f(a.dt[(node0 + v) * a.H + h]) + a.dt_bias[(size_t)layer * a.H + h]);
-          a.log_delta[(node0 + v) * a.H + h] = d;
-        }
-        s.du[s.slot[v]][g] = d;
-      }
+    plen[f] = len;
+  }
+  __syncthreads();
+  float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
+  float* wsC = wsi;                          // [n][kN]
+  float* wsE = wsi + ws_E_off(n);            // [n][H]
+  float* wsP = wsi + ws_P_off(n, H);         // [n][d_inner]
+  // e^{S_v}; C rows (first block); the path coefficients: one warp per (node, path index)
+  for (int i = tid; i < nf * PG; i += TTHREADS) {
+    const int f = i / PG, g = i - f * PG;
+    if (g < heads) wsE[(size_t)s.ls.front[f] * H + h_begin + g] = expf(su[pslot[f * MAXP + plen[f] - 1] * PG + g]);
+  }
+  if (blk == 0)
+    for (int i = tid; i < nf * (kN / 4); i += TTHREADS) {
+      const int f = i / (kN / 4), q = i - f * (kN / 4);
+      reinterpret_cast<float4*>(wsC + (size_t)s.ls.front[f] * kN)[q] = reinterpret_cast<const float4*>(Cf + f * kN)[q];
     }
-    __syncthreads();
-    if (tid < FB * TG) {  // S of the pass's nodes (their parents are ancestors)
-      const int f = tid / TG, g = tid - f * TG;
-      if (f < fc) {
-        const int v = s.front[f0 + f], p = s.par[v], sl = s.slot[v];
-        s.su[sl][g] = (p >= 0 ? s.su[s.slot[p]][g] : 0.f) + s.du[sl][g] * s.A[g];
-      }
-    }
-    if (tid < FB) {  // each pass node's path, root first
-      int len = 0;
-      if (tid < fc) {
-        const int v = s.front[f0 + tid];
-        len = s.dep[v] + 1;
-        int u = v;
-        for (int k = len - 1; k >= 0; --k) {
-          s.pnode[tid][k] = u;
-          s.pslot[tid][k] = s.slot[u];
-          u = s.par[u];
-        }
-      }
-      s.plen[tid] = len;
-    }
-    __syncthreads();
-    // B_m · C_v along each path: one warp per (node, path position)
-    for (int q = warp; q < FB * MAXP; q += TTHREADS / 32) {
-      const int f = q / MAXP, k = q - f * MAXP;
-      if (f >= fc || k >= s.plen[f]) continue;
-      float4 b4;
-      if (k == s.plen[f] - 1)
-        b4 = reinterpret_cast<const float4*>(s.Bf[f])[lane];
-      else
-        b4 = __ldg(reinterpret_cast<const float4*>(a.log_B + (node0 + s.pnode[f][k]) * kN) + lane);
-      const float4 c4 = reinterpret_cast<const float4*>(s.Cf[f])[lane];
-      float d = b4.x * c4.x;
-      d = fmaf(b4.y, c4.y, d);
-      d = fmaf(b4.z, c4.z, d);
-      d = fmaf(b4.w, c4.w, d);
-      d = warp_sum(d);
-      if (lane == 0) s.bc[f][k] = d;
-    }
-    __syncthreads();
-    {
-      static_assert(FB * MAXP * TG == TTHREADS, "one coefficient per thread");
-      const int f = tid / (MAXP * TG), rem = tid - f * (MAXP * TG), k = rem / TG, g = rem - k * TG;
-      if (f < fc && k < s.plen[f]) {
-        const int sv = s.pslot[f][s.plen[f] - 1], sm = s.pslot[f][k];
-        s.coef[f][k][g] = expf(s.su[sv][g] - s.su[sm][g]) * s.du[sm][g] * s.bc[f][k];
-      }
-      if (tid < FB * TG) {
-        const int ff = tid / TG, gg = tid - ff * TG;
-        if (ff < fc) s.E[ff][gg] = expf(s.su[s.slot[s.front[f0 + ff]]][gg]);
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < FB * TROWS; i += TTHREADS) {
-      const int f = i / TROWS, r = i - f * TROWS;
+  for (int q = warp; q < nf * MAXP; q += TTHREADS / 32) {
+    const int f = q / MAXP, k = q - f * MAXP;
+    if (k >= plen[f]) continue;
+    const int sm = pslot[f * MAXP + k], sv = pslot[f * MAXP + plen[f] - 1];
+    const float4 b4 = reinterpret_cast<const float4*>(Bu + sm * kN)[lane];
+    const float4 c4 = reinterpret_cast<const float4*>(Cf + f * kN)[lane];
+    float d = b4.x * c4.x;
+    d = fmaf(b4.y, c4.y, d);
+    d = fmaf(b4.z, c4.z, d);
+    d = fmaf(b4.w, c4.w, d);
+    d = warp_sum(d);
+    if (lane < PG) coef[(f * MAXP + k) * PG + lane] = expf(su[sv * PG + lane] - su[sm * PG + lane]) * du[sm * PG + lane] * d;
+  }
+  __syncthreads();
+  // path sums of the block's rows: Σ_k coef_k x_{m_k}[row] + D x_v[row]
+  if (tid < rows) {
+    const int g = tid / kP;
+    for (int f = 0; f < nf; ++f) {
+      const int len = plen[f];
       float b = 0.f;
-      if (f < fc && r < rows) {
-        const int g = r / kP, len = s.plen[f];
-        for (int k = 0; k < len; ++k) b = fmaf(s.coef[f][k][g], s.xu[s.pslot[f][k]][r], b);
-        b = fmaf(s.Dh[g], s.xu[s.pslot[f][len - 1]][r], b);
-      }
-      s.base[f][r] = b;
+      for (int k = 0; k < len; ++k) b = fmaf(coef[(f * MAXP + k) * PG + g], xu[pslot[f * MAXP + k] * PROWS + tid], b);
+      b = fmaf(s.Dh[g], xu[pslot[f * MAXP + len - 1] * PROWS + tid], b);
+      wsP[(size_t)s.ls.front[f] * d_inner + h_begin * kP + tid] = b;
     }
-    __syncthreads();
-    // y_v = e^{S_v} (C_v · h_ckpt) + base, from the state values held in registers; each
-    // C float4 is read once and used for all of the thread's rows
-    float acc[TSWEEPS][FB];
+  }
+}
+
+constexpr int MTHREADS = 128;                    // level kernel: one head, 8 lanes per row
+constexpr int MSWEEPS = kP / (MTHREADS / 8);      // 4 sweeps of 16 rows
+
+struct MainFixed {
+  unsigned long long bar;  // completion of the state-row copy
+  LevelSetup ls;
+};
+__host__ __device__ inline int main_h_offset() { return (int)((sizeof(MainFixed) + 127) & ~(size_t)127); }
+__host__ __device__ inline int level_smem_bytes() { return main_h_offset() + kP * kN * 4; }
+
+__global__ void __launch_bounds__(MTHREADS, 6) draft_tree_level_kernel(DraftTreeArgs a, const float* ws) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  MainFixed& s = *reinterpret_cast<MainFixed*>(smem);
+  float* hsm = reinterpret_cast<float*>(smem + main_h_offset());
+  const int n = a.n;
+  const int tid = threadIdx.x, warp = tid >> 5, o = tid & 7, rsub = tid >> 3;
+  const int H = a.H, d_inner = H * kP;
+  const int hh = blockIdx.x % H;
+  const long long inst = blockIdx.x / H;
+  const int seq = (int)(inst / a.L);
+  const size_t node0 = (size_t)inst * n;
+  const uint32_t bar = smem_u32(&s.bar);
+
+  if (tid == 0) {  // the head's 64 committed state rows (32 KB), copied while the CTA waits
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, (uint32_t)(kP * kN * 4));
+    bulk_load(smem_u32(hsm), a.h + ((size_t)inst * H + hh) * kP * kN, (uint32_t)(kP * kN * 4), bar);
+  }
+  if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, false);
+  __syncthreads();
+  const int nf = s.ls.nf;
+  bool ok = true;
+  if (nf > 0) {
+    grid_dependency_wait();  // the prep grid's workspace rows
+    ok = mbar_wait(bar, 0);
+  } else {
+    ok = mbar_wait(bar, 0);  // nothing to do; the copy must land before the CTA exits
+  }
+  if (!ok) {
+    if (tid == 0) flag(a.status, SSM_STATUS_TIMEOUT);
+    mbar_wait(bar, 0);
+    return;
+  }
+  if (nf == 0) return;
+  const float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
+  const float* wsE = wsi + ws_E_off(n);
+  const float* wsP = wsi + ws_P_off(n, H);
+  // y_v = e^{S_v} (C_v · h_ckpt) + path sum, 8 level nodes per pass; C rows are read through
+  // the cache (shared by the instance's heads), the state rows from shared memory
+  for (int f0 = 0; f0 < nf; f0 += FB) {
+    float acc[MSWEEPS][FB];
 #pragma unroll
-    for (int i = 0; i < TSWEEPS; ++i)
+    for (int i = 0; i < MSWEEPS; ++i)
 #pragma unroll
       for (int f = 0; f < FB; ++f) acc[i][f] = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      float4 hr[MSWEEPS];
+#pragma unroll
+      for (int i = 0; i < MSWEEPS; ++i) hr[i] = reinterpret_cast<const float4*>(hsm + (rsub + 16 * i) * kN)[o + 8 * j];
 #pragma unroll
       for (int f = 0; f < FB; ++f) {
-        const float4 c = reinterpret_cast<const float4*>(s.Cf[f])[o + 8 * j];
+        const float4 cc = f0 + f < nf
+                              ? __ldg(reinterpret_cast<const float4*>(wsi + (size_t)s.ls.front[f0 + f] * kN) + o + 8 * j)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < TSWEEPS; ++i) {
-          acc[i][f] = fmaf(hv[i][j].x, c.x, acc[i][f]);
-          acc[i][f] = fmaf(hv[i][j].y, c.y, acc[i][f]);
-          acc[i][f] = fmaf(hv[i][j].z, c.z, acc[i][f]);
-          acc[i][f] = fmaf(hv[i][j].w, c.w, acc[i][f]);
+        for (int i = 0; i < MSWEEPS; ++i) {
+          acc[i][f] = fmaf(hr[i].x, cc.x, acc[i][f]);
+          acc[i][f] = fmaf(hr[i].y, cc.y, acc[i][f]);
+          acc[i][f] = fmaf(hr[i].z, cc.z, acc[i][f]);
+          acc[i][f] = fmaf(hr[i].w, cc.w, acc[i][f]);
         }
       }
     }
+    const int f = f0 + o;
+    const int v = f < nf ? s.ls.front[f] : 0;
+    const float e = f < nf ? __ldg(wsE + (size_t)v * H + hh) : 0.f;
 #pragma unroll
-    for (int i = 0; i < TSWEEPS; ++i) {
-      const int row = rsub + 32 * i;
+    for (int i = 0; i < MSWEEPS; ++i) {
+      const int row = rsub + 16 * i;
       const float sum = reduce_scatter8(acc[i], o);
-      if (o < fc && row < rows) {
-        const int g = row / kP, v = s.front[f0 + o];
-        a.y[(node0 + v) * d_inner + h_begin * kP + row] = fmaf(s.E[o][g], sum, s.base[o][row]);
+      if (f < nf) {
+        const size_t yo = (node0 + v) * d_inner + (size_t)hh * kP + row;
+        a.y[yo] = fmaf(e, sum, __ldg(wsP + (size_t)v * d_inner + (size_t)hh * kP + row));
       }
     }
-    __syncthreads();  // the next pass rewrites Cf, Bf, xu of its nodes, base
   }
 }
 
@@ -330,9 +490,11 @@ constexpr int CROWS = CH * kP;      // 128 state rows, 16 per warp
 constexpr int CTHREADS = 256;
 constexpr int CT = 16;              // path nodes per pass
 
-// Length of the valid prefix of a sequence's accepted path: path[0] = 0, then each entry a
-// child of the one before, at most max_path entries; anything else is flagged.
+// Length of the valid prefix of a sequence's accepted path (path[0] = 0, then each entry a
+// child of the one before, at most max_path entries), checked by a whole warp at once;
+// anything else is flagged when `report`.  Every lane returns the same value.
 __device__ int tree_path_len(const DraftTreeCommitArgs& a, int seq, bool report) {
+  const int lane = threadIdx.x & 31;
   int len = a.path_len[seq];
   bool bad = false;
   if (len < 0 || len > a.max_path) {
@@ -341,25 +503,35 @@ __device__ int tree_path_len(const DraftTreeCommitArgs& a, int seq, bool report)
   }
   const int32_t* p = a.path + (size_t)seq * a.max_path;
   const ssm_node* lay = a.layout + (size_t)seq * a.n;
-  int prev = -1, good = 0;
-  for (int j = 0; j < len; ++j) {
-    const int v = p[j];
-    const bool ok = j == 0 ? v == 0 : (v > prev && v < a.n && lay[v].parent == prev);
-    if (!ok) {
+  int good = len;
+  for (int base = 0; base < len; base += 32) {
+    const int j = base + lane;
+    bool ok = true;
+    if (j < len) {
+      const int v = p[j];
+      if (j == 0) {
+        ok = v == 0;
+      } else {
+        const int prev = p[j - 1];
+        ok = v > prev && prev >= 0 && v < a.n && lay[v].parent == prev;
+      }
+    }
+    const unsigned fail = __ballot_sync(0xffffffffu, !ok);
+    if (fail) {
+      good = base + __ffs(fail) - 1;
       bad = true;
       break;
     }
-    prev = v;
-    ++good;
   }
-  if (bad && report) flag(a.status, SSM_STATUS_PATH_RANGE);
+  if (bad && report && lane == 0) flag(a.status, SSM_STATUS_PATH_RANGE);
   return good;
 }
 
-__global__ void __launch_bounds__(CTHREADS) draft_tree_commit_kernel(DraftTreeCommitArgs a) {
+__global__ void __launch_bounds__(CTHREADS, 2) draft_tree_commit_kernel(DraftTreeCommitArgs a) {
   __shared__ float us[CT][CROWS];  // Δ_t·x_t[row]
   __shared__ float decs[CT][CH];
-  __shared__ int nodes[CT];
+  __shared__ __align__(16) float Bs[CT][kN];
+  __shared__ int nodes[SSM_MAX_PATH];
   __shared__ int s_len;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_groups = (a.H + CH - 1) / CH;
@@ -369,60 +541,70 @@ __global__ void __launch_bounds__(CTHREADS) draft_tree_commit_kernel(DraftTreeCo
   const int h_begin = grp * CH, heads = min(CH, a.H - h_begin), rows = heads * kP;
   const int d_inner = a.H * kP;
   const size_t node0 = (size_t)inst * a.n;
-  if (tid == 0) s_len = tree_path_len(a, seq, grp == 0 && layer == 0);
-  __syncthreads();
-  const int len = s_len;
   float* hs = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
   const int row0 = warp * (CROWS / 8);
   const int g = row0 / kP;
-
+  const bool mine = g < heads;
+  // the warp's 16 rows, all in flight while the path is checked and the log staged
+  float4 hr[16];
+  if (mine) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) hr[r] = reinterpret_cast<const float4*>(hs + (size_t)(row0 + r) * kN)[lane];
+  }
+  if (warp == 0) {
+    const int len = tree_path_len(a, seq, grp == 0 && layer == 0);
+    for (int j = lane; j < len; j += 32) nodes[j] = a.path[(size_t)seq * a.max_path + j];
+    if (lane == 0) s_len = len;
+  }
+  __syncthreads();
+  const int len = s_len;
+  if (len == 0) return;
+  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid & 1, heads - 1)]);
   for (int t0 = 0; t0 < len; t0 += CT) {
     const int cnt = min(CT, len - t0);
-    if (t0 > 0) __syncthreads();  // the previous pass is done with nodes, us, decs
-    if (tid < cnt) nodes[tid] = a.path[(size_t)seq * a.max_path + t0 + tid];
-    __syncthreads();
-    for (int i = tid; i < cnt * CROWS; i += CTHREADS) {
-      const int t = i / CROWS, r = i - t * CROWS;
-      float u = 0.f;
-      if (r < rows) {
-        const size_t lr = node0 + nodes[t];
-        u = __fmul_rn(a.log_delta[lr * a.H + h_begin + r / kP], a.log_x[lr * d_inner + h_begin * kP + r]);
-      }
-      us[t][r] = u;
-    }
-    if (tid < cnt * CH) {
-      const int t = tid / CH, gg = tid - t * CH;
-      float e = 1.f;
-      if (gg < heads) {
-        const int h = h_begin + gg;
-        e = decay_of(a.log_delta[(node0 + nodes[t]) * a.H + h], neg_exp(a.A_log[(size_t)layer * a.H + h]));
-      }
-      decs[t][gg] = e;
-    }
-    float4 bt[CT];
+    if (t0 > 0) __syncthreads();  // the previous pass is done with us, decs, Bs
+    // every log value of the pass in flight at once: Δ and x for (row, step) pairs, B rows,
+    // then the products and decays into shared memory
+    const int r = tid & (CROWS - 1), th = tid >> 7;
+    float dl[CT / 2], xv[CT / 2];
 #pragma unroll
-    for (int t = 0; t < CT; ++t)
-      bt[t] = t < cnt ? __ldg(reinterpret_cast<const float4*>(a.log_B + (node0 + nodes[t]) * kN) + lane)
+    for (int j = 0; j < CT / 2; ++j) {
+      const int t = th + 2 * j;
+      dl[j] = 0.f;
+      xv[j] = 0.f;
+      if (t < cnt && r < rows) {
+        const size_t lr = node0 + nodes[t0 + t];
+        dl[j] = a.log_delta[lr * a.H + h_begin + r / kP];
+        xv[j] = a.log_x[lr * d_inner + h_begin * kP + r];
+      }
+    }
+    float4 bv[CT * (kN / 4) / CTHREADS];
+#pragma unroll
+    for (int q = 0; q < CT * (kN / 4) / CTHREADS; ++q) {
+      const int i = tid + q * CTHREADS, t = i / (kN / 4), c4 = i - t * (kN / 4);
+      bv[q] = t < cnt ? reinterpret_cast<const float4*>(a.log_B + (node0 + nodes[t0 + t]) * kN)[c4]
                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    __syncthreads();
-    if (g < heads) {
-      float4 nx = reinterpret_cast<const float4*>(hs + (size_t)row0 * kN)[lane];
-      for (int r = row0; r < row0 + CROWS / 8; ++r) {  // one row in work, the next in flight
-        float4 h = nx;
-        if (r + 1 < row0 + CROWS / 8) nx = reinterpret_cast<const float4*>(hs + (size_t)(r + 1) * kN)[lane];
-#pragma unroll
-        for (int t = 0; t < CT; ++t) {
-          if (t < cnt) {
-            const float u = us[t][r], dec = decs[t][g];
-            h.x = ssm_update(dec, h.x, u, bt[t].x);
-            h.y = ssm_update(dec, h.y, u, bt[t].y);
-            h.z = ssm_update(dec, h.z, u, bt[t].z);
-            h.w = ssm_update(dec, h.w, u, bt[t].w);
-          }
-        }
-        reinterpret_cast<float4*>(hs + (size_t)r * kN)[lane] = h;
-      }
     }
+    float dd = 0.f;
+    const int dt_ = tid / CH, dg = tid - dt_ * CH;
+    if (tid < cnt * CH && dg < heads) dd = a.log_delta[(node0 + nodes[t0 + dt_]) * a.H + h_begin + dg];
+#pragma unroll
+    for (int j = 0; j < CT / 2; ++j) {
+      const int t = th + 2 * j;
+      if (t < cnt) us[t][r] = __fmul_rn(dl[j], xv[j]);
+    }
+#pragma unroll
+    for (int q = 0; q < CT * (kN / 4) / CTHREADS; ++q) {
+      const int i = tid + q * CTHREADS, t = i / (kN / 4), c4 = i - t * (kN / 4);
+      reinterpret_cast<float4*>(Bs[t])[c4] = bv[q];
+    }
+    if (tid < cnt * CH) decs[dt_][dg] = dg < heads ? decay_of(dd, A_g) : 1.f;
+    __syncthreads();
+    if (mine) apply_logged_updates(hr, cnt, &us[0][0], CROWS, row0, &Bs[0][0], &decs[0][g], CH, lane);
+  }
+  if (mine) {
+#pragma unroll
+    for (int r = 0; r < 16; ++r) reinterpret_cast<float4*>(hs + (size_t)(row0 + r) * kN)[lane] = hr[r];
   }
 }
 
@@ -432,13 +614,15 @@ __global__ void draft_tree_ring_kernel(DraftTreeCommitArgs a) {
   const long long inst = blockIdx.x;
   const int seq = (int)(inst / a.L);
   const int conv_dim = a.H * kP + 2 * kN;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
     const int len = tree_path_len(a, seq, false);
-    s_len = len;
-    s_head = a.ring_head[inst];
-    for (int j = 0; j < 3; ++j) {
-      const int jj = len - 3 + j;
-      rows3[j] = jj >= 0 ? a.path[(size_t)seq * a.max_path + jj] : -1;
+    if (threadIdx.x == 0) {
+      s_len = len;
+      s_head = a.ring_head[inst];
+      for (int j = 0; j < 3; ++j) {
+        const int jj = len - 3 + j;
+        rows3[j] = jj >= 0 ? a.path[(size_t)seq * a.max_path + jj] : -1;
+      }
     }
   }
   __syncthreads();
@@ -459,15 +643,35 @@ __global__ void draft_tree_ring_kernel(DraftTreeCommitArgs a) {
 
 }  // namespace
 
-cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, cudaStream_t s) {
+size_t draft_tree_workspace_bytes(int n, int H, long long n_inst) {
+  return (size_t)n_inst * ws_floats_per_inst(n, H) * sizeof(float);
+}
+
+cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, void* workspace, cudaStream_t s) {
   const long long inst = (long long)a.n_seq * a.L;
   if (inst == 0) return cudaSuccess;
-  const int n_groups = (a.H + TG - 1) / TG;
-  const int smem = (int)sizeof(LevelSmem);
-  cudaError_t e = cudaFuncSetAttribute(draft_tree_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  float* ws = static_cast<float*>(workspace);
+  const int n_blocks = (a.H + PG - 1) / PG;
+  const int psmem = prep_layout(a.n).total;
+  cudaError_t e = cudaFuncSetAttribute(draft_tree_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
   if (e != cudaSuccess) return e;
-  draft_tree_level_kernel<<<(unsigned)(inst * n_groups), TTHREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  draft_tree_prep_kernel<<<(unsigned)(inst * n_blocks), TTHREADS, psmem, s>>>(a, ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int smem = level_smem_bytes();
+  e = cudaFuncSetAttribute(draft_tree_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(inst * a.H));
+  cfg.blockDim = dim3(MTHREADS);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the prep runs
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, draft_tree_level_kernel, a, static_cast<const float*>(ws));
 }
 
 cudaError_t launch_draft_tree_commit(const DraftTreeCommitArgs& a, cudaStream_t s) {

@@ -18,7 +18,9 @@ struct DraftTreeArgs {
   float* y;                             // [I][n][d_inner]
   int32_t* status;
 };
-cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, cudaStream_t s);
+// workspace: per instance the level's C rows, e^{S_v} and path sums, draft_tree_workspace_bytes()
+size_t draft_tree_workspace_bytes(int n, int H, long long n_inst);
+cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, void* workspace, cudaStream_t s);
 
 // The accepted path's logged updates into the committed draft state, its rows into the ring.
 struct DraftTreeCommitArgs {

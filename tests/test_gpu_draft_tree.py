@@ -36,8 +36,9 @@ def upload(b, w):
 
 
 def draft_levels(d, levels=None):
-    from speculative_decoding_mamba2_gb300 import ssm_draft_tree_level
+    from speculative_decoding_mamba2_gb300 import ssm_draft_tree_level, ssm_draft_tree_workspace_size
     dims, I, n = d["dims"], d["I"], d["n"]
+    ws = torch.empty(ssm_draft_tree_workspace_size(dims, d["S"], n), dtype=torch.uint8, device="cuda")
     logs = dict(delta=torch.full((I, n, dims.n_heads), float("nan"), device="cuda"),
                 B=torch.full((I, n, dims.d_state), float("nan"), device="cuda"),
                 x=torch.full((I, n, dims.d_inner), float("nan"), device="cuda"))
@@ -45,7 +46,7 @@ def draft_levels(d, levels=None):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for lv in (range(d["depth"] + 1) if levels is None else levels):
         ssm_draft_tree_level(dims, d["prm"], d["S"], n, lv, d["layout"], d["xBC"], d["dt"], d["h"], d["ring"],
-                             d["head"], logs["delta"], logs["B"], logs["x"], y, status)
+                             d["head"], logs["delta"], logs["B"], logs["x"], y, ws, status)
     torch.cuda.synchronize()
     return y, logs, status
 
