@@ -402,7 +402,7 @@ struct MainFixed {
 __host__ __device__ inline int main_h_offset() { return (int)((sizeof(MainFixed) + 127) & ~(size_t)127); }
 __host__ __device__ inline int level_smem_bytes() { return main_h_offset() + kP * kN * 4; }
 
-__global__ void __launch_bounds__(MTHREADS, 6) draft_tree_level_kernel(DraftTreeArgs a, const float* ws) {
+__global__ void __launch_bounds__(MTHREADS, 5) draft_tree_level_kernel(DraftTreeArgs a, const float* ws) {
   extern __shared__ __align__(128) unsigned char smem[];
   MainFixed& s = *reinterpret_cast<MainFixed*>(smem);
   float* hsm = reinterpret_cast<float*>(smem + main_h_offset());
