@@ -137,10 +137,10 @@ __global__ void __launch_bounds__(DTHREADS) draft_step_kernel(DraftArgs a) {
 // head, B per step) and applies them with the draft step's operations
 // (apply_logged_updates)
 // ---------------------------------------------------------------------------
-constexpr int RW = 8;               // warps per CTA
+constexpr int RW = 4;               // warps per CTA
 constexpr int RTHREADS = RW * 32;
-constexpr int RH = 2;               // heads per CTA
-constexpr int RROWS = RH * kP;      // 128 state rows, 16 per warp
+constexpr int RH = 1;               // heads per CTA
+constexpr int RROWS = RH * kP;      // 64 state rows, 16 per warp
 constexpr int RT = 16;              // logged steps per pass
 
 __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool report) {
@@ -154,7 +154,7 @@ __device__ __forceinline__ int replay_k(const ReplayArgs& a, int inst, bool repo
   return k;
 }
 
-__global__ void __launch_bounds__(RTHREADS, 2) replay_kernel(ReplayArgs a) {
+__global__ void __launch_bounds__(RTHREADS, 4) replay_kernel(ReplayArgs a) {
   __shared__ float us[RT][RROWS];  // u = Δ_t·x_t[row]
   __shared__ float decs[RT][RH];
   __shared__ __align__(16) float Bs[RT][kN];
@@ -178,13 +178,14 @@ __global__ void __launch_bounds__(RTHREADS, 2) replay_kernel(ReplayArgs a) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) hr[r] = reinterpret_cast<const float4*>(hs + (size_t)(row0 + r) * kN)[lane];
   }
-  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid & 1, heads - 1)]);
+  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid % RH, heads - 1)]);
   for (int t0 = 0; t0 < k; t0 += RT) {
     const int cnt = min(RT, k - t0);
     if (t0 > 0) __syncthreads();  // the previous pass is done with us, decs, Bs
     // every log value of the pass in flight at once: Δ and x for (row, step) pairs, B rows,
     // then the products and decays into shared memory
-    const int r = tid & (RROWS - 1), th = tid >> 7;
+    static_assert(RTHREADS == 2 * RROWS, "two threads per row, each half of the steps");
+    const int r = tid % RROWS, th = tid / RROWS;
     float dl[RT / 2], xv[RT / 2];
 #pragma unroll
     for (int j = 0; j < RT / 2; ++j) {

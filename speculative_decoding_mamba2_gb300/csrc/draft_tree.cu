@@ -392,102 +392,135 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
   }
 }
 
-constexpr int MTHREADS = 128;                    // level kernel: one head, 8 lanes per row
-constexpr int MSWEEPS = kP / (MTHREADS / 8);      // 4 sweeps of 16 rows
+constexpr int MTHREADS = 256;                    // level kernel: 8 lanes per row, 32 rows per sweep
+constexpr int MSWEEPS = kP / (MTHREADS / 8);      // 2 sweeps cover one head's 64 rows
+constexpr int MSTAGES = 3;                        // heads' state rows in flight per CTA
 
 struct MainFixed {
-  unsigned long long bar;  // completion of the state-row copy
+  unsigned long long bar[MSTAGES];  // completion of each stage's state-row copy
   LevelSetup ls;
+  int seq_ready;                    // the sequence whose layout ls holds
+  int ok;                           // the current stage's copy has landed
+  int issued;                       // items whose copies have been issued
 };
 __host__ __device__ inline int main_h_offset() { return (int)((sizeof(MainFixed) + 127) & ~(size_t)127); }
-__host__ __device__ inline int level_smem_bytes() { return main_h_offset() + kP * kN * 4; }
+__host__ __device__ inline int level_smem_bytes() { return main_h_offset() + MSTAGES * kP * kN * 4; }
 
-__global__ void __launch_bounds__(MTHREADS, 5) draft_tree_level_kernel(DraftTreeArgs a, const float* ws) {
+// Persistent: CTA c takes the contiguous run of (instance, head) items
+// [c·items/G, (c+1)·items/G), G = the grid, and keeps the next MSTAGES heads' 64 state rows in
+// flight (bulk copies into a ring of shared-memory stages, one mbarrier each) while it
+// computes the current one, so the memory pipe never waits for the compute.
+__global__ void __launch_bounds__(MTHREADS, 2) draft_tree_level_kernel(DraftTreeArgs a, const float* ws) {
   extern __shared__ __align__(128) unsigned char smem[];
   MainFixed& s = *reinterpret_cast<MainFixed*>(smem);
-  float* hsm = reinterpret_cast<float*>(smem + main_h_offset());
+  float* stages = reinterpret_cast<float*>(smem + main_h_offset());
   const int n = a.n;
   const int tid = threadIdx.x, warp = tid >> 5, o = tid & 7, rsub = tid >> 3;
   const int H = a.H, d_inner = H * kP;
-  const int hh = blockIdx.x % H;
-  const long long inst = blockIdx.x / H;
-  const int seq = (int)(inst / a.L);
-  const size_t node0 = (size_t)inst * n;
-  const uint32_t bar = smem_u32(&s.bar);
+  const long long items = (long long)a.n_seq * a.L * H;
+  const long long it0 = blockIdx.x * items / gridDim.x, it1 = (blockIdx.x + 1) * items / gridDim.x;
+  const int count = (int)(it1 - it0);
+  constexpr uint32_t kBytes = kP * kN * 4;
 
-  if (tid == 0) {  // the head's 64 committed state rows (32 KB), copied while the CTA waits
-    mbar_init(bar, 1);
+  auto issue = [&](int k) {  // the k-th item of this CTA into stage k mod MSTAGES
+    const long long it = it0 + k;
+    const uint32_t bar = smem_u32(&s.bar[k % MSTAGES]);
+    mbar_arrive_expect_tx(bar, kBytes);
+    bulk_load(smem_u32(stages + (size_t)(k % MSTAGES) * kP * kN), a.h + (size_t)it * kP * kN, kBytes, bar);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < MSTAGES; ++st) mbar_init(smem_u32(&s.bar[st]), 1);
     fence_barrier_init();
-    mbar_arrive_expect_tx(bar, (uint32_t)(kP * kN * 4));
-    bulk_load(smem_u32(hsm), a.h + ((size_t)inst * H + hh) * kP * kN, (uint32_t)(kP * kN * 4), bar);
+    for (int k = 0; k < MSTAGES && k < count; ++k) issue(k);
+    s.issued = count < MSTAGES ? count : MSTAGES;
+    s.seq_ready = -1;
   }
-  if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, false);
   __syncthreads();
-  const int nf = s.ls.nf;
-  bool ok = true;
-  if (nf > 0) {
-    grid_dependency_wait();  // the prep grid's workspace rows
-    ok = mbar_wait(bar, 0);
-  } else {
-    ok = mbar_wait(bar, 0);  // nothing to do; the copy must land before the CTA exits
-  }
-  if (!ok) {
-    if (tid == 0) flag(a.status, SSM_STATUS_TIMEOUT);
-    mbar_wait(bar, 0);
-    return;
-  }
-  if (nf == 0) return;
-  const float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
-  const float* wsE = wsi + ws_E_off(n);
-  const float* wsP = wsi + ws_P_off(n, H);
-  // y_v = e^{S_v} (C_v · h_ckpt) + path sum, 8 level nodes per pass; C rows are read through
-  // the cache (shared by the instance's heads), the state rows from shared memory
-  for (int f0 = 0; f0 < nf; f0 += FB) {
-    float acc[MSWEEPS][FB];
+  grid_dependency_wait();  // the prep grid's workspace rows and log rows
+  int k_fail = -1;
+  for (int k = 0; k < count; ++k) {
+    const long long it = it0 + k;
+    const long long inst = it / H;
+    const int hh = (int)(it - inst * H);
+    const int seq = (int)(inst / a.L);
+    if (seq != s.seq_ready) {  // this sequence's level nodes (uniform across the CTA)
+      __syncthreads();
+      if (warp == 0) {
+        level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, false);
+        if (tid == 0) s.seq_ready = seq;
+      }
+      __syncthreads();
+    }
+    const int nf = s.ls.nf;
+    const float* hsm = stages + (size_t)(k % MSTAGES) * kP * kN;
+    if (tid == 0) s.ok = mbar_wait(smem_u32(&s.bar[k % MSTAGES]), (uint32_t)((k / MSTAGES) & 1));
+    __syncthreads();
+    if (!s.ok) {  // uniform across the CTA
+      k_fail = k;
+      break;
+    }
+    const size_t node0 = (size_t)inst * n;
+    const float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
+    const float* wsE = wsi + ws_E_off(n);
+    const float* wsP = wsi + ws_P_off(n, H);
+    // y_v = e^{S_v} (C_v · h_ckpt) + path sum, 8 level nodes per pass; C rows through the
+    // cache (shared by the instance's heads), the state rows from the stage
+    for (int f0 = 0; f0 < nf; f0 += FB) {
+      float acc[MSWEEPS][FB];
 #pragma unroll
-    for (int i = 0; i < MSWEEPS; ++i)
+      for (int i = 0; i < MSWEEPS; ++i)
 #pragma unroll
-      for (int f = 0; f < FB; ++f) acc[i][f] = 0.f;
+        for (int f = 0; f < FB; ++f) acc[i][f] = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float4 hr[MSWEEPS];
+      for (int j = 0; j < 4; ++j) {
+        float4 hr[MSWEEPS];
 #pragma unroll
-      for (int i = 0; i < MSWEEPS; ++i) hr[i] = reinterpret_cast<const float4*>(hsm + (rsub + 16 * i) * kN)[o + 8 * j];
+        for (int i = 0; i < MSWEEPS; ++i) hr[i] = reinterpret_cast<const float4*>(hsm + (rsub + 32 * i) * kN)[o + 8 * j];
 #pragma unroll
-      for (int f = 0; f < FB; ++f) {
-        const float4 cc = f0 + f < nf
-                              ? __ldg(reinterpret_cast<const float4*>(wsi + (size_t)s.ls.front[f0 + f] * kN) + o + 8 * j)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int f = 0; f < FB; ++f) {
+          const float4 cc = f0 + f < nf
+                                ? __ldg(reinterpret_cast<const float4*>(wsi + (size_t)s.ls.front[f0 + f] * kN) + o + 8 * j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < MSWEEPS; ++i) {
-          acc[i][f] = fmaf(hr[i].x, cc.x, acc[i][f]);
-          acc[i][f] = fmaf(hr[i].y, cc.y, acc[i][f]);
-          acc[i][f] = fmaf(hr[i].z, cc.z, acc[i][f]);
-          acc[i][f] = fmaf(hr[i].w, cc.w, acc[i][f]);
+          for (int i = 0; i < MSWEEPS; ++i) {
+            acc[i][f] = fmaf(hr[i].x, cc.x, acc[i][f]);
+            acc[i][f] = fmaf(hr[i].y, cc.y, acc[i][f]);
+            acc[i][f] = fmaf(hr[i].z, cc.z, acc[i][f]);
+            acc[i][f] = fmaf(hr[i].w, cc.w, acc[i][f]);
+          }
+        }
+      }
+      const int f = f0 + o;
+      const int v = f < nf ? s.ls.front[f] : 0;
+      const float e = f < nf ? __ldg(wsE + (size_t)v * H + hh) : 0.f;
+#pragma unroll
+      for (int i = 0; i < MSWEEPS; ++i) {
+        const int row = rsub + 32 * i;
+        const float sum = reduce_scatter8(acc[i], o);
+        if (f < nf) {
+          const size_t yo = (node0 + v) * d_inner + (size_t)hh * kP + row;
+          a.y[yo] = fmaf(e, sum, __ldg(wsP + (size_t)v * d_inner + (size_t)hh * kP + row));
         }
       }
     }
-    const int f = f0 + o;
-    const int v = f < nf ? s.ls.front[f] : 0;
-    const float e = f < nf ? __ldg(wsE + (size_t)v * H + hh) : 0.f;
-#pragma unroll
-    for (int i = 0; i < MSWEEPS; ++i) {
-      const int row = rsub + 16 * i;
-      const float sum = reduce_scatter8(acc[i], o);
-      if (f < nf) {
-        const size_t yo = (node0 + v) * d_inner + (size_t)hh * kP + row;
-        a.y[yo] = fmaf(e, sum, __ldg(wsP + (size_t)v * d_inner + (size_t)hh * kP + row));
-      }
+    __syncthreads();  // every thread is done with this stage
+    if (tid == 0 && k + MSTAGES < count) {
+      issue(k + MSTAGES);
+      s.issued = k + MSTAGES + 1;
     }
+  }
+  if (k_fail >= 0 && tid == 0) {  // give the copies still in flight a last bounded wait before exiting
+    flag(a.status, SSM_STATUS_TIMEOUT);
+    for (int kk = k_fail; kk < s.issued; ++kk) mbar_wait(smem_u32(&s.bar[kk % MSTAGES]), (uint32_t)((kk / MSTAGES) & 1));
   }
 }
 
 // ---------------------------------------------------------------------------
 // commit of the accepted path from the log
 // ---------------------------------------------------------------------------
-constexpr int CH = 2;               // heads per CTA
-constexpr int CROWS = CH * kP;      // 128 state rows, 16 per warp
-constexpr int CTHREADS = 256;
+constexpr int CH = 1;               // heads per CTA
+constexpr int CROWS = CH * kP;      // 64 state rows, 16 per warp
+constexpr int CTHREADS = 128;
 constexpr int CT = 16;              // path nodes per pass
 
 // Length of the valid prefix of a sequence's accepted path (path[0] = 0, then each entry a
@@ -527,7 +560,7 @@ __device__ int tree_path_len(const DraftTreeCommitArgs& a, int seq, bool report)
   return good;
 }
 
-__global__ void __launch_bounds__(CTHREADS, 2) draft_tree_commit_kernel(DraftTreeCommitArgs a) {
+__global__ void __launch_bounds__(CTHREADS, 4) draft_tree_commit_kernel(DraftTreeCommitArgs a) {
   __shared__ float us[CT][CROWS];  // Δ_t·x_t[row]
   __shared__ float decs[CT][CH];
   __shared__ __align__(16) float Bs[CT][kN];
@@ -542,7 +575,7 @@ __global__ void __launch_bounds__(CTHREADS, 2) draft_tree_commit_kernel(DraftTre
   const int d_inner = a.H * kP;
   const size_t node0 = (size_t)inst * a.n;
   float* hs = a.h + ((size_t)inst * a.H + h_begin) * kP * kN;
-  const int row0 = warp * (CROWS / 8);
+  const int row0 = warp * (CROWS / (CTHREADS / 32));
   const int g = row0 / kP;
   const bool mine = g < heads;
   // the warp's 16 rows, all in flight while the path is checked and the log staged
@@ -559,13 +592,14 @@ __global__ void __launch_bounds__(CTHREADS, 2) draft_tree_commit_kernel(DraftTre
   __syncthreads();
   const int len = s_len;
   if (len == 0) return;
-  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid & 1, heads - 1)]);
+  const float A_g = neg_exp(a.A_log[(size_t)layer * a.H + h_begin + min(tid % CH, heads - 1)]);
   for (int t0 = 0; t0 < len; t0 += CT) {
     const int cnt = min(CT, len - t0);
     if (t0 > 0) __syncthreads();  // the previous pass is done with us, decs, Bs
     // every log value of the pass in flight at once: Δ and x for (row, step) pairs, B rows,
     // then the products and decays into shared memory
-    const int r = tid & (CROWS - 1), th = tid >> 7;
+    static_assert(CTHREADS == 2 * CROWS, "two threads per row, each half of the steps");
+    const int r = tid % CROWS, th = tid / CROWS;
     float dl[CT / 2], xv[CT / 2];
 #pragma unroll
     for (int j = 0; j < CT / 2; ++j) {
@@ -661,8 +695,13 @@ cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, void* workspace, cud
   const int smem = level_smem_bytes();
   e = cudaFuncSetAttribute(draft_tree_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const long long items = inst * a.H;
+  const long long grid = items < 2LL * sms ? items : 2LL * sms;  // persistent: two CTAs per SM
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(inst * a.H));
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(MTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
