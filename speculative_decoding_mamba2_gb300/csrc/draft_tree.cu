@@ -124,13 +124,6 @@ __device__ void level_setup(LevelSetup& s, const ssm_node* lay, int n, int level
   }
 }
 
-// Pre-conv value of channel c at tap source src of this instance (node row or ring row).
-__device__ __forceinline__ float tap_ldg(const uint16_t* xbc, const uint16_t* ring, int head, int R, int conv_dim,
-                                         int src, int c) {
-  const uint16_t* p = src >= 0 ? xbc + (size_t)src * conv_dim : ring + (size_t)ring_pos(head, src, R) * conv_dim;
-  return bf16f(__ldg(p + c));
-}
-
 // 8 partial sums per lane, over the 8 lanes o = 0..7 of an aligned lane group: returns
 // the full sum of value o (recursive halving: 4 + 2 + 1 shuffles).
 __device__ __forceinline__ float reduce_scatter8(const float (&v)[FB], int o) {
@@ -168,7 +161,6 @@ __host__ __device__ inline size_t ws_floats_per_inst(int n, int H) {
 
 struct PrepFixed {
   LevelSetup ls;
-  const uint16_t* tp[MAXN][3];  // the pre-conv rows of each node's taps (node row or ring row)
   float A[PG], Dh[PG];
 };
 
@@ -218,6 +210,8 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
   const int H = a.H, d_inner = H * kP, conv_dim = d_inner + 2 * kN;
   const size_t node0 = (size_t)inst * n;
 
+  int hm = a.ring_head[inst] % a.R;  // ring position of the committed head (loaded with the layout)
+  if (hm < 0) hm += a.R;
   if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, blk == 0);
   if (warp == 1 && lane < PG) {
     const bool on = lane < heads;
@@ -225,19 +219,21 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
     s.Dh[lane] = on ? a.D[(size_t)layer * H + h_begin + lane] : 0.f;
   }
   __syncthreads();
-  const int nf = s.ls.nf, nu = s.ls.nu;
+  const int nf = s.ls.nf, nu = s.ls.nu, na = nu - nf;  // slots [0, na): the ancestors; then the level
   if (nf == 0) return;
   const uint16_t* xbc = a.xBC + node0 * conv_dim;
-  if (tid < nf * 3) {  // tap rows of the level's nodes, ring positions resolved once
-    const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
-    const int v = s.ls.front[tid / 3], t = tid % 3, src = s.ls.tap[v][t];
-    s.tp[v][t] = src >= 0 ? xbc + (size_t)src * conv_dim
-                          : ring + (size_t)ring_pos(a.ring_head[inst], src, a.R) * conv_dim;
-  }
-  __syncthreads();
+  const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
+  // pre-conv row of tap source src (an earlier node, or the ring row src positions before the head)
+  auto tap_row = [&](int src) -> const uint16_t* {
+    if (src >= 0) return xbc + (size_t)src * conv_dim;
+    int p = hm + src;
+    if (p < 0) p += a.R;
+    return ring + (size_t)p * conv_dim;
+  };
 
-  // ---- every input in one batch: x (the block's channels) and B for each slot, C for each
-  // level node, Δ for each slot; the level's own values through the conv, and logged ----
+  // ---- every input in one batch per round: x (the block's channels) and B of 8 ancestors
+  // (one logged value each), and x, B or C of 4 level nodes (four taps each, through the
+  // conv + SiLU, logged here); Δ for each slot ----
   {
     const float4* cw4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
     const float* cbv = a.conv_b + (size_t)layer * conv_dim;
@@ -257,7 +253,7 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
       const int v = s.ls.snode[d_sl];
       if (d_g < heads) {
         const int h = h_begin + d_g;
-        if (s.ls.dep[v] < a.level) {
+        if (d_sl < na) {
           dval = __ldg(a.log_delta + (node0 + v) * H + h);
         } else {
           d_conv = true;
@@ -265,62 +261,64 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
         }
       }
     }
-    const int nbj = tid < kN ? nu : nf;  // B jobs: every slot; C jobs: every level node
-    for (int j0 = 0; j0 < nu || j0 < nbj; j0 += 4) {
-      float rx[4][4], rb[4][4];
-      bool xcv[4], bcv[4];
+    for (int r0 = 0; 8 * r0 < na || 4 * r0 < nf; ++r0) {
+      float ax[8], ab[8];      // ancestors 8 r0 .. 8 r0 + 7: logged x, logged B
+      float lx[4][4], lb[4][4];  // level nodes 4 r0 .. 4 r0 + 3: taps of x, of B or C
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        xcv[i] = false;
-        bcv[i] = false;
-        const int j = j0 + i;
-        if (j < nu && live) {
-          const int v = s.ls.snode[j];
-          if (s.ls.dep[v] < a.level) {
-            rx[i][0] = __ldg(a.log_x + (node0 + v) * d_inner + cx);
-          } else {
-            xcv[i] = true;
-            rx[i][0] = bf16f(__ldg(s.tp[v][2] + cx));
-            rx[i][1] = bf16f(__ldg(s.tp[v][1] + cx));
-            rx[i][2] = bf16f(__ldg(s.tp[v][0] + cx));
-            rx[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cx));
-          }
-        }
-        if (j < nbj) {
-          const int v = tid < kN ? s.ls.snode[j] : s.ls.front[j];
-          if (tid < kN && s.ls.dep[v] < a.level) {
-            rb[i][0] = __ldg(a.log_B + (node0 + v) * kN + tid);
-          } else {
-            bcv[i] = true;
-            rb[i][0] = bf16f(__ldg(s.tp[v][2] + cb));
-            rb[i][1] = bf16f(__ldg(s.tp[v][1] + cb));
-            rb[i][2] = bf16f(__ldg(s.tp[v][0] + cb));
-            rb[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cb));
-          }
+      for (int i = 0; i < 8; ++i) {
+        const int sl = 8 * r0 + i;
+        if (sl < na) {
+          const int v = s.ls.snode[sl];
+          if (live) ax[i] = __ldg(a.log_x + (node0 + v) * d_inner + cx);
+          if (tid < kN) ab[i] = __ldg(a.log_B + (node0 + v) * kN + tid);
         }
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int j = j0 + i;
-        if (j < nu) {
+        const int f = 4 * r0 + i;
+        if (f < nf) {
+          const int v = s.ls.front[f];
+          const uint16_t* t2 = tap_row(s.ls.tap[v][2]);
+          const uint16_t* t1 = tap_row(s.ls.tap[v][1]);
+          const uint16_t* t0 = tap_row(s.ls.tap[v][0]);
+          const uint16_t* t3 = xbc + (size_t)v * conv_dim;
+          if (live) {
+            lx[i][0] = bf16f(__ldg(t2 + cx));
+            lx[i][1] = bf16f(__ldg(t1 + cx));
+            lx[i][2] = bf16f(__ldg(t0 + cx));
+            lx[i][3] = bf16f(__ldg(t3 + cx));
+          }
+          lb[i][0] = bf16f(__ldg(t2 + cb));
+          lb[i][1] = bf16f(__ldg(t1 + cb));
+          lb[i][2] = bf16f(__ldg(t0 + cb));
+          lb[i][3] = bf16f(__ldg(t3 + cb));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int sl = 8 * r0 + i;
+        if (sl < na) {
+          xu[sl * PROWS + tid] = live ? ax[i] : 0.f;
+          if (tid < kN) Bu[sl * kN + tid] = ab[i];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int f = 4 * r0 + i;
+        if (f < nf) {
+          const int v = s.ls.front[f], sl = na + f;
           float x = 0.f;
           if (live) {
-            x = rx[i][0];
-            if (xcv[i]) {
-              x = conv4_silu(wx, bx, rx[i][0], rx[i][1], rx[i][2], rx[i][3]);
-              a.log_x[(node0 + s.ls.snode[j]) * d_inner + cx] = x;
-            }
+            x = conv4_silu(wx, bx, lx[i][0], lx[i][1], lx[i][2], lx[i][3]);
+            a.log_x[(node0 + v) * d_inner + cx] = x;
           }
-          xu[j * PROWS + tid] = x;
-        }
-        if (j < nbj) {
-          float val = rb[i][0];
-          if (bcv[i]) val = conv4_silu(wb, bb, rb[i][0], rb[i][1], rb[i][2], rb[i][3]);
+          xu[sl * PROWS + tid] = x;
+          const float val = conv4_silu(wb, bb, lb[i][0], lb[i][1], lb[i][2], lb[i][3]);
           if (tid < kN) {
-            Bu[j * kN + tid] = val;
-            if (bcv[i] && blk == 0) a.log_B[(node0 + s.ls.snode[j]) * kN + tid] = val;
+            Bu[sl * kN + tid] = val;
+            if (blk == 0) a.log_B[(node0 + v) * kN + tid] = val;
           } else {
-            Cf[j * kN + tid - kN] = val;
+            Cf[f * kN + tid - kN] = val;
           }
         }
       }
