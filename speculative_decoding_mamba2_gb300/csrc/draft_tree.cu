@@ -12,20 +12,21 @@
 // writes no state.  The ancestors' Δ, B, x are the log rows their own level wrote.
 //
 // draft_tree_prep_kernel (one CTA per instance and block of 4 heads): one warp finds the
-// level's nodes and the nodes on their paths; then every input is loaded in one batch: x of
-// the block's 256 channels and B for every node on the paths (the ancestors' from the log,
-// the level's through the tree conv + SiLU, logged here), C of the level's nodes and Δ.  S,
-// the B·C products and the path coefficients follow in shared memory, and the CTA writes
-// to the workspace, per level node: e^{S_v} for its heads and the path sum
+// level's nodes and the nodes on their paths; then the inputs are loaded in rounds with every
+// load of a round in flight: x of the block's 256 channels and B of 8 ancestors (their logged
+// values) and of 4 level nodes (their conv taps; conv + SiLU, logged here), C of the level's
+// nodes, Δ.  S, the B·C products and the path coefficients follow in shared memory, and the
+// CTA writes to the workspace, per level node: e^{S_v} for its heads and the path sum
 // Σ_k e^{S_v − S_{m_k}} Δ_{m_k} (B_{m_k} · C_v) x_{m_k} + D·x_v for its rows (and C_v, from the
 // first block).
-// draft_tree_level_kernel (one CTA per instance and pair of heads, launched to overlap the
-// prep): each thread loads its share of the pair's 128 committed state rows into registers
-// (8 lanes per row, 16 columns each) and waits for the prep grid; the C_v · h contraction
-// then runs from registers, 8 nodes per pass, the 8 lanes of a row ending with one node's
-// sum each after a 7-shuffle reduce-scatter: y_v = e^{S_v} (C_v · h) + path sum.
+// draft_tree_level_kernel (persistent, two CTAs per SM, launched as a dependent grid of the
+// prep): each CTA walks a contiguous run of (instance, head) items and keeps the next three
+// heads' 64 committed state rows in flight (bulk copies into a ring of shared-memory stages);
+// per head, the C_v · h contraction runs from the stage, 8 nodes per pass, the 8 lanes of a
+// row ending with one node's sum each after a 7-shuffle reduce-scatter:
+// y_v = e^{S_v} (C_v · h) + path sum.
 //
-// draft_tree_commit_kernel (one CTA per instance and pair of heads): each warp holds 16 state
+// draft_tree_commit_kernel (one CTA per instance and head): each warp holds 16 state
 // rows in registers (16 loads in flight per lane) and applies the path's logged updates in
 // path order with the one-token draft step's fp32 operations (apply_logged_updates), so on a
 // chain it reproduces the stepped state bit for bit.  draft_tree_ring_kernel then writes the
@@ -36,10 +37,7 @@
 namespace ssmtree {
 namespace {
 
-constexpr int TG = 2;                            // heads per CTA
-constexpr int TROWS = TG * kP;                   // 128 state rows
-constexpr int TTHREADS = 256;                    // 8 lanes per row: 32 rows per sweep
-constexpr int TSWEEPS = TROWS / (TTHREADS / 8);  // 4
+constexpr int TTHREADS = 256;                    // prep kernel
 constexpr int FB = 8;                            // level nodes per pass
 constexpr int MAXN = SSM_MAX_NODES;              // 64
 constexpr int MAXP = SSM_MAX_DEPTH + 1;          // 16 nodes on a root-to-node path
