@@ -201,3 +201,43 @@ def test_binding_refuses_cpu_tensors(L):
     t = torch.zeros(4)
     with pytest.raises(ValueError):
         B._dev(t, "t", torch.float32, 4)
+
+
+def _level(L, dims, prm, n_seq=1, n=16, level=0, ptr=FAKE, h=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    P = ptr
+    return L.ssm_draft_tree_level(ctypes.byref(dims), ctypes.byref(prm), n_seq, n, level, P, P, P, h, P, P, P, P,
+                                  P, P, ws, ctypes.c_size_t(ws_bytes), None, None)
+
+
+def test_draft_tree_validation(L):
+    d, p = _dims(), _prm()
+    assert _level(L, d, p, n=0) == B.SSM_ERR_INVALID_ARG
+    assert _level(L, d, p, n=65) == B.SSM_ERR_CAPACITY
+    assert _level(L, d, p, level=-1) == B.SSM_ERR_RANGE
+    assert _level(L, d, p, level=16) == B.SSM_ERR_RANGE
+    assert _level(L, d, p, n_seq=-1) == B.SSM_ERR_INVALID_ARG
+    assert _level(L, d, p, n_seq=0, ptr=None, h=None, ws=None) == B.SSM_OK  # nothing to do, no CUDA call
+    assert _level(L, d, p, ptr=None) == B.SSM_ERR_INVALID_ARG
+    assert _level(L, d, p, ws=None) == B.SSM_ERR_INVALID_ARG
+    assert _level(L, d, p, h=ctypes.c_void_p(24)) == B.SSM_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _level(L, d, _prm(null=True)) == B.SSM_ERR_INVALID_ARG
+    need = L.ssm_draft_tree_workspace_size(ctypes.byref(d), 1, 16)
+    assert need >= 16 * (128 + 4 + 4 * 64) * 4 * d.n_layers  # C rows, e^S, path sums per node and instance
+    assert _level(L, d, p, ws_bytes=need - 1) == B.SSM_ERR_CAPACITY
+    assert L.ssm_draft_tree_workspace_size(ctypes.byref(d), 1, 65) == 0
+    P = FAKE
+    # commit: (dims, prm, n_seq, n, layout, max_path, path, path_len, log_d, log_B, log_x, xBC, h, ring, head)
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 0, P, P, P, P, P, P, P, P, P, None,
+                                   None) == B.SSM_ERR_RANGE
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 257, P, P, P, P, P, P, P, P, P, None,
+                                   None) == B.SSM_ERR_RANGE
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 1, 65, P, 5, P, P, P, P, P, P, P, P, P, None,
+                                   None) == B.SSM_ERR_CAPACITY
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 5, P, None, P, P, P, P, P, P, P, None,
+                                   None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 1, 16, P, 5, P, P, P, ctypes.c_void_p(20), P, P,
+                                   P, P, P, None, None) == B.SSM_ERR_INVALID_ARG  # log_B not 16-byte aligned
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(_prm(null=True)), 1, 16, P, 5, P, P, P, P, P, P, P,
+                                   P, P, None, None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 0, 16, None, 5, None, None, None, None, None,
+                                   None, None, None, None, None, None) == B.SSM_OK
