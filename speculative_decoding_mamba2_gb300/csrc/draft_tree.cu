@@ -388,6 +388,42 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
   }
 }
 
+// F partial sums per lane (F = 1, 2, 4 or 8), over the 8 lanes o = 0..7 of an aligned lane
+// group: lane o ends with the full sum of value o mod F (full sums over the lane bits above
+// log2 F, then recursive halving over the bits below).
+template <int F>
+__device__ __forceinline__ float reduce_rows(float (&v)[F], int o) {
+  if constexpr (F == 8) {
+    return reduce_scatter8(v, o);
+  } else {
+    constexpr int LOGF = F == 1 ? 0 : (F == 2 ? 1 : 2);
+#pragma unroll
+    for (int m = 4; m >= F; m >>= 1)  // lane bits that do not select a value: plain sums
+#pragma unroll
+      for (int i = 0; i < F; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], m);
+    if constexpr (LOGF == 0) {
+      return v[0];
+    } else if constexpr (LOGF == 1) {
+      const bool b0 = o & 1;
+      const float keep = b0 ? v[1] : v[0];
+      const float send = b0 ? v[0] : v[1];
+      return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    } else {
+      const bool b1 = o & 2, b0 = o & 1;
+      float s2[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float keep = b1 ? v[2 + i] : v[i];
+        const float send = b1 ? v[i] : v[2 + i];
+        s2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+      }
+      const float keep = b0 ? s2[1] : s2[0];
+      const float send = b0 ? s2[0] : s2[1];
+      return keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+  }
+}
+
 constexpr int MTHREADS = 256;                    // level kernel: 8 lanes per row, 32 rows per sweep
 constexpr int MSWEEPS = kP / (MTHREADS / 8);      // 2 sweeps cover one head's 64 rows
 constexpr int MSTAGES = 3;                        // heads' state rows in flight per CTA
@@ -401,6 +437,51 @@ struct MainFixed {
 };
 __host__ __device__ inline int main_h_offset() { return (int)((sizeof(MainFixed) + 127) & ~(size_t)127); }
 __host__ __device__ inline int level_smem_bytes() { return main_h_offset() + MSTAGES * kP * kN * 4; }
+
+// One pass of the contraction for up to F level nodes (fc of them live) of one head: 8 lanes
+// per state row, 16 columns each (rows rsub + 32 i), C rows through the cache; the lanes of a
+// row end with one node's sum each, and lane o < fc writes y of node o.
+template <int F>
+__device__ __forceinline__ void level_pass(const DraftTreeArgs& a, const int* front, int fc, const float* hsm,
+                                           const float* wsi, const float* wsE, const float* wsP, size_t node0, int hh) {
+  const int tid = threadIdx.x, o = tid & 7, rsub = tid >> 3;
+  const int H = a.H, d_inner = H * kP;
+  float acc[MSWEEPS][F];
+#pragma unroll
+  for (int i = 0; i < MSWEEPS; ++i)
+#pragma unroll
+    for (int f = 0; f < F; ++f) acc[i][f] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float4 hr[MSWEEPS];
+#pragma unroll
+    for (int i = 0; i < MSWEEPS; ++i) hr[i] = reinterpret_cast<const float4*>(hsm + (rsub + 32 * i) * kN)[o + 8 * j];
+#pragma unroll
+    for (int f = 0; f < F; ++f) {
+      const float4 cc = f < fc ? __ldg(reinterpret_cast<const float4*>(wsi + (size_t)front[f] * kN) + o + 8 * j)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < MSWEEPS; ++i) {
+        acc[i][f] = fmaf(hr[i].x, cc.x, acc[i][f]);
+        acc[i][f] = fmaf(hr[i].y, cc.y, acc[i][f]);
+        acc[i][f] = fmaf(hr[i].z, cc.z, acc[i][f]);
+        acc[i][f] = fmaf(hr[i].w, cc.w, acc[i][f]);
+      }
+    }
+  }
+  const bool writer = o < fc;
+  const int v = writer ? front[o] : 0;
+  const float e = writer ? __ldg(wsE + (size_t)v * H + hh) : 0.f;
+#pragma unroll
+  for (int i = 0; i < MSWEEPS; ++i) {
+    const int row = rsub + 32 * i;
+    const float sum = reduce_rows<F>(acc[i], o);
+    if (writer) {
+      const size_t yo = (node0 + v) * d_inner + (size_t)hh * kP + row;
+      a.y[yo] = fmaf(e, sum, __ldg(wsP + (size_t)v * d_inner + (size_t)hh * kP + row));
+    }
+  }
+}
 
 // Persistent: CTA c takes the contiguous run of (instance, head) items
 // [c·items/G, (c+1)·items/G), G = the grid, and keeps the next MSTAGES heads' 64 state rows in
@@ -459,45 +540,18 @@ __global__ void __launch_bounds__(MTHREADS, 2) draft_tree_level_kernel(DraftTree
     const float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
     const float* wsE = wsi + ws_E_off(n);
     const float* wsP = wsi + ws_P_off(n, H);
-    // y_v = e^{S_v} (C_v · h_ckpt) + path sum, 8 level nodes per pass; C rows through the
-    // cache (shared by the instance's heads), the state rows from the stage
+    // y_v = e^{S_v} (C_v · h_ckpt) + path sum, up to 8 level nodes per pass, the pass's
+    // arithmetic sized to its node count (1, 2, 4 or 8)
     for (int f0 = 0; f0 < nf; f0 += FB) {
-      float acc[MSWEEPS][FB];
-#pragma unroll
-      for (int i = 0; i < MSWEEPS; ++i)
-#pragma unroll
-        for (int f = 0; f < FB; ++f) acc[i][f] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float4 hr[MSWEEPS];
-#pragma unroll
-        for (int i = 0; i < MSWEEPS; ++i) hr[i] = reinterpret_cast<const float4*>(hsm + (rsub + 32 * i) * kN)[o + 8 * j];
-#pragma unroll
-        for (int f = 0; f < FB; ++f) {
-          const float4 cc = f0 + f < nf
-                                ? __ldg(reinterpret_cast<const float4*>(wsi + (size_t)s.ls.front[f0 + f] * kN) + o + 8 * j)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int i = 0; i < MSWEEPS; ++i) {
-            acc[i][f] = fmaf(hr[i].x, cc.x, acc[i][f]);
-            acc[i][f] = fmaf(hr[i].y, cc.y, acc[i][f]);
-            acc[i][f] = fmaf(hr[i].z, cc.z, acc[i][f]);
-            acc[i][f] = fmaf(hr[i].w, cc.w, acc[i][f]);
-          }
-        }
-      }
-      const int f = f0 + o;
-      const int v = f < nf ? s.ls.front[f] : 0;
-      const float e = f < nf ? __ldg(wsE + (size_t)v * H + hh) : 0.f;
-#pragma unroll
-      for (int i = 0; i < MSWEEPS; ++i) {
-        const int row = rsub + 32 * i;
-        const float sum = reduce_scatter8(acc[i], o);
-        if (f < nf) {
-          const size_t yo = (node0 + v) * d_inner + (size_t)hh * kP + row;
-          a.y[yo] = fmaf(e, sum, __ldg(wsP + (size_t)v * d_inner + (size_t)hh * kP + row));
-        }
-      }
+      const int fc = min(FB, nf - f0);
+      if (fc == 1)
+        level_pass<1>(a, s.ls.front + f0, fc, hsm, wsi, wsE, wsP, node0, hh);
+      else if (fc == 2)
+        level_pass<2>(a, s.ls.front + f0, fc, hsm, wsi, wsE, wsP, node0, hh);
+      else if (fc <= 4)
+        level_pass<4>(a, s.ls.front + f0, fc, hsm, wsi, wsE, wsP, node0, hh);
+      else
+        level_pass<8>(a, s.ls.front + f0, fc, hsm, wsi, wsE, wsP, node0, hh);
     }
     __syncthreads();  // every thread is done with this stage
     if (tid == 0 && k + MSTAGES < count) {
