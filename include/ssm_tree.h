@@ -355,6 +355,20 @@ int ssm_draft_tree_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n
                           float *h_ckpt, uint16_t *ring, int32_t *ring_head, int32_t *dev_status, void *stream);
 
 /*
+ * ssm_selftest_bounded_wait -- failure detection self-test (no counterpart in the
+ * pages).  Every copy pipeline of this library waits on mbarriers with a bounded
+ * wait: after one second of global time it gives up, sets SSM_STATUS_TIMEOUT in
+ * the caller's status word and the kernel returns, so a lost copy never hangs
+ * the GPU.  This call runs that wait on a barrier nothing arrives at, with a
+ * limit of limit_us microseconds, so the give-up path can be checked: on return
+ * (after a synchronize) *dev_status has SSM_STATUS_TIMEOUT set and the context
+ * is usable.
+ *   limit_us   1..1000000
+ *   dev_status device int32 (required)
+ */
+int ssm_selftest_bounded_wait(int32_t limit_us, int32_t *dev_status, void *stream);
+
+/*
  * ssm_tree_verify_noalloc -- ssm_tree_verify for callers that cannot allocate
  * device memory (a runtime that gives a plugin only the current op's tensors
  * and owns all other device memory, an embedding with allocation forbidden

@@ -99,6 +99,7 @@ _SIGS = {
     "ssm_draft_tree_level": (ctypes.c_int, [_P, _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                             ctypes.c_size_t, _P, _P]),
     "ssm_draft_tree_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
+    "ssm_selftest_bounded_wait": (ctypes.c_int, [_I, _P, _P]),
     "ssm_draft_tree_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -374,6 +375,13 @@ def ssm_draft_tree_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, la
         _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
+
+
+def ssm_selftest_bounded_wait(limit_us: int, status, stream=None):
+    """Run the library's bounded mbarrier wait on a barrier nothing arrives at (it gives up
+    after limit_us and sets SSM_STATUS_TIMEOUT in `status`)."""
+    _check(lib().ssm_selftest_bounded_wait(int(limit_us), _dev(status, "status", torch.int32, 1),
+                                           _stream(stream, status)))
 
 
 # ---------------------------------------------------------------------------

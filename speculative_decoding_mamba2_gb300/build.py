@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "gemm.cu", "norm.cu",
-           "layer_api.cu", "draft_tree.cu", "layout.cpp"]
+           "layer_api.cu", "draft_tree.cu", "selftest.cu", "layout.cpp"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "draft_tree.cuh"), os.path.join(INCLUDE, "ssm_tree.h"), os.path.join(INCLUDE, "ssm_layer.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 LIBNAME = "libssmtree.so"

@@ -473,3 +473,10 @@ extern "C" int ssm_draft_tree_commit(const ssm_dims* dims, const ssm_params* prm
   a.status = dev_status;
   return finish(fn, launch_draft_tree_commit(a, (cudaStream_t)stream));
 }
+
+extern "C" int ssm_selftest_bounded_wait(int32_t limit_us, int32_t* dev_status, void* stream) {
+  const char* fn = "ssm_selftest_bounded_wait";
+  if (limit_us < 1 || limit_us > 1000000) return fail(SSM_ERR_RANGE, fn, "limit_us must be in [1, 1000000]");
+  if (!dev_status) return fail(SSM_ERR_INVALID_ARG, fn, "dev_status is NULL");
+  return finish(fn, launch_selftest_wait(dev_status, (unsigned long long)limit_us * 1000ull, (cudaStream_t)stream));
+}

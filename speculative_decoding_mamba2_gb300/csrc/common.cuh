@@ -204,11 +204,19 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // ---------------------------------------------------------------------------
-// mbarrier + bulk-copy (TMA) helpers.  Every wait is bounded: after
-// kWaitLimit unsuccessful polls it gives up and returns false, and the caller
-// reports SSM_STATUS_TIMEOUT instead of spinning forever.
+// mbarrier + bulk-copy (TMA) helpers.  Every wait is bounded: after one second
+// of global time (or kWaitLimit unsuccessful polls, whichever comes first) it
+// gives up and returns false, and the caller reports SSM_STATUS_TIMEOUT instead
+// of spinning forever.
 // ---------------------------------------------------------------------------
 constexpr unsigned kWaitLimit = 1u << 26;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long global_time_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -235,10 +243,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (unsigned it = 0; it < kWaitLimit; ++it)
+// wait for phase `parity` of `bar`; false once limit_ns of global time (or kWaitLimit polls)
+// have passed without it
+// (the clock is first read after 64 unsuccessful polls, so a wait that succeeds at once costs
+// no timer read)
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  unsigned long long t0 = 0;
+  for (unsigned it = 0; it < kWaitLimit; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 63) {
+      const unsigned long long now = global_time_ns();
+      if (t0 == 0)
+        t0 = now;
+      else if (now - t0 > limit_ns)
+        return false;
+    }
+  }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  return mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
 // Programmatic dependent launch: the primary grid lets its dependent grid be scheduled;
 // the dependent waits until the primary grid has completed and its writes are visible
@@ -355,5 +379,8 @@ struct ReplayArgs {
   int32_t *ring_head, *status;
 };
 cudaError_t launch_replay(const ReplayArgs& a, cudaStream_t s);
+
+// the bounded-wait self-test (one CTA waits on a barrier nothing arrives at)
+cudaError_t launch_selftest_wait(int32_t* status, unsigned long long limit_ns, cudaStream_t s);
 
 }  // namespace ssmtree

@@ -241,3 +241,9 @@ def test_draft_tree_validation(L):
                                    P, P, None, None) == B.SSM_ERR_INVALID_ARG
     assert L.ssm_draft_tree_commit(ctypes.byref(d), ctypes.byref(p), 0, 16, None, 5, None, None, None, None, None,
                                    None, None, None, None, None, None) == B.SSM_OK
+
+
+def test_selftest_bounded_wait_validation(L):
+    assert L.ssm_selftest_bounded_wait(0, FAKE, None) == B.SSM_ERR_RANGE
+    assert L.ssm_selftest_bounded_wait(1000001, FAKE, None) == B.SSM_ERR_RANGE
+    assert L.ssm_selftest_bounded_wait(1000, None, None) == B.SSM_ERR_INVALID_ARG
