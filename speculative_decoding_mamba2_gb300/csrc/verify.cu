@@ -1058,7 +1058,7 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
   if (inst == 0) return cudaSuccess;
   int G = verify_heads_per_group(a.n, a.max_depth, a.H, a.LP);
   if (G == 0) return cudaErrorInvalidValue;
-  if (G == 4) {  // few instances: groups of 2 heads when they fill the SMs' two CTA slots in fewer rounds
+  if (G == 4) {  // few instances: groups of 2 heads when they finish sooner (see the estimate below)
     int sms = dev < 64 ? g_sms[dev] : 0;
     if (sms == 0) {
       e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1069,7 +1069,15 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
     const Ws W2 = ws_layout(a.n, a.max_depth, a.H, a.LP);
     const bool fits2 = a.LP > 0 ? smem_layout<2, true>(a.n, W2.PP, W2.NP, a.LP).total <= SMEM_LIMIT
                                 : smem_layout<2, false>(a.n, W2.PP, W2.NP, 0).total <= SMEM_LIMIT;
-    if (fits2 && c4 < 4 * slots && ((c2 + slots - 1) / slots) * 2 < ((c4 + slots - 1) / slots) * 4) G = 2;
+    // time ~ rounds of CTAs x (fixed cost per CTA + G heads): the fixed part (prologue, the wait
+    // for the prep grid, the group's inputs) measured at about 6 heads' worth at the 2.7B shape,
+    // so 2-head groups win only when they need no more rounds than 4-head groups
+    const long long est4 = (c4 + slots - 1) / slots * (6 + 4), est2 = (c2 + slots - 1) / slots * (6 + 2);
+    if (fits2 && est2 < est4) G = 2;
+    if (const char* o = getenv("SSM_VERIFY_HEADS_PER_GROUP")) {  // tuning / test override: 2 or 4
+      const int v = atoi(o);
+      if (v == 4 || (v == 2 && fits2)) G = v;
+    }
   }
   const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H, a.LP);
   e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);
