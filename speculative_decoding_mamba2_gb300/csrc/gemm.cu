@@ -385,6 +385,10 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
   while (!can_split && g.tchunk > 64 && g.M > g.tchunk / 2 &&
          (long long)tiles_c * ((g.M + g.tchunk / 2 - 1) / (g.tchunk / 2)) <= sms / 2)
     g.tchunk /= 2;
+  if (const char* o = getenv("SSM_LINEAR_TCHUNK")) {  // tuning override: 64, 128 or 256 tokens per CTA
+    const int v = atoi(o);
+    if (v == 64 || v == 128 || v == 256) g.tchunk = v;
+  }
   const int chunk = g.M < g.tchunk ? g.M : g.tchunk;
   const int q = 8 * g.cl > 16 ? 8 * g.cl : 16;
   g.tn = (chunk + q - 1) / q * q;
@@ -430,6 +434,10 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
   }
 }
 
+// dynamic shared memory of a plan: the stage ring (which also holds the epilogue tile), the
+// barriers and the 1024-byte alignment of the ring
+int gemm_smem_bytes(const GemmArgs& g) { return GEMM_RESERVED + g.stages * (FM + g.tn) * GBK * 2; }
+
 cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const void* W, long long ldw, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   int dev = 0;
@@ -461,7 +469,7 @@ cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const voi
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(GTHREADS);
-  cfg.dynamicSmemBytes = GEMM_SMEM;
+  cfg.dynamicSmemBytes = (size_t)gemm_smem_bytes(g);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
