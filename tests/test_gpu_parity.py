@@ -101,6 +101,17 @@ def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
     check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
 
 
+@pytest.mark.parametrize("g", ["2", "4"])
+def test_two_and_four_head_groups(g, monkeypatch):
+    # the same small batch with 2-head and with 4-head groups (H = 10: the last group ragged
+    # either way), against the oracle
+    monkeypatch.setenv("SSM_VERIFY_HEADS_PER_GROUP", g)
+    w = Workload(57, "head groups", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
 def test_single_node_tree():
     w = Workload(52, "root only", Shape(H=4), n_layers=3, batch=2, trees=(("chain", 1),))
     b = batch(w)
