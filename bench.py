@@ -760,13 +760,113 @@ def run_draft_only(args):
     return 0
 
 
+def run_block_steps(args):
+    """One Mamba2-2.7B block's steps at the batched-verify shape (16 sequences x 16 nodes,
+    256 tree tokens), each timed alone as a CUDA graph of 8 consecutive layers' launches
+    (device time per launch): RMSNorm, the input projection, ssm_commit_verify (and its prep
+    and main halves), the gated RMSNorm, the output projection; then the five steps in one
+    graph.  Synthetic weights; the state and inputs of each layer are its own."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_commit_verify,
+                                                   ssm_commit_verify_workspace_size, ssm_gated_rmsnorm, ssm_linear,
+                                                   ssm_rmsnorm, ssm_tree_layout_build)
+    from synth import batch, layer_params, workload
+    dev = torch.device("cuda")
+    w = workload(3)
+    S, n = w.batch, w.n_nodes()
+    H, P, N, R = w.shape.H, w.shape.P, w.shape.N, w.ring_cap
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    d_model = d_inner // 2
+    n_in = d_inner + conv_dim + H
+    T, L = S * n, 8
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    W_in = [(torch.randn(n_in, d_model, device=dev, generator=gen) * 0.02).to(torch.bfloat16) for _ in range(L)]
+    W_out = [(torch.randn(d_model, d_inner, device=dev, generator=gen) * 0.02).to(torch.bfloat16) for _ in range(L)]
+    nw, gw = torch.ones(d_model, device=dev), torch.ones(d_inner, device=dev)
+    b = batch(w, layers=[0])
+    prm_all = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev)
+               for k, v in layer_params(w, range(L)).items()}
+    prm = [{k: v[l:l + 1] for k, v in prm_all.items()} for l in range(L)]
+    h = [torch.randn(S, H, P, N, device=dev, generator=gen) * 0.1 for _ in range(L)]
+    ring = [torch.randn(S, R, conv_dim, device=dev, generator=gen).to(torch.bfloat16) for _ in range(L)]
+    head = [torch.full((S,), 3, dtype=torch.int32, device=dev) for _ in range(L)]
+    x = torch.randn(T, d_model, device=dev, generator=gen)
+    u = torch.empty(T, d_model, dtype=torch.bfloat16, device=dev)
+    z = torch.empty(T, d_inner, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(T, d_inner, device=dev)
+    gb = torch.empty(T, d_inner, dtype=torch.bfloat16, device=dev)
+    xbc = [torch.randn(T, conv_dim, device=dev, generator=gen).to(torch.bfloat16) for _ in range(2)]
+    dtb = [(torch.randn(T, H, device=dev, generator=gen) * 0.5).to(torch.bfloat16) for _ in range(2)]
+    lay, depth = ssm_tree_layout_build(b["parent"])
+    layout = torch.from_numpy(lay).to(dev)
+    mp = depth + 1
+    path = torch.empty((S, mp), dtype=torch.int32, device=dev)
+    plen = torch.empty(S, dtype=torch.int32, device=dev)
+    bonus = torch.empty(S, dtype=torch.int32, device=dev)
+    dims1 = Dims(n_heads=H, n_layers=1, ring_cap=R)
+    ws = torch.empty(ssm_commit_verify_workspace_size(dims1, S, n, depth, mp), dtype=torch.uint8, device=dev)
+    ssm_accept_path(S, n, mp, layout, torch.from_numpy(b["tok"]).to(dev), torch.from_numpy(b["tgt"]).to(dev),
+                    path, plen, bonus)
+    torch.cuda.synchronize()
+
+    def cv(l, s, part="all"):
+        ssm_commit_verify(dims1, prm[l], S, n, layout, mp, path, plen, xbc[1], dtb[1], n, depth, layout, xbc[0],
+                          dtb[0], h[l], ring[l], head[l], y, ws, None, s, part=part)
+
+    steps = {
+        "rmsnorm": lambda l, s: ssm_rmsnorm(x, nw, 1e-5, u, s),
+        "input projection": lambda l, s: ssm_linear(u, W_in[l], [(0, z), (d_inner, xbc[0]),
+                                                                  (d_inner + conv_dim, dtb[0])], stream=s),
+        "ssm_commit_verify": lambda l, s: cv(l, s),
+        "gated rmsnorm": lambda l, s: ssm_gated_rmsnorm(y, z, gw, 1e-5, gb, s),
+        "output projection": lambda l, s: ssm_linear(gb, W_out[l], [(0, x)], residual=x, stream=s),
+    }
+    halves = {"ssm_commit_verify prep": lambda l, s: cv(l, s, "prep"),
+              "ssm_commit_verify main": lambda l, s: cv(l, s, "main")}
+
+    def graph_us(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn(0, side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for l in range(L):
+                fn(l, torch.cuda.current_stream(dev))
+        for _ in range(max(3, args.warmup)):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / L * 1e3
+
+    out = {k: graph_us(f) for k, f in {**steps, **halves}.items()}
+
+    def block(l, s):
+        for f in steps.values():
+            f(l, s)
+
+    out["block (the five steps in one graph)"] = graph_us(block)
+    print(json.dumps({"metric": "block step time (Mamba2-2.7B, 16 sequences x 16 nodes)", "unit": "us",
+                      "higher_is_better": False, "data": "synthetic", "steps_us": out}), flush=True)
+    return 0
+
+
 def run_linear_only(args):
     """The block's two projections alone at the Mamba2-2.7B shape (256 tree tokens: 16
     sequences x 16 nodes): the input projection [256 x 2560] x [10576 x 2560]^T with its
     z | x B C | dt segments, and the output projection [256 x 5120] x [2560 x 5120]^T added
     into the fp32 residual stream.  Launches are captured in a CUDA graph (device time
-    only), the weights rotate over copies larger than L2.  torch.matmul (cuBLAS) on the
-    same product is timed beside it as context."""
+    only), the weights rotate over copies larger than L2 (and, for `us_weights_in_l2`, one
+    copy stays in L2).  torch.matmul (cuBLAS) on the same product is timed beside it as
+    context."""
     import torch
 
     from speculative_decoding_mamba2_gb300 import ssm_linear
@@ -807,20 +907,24 @@ def run_linear_only(args):
     dt = torch.empty(T, H, device=dev, dtype=torch.bfloat16)
     full = torch.empty(T, n_in, device=dev, dtype=torch.bfloat16)
     us = graph_us(lambda i, s: ssm_linear(A, W[i % 4], [(0, z), (d_inner, xbc), (d_inner + conv_dim, dt)], stream=s))
+    warm = graph_us(lambda i, s: ssm_linear(A, W[0], [(0, z), (d_inner, xbc), (d_inner + conv_dim, dt)], stream=s))
     ref = graph_us(lambda i, s: torch.matmul(A, W[i % 4].t(), out=full))
     by, fl = n_in * d_model * 2 + T * d_model * 2 + T * n_in * 2, 2.0 * T * n_in * d_model
     out["in"] = {"shape_MNK": [T, n_in, d_model], "us": us, "GB/s": by / us / 1e3, "TFLOP/s": fl / us / 1e6,
-                 "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "cublas_matmul_us": ref}
+                 "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "us_weights_in_l2": warm,
+                 "cublas_matmul_us": ref}
     G = torch.randn(T, d_inner, device=dev, generator=gen).to(torch.bfloat16)
     Wo = [(torch.randn(d_model, d_inner, device=dev, generator=gen) * d_inner ** -0.5).to(torch.bfloat16)
           for _ in range(8)]
     x = torch.randn(T, d_model, device=dev, generator=gen)
     xo = torch.empty(T, d_model, device=dev, dtype=torch.bfloat16)
     us = graph_us(lambda i, s: ssm_linear(G, Wo[i % 8], [(0, x)], residual=x, stream=s))
+    warm = graph_us(lambda i, s: ssm_linear(G, Wo[0], [(0, x)], residual=x, stream=s))
     ref = graph_us(lambda i, s: torch.matmul(G, Wo[i % 8].t(), out=xo))
     by, fl = d_model * d_inner * 2 + T * d_inner * 2 + T * d_model * 8, 2.0 * T * d_model * d_inner
     out["out"] = {"shape_MNK": [T, d_model, d_inner], "us": us, "GB/s": by / us / 1e3, "TFLOP/s": fl / us / 1e6,
-                  "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "cublas_matmul_us": ref}
+                  "frac_of_hbm_peak": by / us / 1e3 / peaks["hbm_gbs"], "us_weights_in_l2": warm,
+                  "cublas_matmul_us": ref}
     print(json.dumps({"metric": "projection time (Mamba2-2.7B block, 256 tokens)", "unit": "us",
                       "higher_is_better": False, "data": "synthetic", "projections": out}), flush=True)
     return 0
@@ -1276,9 +1380,10 @@ def main():
     ap.add_argument("--no-draft", action="store_true")
     ap.add_argument("--no-chain", action="store_true")
     ap.add_argument("--no-block", action="store_true")
-    ap.add_argument("--only", choices=["linear", "draft"], default=None,
+    ap.add_argument("--only", choices=["linear", "draft", "block-steps"], default=None,
                     help="run one measurement alone: 'linear' = the block's projections, "
-                         "'draft' = the draft side (one-token steps + replay, tree drafting)")
+                         "'draft' = the draft side (one-token steps + replay, tree drafting), "
+                         "'block-steps' = one block's steps timed one by one")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1290,6 +1395,8 @@ def main():
         return run_linear_only(args)
     if args.only == "draft":
         return run_draft_only(args)
+    if args.only == "block-steps":
+        return run_block_steps(args)
     return run_ours(args, w)
 
 
