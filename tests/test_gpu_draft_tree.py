@@ -214,3 +214,14 @@ def test_draft_tree_full_size_sampled():
     assert int(status) == 0
     assert not torch.isnan(y).any()
     check_levels(b, w, d, y, logs, [(0, 0), (0, 23), (0, 47)])
+
+
+def test_draft_tree_runs_across_sequences():
+    # 2 sequences x 8 layers x 32 heads = 512 (instance, head) items for the level kernel's
+    # persistent CTAs: runs cross instances and, at the middle, sequences (different trees)
+    w = Workload(58, "draft tree runs", Shape(H=32), n_layers=8, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    d = upload(b, w)
+    y, logs, status = draft_levels(d)
+    assert int(status) == 0
+    check_levels(b, w, d, y, logs, [(i, j) for i in range(2) for j in (0, 3, 7)])
