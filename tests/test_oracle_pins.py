@@ -135,7 +135,7 @@ def test_closed_form_scalar_chain():
     np.testing.assert_allclose(h, [h1, h2, h3], rtol=1e-15)
     np.testing.assert_allclose(y, [C[0] * h1 + 0.25 * x[0], C[1] * h2 + 0.25 * x[1], C[2] * h3 + 0.25 * x[2]],
                                rtol=1e-15)
-    # the survey's hand values for x = SiLU(1), SiLU(2), B = C = D = 1 (state path only)
+    # hand-computed values for x = SiLU(1), SiLU(2), B = C = D = 1 (state path only)
     hh1 = 0.5 + ln2 * 0.7310585786300049
     assert abs(hh1 - 1.006731192601549) < 1e-15
     assert abs(0.5 * hh1 + ln2 * 1.7615941559557646 - 1.7244096187923894) < 1e-15
