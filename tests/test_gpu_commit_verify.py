@@ -123,7 +123,7 @@ def check_separate(out):
                                       ring_window(out["ring_sep"][inst].view(torch.int16).numpy(), hd))
 
 
-def test_config0_every_element():
+def test_tiny_130m_tree15_every_element():
     w0 = workload(0)
     w1 = next_workload(w0, 60, ("random", 16, 3, 4))
     b0, b1 = batch(w0), batch(w1)
@@ -194,7 +194,7 @@ def test_bad_path_is_cut_and_flagged_like_commit():
     check_separate(out)
 
 
-def test_config3_full_size_sampled():
+def test_2p7b_batch16_full_size_sampled():
     # the default benchmark's launch configuration: 16 sequences x 64 layers, 80 heads
     w0 = workload(3)
     w1 = next_workload(w0, 69, ("random", 16, 3, 4))

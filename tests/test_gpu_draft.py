@@ -76,7 +76,7 @@ def oracle_draft(b, i, j, steps):
     return states, ys, log, ring
 
 
-def test_config1_draft_chain_and_replay():
+def test_370m_draft_chain16_and_replay():
     w = workload(1)
     b = draft_batch(w)
     r = run_draft(b, w, 16)
@@ -128,7 +128,7 @@ def test_replay_k_out_of_range_is_clamped_and_flagged():
     assert head.cpu().tolist() == [9, 9, 3, 3]
 
 
-def test_config4_shape_draft_replay_16():
+def test_780m_batch64_draft_replay_16():
     w = workload(4)
     b = draft_batch(w, seqs=[0, 63], layers=[0, 1, 47])
     r = run_draft(b, w, 16)

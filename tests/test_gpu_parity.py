@@ -55,7 +55,7 @@ def check_instances(b, out, pairs, commit=True):
     assert int(out["status"]) == 0
 
 
-def test_config0_every_element():
+def test_tiny_130m_tree15_every_element():
     w = workload(0)
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -120,7 +120,7 @@ def test_single_node_tree():
     assert out["path_len"].cpu().tolist() == [1, 1]
 
 
-def test_config2_full_size_sampled():
+def test_2p7b_batch1_full_size_sampled():
     w = workload(2)
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -128,7 +128,7 @@ def test_config2_full_size_sampled():
     assert torch.isfinite(out["y"]).all()
 
 
-def test_config3_full_size_sampled():
+def test_2p7b_batch16_full_size_sampled():
     w = workload(3)
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -141,7 +141,7 @@ def test_config3_full_size_sampled():
         assert int(out["bonus"][i]) == bonus_ref
 
 
-def test_config4_ternary_sampled():
+def test_780m_ternary40_sampled():
     w = workload(4)
     b = batch(w, seqs=[0, 21, 63], tree=0)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -221,7 +221,7 @@ def test_chain_kernel_longest_chain():
         assert rel_err(y[j].double().cpu().numpy(), ref) <= TOL, j
 
 
-def test_config4_chain_256_sampled():
+def test_780m_chain256_sampled():
     w = workload(4)
     b = batch(w, seqs=[0, 63], layers=[0, 47], tree=1)
     out = run_tree_step(upload_tree_batch(b, w), max_path=256, commit=False)
