@@ -63,7 +63,7 @@ extern "C" {
 #define SSM_STATUS_TIMEOUT 16    /* a bounded wait on a copy gave up (results   */
                                  /* of that call are invalid)                   */
 
-/* Limits of this build (checked on the host; larger inputs get SSM_ERR_CAPACITY). */
+/* Limits of this library (checked on the host; larger inputs get SSM_ERR_CAPACITY). */
 #define SSM_MAX_NODES 64         /* nodes per branching tree (ssm_tree_verify)  */
 #define SSM_MAX_DEPTH 15         /* deepest node below the root (branching)     */
 #define SSM_MAX_CHAIN_NODES 4096 /* nodes of a chain (parent[v] = v-1)          */
@@ -71,8 +71,8 @@ extern "C" {
 
 typedef struct ssm_dims {
   int32_t n_heads;    /* H                                                     */
-  int32_t head_dim;   /* P (this build: 64)                                    */
-  int32_t d_state;    /* N (this build: 128)                                   */
+  int32_t head_dim;   /* P (this library: 64)                                  */
+  int32_t d_state;    /* N (this library: 128)                                 */
   int32_t conv_width; /* W (must be 4)                                         */
   int32_t n_layers;   /* L                                                     */
   int32_t ring_cap;   /* R: conv-ring rows per instance (>= 3)                 */

@@ -36,8 +36,8 @@ int cuda_fail(const char* fn, cudaError_t e) {
 int check_dims(const char* fn, const ssm_dims* d, bool need_params, const ssm_params* p) {
   if (!d) return fail(SSM_ERR_INVALID_ARG, fn, "dims is NULL");
   if (d->n_heads < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_heads must be >= 1");
-  if (d->head_dim != kP) return fail(SSM_ERR_INVALID_ARG, fn, "head_dim must be 64 in this build");
-  if (d->d_state != kN) return fail(SSM_ERR_INVALID_ARG, fn, "d_state must be 128 in this build");
+  if (d->head_dim != kP) return fail(SSM_ERR_INVALID_ARG, fn, "head_dim must be 64 in this library");
+  if (d->d_state != kN) return fail(SSM_ERR_INVALID_ARG, fn, "d_state must be 128 in this library");
   if (d->conv_width != kW) return fail(SSM_ERR_INVALID_ARG, fn, "conv_width must be 4");
   if (d->n_layers < 1) return fail(SSM_ERR_INVALID_ARG, fn, "n_layers must be >= 1");
   if (d->ring_cap < 3) return fail(SSM_ERR_INVALID_ARG, fn, "ring_cap must be >= 3");
@@ -84,7 +84,7 @@ int check_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_seq, int3
   if (max_depth > SSM_MAX_DEPTH) return fail(SSM_ERR_CAPACITY, fn, "max_depth exceeds SSM_MAX_DEPTH");
   if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads) == 0 ||
       verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads) > 232448)
-    return fail(SSM_ERR_CAPACITY, fn, "tree too large for the shared-memory plan of this build");
+    return fail(SSM_ERR_CAPACITY, fn, "tree too large for the shared-memory plan of this library");
   return SSM_OK;
 }
 }  // namespace
@@ -156,7 +156,7 @@ int check_commit_verify_shape(const char* fn, const ssm_dims* dims, int32_t n_se
     return fail(SSM_ERR_CAPACITY, fn, "ring_cap must be >= prev_max_path + 3 (the rows before the path are read after the path is written)");
   if (verify_heads_per_group(n_nodes, max_depth, dims->n_heads, prev_max_path) == 0 ||
       verify_prep_smem_bytes(n_nodes, max_depth, dims->n_heads, prev_max_path) > 232448)
-    return fail(SSM_ERR_CAPACITY, fn, "tree and path too large for the shared-memory plan of this build");
+    return fail(SSM_ERR_CAPACITY, fn, "tree and path too large for the shared-memory plan of this library");
   return SSM_OK;
 }
 }  // namespace

@@ -8,7 +8,7 @@
 
 namespace ssmtree {
 
-// Shape constants of this build: Mamba2 head_dim 64, d_state 128, conv width 4.
+// Shape constants of this library: Mamba2 head_dim 64, d_state 128, conv width 4.
 constexpr int kP = 64;
 constexpr int kN = 128;
 constexpr int kW = 4;
