@@ -314,8 +314,9 @@ int ssm_replay(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32
  *   y          device fp32 [I][n][d_inner]: rows of depth == level written
  *   workspace  device, 16-byte aligned, >= ssm_draft_tree_workspace_size()
  *              bytes, caller-owned scratch (per level node: C, e^{S_v} per
- *              head and the path sums of every row, written and read within
- *              the call); calls that overlap on the GPU must not share one
+ *              head, the path sums of every row and the B·C products along
+ *              its path, written and read within the call); calls that
+ *              overlap on the GPU must not share one
  * A layout record that points outside its tree sets SSM_STATUS_BAD_LAYOUT and
  * the instance writes nothing.
  */
@@ -327,7 +328,7 @@ int ssm_draft_tree_level(const ssm_dims *dims, const ssm_params *prm, int32_t n_
 
 /*
  * ssm_draft_tree_workspace_size -- host-only.  Bytes of device workspace
- * ssm_draft_tree_level needs: about n_nodes * (N + H + d_inner) * 4 per
+ * ssm_draft_tree_level needs: about n_nodes * (N + H + d_inner + 16) * 4 per
  * instance (each part padded to 128 bytes); 0 if the shape is rejected
  * (reason in ssm_last_error()).
  */

@@ -11,14 +11,16 @@
 // which reads the committed state once per level, whatever the number of branches, and
 // writes no state.  The ancestors' Δ, B, x are the log rows their own level wrote.
 //
-// draft_tree_prep_kernel (one CTA per instance and block of 4 heads): one warp finds the
-// level's nodes and the nodes on their paths; then the inputs are loaded in rounds with every
-// load of a round in flight: x of the block's 256 channels and B of 8 ancestors (their logged
-// values) and of 4 level nodes (their conv taps; conv + SiLU, logged here), C of the level's
-// nodes, Δ.  S, the B·C products and the path coefficients follow in shared memory, and the
-// CTA writes to the workspace, per level node: e^{S_v} for its heads and the path sum
-// Σ_k e^{S_v − S_{m_k}} Δ_{m_k} (B_{m_k} · C_v) x_{m_k} + D·x_v for its rows (and C_v, from the
-// first block).
+// draft_tree_bc_kernel (one CTA per instance): one warp finds the level's nodes and the nodes
+// on their paths; B of the ancestors (their logged values) and B | C of the level's nodes
+// (conv taps, conv + SiLU; B logged) are loaded in rounds with every load of a round in
+// flight; the CTA writes C_v and the products B_{m_k} · C_v along every level node's path to
+// the workspace.  This part is the same for every head, so it is done once per instance.
+// draft_tree_prep_kernel (one CTA per instance and block of 4 heads, a dependent grid of the
+// B | C kernel, so its loads overlap that kernel): x of the block's 256 channels for 8
+// ancestors (logged) and 4 level nodes (conv + SiLU, logged) per round, Δ, S; then, once the
+// products are complete, e^{S_v} for its heads and the path sum
+// Σ_k e^{S_v − S_{m_k}} Δ_{m_k} (B_{m_k} · C_v) x_{m_k} + D·x_v for its rows.
 // draft_tree_level_kernel (persistent, two CTAs per SM, launched as a dependent grid of the
 // prep): each CTA walks a contiguous run of (instance, head) items and keeps the next three
 // heads' 64 committed state rows in flight (bulk copies into a ring of shared-memory stages);
@@ -55,7 +57,7 @@ struct LevelSetup {
 // One warp: loads the records, checks that every parent and tap is an earlier node and the
 // depths agree, and lists the level's nodes and the nodes on their paths.  A record that
 // fails leaves nf = 0 (and sets SSM_STATUS_BAD_LAYOUT when `report`).
-__device__ void level_setup(LevelSetup& s, const ssm_node* lay, int n, int level, int32_t* status, bool report) {
+__device__ __forceinline__ void level_setup(LevelSetup& s, const ssm_node* lay, int n, int level, int32_t* status, bool report) {
   const int lane = threadIdx.x & 31;
   const unsigned full = 0xffffffffu, lt = (1u << lane) - 1u;
   bool ok = true;
@@ -146,15 +148,147 @@ __device__ __forceinline__ float reduce_scatter8(const float (&v)[FB], int o) {
 
 constexpr int PG = 4;             // heads per prep CTA
 constexpr int PROWS = PG * kP;    // 256 channels (x rows) per prep CTA
+static_assert(2 * kN == TTHREADS, "one B | C channel per thread of the B | C kernel");
 
 // Workspace of one instance (floats): C rows [n][kN], e^{S_v} [n][H], path sums [n][d_inner],
+// B·C products [n][MAXP] (node v's row: B_{m_k} · C_v for its path nodes m_0 .. m_d = v),
 // indexed by node; only the level's nodes are written.  Each section (and so each instance)
 // starts on a 128-byte boundary, for the 16-byte vector accesses.
 __host__ __device__ inline size_t ws_pad(size_t f) { return (f + 31) & ~(size_t)31; }
 __host__ __device__ inline size_t ws_E_off(int n) { return ws_pad((size_t)n * kN); }
 __host__ __device__ inline size_t ws_P_off(int n, int H) { return ws_E_off(n) + ws_pad((size_t)n * H); }
-__host__ __device__ inline size_t ws_floats_per_inst(int n, int H) {
-  return ws_P_off(n, H) + ws_pad((size_t)n * H * kP);
+__host__ __device__ inline size_t ws_D_off(int n, int H) { return ws_P_off(n, H) + ws_pad((size_t)n * H * kP); }
+__host__ __device__ inline size_t ws_floats_per_inst(int n, int H) { return ws_D_off(n, H) + ws_pad((size_t)n * MAXP); }
+
+// pre-conv row of tap source src of one instance: an earlier node of the tree, or the ring row
+// src positions before the committed head hm
+__device__ __forceinline__ const uint16_t* tap_row_of(const uint16_t* xbc, const uint16_t* ring, int hm, int R,
+                                                      int conv_dim, int src) {
+  if (src >= 0) return xbc + (size_t)src * conv_dim;
+  int p = hm + src;
+  if (p < 0) p += R;
+  return ring + (size_t)p * conv_dim;
+}
+
+// Shared-memory layout of draft_tree_bc_kernel (byte offsets, multiples of 128).
+struct BcLayout {
+  int Bu, Cf, pslot, plen, total;
+};
+__host__ __device__ inline BcLayout bc_layout(int n) {
+  auto up = [](int b) { return (b + 127) & ~127; };
+  BcLayout L;
+  int o = up((int)sizeof(LevelSetup));
+  L.Bu = o;    o += up(n * kN * 4);      // B, by slot
+  L.Cf = o;    o += up(n * kN * 4);      // C, by position
+  L.pslot = o; o += up(n * MAXP * 4);    // path slots, root first, by position
+  L.plen = o;  o += up(n * 4);
+  L.total = o;
+  return L;
+}
+
+// Root-to-node paths of the level's nodes as slots (threads over positions).
+__device__ __forceinline__ void level_paths(const LevelSetup& ls, int* pslot, int* plen) {
+  for (int f = threadIdx.x; f < ls.nf; f += blockDim.x) {
+    int u = ls.front[f];
+    const int len = ls.dep[u] + 1;
+    for (int k = len - 1; k >= 0; --k) {
+      pslot[f * MAXP + k] = ls.slot[u];
+      u = ls.par[u];
+    }
+    plen[f] = len;
+  }
+}
+
+// One CTA per instance: the per-instance part of a level, done once rather than by each head
+// block.  B of the ancestors (their logged values) and B | C of the level's nodes (four conv
+// taps each, conv + SiLU; B logged), C rows to the workspace, then the B·C products along
+// every level node's path.  Checks and reports the layout.
+__global__ void __launch_bounds__(TTHREADS) draft_tree_bc_kernel(DraftTreeArgs a, float* ws) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  LevelSetup& ls = *reinterpret_cast<LevelSetup*>(smem);
+  const int n = a.n;
+  const BcLayout Lo = bc_layout(n);
+  float* Bu = reinterpret_cast<float*>(smem + Lo.Bu);
+  float* Cf = reinterpret_cast<float*>(smem + Lo.Cf);
+  int* pslot = reinterpret_cast<int*>(smem + Lo.pslot);
+  int* plen = reinterpret_cast<int*>(smem + Lo.plen);
+  // the head blocks may start once every CTA here runs; they wait for this grid's completion
+  // before they read the products
+  launch_dependents();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long inst = blockIdx.x;
+  const int seq = (int)(inst / a.L), layer = (int)(inst % a.L);
+  const int H = a.H, d_inner = H * kP, conv_dim = d_inner + 2 * kN;
+  const size_t node0 = (size_t)inst * n;
+  int hm = a.ring_head[inst] % a.R;
+  if (hm < 0) hm += a.R;
+  if (warp == 0) level_setup(ls, a.layout + (size_t)seq * n, n, a.level, a.status, true);
+  __syncthreads();
+  const int nf = ls.nf, nu = ls.nu, na = nu - nf;  // slots [0, na): the ancestors; then the level
+  if (nf == 0) return;
+  const uint16_t* xbc = a.xBC + node0 * conv_dim;
+  const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
+  const float4* cw4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
+  const int cb = d_inner + tid;  // B (tid < kN) or C channel of this thread
+  const float4 wb = cw4[cb];
+  const float bb = a.conv_b[(size_t)layer * conv_dim + cb];
+  float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
+  // every load of a round in flight: B of 8 ancestors, four taps of 4 level nodes
+  for (int r0 = 0; 8 * r0 < na || 4 * r0 < nf; ++r0) {
+    float ab[8], lb[4][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int sl = 8 * r0 + i;
+      if (sl < na && tid < kN) ab[i] = __ldg(a.log_B + (node0 + ls.snode[sl]) * kN + tid);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int f = 4 * r0 + i;
+      if (f < nf) {
+        const int v = ls.front[f];
+        lb[i][0] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, ls.tap[v][2]) + cb));
+        lb[i][1] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, ls.tap[v][1]) + cb));
+        lb[i][2] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, ls.tap[v][0]) + cb));
+        lb[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cb));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int sl = 8 * r0 + i;
+      if (sl < na && tid < kN) Bu[sl * kN + tid] = ab[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int f = 4 * r0 + i;
+      if (f < nf) {
+        const int v = ls.front[f];
+        const float val = conv4_silu(wb, bb, lb[i][0], lb[i][1], lb[i][2], lb[i][3]);
+        if (tid < kN) {
+          Bu[(na + f) * kN + tid] = val;
+          a.log_B[(node0 + v) * kN + tid] = val;
+        } else {
+          Cf[f * kN + tid - kN] = val;
+          wsi[(size_t)v * kN + tid - kN] = val;
+        }
+      }
+    }
+  }
+  level_paths(ls, pslot, plen);
+  __syncthreads();
+  // B_{m_k} · C_v: one warp per (level node, path index)
+  float* wsD = wsi + ws_D_off(n, H);
+  for (int q = warp; q < nf * MAXP; q += TTHREADS / 32) {
+    const int f = q / MAXP, k = q - f * MAXP;
+    if (k >= plen[f]) continue;
+    const float4 b4 = reinterpret_cast<const float4*>(Bu + pslot[f * MAXP + k] * kN)[lane];
+    const float4 c4 = reinterpret_cast<const float4*>(Cf + f * kN)[lane];
+    float d = b4.x * c4.x;
+    d = fmaf(b4.y, c4.y, d);
+    d = fmaf(b4.z, c4.z, d);
+    d = fmaf(b4.w, c4.w, d);
+    d = warp_sum(d);
+    if (lane == 0) wsD[(size_t)ls.front[f] * MAXP + k] = d;
+  }
 }
 
 struct PrepFixed {
@@ -165,15 +299,13 @@ struct PrepFixed {
 // Shared-memory layout of draft_tree_prep_kernel for trees of n nodes (byte offsets, each a
 // multiple of 128).  Slots index the nodes on the level's paths, positions the level's nodes.
 struct PrepLayout {
-  int xu, Bu, Cf, coef, du, su, pslot, plen, total;
+  int xu, coef, du, su, pslot, plen, total;
 };
 __host__ __device__ inline PrepLayout prep_layout(int n) {
   auto up = [](int b) { return (b + 127) & ~127; };
   PrepLayout L;
   int o = up((int)sizeof(PrepFixed));
   L.xu = o;    o += up(n * PROWS * 4);       // x of the block's channels, by slot
-  L.Bu = o;    o += up(n * kN * 4);          // B, by slot
-  L.Cf = o;    o += up(n * kN * 4);          // C, by position
   L.coef = o;  o += up(n * MAXP * PG * 4);   // e^{S_v − S_m} Δ_m (B_m · C_v), by position and path index
   L.du = o;    o += up(n * PG * 4);          // Δ, by slot
   L.su = o;    o += up(n * PG * 4);          // S = Σ Δ·A from the root, inclusive, by slot
@@ -183,14 +315,17 @@ __host__ __device__ inline PrepLayout prep_layout(int n) {
   return L;
 }
 
+// One CTA per instance and block of 4 heads, launched as a dependent grid of
+// draft_tree_bc_kernel: x of the block's channels for the ancestors (logged) and the level's
+// nodes (conv + SiLU, logged), Δ (logged for the level), S along the paths; then, once the
+// B·C products are complete, e^{S_v} and the path coefficients of its heads and the path sums
+// of its rows.
 __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeArgs a, float* ws) {
   extern __shared__ __align__(128) unsigned char smem[];
   PrepFixed& s = *reinterpret_cast<PrepFixed*>(smem);
   const int n = a.n;
   const PrepLayout Lo = prep_layout(n);
   float* xu = reinterpret_cast<float*>(smem + Lo.xu);
-  float* Bu = reinterpret_cast<float*>(smem + Lo.Bu);
-  float* Cf = reinterpret_cast<float*>(smem + Lo.Cf);
   float* coef = reinterpret_cast<float*>(smem + Lo.coef);
   float* du = reinterpret_cast<float*>(smem + Lo.du);
   float* su = reinterpret_cast<float*>(smem + Lo.su);
@@ -210,7 +345,7 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
 
   int hm = a.ring_head[inst] % a.R;  // ring position of the committed head (loaded with the layout)
   if (hm < 0) hm += a.R;
-  if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, blk == 0);
+  if (warp == 0) level_setup(s.ls, a.layout + (size_t)seq * n, n, a.level, a.status, false);
   if (warp == 1 && lane < PG) {
     const bool on = lane < heads;
     s.A[lane] = on ? neg_exp(a.A_log[(size_t)layer * H + h_begin + lane]) : 0.f;
@@ -221,27 +356,17 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
   if (nf == 0) return;
   const uint16_t* xbc = a.xBC + node0 * conv_dim;
   const uint16_t* ring = a.ring + (size_t)inst * a.R * conv_dim;
-  // pre-conv row of tap source src (an earlier node, or the ring row src positions before the head)
-  auto tap_row = [&](int src) -> const uint16_t* {
-    if (src >= 0) return xbc + (size_t)src * conv_dim;
-    int p = hm + src;
-    if (p < 0) p += a.R;
-    return ring + (size_t)p * conv_dim;
-  };
 
-  // ---- every input in one batch per round: x (the block's channels) and B of 8 ancestors
-  // (one logged value each), and x, B or C of 4 level nodes (four taps each, through the
-  // conv + SiLU, logged here); Δ for each slot ----
+  // ---- x of the block's channels, in rounds with every load of a round in flight: 8
+  // ancestors (one logged value each) and 4 level nodes (four taps each, through the conv +
+  // SiLU, logged here); Δ for each slot ----
   {
     const float4* cw4 = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
     const float* cbv = a.conv_b + (size_t)layer * conv_dim;
     const bool live = tid < rows;
     const int cx = h_begin * kP + tid;  // x channel of this thread
-    const int cb = d_inner + tid;       // B (tid < kN) or C channel of this thread
     const float4 wx = live ? cw4[cx] : make_float4(0.f, 0.f, 0.f, 0.f);
     const float bx = live ? cbv[cx] : 0.f;
-    const float4 wb = cw4[cb];
-    const float bb = cbv[cb];
     float dval = 0.f;  // Δ: one (slot, head) per thread
     int d_sl = -1, d_g = 0;
     bool d_conv = false;
@@ -260,64 +385,39 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
       }
     }
     for (int r0 = 0; 8 * r0 < na || 4 * r0 < nf; ++r0) {
-      float ax[8], ab[8];      // ancestors 8 r0 .. 8 r0 + 7: logged x, logged B
-      float lx[4][4], lb[4][4];  // level nodes 4 r0 .. 4 r0 + 3: taps of x, of B or C
+      float ax[8];     // ancestors 8 r0 .. 8 r0 + 7: logged x
+      float lx[4][4];  // level nodes 4 r0 .. 4 r0 + 3: taps of x
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int sl = 8 * r0 + i;
-        if (sl < na) {
-          const int v = s.ls.snode[sl];
-          if (live) ax[i] = __ldg(a.log_x + (node0 + v) * d_inner + cx);
-          if (tid < kN) ab[i] = __ldg(a.log_B + (node0 + v) * kN + tid);
-        }
+        if (sl < na && live) ax[i] = __ldg(a.log_x + (node0 + s.ls.snode[sl]) * d_inner + cx);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int f = 4 * r0 + i;
-        if (f < nf) {
+        if (f < nf && live) {
           const int v = s.ls.front[f];
-          const uint16_t* t2 = tap_row(s.ls.tap[v][2]);
-          const uint16_t* t1 = tap_row(s.ls.tap[v][1]);
-          const uint16_t* t0 = tap_row(s.ls.tap[v][0]);
-          const uint16_t* t3 = xbc + (size_t)v * conv_dim;
-          if (live) {
-            lx[i][0] = bf16f(__ldg(t2 + cx));
-            lx[i][1] = bf16f(__ldg(t1 + cx));
-            lx[i][2] = bf16f(__ldg(t0 + cx));
-            lx[i][3] = bf16f(__ldg(t3 + cx));
-          }
-          lb[i][0] = bf16f(__ldg(t2 + cb));
-          lb[i][1] = bf16f(__ldg(t1 + cb));
-          lb[i][2] = bf16f(__ldg(t0 + cb));
-          lb[i][3] = bf16f(__ldg(t3 + cb));
+          lx[i][0] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, s.ls.tap[v][2]) + cx));
+          lx[i][1] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, s.ls.tap[v][1]) + cx));
+          lx[i][2] = bf16f(__ldg(tap_row_of(xbc, ring, hm, a.R, conv_dim, s.ls.tap[v][0]) + cx));
+          lx[i][3] = bf16f(__ldg(xbc + (size_t)v * conv_dim + cx));
         }
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int sl = 8 * r0 + i;
-        if (sl < na) {
-          xu[sl * PROWS + tid] = live ? ax[i] : 0.f;
-          if (tid < kN) Bu[sl * kN + tid] = ab[i];
-        }
+        if (sl < na) xu[sl * PROWS + tid] = live ? ax[i] : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int f = 4 * r0 + i;
         if (f < nf) {
-          const int v = s.ls.front[f], sl = na + f;
           float x = 0.f;
           if (live) {
             x = conv4_silu(wx, bx, lx[i][0], lx[i][1], lx[i][2], lx[i][3]);
-            a.log_x[(node0 + v) * d_inner + cx] = x;
+            a.log_x[(node0 + s.ls.front[f]) * d_inner + cx] = x;
           }
-          xu[sl * PROWS + tid] = x;
-          const float val = conv4_silu(wb, bb, lb[i][0], lb[i][1], lb[i][2], lb[i][3]);
-          if (tid < kN) {
-            Bu[sl * kN + tid] = val;
-            if (blk == 0) a.log_B[(node0 + v) * kN + tid] = val;
-          } else {
-            Cf[f * kN + tid - kN] = val;
-          }
+          xu[(na + f) * PROWS + tid] = x;
         }
       }
     }
@@ -337,42 +437,25 @@ __global__ void __launch_bounds__(TTHREADS, 3) draft_tree_prep_kernel(DraftTreeA
     for (int u = s.ls.snode[sl]; u >= 0; u = s.ls.par[u]) acc = fmaf(du[s.ls.slot[u] * PG + g], s.A[g], acc);
     su[sl * PG + g] = acc;
   }
-  for (int f = tid; f < nf; f += TTHREADS) {
-    int u = s.ls.front[f];
-    const int len = s.ls.dep[u] + 1;
-    for (int k = len - 1; k >= 0; --k) {
-      pslot[f * MAXP + k] = s.ls.slot[u];
-      u = s.ls.par[u];
-    }
-    plen[f] = len;
-  }
+  level_paths(s.ls, pslot, plen);
   __syncthreads();
   float* wsi = ws + (size_t)inst * ws_floats_per_inst(n, H);
-  float* wsC = wsi;                          // [n][kN]
   float* wsE = wsi + ws_E_off(n);            // [n][H]
   float* wsP = wsi + ws_P_off(n, H);         // [n][d_inner]
-  // e^{S_v}; C rows (first block); the path coefficients: one warp per (node, path index)
+  const float* wsD = wsi + ws_D_off(n, H);   // [n][MAXP], written by draft_tree_bc_kernel
+  // e^{S_v}
   for (int i = tid; i < nf * PG; i += TTHREADS) {
     const int f = i / PG, g = i - f * PG;
     if (g < heads) wsE[(size_t)s.ls.front[f] * H + h_begin + g] = expf(su[pslot[f * MAXP + plen[f] - 1] * PG + g]);
   }
-  if (blk == 0)
-    for (int i = tid; i < nf * (kN / 4); i += TTHREADS) {
-      const int f = i / (kN / 4), q = i - f * (kN / 4);
-      reinterpret_cast<float4*>(wsC + (size_t)s.ls.front[f] * kN)[q] = reinterpret_cast<const float4*>(Cf + f * kN)[q];
-    }
-  for (int q = warp; q < nf * MAXP; q += TTHREADS / 32) {
-    const int f = q / MAXP, k = q - f * MAXP;
+  grid_dependency_wait();  // the B·C products
+  // path coefficients: one (node, path index, head) per thread
+  for (int i = tid; i < nf * MAXP * PG; i += TTHREADS) {
+    const int f = i / (MAXP * PG), r = i - f * (MAXP * PG), k = r / PG, g = r - k * PG;
     if (k >= plen[f]) continue;
     const int sm = pslot[f * MAXP + k], sv = pslot[f * MAXP + plen[f] - 1];
-    const float4 b4 = reinterpret_cast<const float4*>(Bu + sm * kN)[lane];
-    const float4 c4 = reinterpret_cast<const float4*>(Cf + f * kN)[lane];
-    float d = b4.x * c4.x;
-    d = fmaf(b4.y, c4.y, d);
-    d = fmaf(b4.z, c4.z, d);
-    d = fmaf(b4.w, c4.w, d);
-    d = warp_sum(d);
-    if (lane < PG) coef[(f * MAXP + k) * PG + lane] = expf(su[sv * PG + lane] - su[sm * PG + lane]) * du[sm * PG + lane] * d;
+    coef[(f * MAXP + k) * PG + g] =
+        expf(su[sv * PG + g] - su[sm * PG + g]) * du[sm * PG + g] * __ldcg(wsD + (size_t)s.ls.front[f] * MAXP + k);
   }
   __syncthreads();
   // path sums of the block's rows: Σ_k coef_k x_{m_k}[row] + D x_v[row]
@@ -492,8 +575,8 @@ __global__ void __launch_bounds__(MTHREADS, 2) draft_tree_level_kernel(DraftTree
   MainFixed& s = *reinterpret_cast<MainFixed*>(smem);
   float* stages = reinterpret_cast<float*>(smem + main_h_offset());
   const int n = a.n;
-  const int tid = threadIdx.x, warp = tid >> 5, o = tid & 7, rsub = tid >> 3;
-  const int H = a.H, d_inner = H * kP;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int H = a.H;
   const long long items = (long long)a.n_seq * a.L * H;
   const long long it0 = blockIdx.x * items / gridDim.x, it1 = (blockIdx.x + 1) * items / gridDim.x;
   const int count = (int)(it1 - it0);
@@ -735,13 +818,28 @@ cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, void* workspace, cud
   const long long inst = (long long)a.n_seq * a.L;
   if (inst == 0) return cudaSuccess;
   float* ws = static_cast<float*>(workspace);
+  // programmatic dependent launch: each grid may be scheduled while the one before it runs,
+  // and waits for it before reading what it writes
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  const int bsmem = bc_layout(a.n).total;
+  cudaError_t e = cudaFuncSetAttribute(draft_tree_bc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bsmem);
+  if (e != cudaSuccess) return e;
+  draft_tree_bc_kernel<<<(unsigned)inst, TTHREADS, bsmem, s>>>(a, ws);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int n_blocks = (a.H + PG - 1) / PG;
   const int psmem = prep_layout(a.n).total;
-  cudaError_t e = cudaFuncSetAttribute(draft_tree_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
+  e = cudaFuncSetAttribute(draft_tree_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, psmem);
   if (e != cudaSuccess) return e;
-  draft_tree_prep_kernel<<<(unsigned)(inst * n_blocks), TTHREADS, psmem, s>>>(a, ws);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t pcfg = {};
+  pcfg.gridDim = dim3((unsigned)(inst * n_blocks));
+  pcfg.blockDim = dim3(TTHREADS);
+  pcfg.dynamicSmemBytes = (size_t)psmem;
+  pcfg.stream = s;
+  pcfg.attrs = attr;
+  pcfg.numAttrs = 1;
+  if ((e = cudaLaunchKernelEx(&pcfg, draft_tree_prep_kernel, a, ws)) != cudaSuccess) return e;
   const int smem = level_smem_bytes();
   e = cudaFuncSetAttribute(draft_tree_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -755,10 +853,7 @@ cudaError_t launch_draft_tree_level(const DraftTreeArgs& a, void* workspace, cud
   cfg.blockDim = dim3(MTHREADS);
   cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the prep runs
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
+  cfg.attrs = attr;  // may start while the prep runs
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, draft_tree_level_kernel, a, static_cast<const float*>(ws));
 }
