@@ -225,3 +225,21 @@ def test_draft_tree_runs_across_sequences():
     y, logs, status = draft_levels(d)
     assert int(status) == 0
     check_levels(b, w, d, y, logs, [(i, j) for i in range(2) for j in (0, 3, 7)])
+
+
+def test_draft_tree_bad_layout_is_flagged_and_writes_nothing():
+    # sequence 1's node 3 takes a conv tap from a later node: that sequence's instances write
+    # no log row and no y at any level, the status says so, sequence 0 is unaffected
+    from speculative_decoding_mamba2_gb300 import SSM_STATUS_BAD_LAYOUT
+    w = Workload(59, "draft tree bad layout", Shape(H=3), n_layers=2, batch=2, trees=(("random", 12, 3, 4),))
+    b = batch(w)
+    d = upload(b, w)
+    lay = d["layout"].view(2, d["n"], 8)
+    lay[1, 3, 4] = 5  # tap d = 1 of node 3 -> node 5
+    y, logs, status = draft_levels(d)
+    assert int(status) & SSM_STATUS_BAD_LAYOUT
+    L = len(b["layers"])
+    bad = slice(L, 2 * L)
+    assert torch.isnan(y[bad]).all() and torch.isnan(logs["x"][bad]).all()
+    assert torch.isnan(logs["B"][bad]).all() and torch.isnan(logs["delta"][bad]).all()
+    check_levels(b, w, d, y, logs, [(0, 0), (0, 1)])
