@@ -222,7 +222,8 @@ def test_draft_tree_validation(L):
     assert _level(L, d, p, h=ctypes.c_void_p(24)) == B.SSM_ERR_INVALID_ARG  # not 16-byte aligned
     assert _level(L, d, _prm(null=True)) == B.SSM_ERR_INVALID_ARG
     need = L.ssm_draft_tree_workspace_size(ctypes.byref(d), 1, 16)
-    assert need >= 16 * (128 + 4 + 4 * 64) * 4 * d.n_layers  # C rows, e^S, path sums per node and instance
+    # C rows, e^S, path sums and the 16 path products per node and instance, each part 128-byte aligned
+    assert need >= 16 * (128 + d.n_heads + d.n_heads * 64 + 16) * 4 * d.n_layers and need % 128 == 0
     assert _level(L, d, p, ws_bytes=need - 1) == B.SSM_ERR_CAPACITY
     assert L.ssm_draft_tree_workspace_size(ctypes.byref(d), 1, 65) == 0
     P = FAKE
