@@ -167,12 +167,12 @@ def _oracle_task(args):
     return len(parent)
 
 
-def _oracle_inputs(w, seq, layer):
+def _oracle_inputs(w, seq, layer, tree=0):
     import numpy as np
 
     from synth import batch
     from tests.helpers import f64, params_at
-    b = batch(w, seqs=[seq], layers=[layer])
+    b = batch(w, seqs=[seq], layers=[layer], tree=tree)
     return (params_at(b["params"], 0), b["parent"][0], f64(b["xBC"][0, 0]), f64(b["dt"][0, 0]),
             b["h0"][0, 0].astype(np.float64), f64(b["ring"][0, 0]), int(b["ring_head"][0, 0]), b["tok"][0],
             b["tgt"][0])
@@ -181,7 +181,7 @@ def _oracle_inputs(w, seq, layer):
 class OracleRunner:
     """Spawn pool of single-threaded numpy workers over sampled instances."""
 
-    def __init__(self, w, n_inputs=None):
+    def __init__(self, w, n_inputs=None, tree=0):
         import multiprocessing as mp
         self.cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
         saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
@@ -199,7 +199,7 @@ class OracleRunner:
         while len(insts) < (n_inputs or self.cores):
             insts.append((rnd.randrange(w.batch), rnd.randrange(w.n_layers)))
         self.insts = insts
-        self.inputs = [_oracle_inputs(w, s, l) for s, l in insts]
+        self.inputs = [_oracle_inputs(w, s, l, tree) for s, l in insts]
         self.cursor = 0
 
     def step(self):
@@ -215,8 +215,8 @@ class OracleRunner:
         self.pool.join()
 
 
-def cpu_baseline(w, steps=64):
-    r = OracleRunner(w)
+def cpu_baseline(w, steps=64, tree=0):
+    r = OracleRunner(w, tree=tree)
     r.step()  # warm the workers (imports)
     units = secs = 0.0
     for _ in range(steps):
@@ -226,7 +226,7 @@ def cpu_baseline(w, steps=64):
     r.close()
     return {"value": units / secs, "unit": UNIT, "cores": r.cores, "kind": "oracle",
             "sample": f"{steps} x {r.cores} instances (seq, layer) of the same workload, each verify+accept+commit "
-                      f"of one 16-node tree in fp64 numpy, one instance per core; "
+                      f"of one {w.n_nodes(tree)}-node tree in fp64 numpy, one instance per core; "
                       f"{int(units)} node updates in {secs:.1f} s"}
 
 
@@ -329,7 +329,7 @@ def run_ours(args, w):
                                                    ssm_commit_verify_workspace_size, ssm_tree_layout_build,
                                                    ssm_tree_verify, ssm_tree_verify_workspace_size)
     from speculative_decoding_mamba2_gb300 import build as _build
-    from synth import batch
+    from synth import batch, workload
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -481,9 +481,32 @@ def run_ours(args, w):
     if not args.no_draft:
         draft_tree = run_draft_tree(args, dev, stream, peak, world, rank)
 
-    # ---- the stress workload's chain tree (chain kernel) ----
+    # ---- the target tree verify at batch 1 ----
+    config2 = None
+    if not args.no_config2:
+        config2 = run_config2(args, dev, stream, world, rank, peak, peak_kind)
+        if rank == 0 and cpu is not None:
+            config2["cpu_baseline"] = cpu_baseline(workload(2), steps=4)
+
+    # ---- the stress workload: ternary tree, 256-node chain, 16-step replay ----
+    config4 = None
     chain = None
-    if not args.no_chain:
+    if not args.no_config4:
+        config4 = run_config4(args, dev, stream, world, rank, peak, peak_kind)
+        c = config4["chain"]
+        chain = {"workload": config4["workload"] + " (chain tree)", "nodes": c["nodes"],
+                 "instances_per_gpu": config4["instances_per_gpu"], "ms": c["ssm_tree_verify"]["ms"],
+                 "value": c["nodes"] * config4["instances_per_gpu"] * world / (c["ssm_tree_verify"]["ms"] / 1e3),
+                 "unit": "verified tree-node SSM updates/s (ssm_tree_verify alone)",
+                 "roofline": {"bound": "hbm", "achieved": c["ssm_tree_verify"]["GB/s"], "peak": peak, "unit": "GB/s",
+                              "frac": c["ssm_tree_verify"]["frac_of_hbm_peak"], "peak_source": peak_kind,
+                              "traffic": c["ssm_tree_verify"]["traffic"]},
+                 "bytes": c["ssm_tree_verify"]["bytes"], "state_TFLOP/s": c["state_TFLOP/s"], "fp32_alu": c["fp32_alu"]}
+        if rank == 0 and cpu is not None:
+            config4["cpu_baseline"] = cpu_baseline(workload(4), steps=2)
+            config4["cpu_baseline"]["sample"] += ("; the 40-node ternary tree only: the oracle walks every node's "
+                                                  "path, about 46 s per 256-node chain instance on one core")
+    elif not args.no_chain:
         chain = run_chain(args, dev, stream, world, rank)
 
     # ---- whole blocks: the dense steps either side of the SSM ----
@@ -506,6 +529,10 @@ def run_ours(args, w):
             line["draft"] = draft
         if draft_tree is not None:
             line["draft_tree"] = draft_tree
+        if config2 is not None:
+            line["config2"] = config2
+        if config4 is not None:
+            line["config4"] = config4
         if chain is not None:
             line["chain"] = chain
         if block is not None:
@@ -516,6 +543,266 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def folded_rounds(w, b, dev, stream, world, steps, warmup, flush=None, tree=0):
+    """Speculative rounds of one tree workload through the folded call: round r runs
+    ssm_commit_verify (commit of round r-1's accepted path, verify of round r's tree; two
+    input buffers alternate) and ssm_accept_path.  CUDA events around each call of each
+    timed round; `flush` (a device buffer larger than L2) is rewritten before every round,
+    outside the events, when the round's working set would otherwise stay in L2.
+    Returns the mean event times, the path lengths and the device state."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_accept_path, ssm_commit_verify,
+                                                   ssm_commit_verify_workspace_size, ssm_tree_layout_build,
+                                                   ssm_tree_verify, ssm_tree_verify_workspace_size)
+    S, L, n = len(b["seqs"]), w.n_layers, b["n_nodes"]
+    H, P, N = w.shape.H, w.shape.P, w.shape.N
+    I = S * L
+    dims = Dims(n_heads=H, n_layers=L, ring_cap=w.ring_cap)
+    bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    spec = w.trees[tree]
+    layout_h, depth = ssm_tree_layout_build(b["parent"], max_branches=3, max_depth=depth_cap(spec))
+    max_path = depth + 1
+    prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(dev) for k, v in b["params"].items()}
+    layout = torch.from_numpy(layout_h).to(dev)
+    xBC = [bf16(b["xBC"]), bf16(b["xBC"])]
+    dt = [bf16(b["dt"]), bf16(b["dt"])]
+    h = torch.from_numpy(b["h0"]).to(dev)
+    ring = bf16(b["ring"])
+    head = torch.from_numpy(b["ring_head"]).to(dev)
+    tok, tgt = torch.from_numpy(b["tok"]).to(dev), torch.from_numpy(b["tgt"]).to(dev)
+    y = torch.empty((I, n, H * P), device=dev)
+    path = torch.empty((S, max_path), dtype=torch.int32, device=dev)
+    plen = torch.empty(S, dtype=torch.int32, device=dev)
+    bonus = torch.empty(S, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, depth), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(ssm_commit_verify_workspace_size(dims, S, n, depth, max_path), dtype=torch.uint8, device=dev)
+    # the rounds start from a verified and accepted tree whose commit is pending
+    ssm_tree_verify(dims, prm, S, n, depth, layout, xBC[0], dt[0], h, ring, head, y, ws, status)
+    ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status)
+    del ws
+    rounds = [0]
+
+    def one(ev=None):
+        cur, prev = (rounds[0] + 1) % 2, rounds[0] % 2
+        rounds[0] += 1
+        if flush is not None:
+            flush.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
+        ssm_commit_verify(dims, prm, S, n, layout, max_path, path, plen, xBC[prev], dt[prev], n, depth, layout,
+                          xBC[cur], dt[cur], h, ring, head, y, ws_f, status)
+        if ev is not None:
+            ev[1].record(stream)
+        ssm_accept_path(S, n, max_path, layout, tok, tgt, path, plen, bonus, status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    path_lens = plen.cpu().numpy()
+    _, evs = _timed(steps, lambda k, ev: one(ev), world, stream, 3)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the rounds of {w.name}")
+    cv_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+    acc_ms = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in evs), world, dev)
+    round_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in evs), world, dev)
+    return {"cv_ms": cv_ms, "acc_ms": acc_ms, "round_ms": round_ms, "path_lens": path_lens, "h": h, "ring": ring,
+            "head": head, "prm": prm, "dims": dims, "S": S, "L": L, "n": n, "depth": depth}
+
+
+def depth_cap(spec):
+    """max_depth cap passed to the layout build for a tree spec (the tree_config of the workload)."""
+    if spec[0] == "random":
+        return spec[3]
+    if spec[0] == "full":
+        return spec[2]
+    return spec[1] - 1
+
+
+def tree_roofline(w, r, peak, peak_kind, n_units, world):
+    """Roofline of one folded round (ssm_commit_verify) and the round's throughput."""
+    import numpy as np
+    H, P, N = w.shape.H, w.shape.P, w.shape.N
+    pb = r["L"] * params_bytes_per_layer(H, P, N)
+    fb = sum(r["L"] * commit_verify_bytes_per_instance(H, P, N, r["n"], int(pl)) for pl in r["path_lens"]) + pb
+    ach = fb / r["cv_ms"] / 1e6
+    return {"value": n_units * world / (r["round_ms"] / 1e3), "unit": UNIT, "ms_per_round": r["round_ms"],
+            "ssm_commit_verify": {"ms": r["cv_ms"], "launches_per_round": 2},
+            "ssm_accept_path": {"ms": r["acc_ms"], "launches_per_round": 1},
+            "mean_accepted_path": float(np.mean(r["path_lens"])),
+            "roofline": {"bound": "hbm", "kernel": "ssm_commit_verify (tree_prep_kernel + tree_verify_kernel)",
+                         "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback", "algorithmic_bytes": fb}}
+
+
+def run_config2(args, dev, stream, world, rank, peak, peak_kind):
+    """The target tree verify at batch 1 (Mamba2-2.7B shape, 64 layers, one 16-node random
+    tree per rank): folded rounds (ssm_commit_verify + ssm_accept_path).  The round touches
+    about 0.33 GB, a little more than L2, so a 256 MB buffer is rewritten before every
+    round (outside the events): every round reads the state from HBM."""
+    import torch
+
+    from synth import batch, workload
+    w = workload(2)
+    b = batch(w, seqs=shard_sequences(w.batch, rank))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    steps = max(20, min(args.steps, 200))
+    r = folded_rounds(w, b, dev, stream, world, steps, args.warmup, flush=flush)
+    out = {"workload": w.name, "sequences_per_gpu": r["S"], "layers": r["L"], "nodes_per_tree": r["n"],
+           "steps": steps, "l2": "256 MB written before every round (outside the timed events)"}
+    out.update(tree_roofline(w, r, peak, peak_kind, r["n"] * r["L"] * r["S"], world))
+    return out
+
+
+def run_config4(args, dev, stream, world, rank, peak, peak_kind):
+    """The stress workload (Mamba2-780M shape, 48 layers, batch 64 per rank), each round:
+      * ternary: the 40-node full ternary tree of depth 3 through the folded call
+        (ssm_commit_verify: commit of the previous round's accepted path, verify) +
+        ssm_accept_path;
+      * chain: the 256-node chain tree verified from the same committed state
+        (ssm_tree_verify, which takes the chain kernels), ssm_accept_path, and ssm_commit
+        of its accepted path into a state buffer of its own (set up as a copy of the
+        committed state; the per-round copy is not part of the timed work);
+      * replay: the draft's ssm_replay of 16 logged steps for every instance (the logs
+        written by 16 ssm_draft_step calls before the timed rounds).
+    Every part touches far more than L2.  Inputs come from the seeded generator on a pool
+    of host processes (synth.batch_parallel, identical to synth.batch)."""
+    import numpy as np
+    import torch
+
+    from speculative_decoding_mamba2_gb300 import (ssm_accept_path, ssm_commit, ssm_draft_step, ssm_replay,
+                                                   ssm_tree_layout_build, ssm_tree_verify,
+                                                   ssm_tree_verify_workspace_size)
+    from synth import batch_parallel, draft_inputs, workload
+    w = workload(4)
+    seqs = shard_sequences(w.batch, rank)
+    t_gen = time.perf_counter()
+    b = batch_parallel(w, seqs=seqs)
+    bc = batch_parallel(w, seqs=seqs, tree=1, with_state=False)
+    t_gen = time.perf_counter() - t_gen
+    H, P, N = w.shape.H, w.shape.P, w.shape.N
+    steps = max(5, min(args.steps, 10))
+    r = folded_rounds(w, b, dev, stream, world, steps, args.warmup)
+    tern = tree_roofline(w, r, peak, peak_kind, r["n"] * r["L"] * r["S"], world)
+    dims, prm, S, L = r["dims"], r["prm"], r["S"], r["L"]
+    I = S * L
+    del b
+
+    # ---- the chain tree, from the committed state ----
+    bf16 = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    nc = bc["n_nodes"]
+    lay_c, depth_c = ssm_tree_layout_build(bc["parent"])
+    lay_c = torch.from_numpy(lay_c).to(dev)
+    xc, dc = bf16(bc["xBC"]), bf16(bc["dt"])
+    tok_c, tgt_c = torch.from_numpy(bc["tok"]).to(dev), torch.from_numpy(bc["tgt"]).to(dev)
+    del bc
+    h, ring, head = r["h"], r["ring"], r["head"]
+    h_c, ring_c, head_c = h.clone(), ring.clone(), head.clone()
+    yc = torch.empty((I, nc, dims.d_inner), device=dev)
+    ws_c = torch.empty(ssm_tree_verify_workspace_size(dims, S, nc, depth_c), dtype=torch.uint8, device=dev)
+    mp_c = nc
+    path_c = torch.empty((S, mp_c), dtype=torch.int32, device=dev)
+    plen_c = torch.empty(S, dtype=torch.int32, device=dev)
+    bonus_c = torch.empty(S, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def chain_round(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ssm_tree_verify(dims, prm, S, nc, depth_c, lay_c, xc, dc, h, ring, head, yc, ws_c, status)
+        if ev is not None:
+            ev[1].record(stream)
+        ssm_accept_path(S, nc, mp_c, lay_c, tok_c, tgt_c, path_c, plen_c, bonus_c, status)
+        if ev is not None:
+            ev[2].record(stream)
+        ssm_commit(dims, prm, S, nc, lay_c, mp_c, path_c, plen_c, xc, dc, h_c, ring_c, head_c, status)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(2):
+        chain_round()
+    torch.cuda.synchronize()
+    _, evs = _timed(steps, lambda k, ev: chain_round(ev), world, stream, 4)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the chain rounds")
+    cvm = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+    cam = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in evs), world, dev)
+    ccm = max_over_ranks(statistics.mean(e[2].elapsed_time(e[3]) for e in evs), world, dev)
+    plc = plen_c.cpu().numpy()
+    del yc, ws_c, xc, dc, h_c, ring_c
+    d_inner, conv_dim = H * P, H * P + 2 * N
+    cby = I * (H * P * N * 4 + nc * conv_dim * 2 + nc * H * 2 + 3 * conv_dim * 2 + nc * d_inner * 4)
+    ccb = sum(L * commit_bytes_per_instance(H, P, N, int(pl)) for pl in plc) + L * params_bytes_per_layer(H, P, N)
+    chain = {"nodes": nc, "ms_per_round": cvm + cam + ccm, "mean_accepted_path": float(plc.mean()),
+             "value": nc * I * world / ((cvm + cam + ccm) / 1e3), "unit": UNIT,
+             "ssm_tree_verify": {"ms": cvm, "bytes": cby, "GB/s": cby / cvm / 1e6,
+                                 "frac_of_hbm_peak": cby / cvm / 1e6 / peak,
+                                 "traffic": ncu_traffic("ssm_tree_verify_chain", I)},
+             "ssm_accept_path": {"ms": cam},
+             "ssm_commit": {"ms": ccm, "bytes": ccb, "GB/s": ccb / ccm / 1e6, "frac_of_hbm_peak": ccb / ccm / 1e6 / peak}}
+    flops = 4.0 * nc * H * P * N * I
+    tf = flops / (cvm / 1e3) / 1e12
+    chain["state_TFLOP/s"] = tf
+    chain["fp32_alu"] = {"achieved": tf, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_ALU_TFLOPS,
+                         "note": "context only: the CUDA-core bound of a plain recurrence; the chain kernels "
+                                 "run their products on the tensor cores"}
+
+    # ---- the draft's replay of 16 logged steps (780M shape, every instance) ----
+    T = w.draft_steps
+    xs = torch.empty((T, I, conv_dim), dtype=torch.int16)
+    dts = torch.empty((T, I, H), dtype=torch.int16)
+    for i, q in enumerate(seqs):
+        for l in range(L):
+            xb, db = draft_inputs(w, q, l)
+            xs[:, i * L + l] = torch.from_numpy(xb.view(np.int16))
+            dts[:, i * L + l] = torch.from_numpy(db.view(np.int16))
+    xs = xs.to(dev).view(torch.bfloat16)
+    dts = dts.to(dev).view(torch.bfloat16)
+    h_ck = h.clone()
+    h_work = torch.empty_like(h_ck)
+    log_d = torch.zeros(I, T, H, device=dev)
+    log_b = torch.zeros(I, T, N, device=dev)
+    log_x = torch.zeros(I, T, d_inner, device=dev)
+    log_len = torch.zeros(I, dtype=torch.int32, device=dev)
+    yd = torch.empty(I, d_inner, device=dev)
+    for t in range(T):
+        ssm_draft_step(dims, prm, S, t, T, xs[t], dts[t], h_ck if t == 0 else h_work, h_work, ring, head,
+                       log_d, log_b, log_x, log_len, yd, status)
+    del h_work, xs, dts
+    kk = torch.full((S,), T, dtype=torch.int32, device=dev)
+    head_d = head.clone()
+
+    def replay(ev=None):
+        log_len.fill_(T)  # the logs stay valid; replay consumed the count
+        if ev is not None:
+            ev[0].record(stream)
+        ssm_replay(dims, prm, S, T, kk, log_d, log_b, log_x, log_len, h_ck, head_d, status)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(2):
+        replay()
+    torch.cuda.synchronize()
+    _, evs = _timed(steps, lambda k, ev: replay(ev), world, stream, 2)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the replays")
+    rpm = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in evs), world, dev)
+    rb = replay_bytes(H, P, N, I, T)
+    rep = {"steps_replayed": T, "ms": rpm, "bytes": rb, "GB/s": rb / rpm / 1e6, "frac_of_hbm_peak": rb / rpm / 1e6 / peak}
+    round_ms = tern["ms_per_round"] + chain["ms_per_round"] + rpm
+    out = {"workload": w.name, "sequences_per_gpu": S, "layers": L, "instances_per_gpu": I, "steps": steps,
+           "ms_per_round": round_ms, "value": (r["n"] + nc) * I * world / (round_ms / 1e3), "unit": UNIT,
+           "note": "one round = ternary (ssm_commit_verify + ssm_accept_path) + chain (ssm_tree_verify + "
+                   "ssm_accept_path + ssm_commit) + ssm_replay of 16 steps; every part exceeds L2",
+           "input_generation_s": t_gen, "ternary": tern, "chain": chain, "replay": rep}
+    return out
 
 
 def run_chain(args, dev, stream, world, rank, seqs_per_rank=8):
@@ -1378,7 +1665,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-draft", action="store_true")
-    ap.add_argument("--no-chain", action="store_true")
+    ap.add_argument("--no-chain", action="store_true", help="with --no-config4: skip the chain sample too")
+    ap.add_argument("--no-config2", action="store_true", help="skip the batch-1 target verify workload")
+    ap.add_argument("--no-config4", action="store_true", help="skip the stress workload (batch 64)")
     ap.add_argument("--no-block", action="store_true")
     ap.add_argument("--only", choices=["linear", "draft", "block-steps"], default=None,
                     help="run one measurement alone: 'linear' = the block's projections, "

@@ -370,6 +370,23 @@ int ssm_draft_tree_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n
 int ssm_selftest_bounded_wait(int32_t limit_us, int32_t *dev_status, void *stream);
 
 /*
+ * ssm_set_tuning -- process-wide launch-plan overrides (no counterpart in the
+ * pages; they change how work is spread over the GPU, never the results beyond
+ * fp32 rounding order).  Each knob starts at the value of the environment
+ * variable of the same name, read once when the library is first used, or 0
+ * (automatic plan) when unset; this call replaces it for later calls.
+ *   name   "SSM_VERIFY_GROUPS_PER_CTA"   head groups per CTA of the tree kernel (1..8)
+ *          "SSM_VERIFY_HEADS_PER_GROUP"  heads per group of the tree kernel (2 or 4)
+ *          "SSM_LINEAR_TCHUNK"           tokens per CTA of ssm_linear (64, 128 or 256)
+ *          "SSM_LINEAR_SPLITS"           K-splits of ssm_linear (fp32 accumulator outputs)
+ *          "SSM_LINEAR_STAGES"           copy-ring stages of ssm_linear
+ *   value  0 = automatic; a value the plan cannot use is ignored at launch.
+ * Not thread-safe against calls that launch concurrently on other threads.
+ * Errors: SSM_ERR_INVALID_ARG for an unknown name or a negative value.
+ */
+int ssm_set_tuning(const char *name, int32_t value);
+
+/*
  * ssm_tree_verify_noalloc -- ssm_tree_verify for callers that cannot allocate
  * device memory (a runtime that gives a plugin only the current op's tensors
  * and owns all other device memory, an embedding with allocation forbidden
@@ -381,8 +398,10 @@ int ssm_selftest_bounded_wait(int32_t limit_us, int32_t *dev_status, void *strea
  * whose ssm_tree_verify_workspace_size() exceeds that gets SSM_ERR_CAPACITY.
  * Nothing here calls cudaMalloc/cudaFree or any allocating routine.  The first
  * call on a device looks up the array's address (cudaGetSymbolAddress) with
- * that device current; make it before any stream capture.  All calls share the
- * array, so calls whose GPU work overlaps race; serialise them.
+ * that device current and keeps it for the process; make it before any stream
+ * capture.  A cudaDeviceReset of that device invalidates the kept address, so
+ * do not call this entry point after one.  All calls share the array, so calls
+ * whose GPU work overlaps race; serialise them.
  */
 #define SSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
 int ssm_tree_verify_noalloc(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t n_nodes,

@@ -100,6 +100,7 @@ _SIGS = {
                                             ctypes.c_size_t, _P, _P]),
     "ssm_draft_tree_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
     "ssm_selftest_bounded_wait": (ctypes.c_int, [_I, _P, _P]),
+    "ssm_set_tuning": (ctypes.c_int, [ctypes.c_char_p, _I]),
     "ssm_draft_tree_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -226,18 +227,22 @@ def ssm_tree_verify_noalloc(dims: Dims, params: dict, n_seq: int, n_nodes: int, 
                             ring, ring_head, y, status=None, stream=None):
     """ssm_tree_verify for callers that cannot allocate device memory: the scratch
     is the library's own SSM_NOALLOC_WORKSPACE_BYTES array (shared by every call;
-    overlapping calls race).  Batches needing more raise SSMError(SSM_ERR_CAPACITY)."""
+    overlapping calls race).  Batches needing more raise SSMError(SSM_ERR_CAPACITY).
+    The call runs with h0's device current, so the library looks up that device's array."""
     d, I, n = dims, n_seq * dims.n_layers, n_nodes
     cd = d.c()
     cp = _params(params, d, d.n_layers)
-    _check(lib().ssm_tree_verify_noalloc(
-        ctypes.byref(cd), ctypes.byref(cp), n_seq, n, max_depth,
-        _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
-        _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
-        _dev(h0, "h0", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
-        _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
-        _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
-        _opt_status(status), _stream(stream, h0)))
+    if not isinstance(h0, torch.Tensor) or not h0.is_cuda:
+        raise ValueError("h0: must be a CUDA tensor")
+    with torch.cuda.device(h0.device):
+        _check(lib().ssm_tree_verify_noalloc(
+            ctypes.byref(cd), ctypes.byref(cp), n_seq, n, max_depth,
+            _dev(layout, "layout", torch.int32, n_seq * n * NODE_WORDS),
+            _dev(xBC, "xBC", torch.bfloat16, I * n * d.conv_dim), _dev(dt, "dt", torch.bfloat16, I * n * d.n_heads),
+            _dev(h0, "h0", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
+            _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
+            _dev(ring_head, "ring_head", torch.int32, I), _dev(y, "y", torch.float32, I * n * d.d_inner),
+            _opt_status(status), _stream(stream, h0)))
 
 
 def ssm_accept_path(n_seq: int, n_nodes: int, max_path: int, layout, tok, tgt, path, path_len, bonus, status=None,
@@ -375,6 +380,11 @@ def ssm_draft_tree_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, la
         _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
+
+
+def ssm_set_tuning(name: str, value: int):
+    """Set a process-wide launch-plan override (0 = automatic); see include/ssm_tree.h."""
+    _check(lib().ssm_set_tuning(name.encode(), int(value)))
 
 
 def ssm_selftest_bounded_wait(limit_us: int, status, stream=None):

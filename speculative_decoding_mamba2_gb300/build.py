@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "gemm.cu", "norm.cu",
            "layer_api.cu", "draft_tree.cu", "selftest.cu", "layout.cpp"]
-HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "draft_tree.cuh"), os.path.join(INCLUDE, "ssm_tree.h"), os.path.join(INCLUDE, "ssm_layer.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "draft_tree.cuh", "log_apply.cuh")] + \
+    [os.path.join(INCLUDE, h) for h in ("ssm_tree.h", "ssm_layer.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 LIBNAME = "libssmtree.so"
 

@@ -2,6 +2,8 @@
 // the caller's stream.  Nothing here allocates device memory.
 #include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include <stddef.h>
 
@@ -64,6 +66,40 @@ using namespace ssmtree;
 extern "C" int32_t ssm_version(void) { return 100; }
 
 extern "C" const char* ssm_last_error(void) { return g_error.c_str(); }
+
+namespace {
+const char* const kTuneNames[TUNE_COUNT] = {"SSM_VERIFY_GROUPS_PER_CTA", "SSM_VERIFY_HEADS_PER_GROUP",
+                                            "SSM_LINEAR_TCHUNK", "SSM_LINEAR_SPLITS", "SSM_LINEAR_STAGES"};
+struct TuneTable {
+  int v[TUNE_COUNT];
+  TuneTable() {
+    for (int k = 0; k < TUNE_COUNT; ++k) {
+      const char* e = getenv(kTuneNames[k]);
+      const int x = e ? atoi(e) : 0;
+      v[k] = x > 0 ? x : 0;
+    }
+  }
+};
+TuneTable& tune_table() {
+  static TuneTable t;  // environment read once, on first use
+  return t;
+}
+}  // namespace
+
+int ssmtree::tuning(TuneKey k) { return tune_table().v[k]; }
+
+extern "C" int ssm_set_tuning(const char* name, int32_t value) {
+  static const char* fn = "ssm_set_tuning";
+  if (!name) return fail(SSM_ERR_INVALID_ARG, fn, "name is NULL");
+  if (value < 0) return fail(SSM_ERR_INVALID_ARG, fn, "value must be >= 0");
+  for (int k = 0; k < TUNE_COUNT; ++k)
+    if (strcmp(name, kTuneNames[k]) == 0) {
+      tune_table().v[k] = value;
+      g_error.clear();
+      return SSM_OK;
+    }
+  return fail(SSM_ERR_INVALID_ARG, fn, "unknown tuning name");
+}
 
 namespace {
 // A tree whose deepest node sits at depth n-1 is a chain; long chains take the chain kernel.

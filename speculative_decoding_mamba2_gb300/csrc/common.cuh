@@ -311,6 +311,11 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
 int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
+// Launch-plan overrides (0 = automatic).  Each starts at its environment variable, read once
+// per process; ssm_set_tuning replaces it.  They never change results beyond rounding order.
+enum TuneKey { TUNE_VERIFY_GPC, TUNE_VERIFY_G, TUNE_LINEAR_TCHUNK, TUNE_LINEAR_SPLITS, TUNE_LINEAR_STAGES, TUNE_COUNT };
+int tuning(TuneKey k);
+
 // Projections (gemm.cu): D = A · Wᵀ (+ residual) with the output columns cut into segments.
 struct GemmArgs {
   int M, N, K;
@@ -322,7 +327,7 @@ struct GemmArgs {
   const float* residual;  // nullptr or fp32 [M][ldr], added to the accumulator
   long long ldr;
   int32_t* status;
-  int tn, tchunk, cl, splits, kb_per_split, tmem_cols, stages;  // tile plan, set by launch_gemm_bf16
+  int tn, tchunk, splits, kb_per_split, tmem_cols, stages;  // tile plan, set by launch_gemm_bf16
 };
 int gemm_tile_cols();
 cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const void* W, long long ldw, cudaStream_t s);

@@ -12,15 +12,14 @@
 //  * the MMA computes Dᵀ = W · tokensᵀ: a CTA (4 warps) owns 128 output features (the MMA's
 //    M, TMEM lanes), all tokens of a chunk of up to 256 (the MMA's N) and one K-split, so
 //    each weight tile is read by exactly one CTA and each MMA does 128 x N x 16;
-//  * CTAs come in clusters of up to 4 along the features; every k-block's token tile is
-//    shared: each CTA loads 1/CL of its rows with a multicast bulk tensor copy (TMA) into
-//    the same shared-memory offset of every CTA in the cluster;
+//  * each CTA loads its own weight tile and the chunk's token tile with 2-D bulk tensor copies
+//    (TMA); a CTA runs alone (no cluster), so every copy lands in its own shared memory;
 //  * K-splits, chosen on the host to fill the SMs, accumulate into an fp32 output with
 //    vector reductions (used by the output projection, which adds into the residual
 //    stream anyway);
 //  * warp 0 feeds a ring of as many stages as shared memory holds (a stage is refilled once
-//    every CTA of the cluster has finished with it: the MMAs' completion is multicast to
-//    their `empty` barriers), warp 1 issues tcgen05.mma (operands from shared memory
+//    the MMAs that read it have completed: their commit arrives on the stage's `empty`
+//    barrier), warp 1 issues tcgen05.mma (operands from shared memory
 //    through 128-byte-swizzle matrix descriptors) and commits; after the last k-block all
 //    four warps read the accumulator (tcgen05.ld, warp w = TMEM lanes 32w..) into the now
 //    idle stage memory as a [token][feature] tile and write it out row by row with
@@ -28,12 +27,10 @@
 // The epilogue writes up to four column segments to separate outputs (the input
 // projection's z, x|B|C and dt land where the next kernels read them), bf16 or fp32,
 // optionally adding an fp32 residual.  Every wait on an mbarrier is bounded and polled by one
-// thread while its warp (or the CTA) waits at a hardware barrier; the cluster meets at a
-// barrier before any copy and before any CTA leaves.
+// thread while its warp (or the CTA) waits at a hardware barrier; a CTA that gives up waits
+// (bounded again) for the copies it issued before it leaves.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <stdio.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 
@@ -110,21 +107,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// arrive on `bar` (same shared-memory offset) in every CTA of `mask` once this thread's MMAs complete
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n"
-               ::"r"(bar), "h"(mask)
-               : "memory");
-}
-// 2-D bulk tensor copy into the same shared-memory offset (and barrier) of every CTA in `mask`
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
-      "%3}], [%4], %5;\n" ::"r"(dst),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-      : "memory");
-}
 // Wait for phase `parity` of `bar` by polling the non-blocking test_wait from ONE thread (the
 // rest of its warp or CTA waits at a hardware barrier): a thread suspended in try_wait is not
 // always woken as soon as an asynchronous arrival (a bulk copy, an MMA commit) completes the
@@ -147,16 +129,6 @@ __device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity) {
     if ((it & 1023) == 1023 && global_ns() - t0 > 1000000000ull) return false;
   }
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -167,7 +139,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tw, GemmArgs g) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int TN = g.tn, CL = g.cl, GSTAGES = g.stages;
+  const int TN = g.tn, GSTAGES = g.stages;
   const int w_stage = FM * GBK * 2, t_stage = TN * GBK * 2;  // both multiples of 1024
   unsigned char* sw = smem;                      // [GSTAGES][w_stage]: weight rows (MMA operand A)
   unsigned char* st = smem + GSTAGES * w_stage;  // [GSTAGES][t_stage]: token rows (MMA operand B)
@@ -176,34 +148,32 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   unsigned long long* acc_bar = empty + MAX_STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* issued = abort_flag + 1;  // k-blocks whose copies the producer issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int f0 = blockIdx.x * FM, t0 = blockIdx.z * g.tchunk;
   const int KB = (g.K + GBK - 1) / GBK;
   const int kb0 = blockIdx.y * g.kb_per_split, kb1 = min(KB, kb0 + g.kb_per_split);
-  const int rank = CL > 1 ? (int)cluster_rank() : 0;
-  const uint16_t cmask = (uint16_t)((1u << CL) - 1u);
-  const int slice_rows = TN / CL;  // token rows this CTA loads for the whole cluster (a multiple of 8)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < GSTAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), CL);  // every CTA of the cluster hands the stage back
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     mbar_init(smem_u32(acc_bar), 1);
     *abort_flag = 0;
+    *issued = 0;
     fence_barrier_init();
   }
   if (warp == 0) tmem_alloc(smem_u32(tmem_slot), (uint32_t)g.tmem_cols);
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // every barrier of the cluster exists before the first multicast
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   // Warp 0 feeds the ring and warp 1 issues the MMAs; each whole warp runs its loop (every lane
   // waits on the same barriers, lane 0 issues).
-  if (warp == 0) {  // producer: this CTA's weight tile and its share of the token tile (to the cluster)
+  if (warp == 0) {  // producer: this CTA's weight tile and the chunk's token tile
     for (int kb = kb0; kb < kb1; ++kb) {
       const int i = kb - kb0, s = i % GSTAGES, use = i / GSTAGES;
       int bad = 0;
@@ -214,11 +184,8 @@ __global__ void __launch_bounds__(GTHREADS, 1)
         } else {
           mbar_arrive_expect_tx(smem_u32(&full[s]), (uint32_t)(w_stage + t_stage));
           tma_load_2d(smem_u32(sw + s * w_stage), &tw, kb * GBK, f0, smem_u32(&full[s]));
-          const uint32_t tdst = smem_u32(st + s * t_stage + rank * slice_rows * GBK * 2);
-          if (CL > 1)
-            tma_load_2d_mc(tdst, &ta, kb * GBK, t0 + rank * slice_rows, smem_u32(&full[s]), cmask);
-          else
-            tma_load_2d(tdst, &ta, kb * GBK, t0, smem_u32(&full[s]));
+          tma_load_2d(smem_u32(st + s * t_stage), &ta, kb * GBK, t0, smem_u32(&full[s]));
+          *issued = i + 1;
         }
       }
       if (__shfl_sync(0xffffffffu, bad, 0)) break;
@@ -240,10 +207,7 @@ __global__ void __launch_bounds__(GTHREADS, 1)
 #pragma unroll
           for (int k = 0; k < GBK / 16; ++k)  // next 16 columns: 32 bytes further in the swizzled rows
             umma_bf16(tmem, wd + 2 * k, td + 2 * k, idesc, (i | k) != 0);
-          if (CL > 1)
-            umma_commit_mc(smem_u32(&empty[s]), cmask);  // the stage is free in every CTA that shares it
-          else
-            umma_commit(smem_u32(&empty[s]));
+          umma_commit(smem_u32(&empty[s]));  // the stage is free once these MMAs complete
         }
       }
       if (__shfl_sync(0xffffffffu, bad, 0)) break;
@@ -258,10 +222,17 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (*abort_flag) {  // CTA-uniform after the barrier: tcgen05.ld needs whole warps
-    if (threadIdx.x == 0) flag(g.status, SSM_STATUS_TIMEOUT);
+    if (threadIdx.x == 0) {
+      flag(g.status, SSM_STATUS_TIMEOUT);
+      // copies issued into stages that no MMA waited for may still be in flight: give each
+      // stage's latest use a bounded chance to land before the CTA's shared memory is released
+      const int n_issued = *issued;
+      for (int i = n_issued > GSTAGES ? n_issued - GSTAGES : 0; i < n_issued; ++i)
+        mbar_poll(smem_u32(&full[i % GSTAGES]), (i / GSTAGES) & 1);
+    }
   } else {
     // (1) accumulator -> shared memory, [token][feature] fp32 (the stage ring is free now: the
-    //     last MMA has read it and every copy into it, a peer's multicast included, has landed)
+    //     last MMA has read it and every copy into it has landed)
     float* tile = reinterpret_cast<float*>(smem);  // TN x FM fp32 <= 128 KB
     const int fl = warp * 32 + lane;               // this thread's feature within the tile
 #pragma unroll 1
@@ -333,7 +304,6 @@ __global__ void __launch_bounds__(GTHREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync();  // no CTA leaves while a peer may still copy into it or arrive on its barriers
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -371,27 +341,24 @@ bool encode_bf16(CUtensorMap* m, const void* base, long long rows, long long col
 int gemm_tile_cols() { return SEG_ALIGN; }
 
 // Tile plan: 128 output features per CTA (the MMA's M), all tokens of a chunk of up to 256
-// (the MMA's N, rounded up to a multiple of 16 and of 8 rows per cluster CTA), clusters of up
-// to 4 CTAs sharing the token tiles, and K-splits (only when the output is an fp32
-// accumulator) so the grid fills the SMs with the least data per SM.
+// (the MMA's N, rounded up to a multiple of 16), and K-splits (only when the output is an fp32
+// accumulator) so the grid fills the SMs with the least data per SM.  Tuning overrides:
+// tokens per CTA, K-splits and ring stages (ssm_set_tuning).
 void plan_gemm(GemmArgs& g, int sms, bool can_split) {
+  const int o_tchunk = tuning(TUNE_LINEAR_TCHUNK);  // 64, 128 or 256 tokens per CTA
+  const int o_splits = tuning(TUNE_LINEAR_SPLITS);  // K-splits (fp32 accumulator outputs only)
+  const int o_stages = tuning(TUNE_LINEAR_STAGES);  // stages of the copy ring
   const int KB = (g.K + GBK - 1) / GBK;
   const int tiles = (g.N + FM - 1) / FM;
-  g.cl = tiles >= 4 ? 4 : (tiles >= 2 ? 2 : 1);
-  const int tiles_c = (tiles + g.cl - 1) / g.cl * g.cl;
   // few feature tiles (a narrow projection) and no K-splits (a bf16 output): cut the tokens into
   // smaller chunks so more CTAs, each with a deeper ring of smaller stages, share the work
   g.tchunk = MAX_TN;
   while (!can_split && g.tchunk > 64 && g.M > g.tchunk / 2 &&
-         (long long)tiles_c * ((g.M + g.tchunk / 2 - 1) / (g.tchunk / 2)) <= sms / 2)
+         (long long)tiles * ((g.M + g.tchunk / 2 - 1) / (g.tchunk / 2)) <= sms / 2)
     g.tchunk /= 2;
-  if (const char* o = getenv("SSM_LINEAR_TCHUNK")) {  // tuning override: 64, 128 or 256 tokens per CTA
-    const int v = atoi(o);
-    if (v == 64 || v == 128 || v == 256) g.tchunk = v;
-  }
+  if (o_tchunk == 64 || o_tchunk == 128 || o_tchunk == 256) g.tchunk = o_tchunk;
   const int chunk = g.M < g.tchunk ? g.M : g.tchunk;
-  const int q = 8 * g.cl > 16 ? 8 * g.cl : 16;
-  g.tn = (chunk + q - 1) / q * q;
+  g.tn = (chunk + 15) / 16 * 16;
   const int tchunks = (g.M + g.tchunk - 1) / g.tchunk;
   double best = 1e300;
   g.splits = 1;
@@ -399,9 +366,9 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
   for (int sp = 1; sp <= (can_split ? 16 : 1); ++sp) {
     const int kbp = (KB + sp - 1) / sp;
     if ((sp - 1) * kbp >= KB) continue;  // every split gets at least one k-block
-    const long long ctas = (long long)tiles_c * sp * tchunks;
+    const long long ctas = (long long)tiles * sp * tchunks;
     const long long waves = (ctas + sms - 1) / sms;
-    const double per_cta = (double)kbp * GBK * 2 * (FM + (double)g.tn / g.cl);
+    const double per_cta = (double)kbp * GBK * 2 * (FM + (double)g.tn);
     const double est = waves * per_cta * (1.0 + 0.02 * sp);  // small charge per split (reductions)
     if (est < best * 0.999) {
       best = est;
@@ -409,16 +376,9 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
       g.kb_per_split = kbp;
     }
   }
-  if (const char* o = getenv("SSM_LINEAR_PLAN")) {  // tuning override: "cl,splits"
-    int cl = 0, sp = 0;
-    if (sscanf(o, "%d,%d", &cl, &sp) == 2 && (cl == 1 || cl == 2 || cl == 4) && cl <= tiles && sp >= 1 &&
-        (sp == 1 || can_split) && (sp - 1) * ((KB + sp - 1) / sp) < KB) {
-      g.cl = cl;
-      const int q2 = 8 * cl > 16 ? 8 * cl : 16;
-      g.tn = (chunk + q2 - 1) / q2 * q2;
-      g.splits = sp;
-      g.kb_per_split = (KB + sp - 1) / sp;
-    }
+  if (o_splits >= 1 && (o_splits == 1 || can_split) && (o_splits - 1) * ((KB + o_splits - 1) / o_splits) < KB) {
+    g.splits = o_splits;
+    g.kb_per_split = (KB + o_splits - 1) / o_splits;
   }
   int cols = 32;
   while (cols < g.tn) cols *= 2;
@@ -428,10 +388,7 @@ void plan_gemm(GemmArgs& g, int sms, bool can_split) {
   if (g.stages > MAX_STAGES) g.stages = MAX_STAGES;
   // the epilogue stages the fp32 [token][feature] tile in the ring's memory
   const int min_stages = (g.tn * FM * 4 + stage_bytes - 1) / stage_bytes;
-  if (const char* o = getenv("SSM_LINEAR_STAGES")) {  // tuning override
-    const int v = atoi(o);
-    if (v >= 2 && v >= min_stages && v < g.stages) g.stages = v;
-  }
+  if (o_stages >= 2 && o_stages >= min_stages && o_stages < g.stages) g.stages = o_stages;
 }
 
 // dynamic shared memory of a plan: the stage ring (which also holds the epilogue tile), the
@@ -461,24 +418,12 @@ cudaError_t launch_gemm_bf16(GemmArgs g, const void* A, long long lda, const voi
   const bool can_split = g.n_seg == 1 && g.seg_f32[0] && g.residual == g.seg_ptr[0] && g.ldr == g.seg_ld[0];
   plan_gemm(g, sms, can_split);
   CUtensorMap ta, tw;
-  if (!encode_bf16(&ta, A, g.M, g.K, lda, g.tn / g.cl) || !encode_bf16(&tw, W, g.N, g.K, ldw, FM))
+  if (!encode_bf16(&ta, A, g.M, g.K, lda, g.tn) || !encode_bf16(&tw, W, g.N, g.K, ldw, FM))
     return cudaErrorInvalidValue;
   const int tiles = (g.N + FM - 1) / FM;
-  const dim3 grid((unsigned)((tiles + g.cl - 1) / g.cl * g.cl), (unsigned)g.splits,
-                  (unsigned)((g.M + g.tchunk - 1) / g.tchunk));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(GTHREADS);
-  cfg.dynamicSmemBytes = (size_t)gemm_smem_bytes(g);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)g.cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_bf16_kernel, ta, tw, g);
+  const dim3 grid((unsigned)tiles, (unsigned)g.splits, (unsigned)((g.M + g.tchunk - 1) / g.tchunk));
+  gemm_bf16_kernel<<<grid, GTHREADS, (size_t)gemm_smem_bytes(g), s>>>(ta, tw, g);
+  return cudaGetLastError();
 }
 
 }  // namespace ssmtree

@@ -50,7 +50,6 @@
 // read by verify and read + written again by a separate commit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
-#include <stdlib.h>
 
 #include "common.cuh"
 
@@ -995,10 +994,8 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
     const int parts = (NG + target - 1) / target;
     gpc = (NG + parts - 1) / parts;
   }
-  if (const char* o = getenv("SSM_VERIFY_GROUPS_PER_CTA")) {  // tuning / test override
-    const int v = atoi(o);
-    if (v >= 1 && v <= MAX_GPC) gpc = v;
-  }
+  const int o_gpc = tuning(TUNE_VERIFY_GPC);  // tuning / test override
+  if (o_gpc >= 1 && o_gpc <= MAX_GPC) gpc = o_gpc;
   a.gpc = gpc;
   const long long blocks = inst * ((NG + gpc - 1) / gpc);
   // h0 as a 2-D tensor: rows (instance, head, p), 128 fp32 columns; one box = G*64 rows x 16 columns
@@ -1074,10 +1071,8 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
     // so 2-head groups win only when they need no more rounds than 4-head groups
     const long long est4 = (c4 + slots - 1) / slots * (6 + 4), est2 = (c2 + slots - 1) / slots * (6 + 2);
     if (fits2 && est2 < est4) G = 2;
-    if (const char* o = getenv("SSM_VERIFY_HEADS_PER_GROUP")) {  // tuning / test override: 2 or 4
-      const int v = atoi(o);
-      if (v == 4 || (v == 2 && fits2)) G = v;
-    }
+    const int o_g = tuning(TUNE_VERIFY_G);  // tuning / test override (2 or 4)
+    if (o_g == 4 || (o_g == 2 && fits2)) G = o_g;
   }
   const int prep_bytes = verify_prep_smem_bytes(a.n, a.max_depth, a.H, a.LP);
   e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);

@@ -19,5 +19,6 @@ from .workloads import (  # noqa: F401
     draft_inputs,
     replay_k,
     batch,
+    batch_parallel,
     draft_batch,
 )

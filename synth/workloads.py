@@ -114,11 +114,13 @@ def _rng(w: Workload, seq: int, layer: int, stream: int, extra: int = 0) -> np.r
 # then read the identical 16-bit patterns)
 # ---------------------------------------------------------------------------
 def to_bf16_bits(a) -> np.ndarray:
-    """Round fp32 values to bf16, nearest-even; returns uint16 bit patterns."""
+    """Round fp32 values to bf16, nearest-even; returns uint16 bit patterns.  In 32-bit
+    arithmetic: for every finite or infinite input the sum stays below 2^32 (the largest
+    finite pattern 0xFF7FFFFF plus 0x8000 is 0xFF807FFF)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    u = a.view(np.uint32)
+    u = u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return (u >> np.uint32(16)).astype(np.uint16)
 
 
 def bf16_bits_to_f32(b) -> np.ndarray:
@@ -293,6 +295,86 @@ def batch(w: Workload, seqs: Sequence[int] | None = None, layers: Sequence[int] 
         for j, l in enumerate(layers):
             out["h0"][i, j], out["ring"][i, j], out["ring_head"][i, j] = instance_state(w, q, l)
             out["xBC"][i, j], out["dt"][i, j] = node_inputs(w, q, l, n, tree)
+    out["params"] = layer_params(w, layers)
+    return out
+
+
+def _fill_part(args):
+    """Worker of batch_parallel: generate sequences seqs[lo:hi] into the shared arrays."""
+    from multiprocessing import shared_memory
+    w, seqs, layers, tree, lo, hi, specs, with_state = args
+    blocks = {k: shared_memory.SharedMemory(name=name) for k, (name, _, _) in specs.items()}
+    try:
+        arr = {k: np.ndarray(shape, dtype, buffer=blocks[k].buf) for k, (_, shape, dtype) in specs.items()}
+        small = []
+        for i in range(lo, hi):
+            q = seqs[i]
+            par = tree_parents(w, q, tree)
+            tok, tgt = tree_tokens(w, q, par, tree)
+            small.append((par, tok, tgt))
+            for j, l in enumerate(layers):
+                if with_state:
+                    arr["h0"][i, j], arr["ring"][i, j], arr["ring_head"][i, j] = instance_state(w, q, l)
+                arr["xBC"][i, j], arr["dt"][i, j] = node_inputs(w, q, l, len(par), tree)
+        del arr
+        return lo, small
+    finally:
+        for b in blocks.values():
+            b.close()
+
+
+def batch_parallel(w: Workload, seqs: Sequence[int] | None = None, layers: Sequence[int] | None = None,
+                   tree: int = 0, workers: int | None = None, with_state: bool = True) -> dict:
+    """batch() with the sequences generated by a spawn pool of `workers` processes that
+    write straight into shared memory; every instance comes from its own seeded
+    streams, so the result is identical to batch().  with_state=False leaves out h0,
+    ring and ring_head (a second tree of the same instances reuses the first's)."""
+    import multiprocessing as mp
+    import os
+    from concurrent.futures import ProcessPoolExecutor
+    from multiprocessing import shared_memory
+    seqs = list(range(w.batch)) if seqs is None else [int(x) for x in seqs]
+    layers = list(range(w.n_layers)) if layers is None else [int(x) for x in layers]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    workers = max(1, min(workers or cores, len(seqs)))
+    s = w.shape
+    n = w.n_nodes(tree)
+    S, L = len(seqs), len(layers)
+    shapes = {"xBC": ((S, L, n, s.conv_dim), np.uint16), "dt": ((S, L, n, s.H), np.uint16)}
+    if with_state:
+        shapes.update({"h0": ((S, L, s.H, s.P, s.N), np.float32), "ring": ((S, L, w.ring_cap, s.conv_dim), np.uint16),
+                       "ring_head": ((S, L), np.int32)})
+    blocks = {k: shared_memory.SharedMemory(create=True, size=max(1, int(np.prod(sh)) * np.dtype(dt).itemsize))
+              for k, (sh, dt) in shapes.items()}
+    try:
+        specs = {k: (blocks[k].name, sh, dt) for k, (sh, dt) in shapes.items()}
+        if with_state:  # ring rows past the three generated ones start at zero, as in batch()
+            np.ndarray(shapes["ring"][0], np.uint16, buffer=blocks["ring"].buf).fill(0)
+        per = (S + workers - 1) // workers
+        tasks = [(w, seqs, layers, tree, lo, min(S, lo + per), specs, with_state) for lo in range(0, S, per)]
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        try:
+            with ProcessPoolExecutor(len(tasks), mp_context=mp.get_context("spawn")) as ex:
+                parts = list(ex.map(_fill_part, tasks))
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k)
+                else:
+                    os.environ[k] = v
+        out = dict(seqs=np.asarray(seqs, np.int32), layers=np.asarray(layers, np.int32), n_nodes=n,
+                   parent=np.empty((S, n), np.int32), tok=np.empty((S, n), np.int32), tgt=np.empty((S, n), np.int32))
+        for lo, small in parts:
+            for k, (par, tok, tgt) in enumerate(small):
+                out["parent"][lo + k], out["tok"][lo + k], out["tgt"][lo + k] = par, tok, tgt
+        for k, (sh, dt) in shapes.items():
+            out[k] = np.ndarray(sh, dt, buffer=blocks[k].buf).copy()
+    finally:
+        for b in blocks.values():
+            b.close()
+            b.unlink()
     out["params"] = layer_params(w, layers)
     return out
 

@@ -248,3 +248,16 @@ def test_selftest_bounded_wait_validation(L):
     assert L.ssm_selftest_bounded_wait(0, FAKE, None) == B.SSM_ERR_RANGE
     assert L.ssm_selftest_bounded_wait(1000001, FAKE, None) == B.SSM_ERR_RANGE
     assert L.ssm_selftest_bounded_wait(1000, None, None) == B.SSM_ERR_INVALID_ARG
+
+
+def test_set_tuning_validation(L):
+    # no CUDA call: the knobs are host-side plan overrides
+    from speculative_decoding_mamba2_gb300 import SSM_ERR_INVALID_ARG, SSM_OK
+    for name in (b"SSM_VERIFY_GROUPS_PER_CTA", b"SSM_VERIFY_HEADS_PER_GROUP", b"SSM_LINEAR_TCHUNK",
+                 b"SSM_LINEAR_SPLITS", b"SSM_LINEAR_STAGES"):
+        assert L.ssm_set_tuning(name, 2) == SSM_OK
+        assert L.ssm_set_tuning(name, 0) == SSM_OK
+    assert L.ssm_set_tuning(b"SSM_NO_SUCH_KNOB", 1) == SSM_ERR_INVALID_ARG
+    assert "unknown" in L.ssm_last_error().decode()
+    assert L.ssm_set_tuning(b"SSM_LINEAR_STAGES", -1) == SSM_ERR_INVALID_ARG
+    assert L.ssm_set_tuning(None, 1) == SSM_ERR_INVALID_ARG

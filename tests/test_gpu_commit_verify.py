@@ -146,9 +146,9 @@ def test_ragged_heads_and_trees_of_different_sizes():
 
 
 @pytest.mark.parametrize("gpc", ["2", "3"])
-def test_several_head_groups_per_cta(gpc, monkeypatch):
+def test_several_head_groups_per_cta(gpc, tuning):
     # per-group committed-path rows arrive while the previous group is still being consumed
-    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", gpc)
     w0 = Workload(63, "groups", Shape(H=24), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
     w1 = next_workload(w0, 64, ("full", 2, 3))
     b0, b1 = batch(w0), batch(w1)
@@ -230,9 +230,9 @@ def test_stress_shape_ternary_next_tree_sampled():
 
 
 @pytest.mark.parametrize("gpc", ["2", "3"])
-def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
+def test_several_head_groups_and_node_tiles(gpc, tuning):
     # several head groups per CTA (H = 10: the last one ragged) with a 40-node next tree
-    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", gpc)
     w0 = Workload(73, "groups x tiles", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),),
                   p_accept=0.9)
     w1 = next_workload(w0, 74, ("full", 3, 3))

@@ -80,10 +80,10 @@ def test_tree_shapes(spec):
 
 
 @pytest.mark.parametrize("gpc", ["2", "3"])
-def test_several_head_groups_per_cta(gpc, monkeypatch):
+def test_several_head_groups_per_cta(gpc, tuning):
     # one CTA walks several head groups (the last one ragged): inputs of the next group
     # arrive while the current group's epilogue still reads its own
-    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", gpc)
     w = Workload(55, "groups", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -91,10 +91,10 @@ def test_several_head_groups_per_cta(gpc, monkeypatch):
 
 
 @pytest.mark.parametrize("gpc", ["2", "3"])
-def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
+def test_several_head_groups_and_node_tiles(gpc, tuning):
     # several head groups per CTA (the last one ragged) with a 40-node tree (three node
     # tiles): the next group's x conv runs inside the last tile of the current group
-    monkeypatch.setenv("SSM_VERIFY_GROUPS_PER_CTA", gpc)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", gpc)
     w = Workload(56, "groups x tiles", Shape(H=10), n_layers=2, batch=2, trees=(("full", 3, 3),))
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -102,10 +102,10 @@ def test_several_head_groups_and_node_tiles(gpc, monkeypatch):
 
 
 @pytest.mark.parametrize("g", ["2", "4"])
-def test_two_and_four_head_groups(g, monkeypatch):
+def test_two_and_four_head_groups(g, tuning):
     # the same small batch with 2-head and with 4-head groups (H = 10: the last group ragged
     # either way), against the oracle
-    monkeypatch.setenv("SSM_VERIFY_HEADS_PER_GROUP", g)
+    tuning("SSM_VERIFY_HEADS_PER_GROUP", g)
     w = Workload(57, "head groups", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))

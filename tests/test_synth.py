@@ -57,3 +57,18 @@ def test_acceptance_rate_is_near_p():
                 tot += 1
                 hits += int(any(tok[c] == tgt[u] for c in ch))
     assert abs(hits / tot - 0.8) < 0.05
+
+
+def test_batch_parallel_is_batch():
+    # the pool generator writes the same seeded streams into shared memory: identical arrays
+    from synth import batch, batch_parallel, workload
+    w = workload(4)
+    a = batch_parallel(w, seqs=[0, 7, 63], layers=[0, 47], workers=2)
+    b = batch(w, seqs=[0, 7, 63], layers=[0, 47])
+    for k in ("parent", "tok", "tgt", "xBC", "dt", "h0", "ring", "ring_head"):
+        assert np.array_equal(a[k], b[k]), k
+    c = batch_parallel(w, seqs=[5, 6], layers=[3], tree=1, workers=2, with_state=False)
+    d = batch(w, seqs=[5, 6], layers=[3], tree=1)
+    assert "h0" not in c
+    for k in ("parent", "tok", "tgt", "xBC", "dt"):
+        assert np.array_equal(c[k], d[k]), k

@@ -1,19 +1,20 @@
 """ssm_tree_verify_noalloc -- the entry point for callers that cannot allocate
 device memory (its scratch is an array compiled into the library) -- gives the
-same outputs as ssm_tree_verify with a caller-allocated workspace, on two calls
-in a row with different batches (the shared array keeps the first call's
-contents when the second starts).  Kept in a file of its own, collected last."""
+same outputs as ssm_tree_verify with a caller-allocated workspace, bit for bit
+(the same kernels run on the same inputs; only the scratch address differs), on
+calls in a row with different batches (the shared array keeps the previous
+call's contents when the next starts): two tree batches, then a long chain tree,
+which takes the chain kernels and their own scratch records.  Kept in a file of
+its own, collected last."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from synth import Shape, Workload, batch, workload
-from tests.helpers import rel_err, upload_tree_batch
+from tests.helpers import upload_tree_batch
 
 pytestmark = pytest.mark.gpu
-TOL = 1e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,12 +46,20 @@ def test_noalloc_matches_workspace_entry_point_twice():
     w1 = Workload(70, "noalloc a", Shape(H=80), n_layers=8, batch=2, trees=(("random", 16, 3, 4),))
     y, y_ref = _both(upload_tree_batch(batch(w1), w1))
     assert torch.isfinite(y).all()
-    assert rel_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= TOL
+    assert torch.equal(y, y_ref)
     # second call right after, another shape and tree: the array holds the first call's data
     w2 = workload(0)
     y, y_ref = _both(upload_tree_batch(batch(w2), w2))
     assert torch.isfinite(y).all()
-    assert rel_err(y.cpu().numpy(), y_ref.cpu().numpy()) <= TOL
+    assert torch.equal(y, y_ref)
+    # third call: a 40-node chain (deeper than the tree kernels take), so the chain kernels
+    # read their per-chunk records from the same array, over the tree calls' contents
+    w3 = Workload(71, "noalloc chain", Shape(H=6), n_layers=1, batch=2, trees=(("chain", 40),))
+    d3 = upload_tree_batch(batch(w3), w3)
+    assert d3["depth"] == 39
+    y, y_ref = _both(d3)
+    assert torch.isfinite(y).all()
+    assert torch.equal(y, y_ref)
 
 
 def test_noalloc_rejects_batches_beyond_its_array():
