@@ -370,6 +370,20 @@ int ssm_draft_tree_commit(const ssm_dims *dims, const ssm_params *prm, int32_t n
 int ssm_selftest_bounded_wait(int32_t limit_us, int32_t *dev_status, void *stream);
 
 /*
+ * ssm_selftest_silu -- the SiLU forms the kernels evaluate, on n given inputs (no
+ * counterpart in the pages; SiLU is the activation after the conv, LightMamba page
+ * "为什么 Mamba 难加速").  For each v[i]:
+ *   out[i]        the FMA-pipe form of the tree kernel's x conv: v / (1 + 2^t),
+ *                 t = -v·log2(e), 2^t by Cody-Waite reduction and a degree-6
+ *                 Taylor series, the reciprocal by three Newton-Raphson steps;
+ *   out[n + i]    the special-function form (fast exp and divide intrinsics) of
+ *                 the prep kernels' B | C conv;
+ *   out[2n + i]   v / (1 + expf(-v)) with a rounded divide (commit, draft step).
+ *   v    device fp32 [n]     out device fp32 [3][n]
+ */
+int ssm_selftest_silu(const float *v, float *out, int64_t n, void *stream);
+
+/*
  * ssm_set_tuning -- process-wide launch-plan overrides (no counterpart in the
  * pages; they change how work is spread over the GPU, never the results beyond
  * fp32 rounding order).  Each knob starts at the value of the environment

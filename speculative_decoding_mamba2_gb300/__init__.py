@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     ssm_replay,
     ssm_rmsnorm,
     ssm_selftest_bounded_wait,
+    ssm_selftest_silu,
     ssm_set_tuning,
     ssm_tree_layout_build,
     ssm_tree_verify,

@@ -101,6 +101,7 @@ _SIGS = {
     "ssm_draft_tree_workspace_size": (ctypes.c_size_t, [_P, _I, _I]),
     "ssm_selftest_bounded_wait": (ctypes.c_int, [_I, _P, _P]),
     "ssm_set_tuning": (ctypes.c_int, [ctypes.c_char_p, _I]),
+    "ssm_selftest_silu": (ctypes.c_int, [_P, _P, ctypes.c_int64, _P]),
     "ssm_draft_tree_commit": (ctypes.c_int, [_P, _P, _I, _I, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
@@ -380,6 +381,17 @@ def ssm_draft_tree_commit(dims: Dims, params: dict, n_seq: int, n_nodes: int, la
         _dev(h_ckpt, "h_ckpt", torch.float32, I * d.n_heads * d.head_dim * d.d_state),
         _dev(ring, "ring", torch.bfloat16, I * d.ring_cap * d.conv_dim),
         _dev(ring_head, "ring_head", torch.int32, I), _opt_status(status), _stream(stream, h_ckpt)))
+
+
+def ssm_selftest_silu(v, out=None, stream=None):
+    """The kernels' three SiLU forms on the fp32 CUDA tensor v: returns out [3, n]
+    (FMA-pipe polynomial form, special-function form, expf form)."""
+    n = v.numel()
+    if out is None:
+        out = torch.empty((3, n), dtype=torch.float32, device=v.device)
+    _check(lib().ssm_selftest_silu(_dev(v, "v", torch.float32, n), _dev(out, "out", torch.float32, 3 * n), n,
+                                   _stream(stream, v)))
+    return out
 
 
 def ssm_set_tuning(name: str, value: int):

@@ -516,3 +516,10 @@ extern "C" int ssm_selftest_bounded_wait(int32_t limit_us, int32_t* dev_status, 
   if (!dev_status) return fail(SSM_ERR_INVALID_ARG, fn, "dev_status is NULL");
   return finish(fn, launch_selftest_wait(dev_status, (unsigned long long)limit_us * 1000ull, (cudaStream_t)stream));
 }
+
+extern "C" int ssm_selftest_silu(const float* v, float* out, int64_t n, void* stream) {
+  const char* fn = "ssm_selftest_silu";
+  if (n < 0) return fail(SSM_ERR_RANGE, fn, "n must be >= 0");
+  if (n > 0 && (!v || !out)) return fail(SSM_ERR_INVALID_ARG, fn, "v or out is NULL");
+  return finish(fn, launch_selftest_silu(v, out, (long long)n, (cudaStream_t)stream));
+}

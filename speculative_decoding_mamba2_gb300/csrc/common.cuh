@@ -387,5 +387,6 @@ cudaError_t launch_replay(const ReplayArgs& a, cudaStream_t s);
 
 // the bounded-wait self-test (one CTA waits on a barrier nothing arrives at)
 cudaError_t launch_selftest_wait(int32_t* status, unsigned long long limit_ns, cudaStream_t s);
+cudaError_t launch_selftest_silu(const float* v, float* out, long long n, cudaStream_t s);
 
 }  // namespace ssmtree

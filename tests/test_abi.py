@@ -261,3 +261,10 @@ def test_set_tuning_validation(L):
     assert "unknown" in L.ssm_last_error().decode()
     assert L.ssm_set_tuning(b"SSM_LINEAR_STAGES", -1) == SSM_ERR_INVALID_ARG
     assert L.ssm_set_tuning(None, 1) == SSM_ERR_INVALID_ARG
+
+
+def test_selftest_silu_validation(L):
+    assert L.ssm_selftest_silu(FAKE, FAKE, -1, None) == B.SSM_ERR_RANGE
+    assert L.ssm_selftest_silu(None, FAKE, 4, None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_selftest_silu(FAKE, None, 4, None) == B.SSM_ERR_INVALID_ARG
+    assert L.ssm_selftest_silu(None, None, 0, None) == B.SSM_OK  # nothing to do, no CUDA call
