@@ -394,6 +394,12 @@ int ssm_selftest_silu(const float *v, float *out, int64_t n, void *stream);
  *          "SSM_LINEAR_TCHUNK"           tokens per CTA of ssm_linear (64, 128 or 256)
  *          "SSM_LINEAR_SPLITS"           K-splits of ssm_linear (fp32 accumulator outputs)
  *          "SSM_LINEAR_STAGES"           copy-ring stages of ssm_linear
+ *          "SSM_VERIFY_KERNEL"           tree kernels of ssm_tree_verify / ssm_commit_verify:
+ *                                        0 or 1 = warp-level mma.sync (the default),
+ *                                        2 = the state contraction on tcgen05 with tensor-
+ *                                        memory accumulators (measured slower here)
+ *          "SSM_VERIFY_CTAS"             at most this many CTAs of the persistent tcgen05 tree
+ *                                        kernel (each walks a run of head pairs)
  *   value  0 = automatic; a value the plan cannot use is ignored at launch.
  * Not thread-safe against calls that launch concurrently on other threads.
  * Errors: SSM_ERR_INVALID_ARG for an unknown name or a negative value.

@@ -19,9 +19,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = ["api.cu", "verify.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "gemm.cu", "norm.cu",
+SOURCES = ["api.cu", "verify.cu", "verify_tc.cu", "commit.cu", "draft.cu", "noalloc.cu", "chain.cu", "gemm.cu", "norm.cu",
            "layer_api.cu", "draft_tree.cu", "selftest.cu", "layout.cpp"]
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "draft_tree.cuh", "log_apply.cuh")] + \
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "draft_tree.cuh", "log_apply.cuh", "tc.cuh")] + \
     [os.path.join(INCLUDE, h) for h in ("ssm_tree.h", "ssm_layer.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 LIBNAME = "libssmtree.so"

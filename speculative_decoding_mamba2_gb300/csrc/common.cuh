@@ -33,7 +33,7 @@ __device__ __forceinline__ float silu_fast(float v) {
 //  * 2^t: Cody-Waite range reduction -- n = round(t) by adding and subtracting 1.5·2^23,
 //    f = t - n in [-1/2, 1/2] -- then the degree-6 Taylor series of 2^f = e^{f·ln 2}
 //    (coefficients (ln 2)^k / k!, remainder about 1e-7 on that interval), scaled by 2^n
-//    through the exponent field; t is clamped to [-126, 126] (v beyond ±87 gives v or 0).
+//    through the exponent field; t is clamped to [-126, 126].
 //  * 1 / d: Newton-Raphson r <- r·(2 - d·r), three steps from the linear bit-pattern guess
 //    0x7F000000 - bits(d) (relative error below 1/8, then 2^-6, 2^-12, 2^-24).
 // Relative error of the result about 4e-6, like the special-function version above.
@@ -56,7 +56,11 @@ __device__ __forceinline__ float recip_nr(float d) {
   for (int i = 0; i < 3; ++i) r = fmaf(r, fmaf(-d, r, 1.0f), r);
   return r;
 }
-__device__ __forceinline__ float silu_fma(float v) { return v * recip_nr(1.0f + exp2_poly(-1.4426950408889634f * v)); }
+// below -87 the exact result is below 2e-36 in magnitude and 0 is returned (the clamped 2^t
+// would give v·2^-126 there, which is not small once |v| is large)
+__device__ __forceinline__ float silu_fma(float v) {
+  return v < -87.0f ? 0.0f : v * recip_nr(1.0f + exp2_poly(-1.4426950408889634f * v));
+}
 
 // softplus(v) = log(1 + e^v); above 20 it equals v to fp32 precision.
 __device__ __forceinline__ float softplus_f(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
@@ -311,9 +315,15 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP = 0);
 int verify_heads_per_group(int n, int max_depth, int H, int LP = 0);  // 0: the plan does not fit in shared memory
 int verify_prep_smem_bytes(int n, int max_depth, int H, int LP = 0);
+// The same calls with the state contraction on tcgen05 (verify_tc.cu); launch_verify routes
+// trees here unless the SSM_VERIFY_KERNEL override selects the warp-level kernels above.
+cudaError_t launch_verify_tc(const VerifyArgs& a, void* workspace, cudaStream_t s, int which);
+size_t verify_tc_workspace_bytes(int n, int max_depth, int H, int LP, long long n_inst);
+bool verify_tc_fits(int n, int max_depth, int LP);
 // Launch-plan overrides (0 = automatic).  Each starts at its environment variable, read once
 // per process; ssm_set_tuning replaces it.  They never change results beyond rounding order.
-enum TuneKey { TUNE_VERIFY_GPC, TUNE_VERIFY_G, TUNE_LINEAR_TCHUNK, TUNE_LINEAR_SPLITS, TUNE_LINEAR_STAGES, TUNE_COUNT };
+enum TuneKey { TUNE_VERIFY_GPC, TUNE_VERIFY_G, TUNE_LINEAR_TCHUNK, TUNE_LINEAR_SPLITS, TUNE_LINEAR_STAGES,
+               TUNE_VERIFY_KERNEL, TUNE_VERIFY_CTAS, TUNE_COUNT };
 int tuning(TuneKey k);
 
 // Projections (gemm.cu): D = A · Wᵀ (+ residual) with the output columns cut into segments.

@@ -1025,8 +1025,11 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
 
 }  // namespace
 
+// one workspace serves both kernel sets (the larger of their per-instance records)
 size_t verify_workspace_bytes(int n, int max_depth, int H, long long n_inst, int LP) {
-  return ws_layout(n, max_depth, H, LP).stride * (size_t)n_inst;
+  const size_t a = ws_layout(n, max_depth, H, LP).stride * (size_t)n_inst;
+  const size_t b = verify_tc_workspace_bytes(n, max_depth, H, LP, n_inst);
+  return a > b ? a : b;
 }
 
 // heads per group used for n nodes (4 while the shared-memory plan fits, else 2; 0 if neither fits)
@@ -1048,6 +1051,11 @@ int verify_prep_smem_bytes(int n, int max_depth, int H, int LP) {
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, int which) {
+  // the warp-level kernels below; the override 2 selects the tensor-memory kernels (verify_tc.cu),
+  // which measured slower on every workload of this library (the per-chunk copies of 128 rows
+  // keep too few bytes in flight and the per-item work runs on four warps)
+  if (tuning(TUNE_VERIFY_KERNEL) == 2 && verify_tc_fits(a.n, a.max_depth, a.LP))
+    return launch_verify_tc(a, workspace, s, which);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

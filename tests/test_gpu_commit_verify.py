@@ -4,7 +4,11 @@ and against the separate GPU calls ssm_commit then ssm_tree_verify.
 
 Bar: accepted path, ring rows and heads bit-exact; y and the committed state
 max |gpu - ref| <= 1e-3 * (1 + |ref|) against the oracle; the fused and the
-separate GPU calls agree to 1e-5 * (1 + |ref|) (fp32, different rounding order)."""
+separate GPU calls agree to 5e-5 * (1 + |ref|).  They round differently: the fused
+call contracts C with the state as read and adds the commit's rank-len update to y
+through the products C_v·B_j (y = e^S·(E·C·h + Σ_j u_j·C·B_j)), and forms the
+committed state's update U·Bᵀ from bf16 hi/lo splits (~2^-16 of the update); the
+separate calls contract C with the committed state."""
 import dataclasses
 
 import numpy as np
@@ -17,7 +21,7 @@ from tests.helpers import bf16_dev, dev, f64, params_at, rel_err, ring_window, u
 
 pytestmark = pytest.mark.gpu
 TOL = 1e-3
-TOL_GPU = 1e-5
+TOL_GPU = 5e-5
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -302,3 +306,33 @@ def test_split_prep_then_main_is_the_folded_call():
         for a, b in zip(outs[0], other):
             assert torch.equal(a.view(torch.int32) if a.dtype == torch.float32 else a,
                                b.view(torch.int32) if b.dtype == torch.float32 else b)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 0])
+def test_persistent_ctas_walk_many_items(ctas, tuning):
+    # the tensor-memory tree kernels are persistent: with 1 or 3 CTAs each walks many (instance,
+    # head pair) items across instance boundaries (tables reloaded, accumulators and stages
+    # reused); 0 = the default grid
+    tuning("SSM_VERIFY_KERNEL", 2)
+    tuning("SSM_VERIFY_CTAS", ctas)
+    w0 = Workload(82, "multi-item", Shape(H=10), n_layers=3, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
+    w1 = next_workload(w0, 83, ("random", 16, 3, 4))
+    b0, b1 = batch(w0), batch(w1)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(3)])
+    check_separate(out)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_both_tree_kernel_sets(kernel, tuning):
+    # 1: warp-level mma.sync (the default); 2: state contraction on tcgen05 with tensor-memory
+    # accumulators
+    tuning("SSM_VERIFY_KERNEL", kernel)
+    w0 = Workload(84, "kernel sets", Shape(H=6), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
+    w1 = next_workload(w0, 85, ("full", 3, 3))
+    b0, b1 = batch(w0), batch(w1)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
+    check_separate(out)

@@ -247,3 +247,15 @@ def test_verify_is_deterministic():
     a = run_tree_step(d)
     c = run_tree_step(d)
     assert torch.equal(a["y"], c["y"]) and torch.equal(a["h"], c["h"])
+
+
+@pytest.mark.parametrize("ctas", [1, 2])
+def test_persistent_ctas_walk_many_items(ctas, tuning):
+    # the tensor-memory tree kernels with one or two persistent CTAs walking every (instance,
+    # head pair) item, the instance tables reloaded at each instance boundary; a 40-node tree
+    tuning("SSM_VERIFY_KERNEL", 2)
+    tuning("SSM_VERIFY_CTAS", ctas)
+    w = Workload(86, "multi-item plain", Shape(H=6), n_layers=3, batch=2, trees=(("full", 3, 3),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(3)])
