@@ -29,16 +29,16 @@ __device__ __forceinline__ float silu_fast(float v) {
 }
 
 // SiLU on the FMA pipe only (no special-function unit), for conv work that runs next to
-// tensor-core work: v / (1 + 2^t), t = -v·log2(e).
-//  * 2^t: Cody-Waite range reduction -- n = round(t) by adding and subtracting 1.5·2^23,
-//    f = t - n in [-1/2, 1/2] -- then the degree-6 Taylor series of 2^f = e^{f·ln 2}
-//    (coefficients (ln 2)^k / k!, remainder about 1e-7 on that interval), scaled by 2^n
-//    through the exponent field; t is clamped to [-126, 126].
+// tensor-core work: v / (1 + 2^t), t = -v·log2(e), with v first raised to -87 (below it the
+// exact result is under 2e-36 in magnitude, and silu(-87) is returned, about -1.4e-36).
+//  * 2^t: t <= 125.5 after that, and t is raised to -126 (large v give v); Cody-Waite range
+//    reduction -- n = round(t) by adding and subtracting 1.5·2^23, f = t - n in [-1/2, 1/2] --
+//    then the degree-6 Taylor series of 2^f = e^{f·ln 2} (coefficients (ln 2)^k / k!,
+//    remainder about 1e-7 on that interval), scaled by 2^n through the exponent field.
 //  * 1 / d: Newton-Raphson r <- r·(2 - d·r), three steps from the linear bit-pattern guess
 //    0x7F000000 - bits(d) (relative error below 1/8, then 2^-6, 2^-12, 2^-24).
 // Relative error of the result about 4e-6, like the special-function version above.
-__device__ __forceinline__ float exp2_poly(float t) {
-  t = fminf(fmaxf(t, -126.0f), 126.0f);
+__device__ __forceinline__ float exp2_poly(float t) {  // t in [-126, 126]
   const float m = t + 12582912.0f;  // 1.5·2^23: m's low mantissa bits hold round(t)
   const float f = t - (m - 12582912.0f);
   float p = 1.5403530393381608e-4f;
@@ -56,10 +56,9 @@ __device__ __forceinline__ float recip_nr(float d) {
   for (int i = 0; i < 3; ++i) r = fmaf(r, fmaf(-d, r, 1.0f), r);
   return r;
 }
-// below -87 the exact result is below 2e-36 in magnitude and 0 is returned (the clamped 2^t
-// would give v·2^-126 there, which is not small once |v| is large)
 __device__ __forceinline__ float silu_fma(float v) {
-  return v < -87.0f ? 0.0f : v * recip_nr(1.0f + exp2_poly(-1.4426950408889634f * v));
+  const float vc = fmaxf(v, -87.0f);
+  return vc * recip_nr(1.0f + exp2_poly(fmaxf(-1.4426950408889634f * vc, -126.0f)));
 }
 
 // softplus(v) = log(1 + e^v); above 20 it equals v to fp32 precision.
@@ -292,7 +291,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // Kernel launchers (defined in the .cu files, called by api.cu).
 struct VerifyArgs {
   int H, L, R, n_seq, n, max_depth;
-  int gpc;  // head groups per CTA (set by launch_verify)
+  int gpc;      // head groups per CTA (set by launch_verify)
+  int prep_hb;  // CTAs per instance of the prep kernel (set by launch_verify)
   const float *conv_w, *conv_b, *dt_bias, *A_log, *D;
   const ssm_node* layout;
   const uint16_t *xBC, *dt, *ring;

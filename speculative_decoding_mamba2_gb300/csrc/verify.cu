@@ -185,7 +185,14 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   // the main kernel may be scheduled once every prep CTA is running; it waits for this grid's
   // completion before it reads anything written here
   launch_dependents();
-  const int inst = blockIdx.x;
+  // the instance's heads may be split over several CTAs (few instances): each redoes the shared
+  // part (cheap) and computes its own heads; block 0 alone writes the shared tables, the ring
+  // rows and the head, and reports bad inputs
+  const int nhb = a.prep_hb > 1 ? a.prep_hb : 1;
+  const int inst = blockIdx.x / nhb, hblk = blockIdx.x % nhb;
+  const int hper = (H + nhb - 1) / nhb, h_lo = hblk * hper, h_hi = min(H, h_lo + hper), nh = h_hi - h_lo;
+  const bool lead = hblk == 0;
+  int32_t* const status = lead ? a.status : nullptr;
   const int seq = inst / a.L, layer = inst % a.L;
   const int d_inner = H * kP, conv_dim = d_inner + 2 * kN, R = a.R;
   const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
@@ -211,10 +218,10 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     hD[h] = a.D[(size_t)layer * H + h];
   }
   if (tid >= t0) {
-    for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, a.status);
-    for (int i = tid - t0; i < n * H; i += THREADS - t0) {
-      const int v = i / H, h = i - v * H;
-      dl[i] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
+    for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, status);
+    for (int i = tid - t0; i < n * nh; i += THREADS - t0) {
+      const int v = i / nh, h = h_lo + (i - v * nh);
+      dl[v * H + h] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
     }
   }
   if (fuse) {
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
         if (good == 0) pp[0] = 0;
         pp[16] = good < 1 ? 1 : good;
         pp[17] = a.ring_head[inst];
-        if (bad_len || badm) flag(a.status, SSM_STATUS_PATH_RANGE);
+        if (bad_len || badm) flag(status, SSM_STATUS_PATH_RANGE);
       }
     }
   }
@@ -302,8 +309,8 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   }
   // S_v per head: Σ over the path of Δ·A, root first; e^{S_v} to the workspace (v fastest:
   // contiguous stores), Δ_v·e^{-S_v} kept for the coefficients
-  for (int i = tid; i < n * H; i += THREADS) {
-    const int h = i / n, v = i - h * n;
+  for (int i = tid; i < n * nh; i += THREADS) {
+    const int h = h_lo + i / n, v = i % n;
     const float A = hA[h];
     float s = 0.f;
     const int dv = nodes[v].depth;
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
       if (lane == 0) Gm[pr] = s;
     }
   }
-  {  // workspace: C table, path tables
+  if (lead) {  // workspace: C table, path tables
     // C split once for the tensor cores: C = hi + lo (bf16 pairs, 2^-18 relative)
     uint32_t* dhi = reinterpret_cast<uint32_t*>(ws + W.C);
     uint32_t* dlo = dhi + n * CSTR / 2;
@@ -350,8 +357,8 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   // on the node's own pair: the path terms and D·x of y_v, divided by e^{S_v} (k fastest:
   // contiguous stores)
   float* wc = reinterpret_cast<float*>(ws + W.coef);
-  for (int i = tid; i < n_pairs * H; i += THREADS) {
-    const int h = i / n_pairs, k = i - h * n_pairs;
+  for (int i = tid; i < n_pairs * nh; i += THREADS) {
+    const int h = h_lo + i / n_pairs, k = i % n_pairs;
     const int pr = pairs[1 + k];
     const int v = pr / DMAX, m = pathn[pr];
     float c = emS[m * H + h] * dl[m * H + h] * Gm[pr];
@@ -363,14 +370,14 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   // ---- the committed path: Δ_j and a_j per head, then w_j = Δ_j·Π_{i>j} a_i, E = Π_j a_j, B_j ----
   float* wP = reinterpret_cast<float*>(smem + L.wP);
   float* aP = reinterpret_cast<float*>(smem + L.aP);
-  for (int i = tid; i < lenP * H; i += THREADS) {
-    const int j = i / H, h = i - j * H;
+  for (int i = tid; i < lenP * nh; i += THREADS) {
+    const int j = i / nh, h = h_lo + i % nh;
     const float d = softplus_f(bf16f(a.prev_dt[((size_t)inst * a.prev_n + pp[j]) * H + h]) + hBias[h]);
-    wP[i] = d;
-    aP[i] = decay_of(d, hA[h]);
+    wP[j * H + h] = d;
+    aP[j * H + h] = decay_of(d, hA[h]);
   }
   __syncthreads();
-  for (int h = tid; h < H; h += THREADS) {
+  for (int h = h_lo + tid; h < h_hi; h += THREADS) {
     float* eh = reinterpret_cast<float*>(ws + W.eS) + h * W.NP;
     float run = 1.f;
     for (int j = lenP - 1; j >= 0; --j) {
@@ -379,6 +386,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     }
     eh[n] = run;  // E_h
   }
+  if (!lead) return;
   {  // conv + SiLU of the path's B channels over [ring rows before the path ‖ path rows]:
      // 4 channels per thread, 8-byte loads, up to 5 path rows per pass with all 8 window rows
      // in flight before the first is used (the x channels are done per head group by the
@@ -488,7 +496,11 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   return s;
 }
 
-template <int G, bool FUSE>
+// NTL: node tiles contracted per pass over a chunk.  With NTL = 1 a tree of several 16-node
+// tiles streams each state chunk once per tile; with NTL > 1 (up to NTL tiles) every chunk is
+// read, committed and split once and contracted against all tiles, their accumulators held
+// side by side.
+template <int G, bool FUSE, int NTL>
 __global__ void __launch_bounds__(THREADS, 2)
     tree_verify_kernel(VerifyArgs a, const unsigned char* __restrict__ ws_base, const __grid_constant__ CUtensorMap tmap) {
   constexpr int ROWS = G * kP;
@@ -528,6 +540,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int conv_dim = d_inner + 2 * kN;
   const int R = a.R;
   const int n_tiles = (n + NT - 1) / NT;
+  const int n_tb = (n_tiles + NTL - 1) / NTL;  // passes over the state per group
   const uint16_t* xbc = a.xBC + (size_t)inst * n * conv_dim;
   const uint16_t* ring = a.ring + (size_t)inst * R * conv_dim;
   const unsigned char* ws = ws_base + (size_t)inst * W.stride;
@@ -538,7 +551,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t pro_bar = bar0 + 8 * (2 * STAGES);
   const uint32_t x_bar = bar0 + 8 * (2 * STAGES + 1);
   volatile int& s_abort = *reinterpret_cast<int*>(smem + L.bars + (2 * STAGES + 2) * 8);
-  const int total = g_count * n_tiles * KCH;  // h0 chunks this CTA consumes
+  const int total = g_count * n_tb * KCH;  // h0 chunks this CTA consumes
 
   // swizzled tensor copies need a 128-byte aligned destination; refuse rather than copy
   if (smem_u32(stage) & 127) {
@@ -593,7 +606,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
       if (++pf_k == KCH) {
         pf_k = 0;
-        if (++pf_t == n_tiles) {
+        if (++pf_t == n_tb) {
           pf_t = 0;
           ++pf_g;
         }
@@ -776,7 +789,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const int fg = lane >> 2, ft = lane & 3;  // fragment row group / thread-in-group
   const int wrow = warp * 16 * MT;          // first state row of this warp within the group
   const int whead = wrow / kP;              // every row of a warp belongs to one head
-  float acc[MT][2][4];
+  float acc[NTL][MT][2][4];
   float Ew = 1.f;  // decay of the whole committed path for this warp's head
   int q = 0;       // chunk index
   for (int gi = 0; gi < g_count; ++gi) {
@@ -786,47 +799,55 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
     if (warp == 0 && gi + 1 < g_count && !s_abort) issue_inputs(gi + 1);
     if (FUSE) Ew = eSg[((gi & 1) * G + min(whead, heads - 1)) * W.NP + n];
-    for (int tile = 0; tile < n_tiles; ++tile) {
-      int brow[2];
+    for (int tb = 0; tb < n_tb; ++tb) {
+      const bool last_tb = tb == n_tb - 1;
+      int brow[NTL][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) brow[nt] = min(tile * NT + nt * 8 + fg, n - 1) * CSTR;
+      for (int i = 0; i < NTL; ++i)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) brow[i][nt] = min((tb * NTL + i) * NT + nt * 8 + fg, n - 1) * CSTR;
       for (int kc = 0; kc < KCH; ++kc, ++q) {
         if (warp == 0) produce(q + STAGES);  // refill the stage chunk q-1 used
         if (kc == 0) {
-          // the tile's accumulator starts at Σ_m coef[v,m]·x_m[p] (path terms and D·x over e^{S_v}):
+          // each tile's accumulator starts at Σ_m coef[v,m]·x_m[p] (path terms and D·x over e^{S_v}):
           // A = x rows of the nodes m (K), B = coef of node v (N; zero off v's path)
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int e = 0; e < 4; ++e) acc[mt][nt][e] = 0.f;
           const float* chd = coefg + ((gi & 1) * G + min(whead, heads - 1)) * W.PP;
-          const int ksteps = min(tile + 1, NX / 16);  // ancestors precede their nodes
-          for (int k16 = 0; k16 < ksteps; ++k16) {
-            // k = node m: lane (fg, ft) holds m = 2ft, 2ft+1 and 2ft+8, 2ft+9 of the k-step
-            const int m0 = k16 * 16 + 2 * ft;
-            uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-              const int v = tile * NT + nt * 8 + fg;
-              split_bf16x2(path_coef(chd, v, m0), path_coef(chd, v, m0 + 1), bhi[nt][0], blo[nt][0]);
-              split_bf16x2(path_coef(chd, v, m0 + 8), path_coef(chd, v, m0 + 9), bhi[nt][1], blo[nt][1]);
-            }
-            const float* xa = xs + m0 * XSTR + wrow + fg;
+          for (int i = 0; i < NTL; ++i) {
+            const int tile = tb * NTL + i;
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              const float* x0 = xa + mt * 16;
-              uint32_t ahi[4], alo[4];
-              split_bf16x2(x0[0], x0[XSTR], ahi[0], alo[0]);
-              split_bf16x2(x0[8], x0[XSTR + 8], ahi[1], alo[1]);
-              split_bf16x2(x0[8 * XSTR], x0[9 * XSTR], ahi[2], alo[2]);
-              split_bf16x2(x0[8 * XSTR + 8], x0[9 * XSTR + 8], ahi[3], alo[3]);
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][mt][nt][e] = 0.f;
+            if (tile >= n_tiles) continue;
+            const int ksteps = min(tile + 1, NX / 16);  // ancestors precede their nodes
+            for (int k16 = 0; k16 < ksteps; ++k16) {
+              // k = node m: lane (fg, ft) holds m = 2ft, 2ft+1 and 2ft+8, 2ft+9 of the k-step
+              const int m0 = k16 * 16 + 2 * ft;
+              uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
-                mma_bf16(acc[mt][nt], alo, bhi[nt]);
-                mma_bf16(acc[mt][nt], ahi, blo[nt]);
-                mma_bf16(acc[mt][nt], ahi, bhi[nt]);
+                const int v = tile * NT + nt * 8 + fg;
+                split_bf16x2(path_coef(chd, v, m0), path_coef(chd, v, m0 + 1), bhi[nt][0], blo[nt][0]);
+                split_bf16x2(path_coef(chd, v, m0 + 8), path_coef(chd, v, m0 + 9), bhi[nt][1], blo[nt][1]);
+              }
+              const float* xa = xs + m0 * XSTR + wrow + fg;
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const float* x0 = xa + mt * 16;
+                uint32_t ahi[4], alo[4];
+                split_bf16x2(x0[0], x0[XSTR], ahi[0], alo[0]);
+                split_bf16x2(x0[8], x0[XSTR + 8], ahi[1], alo[1]);
+                split_bf16x2(x0[8 * XSTR], x0[9 * XSTR], ahi[2], alo[2]);
+                split_bf16x2(x0[8 * XSTR + 8], x0[9 * XSTR + 8], ahi[3], alo[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                  mma_bf16(acc[i][mt][nt], alo, bhi[nt]);
+                  mma_bf16(acc[i][mt][nt], ahi, blo[nt]);
+                  mma_bf16(acc[i][mt][nt], ahi, bhi[nt]);
+                }
               }
             }
           }
@@ -870,9 +891,9 @@ __global__ void __launch_bounds__(THREADS, 2)
               rb[mt].w = fmaf(u1, bj.w, rb[mt].w);
             }
           }
-          // every node tile streams the same h and rebuilds h' in registers; only the last
-          // tile stores it, so no tile can read back a chunk that is already committed
-          if (whead < heads && tile == n_tiles - 1) {
+          // with several passes every pass rebuilds h' in registers; only the last one stores
+          // it, so no pass can read back a chunk that is already committed
+          if (whead < heads && last_tb) {
             float* g0 = a.h_w + ((size_t)(inst * a.H + hb) * kP + wrow + fg) * kN + kc * KC + 4 * ft;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
@@ -881,16 +902,20 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
           }
         }
-        uint32_t bhi[2][2], blo[2][2];  // C of this lane's two B-fragment nodes, columns 4*ft .. 4*ft+3
+        // C of this lane's two B-fragment nodes (columns 4*ft .. 4*ft+3) of tile i
+        auto c_frags = [&](int i, uint32_t (&bhi)[2][2], uint32_t (&blo)[2][2]) {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const uint2 h2 = *reinterpret_cast<const uint2*>(Chi + brow[nt] + kc * KC + 4 * ft);
-          const uint2 l2 = *reinterpret_cast<const uint2*>(Clo + brow[nt] + kc * KC + 4 * ft);
-          bhi[nt][0] = h2.x;
-          bhi[nt][1] = h2.y;
-          blo[nt][0] = l2.x;
-          blo[nt][1] = l2.y;
-        }
+          for (int nt = 0; nt < 2; ++nt) {
+            const uint2 h2 = *reinterpret_cast<const uint2*>(Chi + brow[i][nt] + kc * KC + 4 * ft);
+            const uint2 l2 = *reinterpret_cast<const uint2*>(Clo + brow[i][nt] + kc * KC + 4 * ft);
+            bhi[nt][0] = h2.x;
+            bhi[nt][1] = h2.y;
+            blo[nt][0] = l2.x;
+            blo[nt][1] = l2.y;
+          }
+        };
+        uint32_t bhi0[2][2], blo0[2][2];
+        if (NTL == 1) c_frags(0, bhi0, blo0);  // one tile: its fragments serve every m-tile
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           uint32_t ahi[4], alo[4];
@@ -899,15 +924,31 @@ __global__ void __launch_bounds__(THREADS, 2)
           split_bf16x2(ra[mt].z, ra[mt].w, ahi[2], alo[2]);
           split_bf16x2(rb[mt].z, rb[mt].w, ahi[3], alo[3]);
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) {
-            mma_bf16(acc[mt][nt], alo, bhi[nt]);
-            mma_bf16(acc[mt][nt], ahi, blo[nt]);
-            mma_bf16(acc[mt][nt], ahi, bhi[nt]);
+          for (int i = 0; i < NTL; ++i) {
+            if (NTL > 1 && tb * NTL + i >= n_tiles) continue;
+            uint32_t bhi[2][2], blo[2][2];
+            if (NTL == 1) {
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int w2 = 0; w2 < 2; ++w2) {
+                  bhi[nt][w2] = bhi0[nt][w2];
+                  blo[nt][w2] = blo0[nt][w2];
+                }
+            } else {
+              c_frags(i, bhi, blo);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+              mma_bf16(acc[i][mt][nt], alo, bhi[nt]);
+              mma_bf16(acc[i][mt][nt], ahi, blo[nt]);
+              mma_bf16(acc[i][mt][nt], ahi, bhi[nt]);
+            }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
-        if (kc == 1 && tile == n_tiles - 1 && gi + 1 < g_count) {
+        if (kc == 1 && last_tb && gi + 1 < g_count) {
           // the next group's x conv (special-function heavy) runs between this group's chunks,
           // next to other warps' tensor and memory work; every warp must be past this group's
           // last path-term product (its x rows) first
@@ -918,19 +959,23 @@ __global__ void __launch_bounds__(THREADS, 2)
           // ---- epilogue: y = e^{S_v}·acc ----
           const float* eh = eSg + ((gi & 1) * G + whead) * W.NP;
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+          for (int i = 0; i < NTL; ++i) {
+            const int tile = tb * NTL + i;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int v = tile * NT + nt * 8 + 2 * ft + c;
-              if (v >= n) continue;
-              const float es = eh[v];
-              float* yrow = a.y + ((size_t)inst * n + v) * d_inner + hb * kP + wrow + fg;
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                yrow[mt * 16] = es * acc[mt][nt][c];
-                yrow[mt * 16 + 8] = es * acc[mt][nt][2 + c];
+              for (int c = 0; c < 2; ++c) {
+                const int v = tile * NT + nt * 8 + 2 * ft + c;
+                if (v >= n) continue;
+                const float es = eh[v];
+                float* yrow = a.y + ((size_t)inst * n + v) * d_inner + hb * kP + wrow + fg;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                  yrow[mt * 16] = es * acc[i][mt][nt][c];
+                  yrow[mt * 16 + 8] = es * acc[i][mt][nt][2 + c];
+                }
               }
-            }
+          }
         }
       }
     }
@@ -942,7 +987,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 int g_sms[64] = {0};
-int g_configured[5][64] = {{0}};
+int g_configured[10][64] = {{0}};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -968,13 +1013,13 @@ cudaError_t ensure_smem(K kernel, int idx, int dev, int bytes) {
   return cudaSuccess;
 }
 
-template <int G, bool FUSE>
+template <int G, bool FUSE, int NTL>
 cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStream_t s, int dev) {
   VerifyArgs a = a0;
   const int LP = FUSE ? a.LP : 0;
   const Ws W = ws_layout(a.n, a.max_depth, a.H, LP);
   const Smem L = smem_layout<G, FUSE>(a.n, W.PP, W.NP, LP);
-  cudaError_t e = ensure_smem(tree_verify_kernel<G, FUSE>, (G == 4 ? 0 : 1) + (FUSE ? 2 : 0), dev, L.total);
+  cudaError_t e = ensure_smem(tree_verify_kernel<G, FUSE, NTL>, (G == 4 ? 0 : 1) + (FUSE ? 2 : 0) + (NTL > 1 ? 5 : 0), dev, L.total);
   if (e != cudaSuccess) return e;
   int sms = dev < 64 ? g_sms[dev] : 0;
   if (sms == 0) {
@@ -984,15 +1029,20 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
   }
   const long long inst = (long long)a.n_seq * a.L;
   const int NG = (a.H + G - 1) / G;
-  // enough CTAs for ~4 waves of two CTAs per SM; groups per CTA a divisor of NG when possible
-  long long want = (inst * NG) / (8LL * sms);
-  int target = (int)(want < 1 ? 1 : (want > MAX_GPC ? MAX_GPC : want));
+  // groups per CTA: time ~ waves of CTAs x (a fixed part per CTA + one unit per group), the fixed
+  // part (prologue, the wait for the prep grid, the first inputs) measured at about 1.5 groups;
+  // so few instances get fewer, longer CTAs (batch 1 of the 2.7B shape: 256 CTAs of 5 groups
+  // in one wave instead of 1280 of one in five)
+  const long long slots = 2LL * sms;
   int gpc = 1;
-  for (int d = 1; d <= target && d <= NG; ++d)
-    if (NG % d == 0) gpc = d;
-  if (2 * gpc < target) {
-    const int parts = (NG + target - 1) / target;
-    gpc = (NG + parts - 1) / parts;
+  double best = 1e300;
+  for (int g = 1; g <= MAX_GPC && g <= NG; ++g) {
+    const long long ctas = inst * ((NG + g - 1) / g);
+    const double est = (double)((ctas + slots - 1) / slots) * (1.5 + g);
+    if (est < best - 1e-9) {
+      best = est;
+      gpc = g;
+    }
   }
   const int o_gpc = tuning(TUNE_VERIFY_GPC);  // tuning / test override
   if (o_gpc >= 1 && o_gpc <= MAX_GPC) gpc = o_gpc;
@@ -1020,7 +1070,7 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tree_verify_kernel<G, FUSE>, a, ws, tmap);
+  return cudaLaunchKernelEx(&cfg, tree_verify_kernel<G, FUSE, NTL>, a, ws, tmap);
 }
 
 }  // namespace
@@ -1087,12 +1137,32 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
   if (e != cudaSuccess) return e;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (which != 2) {
-    tree_prep_kernel<<<(unsigned)inst, THREADS, prep_bytes, s>>>(a, ws);
+    // few instances: split each instance's heads over enough CTAs to cover the SMs (at most 16
+    // heads per CTA); one CTA per instance once the instances fill them
+    int sms = dev < 64 ? g_sms[dev] : 0;
+    if (sms == 0) {
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) g_sms[dev] = sms;
+    }
+    VerifyArgs ap = a;
+    const long long want = (2LL * sms + inst - 1) / inst;
+    const int max_hb = (a.H + 15) / 16;
+    ap.prep_hb = (int)(want < 1 ? 1 : (want > max_hb ? max_hb : want));
+    tree_prep_kernel<<<(unsigned)(inst * ap.prep_hb), THREADS, prep_bytes, s>>>(ap, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess || which == 1) return e;
   }
-  if (a.LP > 0) return G == 4 ? launch_main<4, true>(a, ws, s, dev) : launch_main<2, true>(a, ws, s, dev);
-  return G == 4 ? launch_main<4, false>(a, ws, s, dev) : launch_main<2, false>(a, ws, s, dev);
+  // trees of 2..4 node tiles: 2-head groups contract every tile per pass over the state
+  const int n_tiles = (a.n + NT - 1) / NT;
+  if (n_tiles > 1 && n_tiles <= 4) {
+    const Ws W2 = ws_layout(a.n, a.max_depth, a.H, a.LP);
+    const bool fits = a.LP > 0 ? smem_layout<2, true>(a.n, W2.PP, W2.NP, a.LP).total <= SMEM_LIMIT
+                               : smem_layout<2, false>(a.n, W2.PP, W2.NP, 0).total <= SMEM_LIMIT;
+    if (fits) return a.LP > 0 ? launch_main<2, true, 4>(a, ws, s, dev) : launch_main<2, false, 4>(a, ws, s, dev);
+  }
+  if (a.LP > 0) return G == 4 ? launch_main<4, true, 1>(a, ws, s, dev) : launch_main<2, true, 1>(a, ws, s, dev);
+  return G == 4 ? launch_main<4, false, 1>(a, ws, s, dev) : launch_main<2, false, 1>(a, ws, s, dev);
 }
 
 }  // namespace ssmtree
