@@ -189,3 +189,82 @@ def test_block_verify_against_oracle():
             e = np.abs(got - ref) / (1 + np.abs(ref))
             assert e.max() <= 1e-2, (i, e.max())
             assert np.median(e) <= 1e-4, (i, np.median(e))
+
+
+def _check_bf16_step(got, ref, what):
+    """A bf16 activation against the oracle's value of the same step (fed the GPU's own inputs)
+    rounded to bf16: equal, except where the GPU's fp32 value and the fp64 value fall on either
+    side of a rounding point -- then one bf16 step apart -- or where the value is so small that
+    the fp32 accumulation's absolute error (about 1e-5 for a 2560- or 5120-term sum of O(1)
+    size) decides its bf16 neighbour; at most 1 % of the values differ at all."""
+    r = oracle.to_bf16(ref)
+    d = np.abs(got - r)
+    assert (d <= 2.0 ** -7 * np.abs(r) + 1e-4).all(), (what, float((d - 2.0 ** -7 * np.abs(r)).max()))
+    assert np.mean(d > 0) <= 1e-2, (what, float(np.mean(d > 0)))
+
+
+@pytest.mark.parametrize("layer", [0, 63])
+def test_block_steps_2p7b_shape(layer):
+    """A whole Mamba2 block at the 2.7B shape (d_model 2560, 80 heads, d_inner 5120), two
+    sequences of 16-node trees, step by step: each step's oracle is fed the GPU's own bf16
+    intermediates, so a rounding flip in one step cannot propagate into the next.  fp32 outputs
+    (y, the residual stream) within 1e-3·(1+|ref|); bf16 outputs per _check_bf16_step."""
+    from speculative_decoding_mamba2_gb300 import (Dims, ssm_gated_rmsnorm, ssm_linear, ssm_rmsnorm,
+                                                   ssm_tree_layout_build, ssm_tree_verify,
+                                                   ssm_tree_verify_workspace_size)
+    H, d_model, S, eps = 80, 2560, 2, 1e-5
+    w = Workload(3, "block steps 2.7B", Shape(H=H), n_layers=64, batch=S, trees=(("random", 16, 3, 4),))
+    b = batch(w, layers=[layer])
+    n = b["n_nodes"]
+    d_inner, conv_dim = H * 64, H * 64 + 256
+    T = S * n
+    rng = np.random.default_rng([90, layer])
+    n_in = d_inner + conv_dim + H
+    W_in = oracle.to_bf16(rng.standard_normal((n_in, d_model)) / np.sqrt(d_model))
+    W_out = oracle.to_bf16(rng.standard_normal((d_model, d_inner)) / np.sqrt(d_inner))
+    nw = (1 + 0.1 * rng.standard_normal(d_model)).astype(np.float32)
+    gw = (1 + 0.1 * rng.standard_normal(d_inner)).astype(np.float32)
+    x_in = rng.standard_normal((T, d_model)).astype(np.float32)
+    dims = Dims(n_heads=H, n_layers=1, ring_cap=w.ring_cap)
+    x = torch.from_numpy(x_in.copy()).cuda()
+    u = torch.empty((T, d_model), device="cuda", dtype=torch.bfloat16)
+    z = torch.empty((T, d_inner), device="cuda", dtype=torch.bfloat16)
+    xBC = torch.empty((T, conv_dim), device="cuda", dtype=torch.bfloat16)
+    dt = torch.empty((T, H), device="cuda", dtype=torch.bfloat16)
+    y = torch.empty((T, d_inner), device="cuda")
+    g = torch.empty((T, d_inner), device="cuda", dtype=torch.bfloat16)
+    prm = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).cuda() for k, v in b["params"].items()}
+    lay, depth = ssm_tree_layout_build(b["parent"])
+    layout = torch.from_numpy(lay).cuda()
+    h0 = torch.from_numpy(b["h0"]).cuda()
+    ring = dev_bf16(b["ring"].reshape(S, -1))
+    head = torch.from_numpy(b["ring_head"]).cuda()
+    ws = torch.empty(ssm_tree_verify_workspace_size(dims, S, n, depth), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ssm_rmsnorm(x, torch.from_numpy(nw).cuda(), eps, u)
+    ssm_linear(u, dev_bf16(bits_of(W_in)), [(0, z), (d_inner, xBC), (d_inner + conv_dim, dt)], status=status)
+    ssm_tree_verify(dims, prm, S, n, depth, layout, xBC, dt, h0, ring, head, y, ws, status)
+    ssm_gated_rmsnorm(y, z, torch.from_numpy(gw).cuda(), eps, g)
+    ssm_linear(g, dev_bf16(bits_of(W_out)), [(0, x)], residual=x, status=status)
+    torch.cuda.synchronize()
+    assert int(status) == 0
+    u_g, z_g, xbc_g, dt_g, y_g, g_g, x_g = (host(t) for t in (u, z, xBC, dt, y, g, x))
+    # 1. RMSNorm of the residual stream
+    _check_bf16_step(u_g, oracle.rmsnorm(x_in, nw.astype(np.float64), eps), "rmsnorm")
+    # 2. input projection of the GPU's u, cut into z | x B C | dt
+    proj = oracle.linear(u_g, W_in)
+    _check_bf16_step(z_g, proj[:, :d_inner], "z")
+    _check_bf16_step(xbc_g, proj[:, d_inner:d_inner + conv_dim], "xBC")
+    _check_bf16_step(dt_g, proj[:, d_inner + conv_dim:], "dt")
+    # 3. tree verify of the GPU's x B C and dt, every element
+    prm0 = params_at(b["params"], 0)
+    for i in range(S):
+        rows = slice(i * n, (i + 1) * n)
+        ref_y = oracle.verify(prm0, b["parent"][i], xbc_g[rows], dt_g[rows], b["h0"][i, 0].astype(np.float64),
+                              f64(b["ring"][i, 0]), int(b["ring_head"][i, 0]))
+        assert (np.abs(y_g[rows] - ref_y) <= 1e-3 * (1 + np.abs(ref_y))).all(), ("y", i)
+    # 4. gated RMSNorm of the GPU's y and z
+    _check_bf16_step(g_g, oracle.gated_rmsnorm(y_g, z_g, gw.astype(np.float64), eps), "gated rmsnorm")
+    # 5. output projection of the GPU's g added to the residual stream
+    ref_x = x_in.astype(np.float64) + oracle.linear(g_g, W_out)
+    assert (np.abs(x_g - ref_x) <= 1e-3 * (1 + np.abs(ref_x))).all(), "residual out"
