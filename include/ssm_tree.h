@@ -400,6 +400,9 @@ int ssm_selftest_silu(const float *v, float *out, int64_t n, void *stream);
  *                                        memory accumulators (measured slower here)
  *          "SSM_VERIFY_CTAS"             at most this many CTAs of the persistent tcgen05 tree
  *                                        kernel (each walks a run of head pairs)
+ *          "SSM_VERIFY_DEEP"             one CTA per SM with a deep pipeline of state chunks:
+ *                                        0 = when the head groups are few per SM, 1 = never,
+ *                                        2 = wherever its shared memory fits
  *   value  0 = automatic; a value the plan cannot use is ignored at launch.
  * Not thread-safe against calls that launch concurrently on other threads.
  * Errors: SSM_ERR_INVALID_ARG for an unknown name or a negative value.

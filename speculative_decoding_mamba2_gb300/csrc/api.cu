@@ -71,7 +71,7 @@ namespace {
 const char* const kTuneNames[TUNE_COUNT] = {"SSM_VERIFY_GROUPS_PER_CTA", "SSM_VERIFY_HEADS_PER_GROUP",
                                             "SSM_LINEAR_TCHUNK",         "SSM_LINEAR_SPLITS",
                                             "SSM_LINEAR_STAGES",         "SSM_VERIFY_KERNEL",
-                                            "SSM_VERIFY_CTAS"};
+                                            "SSM_VERIFY_CTAS",           "SSM_VERIFY_DEEP"};
 struct TuneTable {
   int v[TUNE_COUNT];
   TuneTable() {

@@ -323,7 +323,7 @@ bool verify_tc_fits(int n, int max_depth, int LP);
 // Launch-plan overrides (0 = automatic).  Each starts at its environment variable, read once
 // per process; ssm_set_tuning replaces it.  They never change results beyond rounding order.
 enum TuneKey { TUNE_VERIFY_GPC, TUNE_VERIFY_G, TUNE_LINEAR_TCHUNK, TUNE_LINEAR_SPLITS, TUNE_LINEAR_STAGES,
-               TUNE_VERIFY_KERNEL, TUNE_VERIFY_CTAS, TUNE_COUNT };
+               TUNE_VERIFY_KERNEL, TUNE_VERIFY_CTAS, TUNE_VERIFY_DEEP, TUNE_COUNT };
 int tuning(TuneKey k);
 
 // Projections (gemm.cu): D = A · Wᵀ (+ residual) with the output columns cut into segments.

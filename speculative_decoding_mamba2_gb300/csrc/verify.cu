@@ -62,13 +62,14 @@ constexpr int KC = 16;           // d_state columns per pipeline stage
 constexpr int KCH = kN / KC;     // stages per node tile
 constexpr int STAGES_PLAIN = 4;  // h0 pipeline depth of the plain kernel
 constexpr int STAGES_FUSED = 3;  // ... and of the commit-folding kernel (its extra tables need the room)
+constexpr int STAGES_DEEP = 8;   // ... of either at one CTA per SM (few groups per SM: bytes in flight)
 constexpr int SROW = KC;         // stage row: 64 B, 16-byte pieces swizzled by the copy engine
 constexpr int THREADS = 256;
 constexpr int DMAX = SSM_MAX_DEPTH + 1;
 constexpr int XW = 256;          // channels per staged input row
 constexpr int CSTR = kN + 16;    // padded row of the C tables: fp32 in the prep, bf16 hi/lo in the workspace
                                  // (288-byte bf16 rows: conflict-free 8-byte B-fragment loads)
-constexpr int MAX_GPC = 8;       // head groups per CTA
+constexpr int MAX_GPC = 64;      // head groups per CTA
 constexpr int SMEM_LIMIT = 232448;
 constexpr int kMetaInts = 20;    // folded-commit record: [0] path length, [1] ring head before it, [4..19] nodes
 static_assert(2 * kN == THREADS, "one thread per B|C channel");
@@ -140,7 +141,8 @@ struct PrepSmem {
   int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, hp, total;
 };
 
-__host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0) {
+// per-head arrays sized by the heads one CTA computes (HR)
+__host__ __device__ inline PrepSmem prep_layout(int n, int HR, int PP, int LP = 0) {
   PrepSmem s;
   int o = 0;
   auto take = [&](int b) {
@@ -151,26 +153,31 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int H, int PP, int LP = 0
   s.nodes = take(n * (int)sizeof(ssm_node));
   s.pathn = take(n * DMAX * 4);
   s.pairs = take((PP + 4) * 4);
-  s.xin = take((n + 3) * XW * 2);
+  s.xin = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows ‖ LP path rows][tree nodes]
   s.Bs = take(n * kN * 4);
   s.Cs = take(n * CSTR * 4);
   s.Gm = take(n * DMAX * 4);
-  s.dl = take(n * H * 4);
-  s.S = take(n * H * 4);
-  s.pp = take(LP > 0 ? 20 * 4 : 0);  // committed path nodes [16], its length, the ring head before it
-  s.wP = take(LP * H * 4);           // Δ_j, then Δ_j·Π_{i>j} a_i  [LP][H]
-  s.aP = take(LP * H * 4);           // a_j = exp(Δ_j·A)          [LP][H]
-  s.hp = take(3 * H * 4);            // per head: A = -exp(A_log), dt_bias, D
+  s.dl = take(n * HR * 4);
+  s.S = take(n * HR * 4);
+  s.pp = take(LP > 0 ? 20 * 4 : 0);  // committed path nodes [16], its length, -, a bad root's refetch
+  s.wP = take(LP * HR * 4);          // Δ_j, then Δ_j·Π_{i>j} a_i  [LP][HR]
+  s.aP = take(LP * HR * 4);          // a_j = exp(Δ_j·A)          [LP][HR]
+  s.hp = take(3 * HR * 4);           // per head: A = -exp(A_log), dt_bias, D
   s.total = o;
   return s;
 }
 
-__global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
-  extern __shared__ __align__(128) unsigned char smem[];
+// The prep of instance `inst` for heads [h_lo, h_hi) (everything that does not depend on the head
+// group), by the whole CTA into `smem`: the shared tables (lead), its heads' e^S and coefficients
+// and, with a folded commit, E and w_j into the workspace record; the ring's B | C rows (lead);
+// the ring head (lead).
+__device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_base, int inst, int h_lo, int h_hi,
+                          bool lead, unsigned char* smem) {
   const int n = a.n, H = a.H;
   const bool fuse = a.LP > 0;
   const Ws W = ws_layout(n, a.max_depth, H, a.LP);
-  const PrepSmem L = prep_layout(n, H, W.PP, a.LP);
+  const int HR = h_hi - h_lo, nh = HR;
+  const PrepSmem L = prep_layout(n, HR, W.PP, a.LP);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
   int* pairs = reinterpret_cast<int*>(smem + L.pairs);
@@ -182,16 +189,6 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   float* emS = reinterpret_cast<float*>(smem + L.S);  // e^{-S_v} [n][H]
 
   const int tid = threadIdx.x;
-  // the main kernel may be scheduled once every prep CTA is running; it waits for this grid's
-  // completion before it reads anything written here
-  launch_dependents();
-  // the instance's heads may be split over several CTAs (few instances): each redoes the shared
-  // part (cheap) and computes its own heads; block 0 alone writes the shared tables, the ring
-  // rows and the head, and reports bad inputs
-  const int nhb = a.prep_hb > 1 ? a.prep_hb : 1;
-  const int inst = blockIdx.x / nhb, hblk = blockIdx.x % nhb;
-  const int hper = (H + nhb - 1) / nhb, h_lo = hblk * hper, h_hi = min(H, h_lo + hper), nh = h_hi - h_lo;
-  const bool lead = hblk == 0;
   int32_t* const status = lead ? a.status : nullptr;
   const int seq = inst / a.L, layer = inst % a.L;
   const int d_inner = H * kP, conv_dim = d_inner + 2 * kN, R = a.R;
@@ -200,74 +197,101 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
   unsigned char* ws = ws_base + (size_t)inst * W.stride;
   int* pp = reinterpret_cast<int*>(smem + L.pp);
   float* hA = reinterpret_cast<float*>(smem + L.hp);  // per head: A, then dt_bias, then D
-  float* hBias = hA + H;
-  float* hD = hA + 2 * H;
+  float* hBias = hA + HR;  // all per-head scratch indexed by h - h_lo
+  float* hD = hA + 2 * HR;
   const uint16_t* prev_xbc = fuse ? a.prev_xBC + (size_t)inst * a.prev_n * conv_dim : nullptr;
 
-  // B|C input rows of the tree's nodes in flight first (rows 3..n+2; rows 0..2 follow below)
-  for (int i = tid; i < n * 32; i += THREADS) {
-    const int r = 3 + (i >> 5), pc = i & 31;
-    cp_async16(xin + r * XW + pc * 8, xbc + (size_t)(r - 3) * conv_dim + d_inner + pc * 8);
+  float* wP = reinterpret_cast<float*>(smem + L.wP);
+  float* aP = reinterpret_cast<float*>(smem + L.aP);
+  // Staged B|C rows: rows t < TB are the window (the three ring rows before the committed path,
+  // then the path's rows), row TB + v is tree node v.  Without a folded commit the window is the
+  // three ring rows before the root.
+  const int TB = 3 + (fuse ? a.LP : 0);
+
+  // ---- every global load of the prep is issued before the first barrier: what depends on the
+  // committed path takes the path as given (clamped into the previous tree); warp 0 validates it
+  // meanwhile, and rows fetched past a bad entry are never used ----
+  for (int i = tid; i < n * 32; i += THREADS) {  // tree nodes' rows
+    const int v = i >> 5, pc = i & 31;
+    cp_async16(xin + (TB + v) * XW + pc * 8, xbc + (size_t)v * conv_dim + d_inner + pc * 8);
   }
-  // warp 0 checks the committed path while the other warps load the node records and Δ
+  const int head_old = a.ring_head[inst];  // ring head before the committed path
+  const int32_t* pth = fuse ? a.prev_path + (size_t)seq * a.LP : nullptr;
+  int len_given = 0;  // path length as given, clamped to [1, LP]
+  if (fuse) {
+    const int len = a.prev_path_len[seq];
+    len_given = len < 1 ? 1 : (len > a.LP ? a.LP : len);
+  }
+  auto given_node = [&](int j) {
+    const int v = pth[j];
+    return v < 0 ? 0 : (v >= a.prev_n ? a.prev_n - 1 : v);
+  };
+  for (int i = tid; i < (3 + len_given) * 32; i += THREADS) {  // window rows
+    const int t = i >> 5, pc = i & 31;
+    const uint16_t* src = t < 3 ? ring + (size_t)ring_pos(head_old, t - 3, R) * conv_dim
+                                : prev_xbc + (size_t)given_node(t - 3) * conv_dim;
+    cp_async16(xin + t * XW + pc * 8, src + d_inner + pc * 8);
+  }
+  cp_async_commit();
+  for (int i = tid; i < len_given * nh; i += THREADS) {  // the path rows' dt of this CTA's heads
+    const int j = i / nh, hr = i - j * nh;
+    wP[j * HR + hr] = bf16f(a.prev_dt[((size_t)inst * a.prev_n + given_node(j)) * H + h_lo + hr]);
+  }
   const ssm_node* lay = a.layout + (size_t)seq * n;
   const int t0 = fuse ? 32 : 0;
-  for (int h = tid; h < H; h += THREADS) {
-    hA[h] = neg_exp(a.A_log[(size_t)layer * H + h]);
-    hBias[h] = a.dt_bias[(size_t)layer * H + h];
-    hD[h] = a.D[(size_t)layer * H + h];
+  for (int hr = tid; hr < HR; hr += THREADS) {
+    const int h = h_lo + hr;
+    hA[hr] = neg_exp(a.A_log[(size_t)layer * H + h]);
+    hBias[hr] = a.dt_bias[(size_t)layer * H + h];
+    hD[hr] = a.D[(size_t)layer * H + h];
   }
   if (tid >= t0) {
     for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, status);
     for (int i = tid - t0; i < n * nh; i += THREADS - t0) {
       const int v = i / nh, h = h_lo + (i - v * nh);
-      dl[v * H + h] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
+      dl[v * HR + h - h_lo] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
     }
   }
-  if (fuse) {
+  if (fuse && tid < 32) {
     // the committed path, checked as the stand-alone commit checks it: root first, then each
     // node a child of the one before; it ends at the first bad entry (a bad root commits node 0)
-    if (tid < 32) {
-      const int lane = tid;
-      const int32_t* pth = a.prev_path + (size_t)seq * a.LP;
-      int len = a.prev_path_len[seq];
-      const bool bad_len = len < 1 || len > a.LP;
-      len = len < 1 ? 1 : (len > a.LP ? a.LP : len);
-      const int v = lane < len ? pth[lane] : 0;
-      const int before = __shfl_up_sync(0xffffffffu, v, 1);
-      bool ok = true;
-      if (lane < len)
-        ok = lane == 0 ? v == 0
-                       : (v > before && v >= 1 && v < a.prev_n &&
-                          a.prev_layout[(size_t)seq * a.prev_n + v].parent == before);
-      const unsigned badm = __ballot_sync(0xffffffffu, lane < len && !ok);
-      const int good = badm ? __ffs(badm) - 1 : len;
-      if (lane < good) pp[lane] = v;
-      if (lane == 0) {
-        if (good == 0) pp[0] = 0;
-        pp[16] = good < 1 ? 1 : good;
-        pp[17] = a.ring_head[inst];
-        if (bad_len || badm) flag(status, SSM_STATUS_PATH_RANGE);
-      }
+    const int lane = tid;
+    const int len = a.prev_path_len[seq];
+    const bool bad_len = len < 1 || len > a.LP;
+    const int v = lane < len_given ? pth[lane] : 0;
+    const int before = __shfl_up_sync(0xffffffffu, v, 1);
+    bool ok = true;
+    if (lane < len_given)
+      ok = lane == 0 ? v == 0
+                     : (v > before && v >= 1 && v < a.prev_n &&
+                        a.prev_layout[(size_t)seq * a.prev_n + v].parent == before);
+    const unsigned badm = __ballot_sync(0xffffffffu, lane < len_given && !ok);
+    const int good = badm ? __ffs(badm) - 1 : len_given;
+    if (lane < good) pp[lane] = v;
+    if (lane == 0) {
+      if (good == 0) pp[0] = 0;
+      pp[16] = good < 1 ? 1 : good;
+      pp[18] = good == 0 && given_node(0) != 0;  // node 0's row and dt still to fetch
+      if (bad_len || badm) flag(status, SSM_STATUS_PATH_RANGE);
     }
   }
-  __syncthreads();
-  const int lenP = fuse ? pp[16] : 0;
-  const int head_old = fuse ? pp[17] : a.ring_head[inst];  // ring head before the committed path
-
-  // the three rows before the root: those of the conv ring after the commit, i.e. the path's
-  // last rows, then the ring rows that preceded the path
-  for (int i = tid; i < 3 * 32; i += THREADS) {
-    const int r = i >> 5, pc = i & 31;
-    const int k = 3 - r;  // k-th row before the root
-    const uint16_t* src = k <= lenP ? prev_xbc + (size_t)pp[lenP - k] * conv_dim
-                                    : ring + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim;
-    cp_async16(xin + r * XW + pc * 8, src + d_inner + pc * 8);
-  }
-  cp_async_commit();
+  // conv weights and bias of this thread's B|C channel
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float4 w = cw[d_inner + tid];
   const float bb = a.conv_b[(size_t)layer * conv_dim + d_inner + tid];
+  cp_async_wait<0>();
+  __syncthreads();
+  const int lenP = fuse ? pp[16] : 0;
+  if (fuse && pp[18]) {  // a bad root: node 0 of the previous tree is committed instead
+    for (int i = tid; i < 32; i += THREADS) cp_async16(xin + 3 * XW + i * 8, prev_xbc + d_inner + i * 8);
+    cp_async_commit();
+    for (int hr = tid; hr < nh; hr += THREADS)
+      wP[hr] = bf16f(a.prev_dt[(size_t)inst * a.prev_n * H + h_lo + hr]);
+    cp_async_wait<0>();
+    __syncthreads();
+  }
+
+  // ---- paths and pairs, the B|C conv, the committed path's Δ_j and a_j ----
   for (int v = tid; v < n; v += THREADS) {
     int m = v;
     const int dv = nodes[v].depth;
@@ -281,9 +305,13 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     for (int j = 0; j <= dv; ++j) pairs[1 + off + j] = v * DMAX + j;
     if (v == n - 1) pairs[0] = off + dv + 1;
   }
-  cp_async_wait<0>();
-  __syncthreads();
-  {  // B and C conv + SiLU (thread = channel of B|C), four nodes at a time for ILP
+  {  // B and C conv + SiLU (thread = channel of B|C), four nodes at a time for ILP; a tap before
+     // the root (-k) is the k-th row before it: window row 3 + lenP - k
+    auto taps = [&](int v) {
+      const ssm_node r = nodes[v];
+      auto row = [&](int tap) { return tap < 0 ? 3 + lenP + tap : TB + tap; };
+      return make_int4(row(r.tap[2]), row(r.tap[1]), row(r.tap[0]), TB + v);
+    };
     float* __restrict__ dst = tid < kN ? Bs + tid : Cs + (tid - kN);
     const int dstr = tid < kN ? kN : CSTR;
     const uint16_t* __restrict__ xi = xin + tid;
@@ -292,7 +320,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
       float r[4][4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int4 t = tap_rows(nodes[v + u], v + u);
+        const int4 t = taps(v + u);
         r[u][0] = bf16f(xi[t.x * XW]);
         r[u][1] = bf16f(xi[t.y * XW]);
         r[u][2] = bf16f(xi[t.z * XW]);
@@ -302,24 +330,33 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
       for (int u = 0; u < 4; ++u) dst[(v + u) * dstr] = silu_fast(conv4_acc(w, bb, r[u][0], r[u][1], r[u][2], r[u][3]));
     }
     for (; v < n; ++v) {
-      const int4 t = tap_rows(nodes[v], v);
+      const int4 t = taps(v);
       dst[v * dstr] = silu_fast(conv4_acc(w, bb, bf16f(xi[t.x * XW]), bf16f(xi[t.y * XW]), bf16f(xi[t.z * XW]),
                                           bf16f(xi[t.w * XW])));
     }
   }
+  for (int i = tid; i < lenP * nh; i += THREADS) {
+    const int j = i / nh, hr = i - j * nh;
+    const float d = softplus_f(wP[j * HR + hr] + hBias[hr]);
+    wP[j * HR + hr] = d;
+    aP[j * HR + hr] = decay_of(d, hA[hr]);
+  }
+  __syncthreads();
+
+  // ---- S_v, C·B products, the shared tables, E and w_j, the path's B conv, the ring rows ----
   // S_v per head: Σ over the path of Δ·A, root first; e^{S_v} to the workspace (v fastest:
   // contiguous stores), Δ_v·e^{-S_v} kept for the coefficients
   for (int i = tid; i < n * nh; i += THREADS) {
     const int h = h_lo + i / n, v = i % n;
-    const float A = hA[h];
+    const int hr = h - h_lo;
+    const float A = hA[hr];
     float s = 0.f;
     const int dv = nodes[v].depth;
-    for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * H + h], A, s);
+    for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * HR + hr], A, s);
     const float em = expf(-s);
-    emS[v * H + h] = em;
+    emS[v * HR + hr] = em;
     reinterpret_cast<float*>(ws + W.eS)[h * W.NP + v] = expf(s);
   }
-  __syncthreads();
   const int n_pairs = pairs[0];
   {  // Gm[v][j] = C_v · B_{path_j(v)}: one warp per pair
     const int warp = tid >> 5, lane = tid & 31;
@@ -352,6 +389,46 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     int* dq = reinterpret_cast<int*>(ws + W.pairs);
     for (int i = tid; i < W.PP + 4; i += THREADS) dq[i] = i <= n_pairs ? pairs[i] : 0;
   }
+  if (fuse) {
+    // w_j = Δ_j·Π_{i>j} a_i and E = Π_j a_j per head
+    for (int h = h_lo + tid; h < h_hi; h += THREADS) {
+      float* eh = reinterpret_cast<float*>(ws + W.eS) + h * W.NP;
+      float run = 1.f;
+      for (int j = lenP - 1; j >= 0; --j) {
+        eh[n + 1 + j] = wP[j * HR + h - h_lo] * run;  // w_{j,h}
+        run *= aP[j * HR + h - h_lo];
+      }
+      eh[n] = run;  // E_h
+    }
+  }
+  if (fuse && lead) {
+    // conv + SiLU of the path's B channels over the window (thread = B channel; the x channels
+    // are done per head group by the main kernel): path row j from window rows j .. j+3
+    if (tid < kN) {
+      float* BP = reinterpret_cast<float*>(ws + W.BP);
+      const uint16_t* __restrict__ xi = xin + tid;
+      for (int j = 0; j < lenP; ++j)
+        BP[j * kN + tid] = silu_f(conv4_acc(w, bb, bf16f(xi[j * XW]), bf16f(xi[(j + 1) * XW]), bf16f(xi[(j + 2) * XW]),
+                                            bf16f(xi[(j + 3) * XW])));
+    }
+    // conv ring, B | C channels: the three rows before the new root that are path rows (window
+    // rows 3 + lenP - k) go to their ring positions head+lenP-k (the main kernel writes the x
+    // channels of the same rows from its staged window); rows of the old ring stay where they are
+    uint16_t* rw = a.ring_w + (size_t)inst * R * conv_dim;
+    for (int i = tid; i < 3 * 32; i += THREADS) {
+      const int k = 3 - (i >> 5), pc = i & 31;
+      if (k > lenP) continue;
+      const uint4 v = *reinterpret_cast<const uint4*>(xin + (3 + lenP - k) * XW + pc * 8);
+      *reinterpret_cast<uint4*>(rw + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim + d_inner + pc * 8) = v;
+    }
+    int* meta = reinterpret_cast<int*>(ws + W.meta);
+    if (tid < 16) meta[4 + tid] = tid < lenP ? pp[tid] : 0;
+    if (tid == 0) {
+      meta[0] = lenP;
+      meta[1] = head_old;
+      a.head_w[inst] = head_old + lenP;
+    }
+  }
   __syncthreads();
   // coef[h][k] = e^{-S_m}·Δ_m·(C_v·B_m) for pair k = (v, depth-j ancestor m), plus D·e^{-S_v}
   // on the node's own pair: the path terms and D·x of y_v, divided by e^{S_v} (k fastest:
@@ -361,95 +438,25 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
     const int h = h_lo + i / n_pairs, k = i % n_pairs;
     const int pr = pairs[1 + k];
     const int v = pr / DMAX, m = pathn[pr];
-    float c = emS[m * H + h] * dl[m * H + h] * Gm[pr];
-    if (m == v) c = fmaf(hD[h], emS[v * H + h], c);
+    const int hr = h - h_lo;
+    float c = emS[m * HR + hr] * dl[m * HR + hr] * Gm[pr];
+    if (m == v) c = fmaf(hD[hr], emS[v * HR + hr], c);
     wc[h * W.PP + k] = c;
   }
-  if (!fuse) return;
+}
 
-  // ---- the committed path: Δ_j and a_j per head, then w_j = Δ_j·Π_{i>j} a_i, E = Π_j a_j, B_j ----
-  float* wP = reinterpret_cast<float*>(smem + L.wP);
-  float* aP = reinterpret_cast<float*>(smem + L.aP);
-  for (int i = tid; i < lenP * nh; i += THREADS) {
-    const int j = i / nh, h = h_lo + i % nh;
-    const float d = softplus_f(bf16f(a.prev_dt[((size_t)inst * a.prev_n + pp[j]) * H + h]) + hBias[h]);
-    wP[j * H + h] = d;
-    aP[j * H + h] = decay_of(d, hA[h]);
-  }
-  __syncthreads();
-  for (int h = h_lo + tid; h < h_hi; h += THREADS) {
-    float* eh = reinterpret_cast<float*>(ws + W.eS) + h * W.NP;
-    float run = 1.f;
-    for (int j = lenP - 1; j >= 0; --j) {
-      eh[n + 1 + j] = wP[j * H + h] * run;  // w_{j,h}
-      run *= aP[j * H + h];
-    }
-    eh[n] = run;  // E_h
-  }
-  if (!lead) return;
-  {  // conv + SiLU of the path's B channels over [ring rows before the path ‖ path rows]:
-     // 4 channels per thread, 8-byte loads, up to 5 path rows per pass with all 8 window rows
-     // in flight before the first is used (the x channels are done per head group by the
-     // main kernel)
-    float* BP = reinterpret_cast<float*>(ws + W.BP);
-    const float* cbias = a.conv_b + (size_t)layer * conv_dim;
-    auto window_row = [&](int t) -> const uint16_t* {  // t < 3: ring rows before the path
-      return t < 3 ? ring + (size_t)ring_pos(head_old, t - 3, R) * conv_dim : prev_xbc + (size_t)pp[t - 3] * conv_dim;
-    };
-    for (int i = tid; i < kN / 4; i += THREADS) {
-      const int c0 = d_inner + i * 4;
-      float4 wk[4];
-      float bk[4];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        wk[cc] = cw[c0 + cc];
-        bk[cc] = cbias[c0 + cc];
-      }
-      for (int j0 = 0; j0 < lenP; j0 += 5) {
-        const int cnt = min(5, lenP - j0);
-        uint2 raw[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t)
-          if (t < cnt + 3) raw[t] = *reinterpret_cast<const uint2*>(window_row(j0 + t) + c0);
-#pragma unroll
-        for (int jj = 0; jj < 5; ++jj) {
-          if (jj >= cnt) break;
-          const int j = j0 + jj;
-          float out[4];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            float r[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t word = (cc >> 1) == 0 ? raw[jj + k].x : raw[jj + k].y;
-              r[k] = bf16f((uint16_t)((cc & 1) ? (word >> 16) : (word & 0xffffu)));
-            }
-            out[cc] = silu_f(conv4_acc(wk[cc], bk[cc], r[0], r[1], r[2], r[3]));
-          }
-          *reinterpret_cast<float4*>(BP + j * kN + (c0 - d_inner)) = make_float4(out[0], out[1], out[2], out[3]);
-        }
-      }
-    }
-  }
-  {  // conv ring, B | C channels: the three rows before the new root (staged in xin rows 0..2)
-     // that are path rows go to their ring positions head+j (the main kernel writes the x
-     // channels of the same rows from its staged window); rows of the old ring stay where they are
-    uint16_t* rw = a.ring_w + (size_t)inst * R * conv_dim;
-    for (int i = tid; i < 3 * 32; i += THREADS) {
-      const int r = i >> 5, pc = i & 31;
-      const int k = 3 - r;  // k-th row before the new root = path row lenP - k
-      if (k > lenP) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(xin + r * XW + pc * 8);
-      *reinterpret_cast<uint4*>(rw + (size_t)ring_pos(head_old, lenP - k, R) * conv_dim + d_inner + pc * 8) = v;
-    }
-  }
-  int* meta = reinterpret_cast<int*>(ws + W.meta);
-  if (tid < 16) meta[4 + tid] = tid < lenP ? pp[tid] : 0;
-  if (tid == 0) {
-    meta[0] = lenP;
-    meta[1] = head_old;
-    a.head_w[inst] = head_old + lenP;
-  }
+__global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, unsigned char* __restrict__ ws_base) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  // the main kernel may be scheduled once every prep CTA is running; it waits for this grid's
+  // completion before it reads anything written here
+  launch_dependents();
+  // the instance's heads may be split over several CTAs (few instances): each redoes the shared
+  // part (cheap) and computes its own heads; block 0 alone writes the shared tables, the ring
+  // rows and the head, and reports bad inputs
+  const int nhb = a.prep_hb > 1 ? a.prep_hb : 1;
+  const int inst = blockIdx.x / nhb, hblk = blockIdx.x % nhb;
+  const int hper = (a.H + nhb - 1) / nhb, h_lo = hblk * hper, h_hi = min(a.H, h_lo + hper);
+  prep_body(a, ws_base, inst, h_lo, h_hi, hblk == 0, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -465,10 +472,10 @@ struct Smem {
 template <int G>
 __host__ __device__ constexpr int xs_stride() { return G * kP + 4; }
 
-template <int G, bool FUSE>
+template <int G, bool FUSE, bool DEEP = false>
 __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   constexpr int ROWS = G * kP;
-  constexpr int ST = FUSE ? STAGES_FUSED : STAGES_PLAIN;
+  constexpr int ST = DEEP ? STAGES_DEEP : FUSE ? STAGES_FUSED : STAGES_PLAIN;
   Smem s;
   int o = 0;
   auto take = [&](int bytes) {
@@ -500,16 +507,20 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
 // tiles streams each state chunk once per tile; with NTL > 1 (up to NTL tiles) every chunk is
 // read, committed and split once and contracted against all tiles, their accumulators held
 // side by side.
-template <int G, bool FUSE, int NTL>
-__global__ void __launch_bounds__(THREADS, 2)
+// DEEP: one CTA per SM with STAGES_DEEP chunks in flight instead of two with 3-4 each, for
+// batches with no more head groups than SMs: each CTA has its SM to itself either way, and its
+// stream is bound by the bytes it keeps in flight.  (With more groups two CTAs per SM stream
+// faster: a CTA's warps alone do not hide their own latencies.)
+template <int G, bool FUSE, int NTL, bool DEEP>
+__global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
     tree_verify_kernel(VerifyArgs a, const unsigned char* __restrict__ ws_base, const __grid_constant__ CUtensorMap tmap) {
   constexpr int ROWS = G * kP;
-  constexpr int STAGES = FUSE ? STAGES_FUSED : STAGES_PLAIN;
+  constexpr int STAGES = DEEP ? STAGES_DEEP : FUSE ? STAGES_FUSED : STAGES_PLAIN;
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n;
   const int LP = FUSE ? a.LP : 0;
   const Ws W = ws_layout(n, a.max_depth, a.H, LP);
-  const Smem L = smem_layout<G, FUSE>(n, W.PP, W.NP, LP);
+  const Smem L = smem_layout<G, FUSE, DEEP>(n, W.PP, W.NP, LP);
   float* stage = reinterpret_cast<float*>(smem + L.stage);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int4* rowidx = reinterpret_cast<int4*>(smem + L.rowidx);
@@ -637,6 +648,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     __syncwarp();
     produce(STAGES);
+  }
+  if (warp == 0) {
     grid_dependency_wait();
     if (lane == 0) {
       mbar_arrive_expect_tx(pro_bar, n * (uint32_t)sizeof(ssm_node) + n * CSTR * 4 + n * DMAX * 4 + (W.PP + 4) * 4 +
@@ -683,7 +696,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     bx1 = cb[c + 1];
   }
   grid_dependency_wait();  // nothing below reads the prep kernel's output before it is complete
-  __syncthreads();         // barriers initialised
+  __syncthreads();                  // barriers initialised
   wait_or_abort(pro_bar, 0);
   const int lenP = FUSE ? min(max(s_meta[0], 1), LP) : 0;
   for (int v = tid; v < n; v += THREADS) {
@@ -987,7 +1000,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 int g_sms[64] = {0};
-int g_configured[10][64] = {{0}};
+int g_configured[20][64] = {{0}};
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1013,13 +1026,15 @@ cudaError_t ensure_smem(K kernel, int idx, int dev, int bytes) {
   return cudaSuccess;
 }
 
-template <int G, bool FUSE, int NTL>
+template <int G, bool FUSE, int NTL, bool DEEP = false>
 cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStream_t s, int dev) {
   VerifyArgs a = a0;
   const int LP = FUSE ? a.LP : 0;
   const Ws W = ws_layout(a.n, a.max_depth, a.H, LP);
-  const Smem L = smem_layout<G, FUSE>(a.n, W.PP, W.NP, LP);
-  cudaError_t e = ensure_smem(tree_verify_kernel<G, FUSE, NTL>, (G == 4 ? 0 : 1) + (FUSE ? 2 : 0) + (NTL > 1 ? 5 : 0), dev, L.total);
+  const Smem L = smem_layout<G, FUSE, DEEP>(a.n, W.PP, W.NP, LP);
+  if (L.total > SMEM_LIMIT) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem(tree_verify_kernel<G, FUSE, NTL, DEEP>,
+                              (G == 4 ? 0 : 1) + (FUSE ? 2 : 0) + (NTL > 1 ? 5 : 0) + (DEEP ? 10 : 0), dev, L.total);
   if (e != cudaSuccess) return e;
   int sms = dev < 64 ? g_sms[dev] : 0;
   if (sms == 0) {
@@ -1033,7 +1048,7 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
   // part (prologue, the wait for the prep grid, the first inputs) measured at about 1.5 groups;
   // so few instances get fewer, longer CTAs (batch 1 of the 2.7B shape: 256 CTAs of 5 groups
   // in one wave instead of 1280 of one in five)
-  const long long slots = 2LL * sms;
+  const long long slots = (DEEP ? 1LL : 2LL) * sms;
   int gpc = 1;
   double best = 1e300;
   for (int g = 1; g <= MAX_GPC && g <= NG; ++g) {
@@ -1070,7 +1085,7 @@ cudaError_t launch_main(const VerifyArgs& a0, const unsigned char* ws, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tree_verify_kernel<G, FUSE, NTL>, a, ws, tmap);
+  return cudaLaunchKernelEx(&cfg, tree_verify_kernel<G, FUSE, NTL, DEEP>, a, ws, tmap);
 }
 
 }  // namespace
@@ -1136,15 +1151,16 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
   e = ensure_smem(tree_prep_kernel, 4, dev, prep_bytes);
   if (e != cudaSuccess) return e;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
+  int sms = dev < 64 ? g_sms[dev] : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) g_sms[dev] = sms;
+  }
+  const int n_tiles = (a.n + NT - 1) / NT;
   if (which != 2) {
     // few instances: split each instance's heads over enough CTAs to cover the SMs (at most 16
     // heads per CTA); one CTA per instance once the instances fill them
-    int sms = dev < 64 ? g_sms[dev] : 0;
-    if (sms == 0) {
-      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
-      if (dev < 64) g_sms[dev] = sms;
-    }
     VerifyArgs ap = a;
     const long long want = (2LL * sms + inst - 1) / inst;
     const int max_hb = (a.H + 15) / 16;
@@ -1154,12 +1170,26 @@ cudaError_t launch_verify(const VerifyArgs& a, void* workspace, cudaStream_t s, 
     if (e != cudaSuccess || which == 1) return e;
   }
   // trees of 2..4 node tiles: 2-head groups contract every tile per pass over the state
-  const int n_tiles = (a.n + NT - 1) / NT;
   if (n_tiles > 1 && n_tiles <= 4) {
     const Ws W2 = ws_layout(a.n, a.max_depth, a.H, a.LP);
     const bool fits = a.LP > 0 ? smem_layout<2, true>(a.n, W2.PP, W2.NP, a.LP).total <= SMEM_LIMIT
                                : smem_layout<2, false>(a.n, W2.PP, W2.NP, 0).total <= SMEM_LIMIT;
     if (fits) return a.LP > 0 ? launch_main<2, true, 4>(a, ws, s, dev) : launch_main<2, false, 4>(a, ws, s, dev);
+  }
+  // no more head groups than SMs (every CTA alone on its SM anyway): one CTA per group with the
+  // deep pipeline, where its memory fits
+  const Ws Wd = ws_layout(a.n, a.max_depth, a.H, a.LP);
+  const bool deep_fits = a.LP > 0 ? (G == 4 ? smem_layout<4, true, true>(a.n, Wd.PP, Wd.NP, a.LP).total
+                                            : smem_layout<2, true, true>(a.n, Wd.PP, Wd.NP, a.LP).total) <= SMEM_LIMIT
+                                  : (G == 4 ? smem_layout<4, false, true>(a.n, Wd.PP, Wd.NP, 0).total
+                                            : smem_layout<2, false, true>(a.n, Wd.PP, Wd.NP, 0).total) <= SMEM_LIMIT;
+  const long long groups = inst * ((a.H + G - 1) / G);
+  const int o_deep = tuning(TUNE_VERIFY_DEEP);  // tuning / test override: 1 = never, 2 = where it fits
+  const bool deep = deep_fits && (o_deep == 2 || (o_deep != 1 && groups <= sms));
+  if (deep) {
+    if (a.LP > 0)
+      return G == 4 ? launch_main<4, true, 1, true>(a, ws, s, dev) : launch_main<2, true, 1, true>(a, ws, s, dev);
+    return G == 4 ? launch_main<4, false, 1, true>(a, ws, s, dev) : launch_main<2, false, 1, true>(a, ws, s, dev);
   }
   if (a.LP > 0) return G == 4 ? launch_main<4, true, 1>(a, ws, s, dev) : launch_main<2, true, 1>(a, ws, s, dev);
   return G == 4 ? launch_main<4, false, 1>(a, ws, s, dev) : launch_main<2, false, 1>(a, ws, s, dev);

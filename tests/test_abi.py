@@ -254,7 +254,8 @@ def test_set_tuning_validation(L):
     # no CUDA call: the knobs are host-side plan overrides
     from speculative_decoding_mamba2_gb300 import SSM_ERR_INVALID_ARG, SSM_OK
     for name in (b"SSM_VERIFY_GROUPS_PER_CTA", b"SSM_VERIFY_HEADS_PER_GROUP", b"SSM_LINEAR_TCHUNK",
-                 b"SSM_LINEAR_SPLITS", b"SSM_LINEAR_STAGES"):
+                 b"SSM_LINEAR_SPLITS", b"SSM_LINEAR_STAGES", b"SSM_VERIFY_KERNEL", b"SSM_VERIFY_CTAS",
+                 b"SSM_VERIFY_DEEP"):
         assert L.ssm_set_tuning(name, 2) == SSM_OK
         assert L.ssm_set_tuning(name, 0) == SSM_OK
     assert L.ssm_set_tuning(b"SSM_NO_SUCH_KNOB", 1) == SSM_ERR_INVALID_ARG

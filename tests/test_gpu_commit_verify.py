@@ -162,7 +162,9 @@ def test_several_head_groups_per_cta(gpc, tuning):
     check_separate(out)
 
 
-def test_root_only_and_longest_paths():
+@pytest.mark.parametrize("deep", [1, 2])
+def test_root_only_and_longest_paths(deep, tuning):
+    tuning("SSM_VERIFY_DEEP", deep)  # 1: two CTAs per SM, 3 chunks in flight; 2: one, 8
     # a 16-node chain accepted to its end (path of 16 = the longest the fused call takes),
     # and a root-only path, in one batch
     w0 = Workload(65, "chain16", Shape(H=8), n_layers=2, batch=2, trees=(("chain", 16),), p_accept=1.0)
@@ -179,22 +181,29 @@ def test_root_only_and_longest_paths():
     check_separate(out)
 
 
-def test_bad_path_is_cut_and_flagged_like_commit():
+@pytest.mark.parametrize("deep", [1, 2])
+def test_bad_path_is_cut_and_flagged_like_commit(deep, tuning):
+    tuning("SSM_VERIFY_DEEP", deep)  # 1: two CTAs per SM, 3 chunks in flight; 2: one, 8
     from speculative_decoding_mamba2_gb300 import SSM_STATUS_PATH_RANGE
-    w0 = Workload(67, "badpath", Shape(H=8), n_layers=2, batch=3, trees=(("full", 2, 3),), p_accept=1.0)
+    # the prep fetches the path's rows as given, clamped into the tree, before the path is
+    # checked: a cut path uses only the rows before the cut, a bad root fetches node 0 again
+    w0 = Workload(67, "badpath", Shape(H=8), n_layers=2, batch=5, trees=(("full", 2, 3),), p_accept=1.0)
     w1 = next_workload(w0, 68, ("random", 16, 3, 4))
     b0, b1 = batch(w0), batch(w1)
     lay = oracle.tree_layout(b0["parent"][0])
     good = lay["path"][b0["n_nodes"] - 1]  # root .. deepest node
-    path = torch.full((3, 4), -1, dtype=torch.int32)
+    path = torch.full((5, 4), -1, dtype=torch.int32)
     path[0] = torch.tensor(good, dtype=torch.int32)
     path[1] = torch.tensor([good[0], good[1], 999, good[3]], dtype=torch.int32)  # out of range at 2
     path[2] = torch.tensor([5, good[1], good[2], good[3]], dtype=torch.int32)    # bad root
-    plen = torch.tensor([4, 4, 4], dtype=torch.int32)
+    path[3] = torch.tensor([-2, good[1], good[2], good[3]], dtype=torch.int32)   # bad root below the tree
+    path[4] = torch.tensor(good, dtype=torch.int32)                               # length 0: root only
+    plen = torch.tensor([4, 4, 4, 4, 0], dtype=torch.int32)
     out = run_both(b0, w0, b1, path=path.cuda(), plen=plen.cuda())
     assert out["status"] & SSM_STATUS_PATH_RANGE
     assert out["sep_status"] & SSM_STATUS_PATH_RANGE
-    check_oracle(b0, b1, out, [(i, j) for i in range(3) for j in range(2)], paths=[good, good[:2], [0]])
+    check_oracle(b0, b1, out, [(i, j) for i in range(5) for j in range(2)],
+                 paths=[good, good[:2], [0], [0], [0]])
     check_separate(out)
 
 
@@ -331,6 +340,22 @@ def test_both_tree_kernel_sets(kernel, tuning):
     tuning("SSM_VERIFY_KERNEL", kernel)
     w0 = Workload(84, "kernel sets", Shape(H=6), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
     w1 = next_workload(w0, 85, ("full", 3, 3))
+    b0, b1 = batch(w0), batch(w1)
+    out = run_both(b0, w0, b1)
+    assert out["status"] == 0 and out["sep_status"] == 0
+    check_oracle(b0, b1, out, [(i, j) for i in range(2) for j in range(2)])
+    check_separate(out)
+
+
+@pytest.mark.parametrize("deep", [1, 2])
+def test_deep_and_shallow_pipelines(deep, tuning):
+    # 1: two CTAs per SM, 3 state chunks in flight each; 2: one CTA per SM with the deep
+    # pipeline (8 chunks in flight: more stages than a group's 8 chunks, so the next group's
+    # chunks land during a group's epilogue); 2 groups per CTA, the last ragged
+    tuning("SSM_VERIFY_DEEP", deep)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", 2)
+    w0 = Workload(86, "pipelines", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
+    w1 = next_workload(w0, 87, ("random", 14, 3, 4))
     b0, b1 = batch(w0), batch(w1)
     out = run_both(b0, w0, b1)
     assert out["status"] == 0 and out["sep_status"] == 0

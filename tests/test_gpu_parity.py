@@ -71,8 +71,12 @@ def test_ragged_heads_and_node_tiles():
     check_instances(b, out, [(i, j) for i in range(3) for j in range(2)])
 
 
+@pytest.mark.parametrize("deep", ["1", "2"])
 @pytest.mark.parametrize("spec", [("random", 16, 3, 4), ("random", 64, 4, 15), ("chain", 16), ("full", 2, 5)])
-def test_tree_shapes(spec):
+def test_tree_shapes(spec, deep, tuning):
+    # deep "1": two CTAs per SM with 3-4 chunks in flight; "2": one with 8 (where it fits: one
+    # node tile)
+    tuning("SSM_VERIFY_DEEP", deep)
     w = Workload(51, "shapes", Shape(H=8), n_layers=2, batch=2, trees=(spec,), p_accept=0.85)
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
@@ -107,6 +111,20 @@ def test_two_and_four_head_groups(g, tuning):
     # either way), against the oracle
     tuning("SSM_VERIFY_HEADS_PER_GROUP", g)
     w = Workload(57, "head groups", Shape(H=10), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
+    b = batch(w)
+    out = run_tree_step(upload_tree_batch(b, w))
+    check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
+
+
+@pytest.mark.parametrize("deep", ["1", "2"])
+@pytest.mark.parametrize("g", ["2", "4"])
+def test_deep_and_shallow_pipelines(deep, g, tuning):
+    # the tree kernel with 3-4 state chunks in flight per CTA (1) or 8 at one CTA per SM (2),
+    # 2- and 4-head groups, 3 groups per CTA (the last CTA's ragged)
+    tuning("SSM_VERIFY_DEEP", deep)
+    tuning("SSM_VERIFY_HEADS_PER_GROUP", g)
+    tuning("SSM_VERIFY_GROUPS_PER_CTA", "3")
+    w = Workload(58, "pipelines", Shape(H=14), n_layers=2, batch=2, trees=(("random", 16, 3, 4),))
     b = batch(w)
     out = run_tree_step(upload_tree_batch(b, w))
     check_instances(b, out, [(i, j) for i in range(2) for j in range(2)])
