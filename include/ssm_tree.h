@@ -234,10 +234,12 @@ int ssm_commit_verify(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq
  * being produced.
  *   _prep reads, of this step's tree, only the B | C channels of xBC and dt (plus
  *         the previous path's rows, the ring, the layouts and the parameters); it
- *         writes the workspace, the committed ring rows' B | C channels and ring_head.
+ *         writes the workspace and the committed ring rows' B | C channels; it reads
+ *         ring_head and leaves it as it was.
  *   _main reads the x channels of xBC, h and what _prep wrote; it must run after
  *         _prep on the same workspace (same stream, or ordered by the caller) and
- *         after the x channels are in place.  It writes h, the ring's x channels and y.
+ *         after the x channels are in place.  It writes h, the ring's x channels,
+ *         ring_head (advanced by the committed path's length) and y.
  * Both validate every argument as ssm_commit_verify does.
  */
 int ssm_commit_verify_prep(const ssm_dims *dims, const ssm_params *prm, int32_t n_seq, int32_t prev_n_nodes,

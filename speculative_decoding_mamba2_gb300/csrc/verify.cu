@@ -169,8 +169,8 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int HR, int PP, int LP = 
 
 // The prep of instance `inst` for heads [h_lo, h_hi) (everything that does not depend on the head
 // group), by the whole CTA into `smem`: the shared tables (lead), its heads' e^S and coefficients
-// and, with a folded commit, E and w_j into the workspace record; the ring's B | C rows (lead);
-// the ring head (lead).
+// and, with a folded commit, E and w_j into the workspace record; the ring's B | C rows (lead).
+// The ring head is left to the main kernel (other CTAs of the instance may still read it).
 __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_base, int inst, int h_lo, int h_hi,
                           bool lead, unsigned char* smem) {
   const int n = a.n, H = a.H;
@@ -426,7 +426,6 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     if (tid == 0) {
       meta[0] = lenP;
       meta[1] = head_old;
-      a.head_w[inst] = head_old + lenP;
     }
   }
   __syncthreads();
@@ -671,6 +670,9 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
       } else {
         win = 3 + min(max(s_meta[0], 1), LP);
         head_old = s_meta[1];
+        // the ring head advances here, not in the prep grid: every prep CTA of an instance reads
+        // the old head, and a grid larger than the SMs hold starts some of them late
+        if (lane == 0 && g_first == 0) a.head_w[inst] = head_old + s_meta[0];
       }
     } else {
       head_old = a.ring_head[inst];

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(PREP_THREADS) tc_prep_kernel(VerifyArgs a, uns
   }
   int* meta = reinterpret_cast<int*>(ws + W.meta);
   if (tid < kMeta) meta[tid] = pp[tid];
-  if (tid == 0) a.head_w[inst] = head_old + lenP;
+  // the ring head is advanced by the main kernel: other prep CTAs of the instance still read it
 }
 
 // ---------------------------------------------------------------------------
@@ -603,6 +603,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         if (k >= 2 && !wait_bar(bar(B_XFREE + b), ((k >> 1) - 1) & 1)) break;
         const int lenP = FUSE ? min(max(meta[0], 1), LP) : 0;
         const int head_old = FUSE ? meta[1] : a.ring_head[inst];
+        if (FUSE && hp == 0) a.head_w[inst] = head_old + lenP;  // after the whole prep grid
         const int win = 3 + lenP;
         const int heads = min(2, H - 2 * hp);
         const uint32_t rb = (uint32_t)heads * kP * 2;

@@ -305,6 +305,8 @@ def test_split_prep_then_main_is_the_folded_call():
             ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status)
         else:
             ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status, part="prep")
+            # the prep leaves the ring head to the main half (every prep CTA reads the old one)
+            assert torch.equal(head, d0["ring_head"])
             if mode == "late x":
                 x_in[..., :dims.d_inner] = xBC1[..., :dims.d_inner]
             ssm_commit_verify(*args, x_in, dt1, h, ring, head, y, ws, status, part="main")
