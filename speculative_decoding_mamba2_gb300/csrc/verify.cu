@@ -150,15 +150,16 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int HR, int PP, int LP = 
     o += (b + 15) & ~15;
     return r;
   };
+  const int HRP = HR | 1;  // odd row strides: a warp's reads across nodes hit distinct banks
   s.nodes = take(n * (int)sizeof(ssm_node));
-  s.pathn = take(n * DMAX * 4);
+  s.pathn = take(n * (DMAX + 1) * 4);
   s.pairs = take((PP + 4) * 4);
   s.xin = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows ‖ LP path rows][tree nodes]
   s.Bs = take(n * kN * 4);
   s.Cs = take(n * CSTR * 4);
   s.Gm = take(n * DMAX * 4);
-  s.dl = take(n * HR * 4);
-  s.S = take(n * HR * 4);
+  s.dl = take(n * HRP * 4);
+  s.S = take(n * HRP * 4);
   s.pp = take(LP > 0 ? 20 * 4 : 0);  // committed path nodes [16], its length, -, a bad root's refetch
   s.wP = take(LP * HR * 4);          // Δ_j, then Δ_j·Π_{i>j} a_i  [LP][HR]
   s.aP = take(LP * HR * 4);          // a_j = exp(Δ_j·A)          [LP][HR]
@@ -177,6 +178,8 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   const bool fuse = a.LP > 0;
   const Ws W = ws_layout(n, a.max_depth, H, a.LP);
   const int HR = h_hi - h_lo, nh = HR;
+  const int HRP = HR | 1;  // row stride of dl and e^{-S} (odd: conflict-free across nodes)
+  constexpr int PNS = DMAX + 1;  // row stride of the path table in shared memory (odd)
   const PrepSmem L = prep_layout(n, HR, W.PP, a.LP);
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
@@ -186,7 +189,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   float* Cs = reinterpret_cast<float*>(smem + L.Cs);
   float* Gm = reinterpret_cast<float*>(smem + L.Gm);
   float* dl = reinterpret_cast<float*>(smem + L.dl);
-  float* emS = reinterpret_cast<float*>(smem + L.S);  // e^{-S_v} [n][H]
+  float* emS = reinterpret_cast<float*>(smem + L.S);  // e^{-S_v} [n][HRP]
 
   const int tid = threadIdx.x;
   int32_t* const status = lead ? a.status : nullptr;
@@ -249,7 +252,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, status);
     for (int i = tid - t0; i < n * nh; i += THREADS - t0) {
       const int v = i / nh, h = h_lo + (i - v * nh);
-      dl[v * HR + h - h_lo] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
+      dl[v * HRP + h - h_lo] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
     }
   }
   if (fuse && tid < 32) {
@@ -296,7 +299,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     int m = v;
     const int dv = nodes[v].depth;
     for (int j = dv; j >= 0; --j) {
-      pathn[v * DMAX + j] = m;
+      pathn[v * PNS + j] = m;
       m = m > 0 ? nodes[m].parent : 0;
       if (m < 0) m = 0;
     }
@@ -352,9 +355,9 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     const float A = hA[hr];
     float s = 0.f;
     const int dv = nodes[v].depth;
-    for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * DMAX + j] * HR + hr], A, s);
+    for (int j = 0; j <= dv; ++j) s = fmaf(dl[pathn[v * PNS + j] * HRP + hr], A, s);
     const float em = expf(-s);
-    emS[v * HR + hr] = em;
+    emS[v * HRP + hr] = em;
     reinterpret_cast<float*>(ws + W.eS)[h * W.NP + v] = expf(s);
   }
   const int n_pairs = pairs[0];
@@ -362,7 +365,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     const int warp = tid >> 5, lane = tid & 31;
     for (int k = warp; k < n_pairs; k += THREADS / 32) {
       const int pr = pairs[1 + k];
-      const int v = pr / DMAX, m = pathn[pr];
+      const int v = pr / DMAX, m = pathn[v * PNS + pr - v * DMAX];
       const float4 c4 = reinterpret_cast<const float4*>(Cs + v * CSTR)[lane];
       const float4 b4 = reinterpret_cast<const float4*>(Bs + m * kN)[lane];
       float s = c4.x * b4.x;
@@ -385,7 +388,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
       dlo[i] = lo;
     }
     int* dp = reinterpret_cast<int*>(ws + W.pathn);
-    for (int i = tid; i < n * DMAX; i += THREADS) dp[i] = pathn[i];
+    for (int i = tid; i < n * DMAX; i += THREADS) dp[i] = pathn[(i / DMAX) * PNS + i % DMAX];
     int* dq = reinterpret_cast<int*>(ws + W.pairs);
     for (int i = tid; i < W.PP + 4; i += THREADS) dq[i] = i <= n_pairs ? pairs[i] : 0;
   }
@@ -436,10 +439,10 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   for (int i = tid; i < n_pairs * nh; i += THREADS) {
     const int h = h_lo + i / n_pairs, k = i % n_pairs;
     const int pr = pairs[1 + k];
-    const int v = pr / DMAX, m = pathn[pr];
+    const int v = pr / DMAX, m = pathn[v * PNS + pr - v * DMAX];
     const int hr = h - h_lo;
-    float c = emS[m * HR + hr] * dl[m * HR + hr] * Gm[pr];
-    if (m == v) c = fmaf(hD[hr], emS[v * HR + hr], c);
+    float c = emS[m * HRP + hr] * dl[m * HRP + hr] * Gm[pr];
+    if (m == v) c = fmaf(hD[hr], emS[v * HRP + hr], c);
     wc[h * W.PP + k] = c;
   }
 }
