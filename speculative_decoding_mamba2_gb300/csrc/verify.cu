@@ -138,7 +138,7 @@ __device__ __forceinline__ int4 tap_rows(const ssm_node& r, int v) {
 // prep kernel: everything per instance that does not depend on the head group
 // ---------------------------------------------------------------------------
 struct PrepSmem {
-  int nodes, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, hp, total;
+  int nodes, rrow, pathn, pairs, xin, Bs, Cs, Gm, dl, S, pp, wP, aP, hp, total;
 };
 
 // per-head arrays sized by the heads one CTA computes (HR)
@@ -152,6 +152,7 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int HR, int PP, int LP = 
   };
   const int HRP = HR | 1;  // odd row strides: a warp's reads across nodes hit distinct banks
   s.nodes = take(n * (int)sizeof(ssm_node));
+  s.rrow = take(n * 16);  // staged rows of each node's four conv taps
   s.pathn = take(n * (DMAX + 1) * 4);
   s.pairs = take((PP + 4) * 4);
   s.xin = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows ‖ LP path rows][tree nodes]
@@ -167,6 +168,26 @@ __host__ __device__ inline PrepSmem prep_layout(int n, int HR, int PP, int LP = 
   s.total = o;
   return s;
 }
+
+// (i / d, i % d) along i = i0, i0 + step, i0 + 2·step, ... with two divisions in all rather
+// than two per element
+struct DivWalk {
+  int q, r, sq, sr, d;
+  __device__ __forceinline__ DivWalk(int i0, int step, int d_) : d(d_) {
+    q = i0 / d;
+    r = i0 - q * d;
+    sq = step / d;
+    sr = step - sq * d;
+  }
+  __device__ __forceinline__ void next() {
+    q += sq;
+    r += sr;
+    if (r >= d) {
+      r -= d;
+      ++q;
+    }
+  }
+};
 
 // The prep of instance `inst` for heads [h_lo, h_hi) (everything that does not depend on the head
 // group), by the whole CTA into `smem`: the shared tables (lead), its heads' e^S and coefficients
@@ -250,8 +271,9 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   }
   if (tid >= t0) {
     for (int v = tid - t0; v < n; v += THREADS - t0) nodes[v] = checked_node(lay, v, a.max_depth, status);
-    for (int i = tid - t0; i < n * nh; i += THREADS - t0) {
-      const int v = i / nh, h = h_lo + (i - v * nh);
+    DivWalk w(tid - t0, THREADS - t0, nh);
+    for (int i = tid - t0; i < n * nh; i += THREADS - t0, w.next()) {
+      const int v = w.q, h = h_lo + w.r;
       dl[v * HRP + h - h_lo] = softplus_f(bf16f(a.dt[((size_t)inst * n + v) * H + h]) + a.dt_bias[(size_t)layer * H + h]);
     }
   }
@@ -295,9 +317,11 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   }
 
   // ---- paths and pairs, the B|C conv, the committed path's Δ_j and a_j ----
+  int4* rrow = reinterpret_cast<int4*>(smem + L.rrow);
   for (int v = tid; v < n; v += THREADS) {
     int m = v;
-    const int dv = nodes[v].depth;
+    const ssm_node nd = nodes[v];
+    const int dv = nd.depth;
     for (int j = dv; j >= 0; --j) {
       pathn[v * PNS + j] = m;
       m = m > 0 ? nodes[m].parent : 0;
@@ -307,14 +331,12 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
     for (int u = 0; u < v; ++u) off += nodes[u].depth + 1;
     for (int j = 0; j <= dv; ++j) pairs[1 + off + j] = v * DMAX + j;
     if (v == n - 1) pairs[0] = off + dv + 1;
+    // a tap before the root (-k) is the k-th row before it: window row 3 + lenP - k
+    auto row = [&](int tap) { return tap < 0 ? 3 + lenP + tap : TB + tap; };
+    rrow[v] = make_int4(row(nd.tap[2]), row(nd.tap[1]), row(nd.tap[0]), TB + v);
   }
-  {  // B and C conv + SiLU (thread = channel of B|C), four nodes at a time for ILP; a tap before
-     // the root (-k) is the k-th row before it: window row 3 + lenP - k
-    auto taps = [&](int v) {
-      const ssm_node r = nodes[v];
-      auto row = [&](int tap) { return tap < 0 ? 3 + lenP + tap : TB + tap; };
-      return make_int4(row(r.tap[2]), row(r.tap[1]), row(r.tap[0]), TB + v);
-    };
+  __syncthreads();
+  {  // B and C conv + SiLU (thread = channel of B|C), four nodes at a time for ILP
     float* __restrict__ dst = tid < kN ? Bs + tid : Cs + (tid - kN);
     const int dstr = tid < kN ? kN : CSTR;
     const uint16_t* __restrict__ xi = xin + tid;
@@ -323,7 +345,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
       float r[4][4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int4 t = taps(v + u);
+        const int4 t = rrow[v + u];
         r[u][0] = bf16f(xi[t.x * XW]);
         r[u][1] = bf16f(xi[t.y * XW]);
         r[u][2] = bf16f(xi[t.z * XW]);
@@ -333,7 +355,7 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
       for (int u = 0; u < 4; ++u) dst[(v + u) * dstr] = silu_fast(conv4_acc(w, bb, r[u][0], r[u][1], r[u][2], r[u][3]));
     }
     for (; v < n; ++v) {
-      const int4 t = taps(v);
+      const int4 t = rrow[v];
       dst[v * dstr] = silu_fast(conv4_acc(w, bb, bf16f(xi[t.x * XW]), bf16f(xi[t.y * XW]), bf16f(xi[t.z * XW]),
                                           bf16f(xi[t.w * XW])));
     }
@@ -349,8 +371,9 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   // ---- S_v, C·B products, the shared tables, E and w_j, the path's B conv, the ring rows ----
   // S_v per head: Σ over the path of Δ·A, root first; e^{S_v} to the workspace (v fastest:
   // contiguous stores), Δ_v·e^{-S_v} kept for the coefficients
-  for (int i = tid; i < n * nh; i += THREADS) {
-    const int h = h_lo + i / n, v = i % n;
+  DivWalk ws_(tid, THREADS, n);
+  for (int i = tid; i < n * nh; i += THREADS, ws_.next()) {
+    const int h = h_lo + ws_.q, v = ws_.r;
     const int hr = h - h_lo;
     const float A = hA[hr];
     float s = 0.f;
@@ -436,8 +459,9 @@ __device__ void prep_body(const VerifyArgs& a, unsigned char* __restrict__ ws_ba
   // on the node's own pair: the path terms and D·x of y_v, divided by e^{S_v} (k fastest:
   // contiguous stores)
   float* wc = reinterpret_cast<float*>(ws + W.coef);
-  for (int i = tid; i < n_pairs * nh; i += THREADS) {
-    const int h = h_lo + i / n_pairs, k = i % n_pairs;
+  DivWalk wk(tid, THREADS, max(n_pairs, 1));
+  for (int i = tid; i < n_pairs * nh; i += THREADS, wk.next()) {
+    const int h = h_lo + wk.q, k = wk.r;
     const int pr = pairs[1 + k];
     const int v = pr / DMAX, m = pathn[v * PNS + pr - v * DMAX];
     const int hr = h - h_lo;
