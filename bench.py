@@ -625,8 +625,10 @@ def depth_cap(spec):
     return spec[1] - 1
 
 
-def tree_roofline(w, r, peak, peak_kind, n_units, world):
-    """Roofline of one folded round (ssm_commit_verify) and the round's throughput."""
+def tree_roofline(w, r, peak, peak_kind, n_units, world, traffic_call=None):
+    """Roofline of one folded round (ssm_commit_verify) and the round's throughput; the DRAM
+    traffic of the call when profiles/dram_traffic.txt holds a capture `traffic_call` on the
+    current kernel sources (per instance, scaled to the call's instances)."""
     import numpy as np
     H, P, N = w.shape.H, w.shape.P, w.shape.N
     pb = r["L"] * params_bytes_per_layer(H, P, N)
@@ -639,7 +641,8 @@ def tree_roofline(w, r, peak, peak_kind, n_units, world):
             "roofline": {"bound": "hbm", "kernel": "ssm_commit_verify (tree_prep_kernel + tree_verify_kernel)",
                          "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                         else "fallback", "algorithmic_bytes": fb}}
+                         else "fallback", "algorithmic_bytes": fb,
+                         "traffic": ncu_traffic(traffic_call, r["L"] * r["S"]) if traffic_call else None}}
 
 
 def run_config2(args, dev, stream, world, rank, peak, peak_kind):
@@ -657,7 +660,8 @@ def run_config2(args, dev, stream, world, rank, peak, peak_kind):
     r = folded_rounds(w, b, dev, stream, world, steps, args.warmup, flush=flush)
     out = {"workload": w.name, "sequences_per_gpu": r["S"], "layers": r["L"], "nodes_per_tree": r["n"],
            "steps": steps, "l2": "256 MB written before every round (outside the timed events)"}
-    out.update(tree_roofline(w, r, peak, peak_kind, r["n"] * r["L"] * r["S"], world))
+    # the traffic capture of ssm_commit_verify is taken on this workload (64 instances)
+    out.update(tree_roofline(w, r, peak, peak_kind, r["n"] * r["L"] * r["S"], world, traffic_call="ssm_commit_verify"))
     return out
 
 
