@@ -218,9 +218,10 @@ def test_2p7b_batch16_full_size_sampled():
     check_separate(out)
 
 
-@pytest.mark.parametrize("nxt", [("full", 3, 3), ("random", 64, 4, 15)])
+@pytest.mark.parametrize("nxt", [("full", 2, 4), ("full", 3, 3), ("random", 64, 4, 15)])
 def test_next_tree_of_several_node_tiles(nxt):
-    # 40- and 64-node next trees: several node tiles per head group (the next group's x conv
+    # 31-, 40- and 64-node next trees (two, three and four node tiles, each with accumulators
+    # sized to it): several node tiles per head group (the next group's x conv
     # runs in the last tile; the path-term product spans several k-steps), depth up to 15
     w0 = Workload(70, "tiles", Shape(H=8), n_layers=2, batch=2, trees=(("random", 16, 3, 4),), p_accept=0.9)
     w1 = next_workload(w0, 71, nxt)

@@ -72,7 +72,8 @@ def test_ragged_heads_and_node_tiles():
 
 
 @pytest.mark.parametrize("deep", ["1", "2"])
-@pytest.mark.parametrize("spec", [("random", 16, 3, 4), ("random", 64, 4, 15), ("chain", 16), ("full", 2, 5)])
+@pytest.mark.parametrize("spec", [("random", 16, 3, 4), ("random", 24, 3, 4), ("full", 3, 3), ("random", 64, 4, 15),
+                                  ("chain", 16), ("full", 2, 5)])
 def test_tree_shapes(spec, deep, tuning):
     # deep "1": two CTAs per SM with 3-4 chunks in flight; "2": one with 8 (where it fits: one
     # node tile)
