@@ -715,15 +715,21 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   const int cp = tid % PAIRS, cpart = tid / PAIRS;
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float* cb = a.conv_b + (size_t)layer * conv_dim;
-  float4 wx0 = make_float4(0.f, 0.f, 0.f, 0.f), wx1 = wx0;  // x conv weights of the next group
+  // the x conv weights of the group whose conv runs next (NTL = 1: carried through the previous
+  // group's chunks in registers, fetched early; NTL > 1: loaded by the conv itself, which keeps
+  // them out of the registers the several tiles' accumulators need)
+  float4 wx0 = make_float4(0.f, 0.f, 0.f, 0.f), wx1 = wx0;
   float bx0 = 0.f, bx1 = 0.f;
-  if (2 * cp < min(G, a.H - hc_begin) * kP) {
-    const int c = hc_begin * kP + 2 * cp;
-    wx0 = cw[c];
-    wx1 = cw[c + 1];
-    bx0 = cb[c];
-    bx1 = cb[c + 1];
-  }
+  auto load_xw = [&](int hb) {
+    if (2 * cp < min(G, a.H - hb) * kP) {
+      const int c = hb * kP + 2 * cp;
+      wx0 = cw[c];
+      wx1 = cw[c + 1];
+      bx0 = cb[c];
+      bx1 = cb[c + 1];
+    }
+  };
+  if (NTL == 1) load_xw(hc_begin);
   grid_dependency_wait();  // nothing below reads the prep kernel's output before it is complete
   __syncthreads();                  // barriers initialised
   wait_or_abort(pro_bar, 0);
@@ -754,9 +760,10 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   };
 
   // x conv + SiLU of group g's channels for every tree node (xs), and the committed path's
-  // u_j (uPs buffer g & 1); then the next group's conv weights are fetched.  All threads.
+  // u_j (uPs buffer g & 1).  All threads.
   auto xconv = [&](int g) {
     const int hb = hc_begin + g * G, heads = min(G, a.H - hb);
+    if (NTL > 1) load_xw(hb);  // in flight during the wait for the rows
     wait_or_abort(x_bar, g & 1);
     if (FUSE) {
       // conv ring, this group's x channels: the committed path's last min(len, 3) rows (window
@@ -813,16 +820,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
         }
       }
     }
-    if (g + 1 < g_count) {  // the next group's x conv weights
-      const int hn = hb + G;
-      if (2 * cp < min(G, a.H - hn) * kP) {
-        const int c = hn * kP + 2 * cp;
-        wx0 = cw[c];
-        wx1 = cw[c + 1];
-        bx0 = cb[c];
-        bx1 = cb[c + 1];
-      }
-    }
+    if (NTL == 1 && g + 1 < g_count) load_xw(hb + G);  // the next group's, early
   };
   xconv(0);
 
