@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
 // main kernel
 // ---------------------------------------------------------------------------
 struct Smem {
-  int bars, stage, nodes, rowidx, poff, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
+  int bars, stage, nodes, rowidx, poff, pmask, dep, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
 };
 
 // x rows of a group: node v at xs[v * xs_stride<G>()], rows padded by 4 floats so that the
@@ -515,6 +515,8 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   s.nodes = take(n * (int)sizeof(ssm_node));
   s.rowidx = take(n * 16);
   s.poff = take(n * 4);
+  s.pmask = take(((n + 15) & ~15) * 8);  // per node: which nodes lie on its path (bit m)
+  s.dep = take((n + 15) & ~15);           // per node: its depth
   s.pathn = take(n * DMAX * 4);
   s.pairs = take((PP + 4) * 4);
   s.Cs = take(n * CSTR * 4);
@@ -551,6 +553,8 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   ssm_node* nodes = reinterpret_cast<ssm_node*>(smem + L.nodes);
   int4* rowidx = reinterpret_cast<int4*>(smem + L.rowidx);
   int* poff = reinterpret_cast<int*>(smem + L.poff);
+  unsigned long long* pmask = reinterpret_cast<unsigned long long*>(smem + L.pmask);
+  uint8_t* dep = reinterpret_cast<uint8_t*>(smem + L.dep);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
   int* pairs = reinterpret_cast<int*>(smem + L.pairs);
   const uint16_t* Chi = reinterpret_cast<const uint16_t*>(smem + L.Cs);  // bf16 [n][CSTR]
@@ -750,13 +754,32 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
     for (int u = 0; u < v; ++u) off += nodes[u].depth + 1;
     poff[v] = off;
   }
+  {  // m lies on v's path when v's ancestor at m's depth is m (a ballot per node and 32 m's)
+    const int NXN = (n + 15) & ~15;
+    for (int v = warp; v < NXN; v += THREADS / 32) {
+      unsigned long long mk = 0ull;
+      if (v < n) {
+        const int dv = nodes[v].depth;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int m = lane + 32 * half;
+          bool on = false;
+          if (m <= v) {
+            const int dm = nodes[m].depth;
+            on = dm <= dv && pathn[v * DMAX + dm] == m;
+          }
+          mk |= (unsigned long long)__ballot_sync(0xffffffffu, on) << (32 * half);
+        }
+      }
+      if (lane == 0) pmask[v] = mk;
+    }
+    for (int m = tid; m < NXN; m += THREADS) dep[m] = m < n ? (uint8_t)nodes[m].depth : 0;
+  }
 
-  // coef[v,m] of the tree (this warp's head) for nodes v and m: zero unless m is on v's path
-  auto path_coef = [&](const float* chd, int v, int m) -> float {
-    if (v >= n || m > v) return 0.f;
-    const int dm = nodes[m].depth;
-    if (dm > nodes[v].depth || pathn[v * DMAX + dm] != m) return 0.f;
-    return chd[poff[v] + dm];
+  // coef[v,m] of the tree (this warp's head) for node v (path mask pm, first pair po) and node m:
+  // zero unless m is on v's path
+  auto path_coef = [&](const float* chd, unsigned long long pm, int po, int m) -> float {
+    return (pm >> m) & 1ull ? chd[po + dep[m]] : 0.f;
   };
 
   // x conv + SiLU of group g's channels for every tree node (xs), and the committed path's
@@ -869,9 +892,11 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
               uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
-                const int v = tile * NT + nt * 8 + fg;
-                split_bf16x2(path_coef(chd, v, m0), path_coef(chd, v, m0 + 1), bhi[nt][0], blo[nt][0]);
-                split_bf16x2(path_coef(chd, v, m0 + 8), path_coef(chd, v, m0 + 9), bhi[nt][1], blo[nt][1]);
+                const int v = tile * NT + nt * 8 + fg;  // < NX: the masks are zero past the tree
+                const unsigned long long pm = pmask[v];
+                const int po = v < n ? poff[v] : 0;
+                split_bf16x2(path_coef(chd, pm, po, m0), path_coef(chd, pm, po, m0 + 1), bhi[nt][0], blo[nt][0]);
+                split_bf16x2(path_coef(chd, pm, po, m0 + 8), path_coef(chd, pm, po, m0 + 9), bhi[nt][1], blo[nt][1]);
               }
               const float* xa = xs + m0 * XSTR + wrow + fg;
 #pragma unroll
