@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_prep_kernel(VerifyArgs a, uns
 // main kernel
 // ---------------------------------------------------------------------------
 struct Smem {
-  int bars, stage, nodes, rowidx, poff, pmask, dep, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
+  int bars, stage, nodes, rowidx, poff, pmask, dep, tkm, pathn, pairs, Cs, xs, xinX, eSg, coefg, BPs, uPs, meta, total;
 };
 
 // x rows of a group: node v at xs[v * xs_stride<G>()], rows padded by 4 floats so that the
@@ -517,6 +517,7 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   s.poff = take(n * 4);
   s.pmask = take(((n + 15) & ~15) * 8);  // per node: which nodes lie on its path (bit m)
   s.dep = take((n + 15) & ~15);           // per node: its depth
+  s.tkm = take(4 * 4);                    // per node tile: the k-steps its path terms touch (bit k)
   s.pathn = take(n * DMAX * 4);
   s.pairs = take((PP + 4) * 4);
   s.Cs = take(n * CSTR * 4);
@@ -555,6 +556,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   int* poff = reinterpret_cast<int*>(smem + L.poff);
   unsigned long long* pmask = reinterpret_cast<unsigned long long*>(smem + L.pmask);
   uint8_t* dep = reinterpret_cast<uint8_t*>(smem + L.dep);
+  unsigned* tkm = reinterpret_cast<unsigned*>(smem + L.tkm);
   int* pathn = reinterpret_cast<int*>(smem + L.pathn);
   int* pairs = reinterpret_cast<int*>(smem + L.pairs);
   const uint16_t* Chi = reinterpret_cast<const uint16_t*>(smem + L.Cs);  // bf16 [n][CSTR]
@@ -748,6 +750,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
     const int4 t = tap_rows(r, v);  // rows counted from the last three window rows
     rowidx[v] = make_int4(t.x + lenP, t.y + lenP, t.z + lenP, t.w + lenP);
   }
+  if (tid < 4) tkm[tid] = 0u;
   __syncthreads();
   for (int v = tid; v < n; v += THREADS) {
     int off = 0;
@@ -771,15 +774,22 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
           mk |= (unsigned long long)__ballot_sync(0xffffffffu, on) << (32 * half);
         }
       }
-      if (lane == 0) pmask[v] = mk;
+      if (lane == 0) {
+        pmask[v] = mk;
+        unsigned ks = 0u;  // the 16-node blocks of m this node's path touches
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if ((mk >> (16 * k)) & 0xffffull) ks |= 1u << k;
+        if (ks) atomicOr(&tkm[v >> 4], ks);
+      }
     }
     for (int m = tid; m < NXN; m += THREADS) dep[m] = m < n ? (uint8_t)nodes[m].depth : 0;
   }
 
   // coef[v,m] of the tree (this warp's head) for node v (path mask pm, first pair po) and node m:
   // zero unless m is on v's path
-  auto path_coef = [&](const float* chd, unsigned long long pm, int po, int m) -> float {
-    return (pm >> m) & 1ull ? chd[po + dep[m]] : 0.f;
+  auto path_coef = [&](const float* chd, unsigned long long pm, int po, int m, int dm) -> float {
+    return (pm >> m) & 1ull ? chd[po + dm] : 0.f;
   };
 
   // x conv + SiLU of group g's channels for every tree node (xs), and the committed path's
@@ -885,18 +895,25 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[i][mt][nt][e] = 0.f;
             if (tile >= n_tiles) continue;
-            const int ksteps = min(tile + 1, NX / 16);  // ancestors precede their nodes
-            for (int k16 = 0; k16 < ksteps; ++k16) {
+            // the k-steps (16 nodes m each) where some node of the tile has an ancestor or itself:
+            // ancestors precede their nodes, so never past the tile (the same for the whole CTA)
+            const unsigned kset = tkm[tile];
+            for (int k16 = 0; k16 <= tile; ++k16) {
+              if (!((kset >> k16) & 1u)) continue;
               // k = node m: lane (fg, ft) holds m = 2ft, 2ft+1 and 2ft+8, 2ft+9 of the k-step
               const int m0 = k16 * 16 + 2 * ft;
+              const unsigned d01 = *reinterpret_cast<const uint16_t*>(dep + m0);  // depths of m0, m0 + 1
+              const unsigned d89 = *reinterpret_cast<const uint16_t*>(dep + m0 + 8);
               uint32_t bhi[2][2], blo[2][2];
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt) {
                 const int v = tile * NT + nt * 8 + fg;  // < NX: the masks are zero past the tree
                 const unsigned long long pm = pmask[v];
                 const int po = v < n ? poff[v] : 0;
-                split_bf16x2(path_coef(chd, pm, po, m0), path_coef(chd, pm, po, m0 + 1), bhi[nt][0], blo[nt][0]);
-                split_bf16x2(path_coef(chd, pm, po, m0 + 8), path_coef(chd, pm, po, m0 + 9), bhi[nt][1], blo[nt][1]);
+                split_bf16x2(path_coef(chd, pm, po, m0, d01 & 0xff), path_coef(chd, pm, po, m0 + 1, d01 >> 8),
+                             bhi[nt][0], blo[nt][0]);
+                split_bf16x2(path_coef(chd, pm, po, m0 + 8, d89 & 0xff), path_coef(chd, pm, po, m0 + 9, d89 >> 8),
+                             bhi[nt][1], blo[nt][1]);
               }
               const float* xa = xs + m0 * XSTR + wrow + fg;
 #pragma unroll
