@@ -794,6 +794,10 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
 
   // x conv + SiLU of group g's channels for every tree node (xs), and the committed path's
   // u_j (uPs buffer g & 1).  All threads.
+  // the conv's SiLU: on the FMA pipe for one-tile trees (it runs beside tensor and memory work,
+  // and measured faster there); with the special-function unit for trees of several tiles, whose
+  // conv is 2.5x the work per state byte and issue-bound
+  auto silu_x = [](float v) { return NTL > 1 ? silu_fast(v) : silu_fma(v); };
   auto xconv = [&](int g) {
     const int hb = hc_begin + g * G, heads = min(G, a.H - hb);
     if (NTL > 1) load_xw(hb);  // in flight during the wait for the rows
@@ -828,9 +832,9 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           xo[(v + u) * (XSTR / 2)] =
-              make_float2(silu_fma(conv4_acc(wx0, bx0, bf16_lo(r[u][0]), bf16_lo(r[u][1]), bf16_lo(r[u][2]),
+              make_float2(silu_x(conv4_acc(wx0, bx0, bf16_lo(r[u][0]), bf16_lo(r[u][1]), bf16_lo(r[u][2]),
                                               bf16_lo(r[u][3]))),
-                          silu_fma(conv4_acc(wx1, bx1, bf16_hi(r[u][0]), bf16_hi(r[u][1]), bf16_hi(r[u][2]),
+                          silu_x(conv4_acc(wx1, bx1, bf16_hi(r[u][0]), bf16_hi(r[u][1]), bf16_hi(r[u][2]),
                                               bf16_hi(r[u][3]))));
       }
       for (; v < v1; ++v) {
@@ -838,8 +842,8 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
         const uint32_t r0 = xi[t.x * (XW / 2)], r1 = xi[t.y * (XW / 2)], r2 = xi[t.z * (XW / 2)],
                        r3 = xi[t.w * (XW / 2)];
         xo[v * (XSTR / 2)] =
-            make_float2(silu_fma(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
-                        silu_fma(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
+            make_float2(silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
+                        silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
       }
       if (FUSE) {  // u_j = w_{j,h}·x_j of the committed path (window rows j .. j+3)
         const float* wj = eSg + ((g & 1) * G + (2 * cp) / kP) * W.NP + n + 1;
@@ -848,8 +852,8 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
           const uint32_t r0 = xi[j * (XW / 2)], r1 = xi[(j + 1) * (XW / 2)], r2 = xi[(j + 2) * (XW / 2)],
                          r3 = xi[(j + 3) * (XW / 2)];
           *reinterpret_cast<float2*>(ub + j * ROWS + 2 * cp) = make_float2(
-              wj[j] * silu_fma(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
-              wj[j] * silu_fma(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
+              wj[j] * silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
+              wj[j] * silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
         }
       }
     }
