@@ -16,12 +16,13 @@
 // children are done"); h0 is read from HBM exactly once.
 //
 // Two kernels per call:
-//  * tree_prep_kernel, one CTA per (layer, sequence) instance: B and C conv +
+//  * tree_prep_kernel, one CTA per (layer, sequence) instance, or per (instance,
+//    block of heads) when the instances do not fill the SMs: B and C conv +
 //    SiLU for every node, the path tables, C_v·B_m along every path, Δ, S,
 //    e^S and coef[v,m] for every head, and C split into bf16 hi + lo, written
-//    to a caller-provided workspace (tens of KB per instance, L2-sized).  It
-//    lets the main kernel be scheduled while its last CTAs run (programmatic
-//    dependent launch).
+//    to a caller-provided workspace (tens of KB per instance, L2-sized).  Every
+//    global load it makes goes out before its first barrier.  It lets the main
+//    kernel be scheduled while its last CTAs run (programmatic dependent launch).
 //  * tree_verify_kernel, one CTA (256 threads) per (instance, run of head
 //    groups of G heads).  Warp 0 is the producer: it streams the group's h0
 //    slice through a ring of 16-column chunks (4 stages, 3 with a folded commit;
@@ -30,7 +31,10 @@
 //    each group's inputs (x rows, e^S, coef) on a second barrier.  The x conv +
 //    SiLU of group g+1 runs between group g's chunks.  Each node tile's
 //    accumulator starts at the path terms, a (rows x nodes)·(nodes x nodes)
-//    product on the tensor cores; each chunk is contracted against C on the
+//    product on the tensor cores whose coefficients come through a per-node
+//    bitmask of its path (k-steps no path reaches are skipped); trees of 2-4
+//    tiles contract every chunk against all their tiles in one pass, with
+//    accumulators sized to the tiles; each chunk is contracted against C on the
 //    tensor cores (mma m16n8k16 on bf16 hi/lo splits of both operands, three
 //    products hi·hi + hi·lo + lo·hi, fp32 accumulate: each product to ~2^-17
 //    relative, far inside the 1e-3 output bound); the epilogue scales by
@@ -42,10 +46,11 @@
 //     h' = E·h + Σ_j u_j ⊗ B_j,   E = Π_j a_j,   u_j = w_j·x_j,   w_j = Δ_j·Π_{i>j} a_i,
 // with a_j = exp(Δ_j·A) and x_j, B_j the post-conv rows of path node j (conv over
 // [the ring rows before the path ‖ the path rows]).  The prep kernel computes
-// E, w_j and B_j, writes the path's last rows into the conv ring and advances
-// its head; the main kernel computes its heads' u_j next to the tree's x conv,
-// rewrites every h chunk it streams in as h', stores it over h, and contracts
-// C against h'.
+// E, w_j and B_j and writes the path's last rows into the conv ring; the main
+// kernel advances the ring head (after the whole prep grid: every prep CTA of an
+// instance reads the old one), computes its heads' u_j next to the tree's x
+// conv, rewrites every h chunk it streams in as h', stores it over h, and
+// contracts C against h'.
 // The state is read once and written once per speculative step, instead of
 // read by verify and read + written again by a separate commit.
 #include <cuda.h>
