@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(CTHREADS) commit_kernel(CommitArgs a) {
   __shared__ __align__(16) float xs[PC][CROWS];
   __shared__ float dls[PC][CG];
   __shared__ float decs[PC][CG];
+  __shared__ float Es[CG];
   __shared__ int taps[PC][3];
 
   const int tid = threadIdx.x;
@@ -172,7 +173,28 @@ __global__ void __launch_bounds__(CTHREADS) commit_kernel(CommitArgs a) {
       decs[j][g] = e;
     }
     __syncthreads();
-    // sweep the state slice: h = a_j·h + (Δ_j·x_j[p])·B_j[n] for the path nodes in order
+    // longer sweeps take their nodes as one rank-cnt update (the folded commit's form):
+    //     h' = E·h + Σ_j (w_j·x_j[p])·B_j[n],  w_j = Δ_j·Π_{i>j} a_i,  E = Π_j a_j  (per head),
+    // one FMA per node and element instead of a multiply and an FMA; short ones (the common
+    // accepted paths of a few nodes) keep the node-by-node update, which needs no extra pass
+    const bool folded = cnt > 4;
+    if (folded && tid < CG) {
+      float run = 1.f;
+      for (int j = cnt - 1; j >= 0; --j) {
+        dls[j][tid] *= run;  // w_j
+        run *= decs[j][tid];
+      }
+      Es[tid] = run;
+    }
+    if (folded) {
+      __syncthreads();
+      for (int i = tid; i < cnt * CROWS; i += CTHREADS) {
+        const int j = i / CROWS, r = i - j * CROWS;
+        xs[j][r] *= dls[j][r / kP];  // u_j[p] = w_j·x_j[p]
+      }
+      __syncthreads();
+    }
+    // sweep the state slice
     for (int e0 = tid; e0 < n4; e0 += CTHREADS * 4) {
       float4 hv[4];
 #pragma unroll
@@ -188,14 +210,27 @@ __global__ void __launch_bounds__(CTHREADS) commit_kernel(CommitArgs a) {
         const int g = row / kP;
         const int nn = (e % (kN / 4)) * 4;
         float4 h4 = hv[u];
-        for (int j = 0; j < cnt; ++j) {
-          const float uu = __fmul_rn(dls[j][g], xs[j][row]);
-          const float dec = decs[j][g];
-          const float4 b4 = *reinterpret_cast<const float4*>(&Bs[j][nn]);
-          h4.x = ssm_update(dec, h4.x, uu, b4.x);
-          h4.y = ssm_update(dec, h4.y, uu, b4.y);
-          h4.z = ssm_update(dec, h4.z, uu, b4.z);
-          h4.w = ssm_update(dec, h4.w, uu, b4.w);
+        if (folded) {
+          const float E = Es[g];
+          h4 = make_float4(E * h4.x, E * h4.y, E * h4.z, E * h4.w);
+          for (int j = 0; j < cnt; ++j) {
+            const float uu = xs[j][row];
+            const float4 b4 = *reinterpret_cast<const float4*>(&Bs[j][nn]);
+            h4.x = fmaf(uu, b4.x, h4.x);
+            h4.y = fmaf(uu, b4.y, h4.y);
+            h4.z = fmaf(uu, b4.z, h4.z);
+            h4.w = fmaf(uu, b4.w, h4.w);
+          }
+        } else {
+          for (int j = 0; j < cnt; ++j) {
+            const float uu = __fmul_rn(dls[j][g], xs[j][row]);
+            const float dec = decs[j][g];
+            const float4 b4 = *reinterpret_cast<const float4*>(&Bs[j][nn]);
+            h4.x = ssm_update(dec, h4.x, uu, b4.x);
+            h4.y = ssm_update(dec, h4.y, uu, b4.y);
+            h4.z = ssm_update(dec, h4.z, uu, b4.z);
+            h4.w = ssm_update(dec, h4.w, uu, b4.w);
+          }
         }
         reinterpret_cast<float4*>(hs)[e] = h4;
       }
