@@ -722,7 +722,11 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   constexpr int PAIRS = ROWS / 2;
   constexpr int PARTS = THREADS / PAIRS;
   const int NX = (n + 15) & ~15;
-  for (int i = tid; i < (NX - n) * XSTR; i += THREADS) xs[n * XSTR + i] = 0.f;  // padding nodes
+  {  // padding nodes (trees of several tiles: whole node pairs past the tree, a half pair is
+     // written by the conv)
+    const int x0 = NTL > 1 ? ((n + 1) & ~1) * XSTR : n * XSTR;
+    for (int i = x0 + tid; i < NX * XSTR; i += THREADS) xs[i] = 0.f;
+  }
   const int cp = tid % PAIRS, cpart = tid / PAIRS;
   const float4* cw = reinterpret_cast<const float4*>(a.conv_w + (size_t)layer * conv_dim * kW);
   const float* cb = a.conv_b + (size_t)layer * conv_dim;
@@ -803,6 +807,19 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
   // and measured faster there); with the special-function unit for trees of several tiles, whose
   // conv is 2.5x the work per state byte and issue-bound
   auto silu_x = [](float v) { return NTL > 1 ? silu_fast(v) : silu_fma(v); };
+  // u_j = w_{j,h}·x_j of the committed path (window rows j .. j+3), this thread's channels
+  auto conv_u = [&](int g, const uint32_t* __restrict__ xi) {
+    if (!FUSE) return;
+    const float* wj = eSg + ((g & 1) * G + (2 * cp) / kP) * W.NP + n + 1;
+    float* ub = uPs + (g & 1) * LP * ROWS;
+    for (int j = cpart; j < lenP; j += PARTS) {
+      const uint32_t r0 = xi[j * (XW / 2)], r1 = xi[(j + 1) * (XW / 2)], r2 = xi[(j + 2) * (XW / 2)],
+                     r3 = xi[(j + 3) * (XW / 2)];
+      *reinterpret_cast<float2*>(ub + j * ROWS + 2 * cp) = make_float2(
+          wj[j] * silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
+          wj[j] * silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
+    }
+  };
   auto xconv = [&](int g) {
     const int hb = hc_begin + g * G, heads = min(G, a.H - hb);
     if (NTL > 1) load_xw(hb);  // in flight during the wait for the rows
@@ -818,7 +835,53 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
             *reinterpret_cast<const uint4*>(xinX + (3 + j) * XW + pc * 8);
       }
     }
-    if (2 * cp < heads * kP) {
+    if (NTL > 1 && 2 * cp < heads * kP) {
+      // trees of several tiles: x stored as the path-term A operand, node pairs (v, v + 1) of a
+      // row split into bf16 hi and lo once here instead of once per node tile that reads them;
+      // pair p of row r at xp[p * XSTR + r] = {hi, lo} (the bytes of the fp32 rows)
+      const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
+      uint4* __restrict__ xp = reinterpret_cast<uint4*>(xs) + cp;                       // pair p: xp[p * XSTR/2]
+      const int per = ((n + PARTS - 1) / PARTS + 1) & ~1;  // even: a thread's nodes are whole pairs
+      const int v1 = min(n, (cpart + 1) * per);
+      auto load4 = [&](int v, uint32_t (&r)[4]) {  // the four conv taps' rows of node v
+        const int4 t = rowidx[v];
+        r[0] = xi[t.x * (XW / 2)];
+        r[1] = xi[t.y * (XW / 2)];
+        r[2] = xi[t.z * (XW / 2)];
+        r[3] = xi[t.w * (XW / 2)];
+      };
+      // nodes v and v + 1 (taps ra, rb): conv + SiLU, split, stored as pair v / 2
+      auto store_pair = [&](int v, const uint32_t (&ra)[4], const uint32_t (&rb)[4], bool has_b) {
+        const float a0 = silu_x(conv4_acc(wx0, bx0, bf16_lo(ra[0]), bf16_lo(ra[1]), bf16_lo(ra[2]), bf16_lo(ra[3])));
+        const float a1 = silu_x(conv4_acc(wx1, bx1, bf16_hi(ra[0]), bf16_hi(ra[1]), bf16_hi(ra[2]), bf16_hi(ra[3])));
+        float b0 = 0.f, b1 = 0.f;
+        if (has_b) {
+          b0 = silu_x(conv4_acc(wx0, bx0, bf16_lo(rb[0]), bf16_lo(rb[1]), bf16_lo(rb[2]), bf16_lo(rb[3])));
+          b1 = silu_x(conv4_acc(wx1, bx1, bf16_hi(rb[0]), bf16_hi(rb[1]), bf16_hi(rb[2]), bf16_hi(rb[3])));
+        }
+        uint4 o;
+        split_bf16x2(a0, b0, o.x, o.y);
+        split_bf16x2(a1, b1, o.z, o.w);
+        xp[(v >> 1) * (XSTR / 2)] = o;
+      };
+      int v = cpart * per;
+      for (; v + 4 <= v1; v += 4) {  // two pairs at a time: 16 loads in flight
+        uint32_t r[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load4(v + u, r[u]);
+        store_pair(v, r[0], r[1], true);
+        store_pair(v + 2, r[2], r[3], true);
+      }
+      for (; v < v1; v += 2) {  // a last pair; past the tree's end its second node is zero
+        uint32_t r[2][4] = {};
+        load4(v, r[0]);
+        const bool has_b = v + 1 < n;
+        if (has_b) load4(v + 1, r[1]);
+        store_pair(v, r[0], r[1], has_b);
+      }
+      conv_u(g, xi);
+    }
+    if (NTL == 1 && 2 * cp < heads * kP) {
       const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
       float2* __restrict__ xo = reinterpret_cast<float2*>(xs) + cp;                     // node v: xo[v * XSTR/2]
       const int per = (n + PARTS - 1) / PARTS;
@@ -850,17 +913,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
             make_float2(silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
                         silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
       }
-      if (FUSE) {  // u_j = w_{j,h}·x_j of the committed path (window rows j .. j+3)
-        const float* wj = eSg + ((g & 1) * G + (2 * cp) / kP) * W.NP + n + 1;
-        float* ub = uPs + (g & 1) * LP * ROWS;
-        for (int j = cpart; j < lenP; j += PARTS) {
-          const uint32_t r0 = xi[j * (XW / 2)], r1 = xi[(j + 1) * (XW / 2)], r2 = xi[(j + 2) * (XW / 2)],
-                         r3 = xi[(j + 3) * (XW / 2)];
-          *reinterpret_cast<float2*>(ub + j * ROWS + 2 * cp) = make_float2(
-              wj[j] * silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
-              wj[j] * silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
-        }
-      }
+      conv_u(g, xi);
     }
     if (NTL == 1 && g + 1 < g_count) load_xw(hb + G);  // the next group's, early
   };
@@ -925,14 +978,23 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
                              bhi[nt][1], blo[nt][1]);
               }
               const float* xa = xs + m0 * XSTR + wrow + fg;
+              // several tiles: the pairs (m0, m0 + 1) and (m0 + 8, m0 + 9) already split by the conv
+              const uint2* xq = reinterpret_cast<const uint2*>(xs) + (m0 >> 1) * XSTR + wrow + fg;
 #pragma unroll
               for (int mt = 0; mt < MT; ++mt) {
-                const float* x0 = xa + mt * 16;
                 uint32_t ahi[4], alo[4];
-                split_bf16x2(x0[0], x0[XSTR], ahi[0], alo[0]);
-                split_bf16x2(x0[8], x0[XSTR + 8], ahi[1], alo[1]);
-                split_bf16x2(x0[8 * XSTR], x0[9 * XSTR], ahi[2], alo[2]);
-                split_bf16x2(x0[8 * XSTR + 8], x0[9 * XSTR + 8], ahi[3], alo[3]);
+                if (NTL > 1) {
+                  const uint2* q0 = xq + mt * 16;
+                  const uint2 p0 = q0[0], p1 = q0[8], p2 = q0[4 * XSTR], p3 = q0[4 * XSTR + 8];
+                  ahi[0] = p0.x, alo[0] = p0.y, ahi[1] = p1.x, alo[1] = p1.y;
+                  ahi[2] = p2.x, alo[2] = p2.y, ahi[3] = p3.x, alo[3] = p3.y;
+                } else {
+                  const float* x0 = xa + mt * 16;
+                  split_bf16x2(x0[0], x0[XSTR], ahi[0], alo[0]);
+                  split_bf16x2(x0[8], x0[XSTR + 8], ahi[1], alo[1]);
+                  split_bf16x2(x0[8 * XSTR], x0[9 * XSTR], ahi[2], alo[2]);
+                  split_bf16x2(x0[8 * XSTR + 8], x0[9 * XSTR + 8], ahi[3], alo[3]);
+                }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                   mma_bf16(acc[i][mt][nt], alo, bhi[nt]);
