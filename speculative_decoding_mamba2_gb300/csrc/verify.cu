@@ -527,7 +527,7 @@ __host__ __device__ inline Smem smem_layout(int n, int PP, int NP, int LP) {
   s.pairs = take((PP + 4) * 4);
   s.Cs = take(n * CSTR * 4);
   s.xs = take(((n + 15) & ~15) * xs_stride<G>() * 4);
-  s.xinX = take((n + 3 + LP) * XW * 2);  // [window: 3 ring rows before the path ‖ path rows][tree rows]
+  s.xinX = take((n + 3 + LP) * G * kP * 2);  // [window: 3 ring rows before the path ‖ path rows][tree rows]
   s.eSg = take(2 * G * NP * 4);    // two groups in flight: the next group's inputs land
   s.coefg = take(2 * G * PP * 4);  // before the current group's epilogue
   s.BPs = take(FUSE ? LP * kN * 4 : 0);        // committed path B_j
@@ -549,6 +549,7 @@ template <int G, bool FUSE, int NTL, bool DEEP>
 __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
     tree_verify_kernel(VerifyArgs a, const unsigned char* __restrict__ ws_base, const __grid_constant__ CUtensorMap tmap) {
   constexpr int ROWS = G * kP;
+  constexpr int XWG = G * kP;  // channels per staged x row: this group's
   constexpr int STAGES = DEEP ? STAGES_DEEP : FUSE ? STAGES_FUSED : STAGES_PLAIN;
   extern __shared__ __align__(128) unsigned char smem[];
   const int n = a.n;
@@ -632,7 +633,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
         src = a.prev_xBC + ((size_t)inst * a.prev_n + s_meta[4 + r - 3]) * conv_dim;
       else
         src = xbc + (size_t)(r - win) * conv_dim;
-      bulk_load(smem_u32(xinX + r * XW), src + hb * kP, xb, x_bar);
+      bulk_load(smem_u32(xinX + r * XWG), src + hb * kP, xb, x_bar);
     }
     if (lane == 0)
       bulk_load(smem_u32(eSg + buf * G * W.NP), ws + W.eS + (size_t)hb * W.NP * 4, heads * W.NP * 4, x_bar);
@@ -813,8 +814,8 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
     const float* wj = eSg + ((g & 1) * G + (2 * cp) / kP) * W.NP + n + 1;
     float* ub = uPs + (g & 1) * LP * ROWS;
     for (int j = cpart; j < lenP; j += PARTS) {
-      const uint32_t r0 = xi[j * (XW / 2)], r1 = xi[(j + 1) * (XW / 2)], r2 = xi[(j + 2) * (XW / 2)],
-                     r3 = xi[(j + 3) * (XW / 2)];
+      const uint32_t r0 = xi[j * (XWG / 2)], r1 = xi[(j + 1) * (XWG / 2)], r2 = xi[(j + 2) * (XWG / 2)],
+                     r3 = xi[(j + 3) * (XWG / 2)];
       *reinterpret_cast<float2*>(ub + j * ROWS + 2 * cp) = make_float2(
           wj[j] * silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
           wj[j] * silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
@@ -832,23 +833,23 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
       for (int i = tid; i < (lenP - j0) * per_row; i += THREADS) {
         const int j = j0 + i / per_row, pc = i - (i / per_row) * per_row;
         *reinterpret_cast<uint4*>(rw + (size_t)ring_pos(s_meta[1], j, R) * conv_dim + pc * 8) =
-            *reinterpret_cast<const uint4*>(xinX + (3 + j) * XW + pc * 8);
+            *reinterpret_cast<const uint4*>(xinX + (3 + j) * XWG + pc * 8);
       }
     }
     if (NTL > 1 && 2 * cp < heads * kP) {
       // trees of several tiles: x stored as the path-term A operand, node pairs (v, v + 1) of a
       // row split into bf16 hi and lo once here instead of once per node tile that reads them;
       // pair p of row r at xp[p * XSTR + r] = {hi, lo} (the bytes of the fp32 rows)
-      const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
+      const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XWG/2]
       uint4* __restrict__ xp = reinterpret_cast<uint4*>(xs) + cp;                       // pair p: xp[p * XSTR/2]
       const int per = ((n + PARTS - 1) / PARTS + 1) & ~1;  // even: a thread's nodes are whole pairs
       const int v1 = min(n, (cpart + 1) * per);
       auto load4 = [&](int v, uint32_t (&r)[4]) {  // the four conv taps' rows of node v
         const int4 t = rowidx[v];
-        r[0] = xi[t.x * (XW / 2)];
-        r[1] = xi[t.y * (XW / 2)];
-        r[2] = xi[t.z * (XW / 2)];
-        r[3] = xi[t.w * (XW / 2)];
+        r[0] = xi[t.x * (XWG / 2)];
+        r[1] = xi[t.y * (XWG / 2)];
+        r[2] = xi[t.z * (XWG / 2)];
+        r[3] = xi[t.w * (XWG / 2)];
       };
       // nodes v and v + 1 (taps ra, rb): conv + SiLU, split, stored as pair v / 2
       auto store_pair = [&](int v, const uint32_t (&ra)[4], const uint32_t (&rb)[4], bool has_b) {
@@ -882,7 +883,7 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
       conv_u(g, xi);
     }
     if (NTL == 1 && 2 * cp < heads * kP) {
-      const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XW/2]
+      const uint32_t* __restrict__ xi = reinterpret_cast<const uint32_t*>(xinX) + cp;  // row r: xi[r * XWG/2]
       float2* __restrict__ xo = reinterpret_cast<float2*>(xs) + cp;                     // node v: xo[v * XSTR/2]
       const int per = (n + PARTS - 1) / PARTS;
       const int v1 = min(n, (cpart + 1) * per);
@@ -892,10 +893,10 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int4 t = rowidx[v + u];
-          r[u][0] = xi[t.x * (XW / 2)];
-          r[u][1] = xi[t.y * (XW / 2)];
-          r[u][2] = xi[t.z * (XW / 2)];
-          r[u][3] = xi[t.w * (XW / 2)];
+          r[u][0] = xi[t.x * (XWG / 2)];
+          r[u][1] = xi[t.y * (XWG / 2)];
+          r[u][2] = xi[t.z * (XWG / 2)];
+          r[u][3] = xi[t.w * (XWG / 2)];
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
@@ -907,8 +908,8 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
       }
       for (; v < v1; ++v) {
         const int4 t = rowidx[v];
-        const uint32_t r0 = xi[t.x * (XW / 2)], r1 = xi[t.y * (XW / 2)], r2 = xi[t.z * (XW / 2)],
-                       r3 = xi[t.w * (XW / 2)];
+        const uint32_t r0 = xi[t.x * (XWG / 2)], r1 = xi[t.y * (XWG / 2)], r2 = xi[t.z * (XWG / 2)],
+                       r3 = xi[t.w * (XWG / 2)];
         xo[v * (XSTR / 2)] =
             make_float2(silu_x(conv4_acc(wx0, bx0, bf16_lo(r0), bf16_lo(r1), bf16_lo(r2), bf16_lo(r3))),
                         silu_x(conv4_acc(wx1, bx1, bf16_hi(r0), bf16_hi(r1), bf16_hi(r2), bf16_hi(r3))));
