@@ -1051,6 +1051,29 @@ def run_draft_only(args):
     return 0
 
 
+def run_ternary_only(args):
+    """The stress workload's 40-node ternary tree alone (Mamba2-780M shape, 48 layers):
+    the folded rounds of config4.ternary on the first `--seqs` sequences (all 64 by
+    default), with the same timing and roofline; a smaller --seqs gives a case small
+    enough for a profiler capture."""
+    import torch
+
+    from synth import batch_parallel, workload
+    dev = torch.device("cuda")
+    stream = torch.cuda.current_stream()
+    peak, peak_kind = measured_peaks()
+    w = workload(4)
+    seqs = list(range(min(max(args.seqs, 1), w.batch)))
+    b = batch_parallel(w, seqs=seqs)
+    r = folded_rounds(w, b, dev, stream, 1, max(5, min(args.steps, 10)), args.warmup)
+    out = {"workload": w.name + f" (40-node ternary tree, {len(seqs)} sequences)",
+           "instances": r["L"] * r["S"], "mean_accepted_path": float(r["path_lens"].mean())}
+    out.update(tree_roofline(w, r, peak, peak_kind, r["n"] * r["L"] * r["S"], 1))
+    print(json.dumps({"metric": "ternary-tree folded rounds", "higher_is_better": True, "data": "synthetic",
+                      **out}), flush=True)
+    return 0
+
+
 def run_block_steps(args):
     """One Mamba2-2.7B block's steps at the batched-verify shape (16 sequences x 16 nodes,
     256 tree tokens), each timed alone as a CUDA graph of 8 consecutive layers' launches
@@ -1680,10 +1703,12 @@ def main():
     ap.add_argument("--no-config2", action="store_true", help="skip the batch-1 target verify workload")
     ap.add_argument("--no-config4", action="store_true", help="skip the stress workload (batch 64)")
     ap.add_argument("--no-block", action="store_true")
-    ap.add_argument("--only", choices=["linear", "draft", "block-steps"], default=None,
+    ap.add_argument("--only", choices=["linear", "draft", "block-steps", "ternary"], default=None,
                     help="run one measurement alone: 'linear' = the block's projections, "
                          "'draft' = the draft side (one-token steps + replay, tree drafting), "
-                         "'block-steps' = one block's steps timed one by one")
+                         "'block-steps' = one block's steps timed one by one, "
+                         "'ternary' = the stress workload's ternary tree (see --seqs)")
+    ap.add_argument("--seqs", type=int, default=64, help="with --only ternary: sequences of the stress workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1697,6 +1722,8 @@ def main():
         return run_draft_only(args)
     if args.only == "block-steps":
         return run_block_steps(args)
+    if args.only == "ternary":
+        return run_ternary_only(args)
     return run_ours(args, w)
 
 
