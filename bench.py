@@ -1514,6 +1514,37 @@ def ancestors_at(parent, dep, level):
     return out
 
 
+def e2e_chunk_sizes(split, S, chunks=4):
+    """Sequences per chunk of an e2e round (S sequences in all).
+    'pairs': 1, 1, then 2 at a time: the first chunk lands early, and two compute streams
+    fill each other's tails (measured at batch 16: 1.26 ms per round, against 1.26-1.29 for
+    2 x 8 or 1 x 8 + 2 x 4, 1.33-1.35 for the ramp or 16 x 1, 1.38 for 4 x 4).
+    'ramp': 1, 1, 2, 3, ...: the first chunk lands early, later ones keep up (a small tail
+    chunk is folded into the one before).
+    A list such as '2,2,4,8': those sizes (positive, summing to S).
+    '': `chunks` equal chunks (one chunk when S is not a multiple)."""
+    if split == "pairs":
+        sizes = [1] * min(S, 2)
+        while sum(sizes) < S:
+            sizes.append(min(2, S - sum(sizes)))
+    elif split == "ramp":
+        sizes, nxt = [1], 1
+        while sum(sizes) < S:
+            sizes.append(min(nxt, S - sum(sizes)))
+            nxt += 1
+        if len(sizes) > 2 and 2 * sizes[-1] < sizes[-2]:
+            tail = sizes.pop()
+            sizes[-1] += tail
+    elif split:
+        sizes = [int(v) for v in split.split(",")]
+        if sum(sizes) != S or min(sizes) < 1:
+            raise SystemExit(f"--e2e-split must be positive sizes summing to {S}")
+    else:
+        k = chunks if chunks >= 1 and S % chunks == 0 else 1
+        sizes = [S // k] * k
+    return sizes
+
+
 def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     """Same rounds through the public API with each round's inputs in pinned host
     memory.  Per round, inside the timed region: the host layout build; the H2D of
@@ -1555,27 +1586,7 @@ def run_e2e(args, w, b, dims, prm, h, ring, head, ws_f, dev, stream, world):
     out_bonus = torch.empty(S, dtype=torch.int32).pin_memory()
     lay_pin = torch.empty((S, n, 8), dtype=torch.int32).pin_memory()
     copy_stream = torch.cuda.Stream(dev)
-    if args.e2e_split == "pairs":  # 1, 1, then 2 at a time: the first chunk lands early, and two
-        # compute streams fill each other's tails (measured at batch 16: 1.26 ms per round, against
-        # 1.26-1.29 for 2 x 8 or 1 x 8 + 2 x 4, 1.33-1.35 for the ramp or 16 x 1, 1.38 for 4 x 4)
-        sizes = [1] * min(S, 2)
-        while sum(sizes) < S:
-            sizes.append(min(2, S - sum(sizes)))
-    elif args.e2e_split == "ramp":  # 1, 1, 2, 3, ...: the first chunk lands early, later ones keep up
-        sizes, nxt = [1], 1
-        while sum(sizes) < S:
-            sizes.append(min(nxt, S - sum(sizes)))
-            nxt += 1
-        if len(sizes) > 2 and 2 * sizes[-1] < sizes[-2]:  # fold a small tail chunk into the one before
-            tail = sizes.pop()
-            sizes[-1] += tail
-    elif args.e2e_split:  # explicit chunk sizes in sequences, e.g. "2,2,4,8"
-        sizes = [int(v) for v in args.e2e_split.split(",")]
-        if sum(sizes) != S or min(sizes) < 1:
-            raise SystemExit(f"--e2e-split must be positive sizes summing to {S}")
-    else:
-        k = args.e2e_chunks if S % args.e2e_chunks == 0 else 1
-        sizes = [S // k] * k
+    sizes = e2e_chunk_sizes(args.e2e_split, S, args.e2e_chunks)
     bounds = [sum(sizes[:i]) for i in range(len(sizes) + 1)]
     n_chunks = len(sizes)
     state = {"r": 0, "depth": depth}
