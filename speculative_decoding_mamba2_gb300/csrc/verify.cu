@@ -943,7 +943,6 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) brow[i][nt] = min((tb * NTL + i) * NT + nt * 8 + fg, n - 1) * CSTR;
       for (int kc = 0; kc < KCH; ++kc, ++q) {
-        if (warp == 0) produce(q + STAGES);  // refill the stage chunk q-1 used
         if (kc == 0) {
           // each tile's accumulator starts at Σ_m coef[v,m]·x_m[p] (path terms and D·x over e^{S_v}):
           // A = x rows of the nodes m (K), B = coef of node v (N; zero off v's path)
@@ -1021,6 +1020,12 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
           ra[mt] = *reinterpret_cast<const float4*>(r0 + off);
           rb[mt] = *reinterpret_cast<const float4*>(r0 + 8 * SROW * 4 + off);
         }
+        // the chunk's rows are in registers: the stage is free once every warp has them, and
+        // warp 0 refills it with chunk q + STAGES before this chunk's arithmetic, so STAGES
+        // chunks stay in flight while it runs
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(slot));
+        if (warp == 0) produce(q + STAGES + 1);
         if (FUSE) {
           // h' = E·h + Σ_j u_j[row]·B_j[col] on this lane's 4 x 2*MT elements, then h' over h
 #pragma unroll
@@ -1100,8 +1105,6 @@ __global__ void __launch_bounds__(THREADS, DEEP ? 1 : 2)
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(slot));  // this warp is done with the stage
         if (kc == 1 && last_tb && gi + 1 < g_count) {
           // the next group's x conv (special-function heavy) runs between this group's chunks,
           // next to other warps' tensor and memory work; every warp must be past this group's
